@@ -1,0 +1,191 @@
+"""fp64 CPU oracle for the Gated DeltaNet forward pass -- TEST INFRASTRUCTURE.
+
+Only tests/, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  It shares no code with the CUDA library
+(``gated_deltanet_chunked_gdn_gb300``) and never imports it.
+
+The arithmetic lives in ``gdn_oracle.c`` (plain C, fp64, OpenMP over
+independent (sequence, value-head) chains); this file builds it with gcc and
+marshals numpy arrays.  Forms:
+
+* :func:`recurrent` -- the token recurrence (the operator's definition).
+* :func:`chunked` -- the chunked form with an explicit Gauss-Jordan inverse.
+* :func:`chunked_stages` -- the chunked form of one chain, returning every
+  per-chunk intermediate (gamma, A, T, W, U, S0, V').
+
+Tensor conventions (same as the library): q, k ``[B, T, Hqk, K]``;
+v ``[B, T, Hv, V]``; g, beta ``[B, T, Hv]``; h0 / ht ``[N, Hv, K, V]``;
+with ``cu_seqlens`` (length N+1) the batch is packed and B must be 1.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libgdn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile gdn_oracle.c into oracle/_build/libgdn_oracle.so (gcc, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _bind(lib):
+    dp = ctypes.POINTER(ctypes.c_double)
+    i64p = ctypes.POINTER(ctypes.c_int64)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    common = [ctypes.c_int64, ctypes.c_int, i64p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.oracle_recurrent.argtypes = common + [dp] * 5 + [ctypes.c_double, dp, dp, dp, i32p, ctypes.c_int, ctypes.c_int]
+    lib.oracle_recurrent.restype = ctypes.c_int
+    lib.oracle_chunked.argtypes = common + [ctypes.c_int] + [dp] * 5 + [ctypes.c_double, dp, dp, dp, i32p, ctypes.c_int, ctypes.c_int]
+    lib.oracle_chunked.restype = ctypes.c_int
+    lib.oracle_chunked_stages.argtypes = (common + [ctypes.c_int] + [dp] * 5 + [ctypes.c_double, dp, ctypes.c_int, ctypes.c_int]
+                                          + [dp] * 9)
+    lib.oracle_chunked_stages.restype = ctypes.c_int
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(ctypes.CDLL(build()))
+    return _lib
+
+
+class Oracle:
+    """The same entry points bound to another build of gdn_oracle.c (used by
+    the mutation tests, which compile copies with a planted mistake)."""
+
+    def __init__(self, so_path: str):
+        self._lib = _bind(ctypes.CDLL(so_path))
+
+    def recurrent(self, *a, **kw):
+        return recurrent(*a, _lib=self._lib, **kw)
+
+    def chunked(self, *a, **kw):
+        return chunked(*a, _lib=self._lib, **kw)
+
+
+def _f64(x):
+    if x is None:
+        return None
+    try:  # torch tensors (bf16 included) without importing torch here
+        import torch  # noqa: WPS433 (local import keeps numpy-only callers light)
+        if isinstance(x, torch.Tensor):
+            x = x.detach().to("cpu", dtype=torch.float64).numpy()
+    except ImportError:
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i64(x):
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().to("cpu").numpy()
+    except ImportError:
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int64))
+
+
+def _ptr(a):
+    if a is None:
+        return ctypes.POINTER(ctypes.c_double)()
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _prep(q, k, v, g, beta, h0, cu_seqlens):
+    q, k, v, g, beta, h0 = (_f64(t) for t in (q, k, v, g, beta, h0))
+    B, T, Hqk, K = q.shape
+    Hv, V = v.shape[2], v.shape[3]
+    if cu_seqlens is None:
+        N = B
+        cu = np.arange(0, (B + 1) * T, T, dtype=np.int64)[: B + 1]
+    else:
+        cu = _i64(cu_seqlens)
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        N = cu.shape[0] - 1
+    return q, k, v, g, beta, h0, cu, B, T, Hqk, K, Hv, V, N
+
+
+def _chains(chains):
+    if chains is None:
+        return ctypes.POINTER(ctypes.c_int32)(), 0, None
+    arr = np.ascontiguousarray(np.asarray(chains, dtype=np.int32))
+    return arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), int(arr.shape[0]), arr
+
+
+def recurrent(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, chains=None, nthreads=0, _lib=None):
+    """Token recurrence. Returns (o [B,T,Hv,V], ht [N,Hv,K,V]) as float64.
+
+    ``chains``: optional list of chain ids ``n * Hv + h``; other chains' outputs
+    are left as NaN.
+    """
+    q, k, v, g, beta, h0, cu, B, T, Hqk, K, Hv, V, N = _prep(q, k, v, g, beta, h0, cu_seqlens)
+    o = np.full((B, T, Hv, V), np.nan if chains is not None else 0.0)
+    ht = np.full((N, Hv, K, V), np.nan if chains is not None else 0.0)
+    cp, nc, _keep = _chains(chains)
+    rc = (_lib or _load()).oracle_recurrent(B * T, N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), Hqk, Hv, K, V,
+                                  _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(h0),
+                                  _ptr(o), _ptr(ht), cp, nc, int(nthreads))
+    if rc:
+        raise RuntimeError(f"oracle_recurrent failed: {rc}")
+    return o, ht
+
+
+def chunked(q, k, v, g, beta, scale, C, h0=None, cu_seqlens=None, chains=None, nthreads=0, _lib=None):
+    """Naive chunked form (explicit inverse). Returns (o, ht) as float64."""
+    q, k, v, g, beta, h0, cu, B, T, Hqk, K, Hv, V, N = _prep(q, k, v, g, beta, h0, cu_seqlens)
+    o = np.full((B, T, Hv, V), np.nan if chains is not None else 0.0)
+    ht = np.full((N, Hv, K, V), np.nan if chains is not None else 0.0)
+    cp, nc, _keep = _chains(chains)
+    rc = (_lib or _load()).oracle_chunked(B * T, N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), Hqk, Hv, K, V, int(C),
+                                _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), _ptr(h0),
+                                _ptr(o), _ptr(ht), cp, nc, int(nthreads))
+    if rc:
+        raise RuntimeError(f"oracle_chunked failed: {rc}")
+    return o, ht
+
+
+def chunked_stages(q, k, v, g, beta, scale, C, n, h, h0=None, cu_seqlens=None):
+    """Chunked form of chain (n, h) with its per-chunk intermediates.
+
+    Returns a dict with gamma [NT,C], A [NT,C,C], T [NT,C,C], W [NT,C,K],
+    U [NT,C,V], S0 [NT,K,V], Vn [NT,C,V] (rows past a tail chunk's length are
+    zero), plus o [B,T,Hv,V] (this chain's rows only) and ht [N,Hv,K,V].
+    """
+    q, k, v, g, beta, h0, cu, B, T, Hqk, K, Hv, V, N = _prep(q, k, v, g, beta, h0, cu_seqlens)
+    L = int(cu[n + 1] - cu[n])
+    NT = max(1, -(-L // C))
+    out = {
+        "gamma": np.zeros((NT, C)), "A": np.zeros((NT, C, C)), "T": np.zeros((NT, C, C)),
+        "W": np.zeros((NT, C, K)), "U": np.zeros((NT, C, V)), "S0": np.zeros((NT, K, V)),
+        "Vn": np.zeros((NT, C, V)),
+    }
+    o = np.full((B, T, Hv, V), np.nan)
+    ht = np.full((N, Hv, K, V), np.nan)
+    rc = _load().oracle_chunked_stages(B * T, N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), Hqk, Hv, K, V,
+                                       int(C), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                       _ptr(h0), int(n), int(h), _ptr(o), _ptr(ht),
+                                       *(_ptr(out[key]) for key in ("gamma", "A", "T", "W", "U", "S0", "Vn")))
+    if rc:
+        raise RuntimeError(f"oracle_chunked_stages failed: {rc}")
+    out["o"], out["ht"] = o, ht
+    return out
