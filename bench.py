@@ -1,0 +1,345 @@
+#!/usr/bin/env python
+"""Throughput of the Gated DeltaNet chunked forward pass on GB300.
+
+Workload: the pages' kernel bench shape -- 16 sequences x 8192 tokens,
+Hqk = Hv = 32 (``--H``), K = V = 128, chunk C = 128, bf16 q/k/v/o, fp32
+g/beta/h0/ht, synthetic seeded inputs generated on the device (4.4 GB of
+compulsory traffic per step, far larger than the 129 MB L2, so no flush is
+needed between steps).
+
+One step = one ``gdn_chunk_fwd`` call over the whole batch (all stages of the
+hot path).  Prints ONE JSON line (rank 0).  Multi-GPU (torchrun): every rank
+runs its own independent batch (weak scaling, no data-path collective); the
+timed region is bracketed by barriers and the max over ranks is reported.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(bounded samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunk-fwd tokens/s (16x8192, H=32, K=V=128, bf16); % roofline"
+
+
+def peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def algorithmic(B, T, Hqk, Hv, K, V, C, elem=2, h0=True):
+    """Compulsory bytes and algorithmic FLOPs of one forward pass.
+
+    Bytes: q, k, v, o in the input dtype, g and beta fp32, h0 and ht fp32.
+    FLOPs (triangular products counted as half, KK^T / QK^T once per qk head):
+    per token Hqk*(C*K + C*K) + Hv*(C*V + C*K + C*V + 6*K*V + C*C/3).
+    """
+    tokens = B * T
+    N = B
+    per_tok = 2 * Hqk * K * elem + 2 * Hv * V * elem + 8 * Hv
+    state = N * Hv * K * V * 4 * (2 if h0 else 1)
+    nbytes = tokens * per_tok + state
+    flops = tokens * (Hqk * 2 * C * K + Hv * (2 * C * V + C * K + 6 * K * V + C * C / 3))
+    return nbytes, flops
+
+
+class ClockSampler:
+    """nvidia-smi sampler for SM clocks, power and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.error = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.error = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.error or not self.samples:
+            return {"error": self.error or "no samples"}
+        win = [p for t, p in self.samples if t0 - 0.15 <= t <= t1 + 0.15] or [self.samples[-1][1]]
+        sm = [float(p[1]) for p in win if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for p in win if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[5 + i].lower() == "active"})
+        pw = [float(p[3]) for p in win if p[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win), "power_w_max": max(pw) if pw else None}
+
+
+def gpu_uuid(dev: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:  # noqa: BLE001 - fall back to the ordinal
+        return str(dev)
+
+
+def cpu_oracle_sample(x: dict, w, nthreads: int, budget_s: float, n_chains: int | None = None) -> dict:
+    """Time the fp64 oracle on whole (sequence, head) chains of ``x``.
+
+    With ``n_chains`` unset, one chain is first timed on one thread and the
+    sample is sized to about ``budget_s`` CPU-seconds (a multiple of the
+    thread count, at most every chain of ``x``).
+    """
+    from oracle import oracle
+    oracle.build()
+    H = w.Hv
+    Bx = x["q"].shape[0]
+    if n_chains is None:
+        s0 = {k: x[k][0:1].cpu() for k in ("q", "k", "v", "g", "beta")}
+        h0 = x["h0"][0:1].cpu() if x["h0"] is not None else None
+        t = time.perf_counter()
+        oracle.recurrent(s0["q"], s0["k"], s0["v"], s0["g"], s0["beta"], x["scale"], h0=h0, chains=[0], nthreads=1)
+        t1 = time.perf_counter() - t
+        n = max(1, int(budget_s / max(t1, 1e-3)))      # budget in CPU-seconds
+        n = max(1, (n // nthreads) * nthreads) if n >= nthreads else n
+    else:
+        n = n_chains
+    n = min(n, Bx * H)
+    nseq = math.ceil(n / H)
+    sub = {k: x[k][:nseq].cpu() for k in ("q", "k", "v", "g", "beta")}
+    hs = x["h0"][:nseq].cpu() if x["h0"] is not None else None
+    t = time.perf_counter()
+    oracle.recurrent(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], x["scale"], h0=hs,
+                     chains=list(range(n)), nthreads=nthreads)
+    wall = time.perf_counter() - t
+    tokens = n * w.T / H        # token positions of all Hv heads
+    return {"value": tokens / wall, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{n} (sequence, head) chains of {w.T} tokens of the {w.B}x{w.T} H={H} workload, "
+                      f"fp64 recurrence, {nthreads} threads, {wall:.2f} s wall",
+            "wall_s": wall, "chains": n}
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    if rank != 0:
+        return
+    import torch
+    from gated_deltanet_chunked_gdn_gb300 import inputs as I
+    w = I.WORKLOADS[2].with_(Hqk=args.H, Hv=args.H)
+    nthreads = os.cpu_count() or 1
+    # Each step: one chain per host thread, drawn from the same recipe (only
+    # the sequences the sample needs are generated).
+    nseq = math.ceil(nthreads / w.Hv)
+    x = I.make_inputs(w.with_(B=nseq), "cpu")
+    for _ in range(args.warmup):
+        cpu_oracle_sample(x, w, nthreads, 0.0, n_chains=nthreads)
+    vals, walls = [], []
+    for _ in range(args.steps):
+        r = cpu_oracle_sample(x, w, nthreads, 0.0, n_chains=nthreads)
+        vals.append(r["value"])
+        walls.append(r["wall_s"])
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * statistics.median(walls),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"batched_16x8192_H{args.H}", "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv,
+                   "K": w.K, "V": w.V, "C": w.C, "sample": r["sample"]},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    del torch
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--H", type=int, default=32, choices=[16, 32, 48, 64])
+    ap.add_argument("--path", default="auto", choices=["auto", "staged", "fused"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    from gated_deltanet_chunked_gdn_gb300 import binding
+    from gated_deltanet_chunked_gdn_gb300 import inputs as I
+
+    binding.load()
+    w = I.WORKLOADS[2].with_(Hqk=args.H, Hv=args.H, seed=2 + rank)
+    x = I.make_inputs(w, dev)
+    p = binding.problem_of(x["q"], x["v"], w.C)
+    path = args.path if args.path != "auto" else binding.gdn_resolve_path(p)
+    o = torch.empty_like(x["v"])
+    ht = torch.empty((p.N, p.Hv, p.K, p.V), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.gdn_chunk_fwd_workspace_size(p, path), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q=x["q"], k=x["k"], v=x["v"], g=x["g"], beta=x["beta"], h0=x["h0"]):
+        binding.gdn_chunk_fwd(q, k, v, g, beta, x["scale"], h0=h0, C=w.C, path=path, o=o, ht=ht, workspace=ws,
+                              stream=stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    st = binding.gdn_get_device_status(p, path, ws)
+    if st != binding.DEV_OK:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    sampler = ClockSampler(gpu_uuid(local))
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    tokens_step = w.B * w.T
+    value = world * tokens_step * args.steps / (ms / 1000.0)
+
+    # End to end through the public API: inputs from pinned host memory, o and
+    # ht read back, every step.
+    host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    host["h0"] = x["h0"].cpu().pin_memory()
+    dev_in = {k: torch.empty_like(x[k]) for k in ("q", "k", "v", "g", "beta", "h0")}
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    ht_host = torch.empty(ht.shape, dtype=ht.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * o_host.element_size() + ht_host.numel() * ht_host.element_size()
+
+    def e2e_step():
+        for k_ in dev_in:
+            dev_in[k_].copy_(host[k_], non_blocking=True)
+        step(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["h0"])
+        o_host.copy_(o, non_blocking=True)
+        ht_host.copy_(ht, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e_value = world * tokens_step * args.e2e_steps / e2e_s
+
+    pk = peaks()
+    nbytes, flops = algorithmic(w.B, w.T, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=True)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    sec = ms_step / 1000.0
+    if bound == "hbm":
+        achieved, peak, unit = nbytes / sec / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = flops / sec / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    launches = {"staged": 7, "fused": 2}[path]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"batched_16x8192_H{args.H}", "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv,
+                   "K": w.K, "V": w.V, "C": w.C, "path": path, "parallelism": f"dp{world} (independent batches)",
+                   "l2": "inputs larger than L2 (4.4 GB compulsory traffic per step)"},
+        "tflops_alg": flops / sec / 1e12,
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "traffic": None, "peak_source": pk["source"],
+                     "kernel": "gdn_chunk_fwd call (all launches of one step)",
+                     "alg_bytes": nbytes, "alg_flops": flops,
+                     "t_hbm_ms": 1e3 * t_hbm, "t_tensor_ms": 1e3 * t_tc},
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": args.e2e_steps},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = {k_: v_ for k_, v_ in cpu_oracle_sample(x, w, os.cpu_count() or 1,
+                                                                       args.cpu_seconds).items()
+                                if k_ in ("value", "unit", "cores", "kind", "sample")}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

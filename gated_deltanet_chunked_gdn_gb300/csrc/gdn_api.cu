@@ -1,0 +1,156 @@
+// gdn_api.cu -- the C ABI of libgdn.so (declared in include/gdn.h): host-side
+// validation, workspace sizing, path selection and the device status word.
+#include <string.h>
+
+#include "gdn_internal.h"
+
+using namespace gdn;
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool dim_ok(int d) { return d == 64 || d == 128 || d == 256; }
+
+// Shape checks that need no pointer.  Also normalises N for fixed length.
+bool problem_ok(const gdn_problem* pp, gdn_problem* out) {
+  if (!pp) return false;
+  gdn_problem p = *pp;
+  if (p.dt != GDN_F32 && p.dt != GDN_BF16) return false;
+  if (p.Hqk <= 0 || p.Hv <= 0 || p.Hv % p.Hqk != 0 || p.Hv > 1024) return false;
+  if (!dim_ok(p.K) || !dim_ok(p.V)) return false;
+  if (p.C != 64 && p.C != 128) return false;
+  if (p.varlen) {
+    if (p.B != 1 || p.N <= 0 || p.T < 0) return false;
+  } else {
+    if (p.B <= 0 || p.T <= 0) return false;
+    p.N = p.B;
+  }
+  // Token indices are int32 inside the kernels; element offsets are int64.
+  if ((int64_t)p.B * p.T >= ((int64_t)1 << 31)) return false;
+  if ((int64_t)p.N * p.Hv >= ((int64_t)1 << 31)) return false;
+  *out = p;
+  return true;
+}
+
+gdn_path resolve(const gdn_problem& p, gdn_path path) {
+  if (path == GDN_PATH_AUTO) return fused_supported(p) ? GDN_PATH_FUSED : GDN_PATH_STAGED;
+  return path;
+}
+
+size_t workspace_for(const gdn_problem& p, gdn_path path) {
+  if (path == GDN_PATH_FUSED) return fused_workspace_bytes(p);
+  gdn_staged_layout_t L;
+  staged_layout(p, &L);
+  return L.total;
+}
+
+size_t status_offset(const gdn_problem& p, gdn_path path) {
+  if (path == GDN_PATH_FUSED) return fused_status_offset(p);
+  gdn_staged_layout_t L;
+  staged_layout(p, &L);
+  return L.status;
+}
+
+gdn_status check_call(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, const float* h0, const int32_t* cu, const void* o, const float* ht,
+                      const void* ws, size_t ws_bytes, size_t need) {
+  const bool any_tokens = (int64_t)p.B * p.T > 0;
+  if (any_tokens && (!q || !k || !v || !g || !beta || !o)) return GDN_ERR_INVALID_ARG;
+  if (p.varlen && !cu) return GDN_ERR_INVALID_ARG;
+  if (!p.varlen && cu) return GDN_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < need || !aligned(ws, kAlign)) return GDN_ERR_INVALID_ARG;
+  const void* a16[] = {q, k, v, o};
+  for (const void* x : a16)
+    if (x && !aligned(x, 16)) return GDN_ERR_INVALID_ARG;
+  const void* a4[] = {g, beta, h0, ht, cu};
+  for (const void* x : a4)
+    if (x && !aligned(x, 4)) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_chunk_fwd_workspace_size(const gdn_problem* pp, gdn_path path) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p)) return 0;
+  path = resolve(p, path);
+  if (path == GDN_PATH_FUSED && !fused_supported(p)) return 0;
+  return workspace_for(p, path);
+}
+
+gdn_path gdn_resolve_path(const gdn_problem* pp) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p)) return GDN_PATH_STAGED;
+  return resolve(p, GDN_PATH_AUTO);
+}
+
+gdn_status gdn_chunk_fwd(const gdn_problem* pp, gdn_path path, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, float scale, const float* h0,
+                         const int32_t* cu_seqlens, void* o, float* ht, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
+  if (path != GDN_PATH_AUTO && path != GDN_PATH_STAGED && path != GDN_PATH_FUSED) return GDN_ERR_INVALID_ARG;
+  path = resolve(p, path);
+  if (path == GDN_PATH_FUSED && !fused_supported(p)) return GDN_ERR_UNSUPPORTED;
+  gdn_status st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, workspace, workspace_bytes,
+                             workspace_for(p, path));
+  if (st != GDN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (path == GDN_PATH_FUSED) return run_fused(p, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, s);
+  return run_staged(p, 6, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, s);
+}
+
+gdn_status gdn_chunk_fwd_staged(const gdn_problem* pp, int stop_after, const void* q, const void* k, const void* v,
+                                const float* g, const float* beta, float scale, const float* h0,
+                                const int32_t* cu_seqlens, void* o, float* ht, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
+  if (stop_after < 0 || stop_after > 6) return GDN_ERR_INVALID_ARG;
+  gdn_status st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, workspace, workspace_bytes,
+                             workspace_for(p, GDN_PATH_STAGED));
+  if (st != GDN_OK) return st;
+  return run_staged(p, stop_after, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace,
+                    static_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_staged_layout(const gdn_problem* pp, gdn_staged_layout_t* out) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p) || !out) return GDN_ERR_INVALID_ARG;
+  return staged_layout(p, out);
+}
+
+gdn_status gdn_get_device_status(const gdn_problem* pp, gdn_path path, void* workspace, void* stream,
+                                 int* dev_status) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p) || !workspace || !dev_status) return GDN_ERR_INVALID_ARG;
+  if (path != GDN_PATH_AUTO && path != GDN_PATH_STAGED && path != GDN_PATH_FUSED) return GDN_ERR_INVALID_ARG;
+  path = resolve(p, path);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t* word = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + status_offset(p, path));
+  int32_t host = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemcpy(&host, word, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemset(word, 0, sizeof(int32_t)) != cudaSuccess) return GDN_ERR_CUDA;
+  *dev_status = host;
+  return GDN_OK;
+}
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_INVALID_ARG: return "invalid argument";
+    case GDN_ERR_UNSUPPORTED: return "unsupported problem for this path";
+    case GDN_ERR_CUDA: return "CUDA runtime error";
+    case GDN_ERR_DEVICE: return "device reported an error";
+  }
+  return "unknown status";
+}
+
+const char* gdn_version(void) { return "gdn 0.1 sm_103a"; }
+
+}  // extern "C"

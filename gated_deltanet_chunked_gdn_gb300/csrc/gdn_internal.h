@@ -1,0 +1,70 @@
+// gdn_internal.h -- shared host/device helpers of libgdn (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr size_t kAlign = 256;
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Chunk tables written by the prepare kernel (layout documented in gdn.h,
+// gdn_staged_layout_t::tables).  nc < 0 marks malformed cu_seqlens.
+struct Tables {
+  int32_t* seq_chunk0;  // [N + 1]
+  int32_t* chunk_seq;   // [nc_max]
+  int32_t* chunk_tok0;  // [nc_max]
+  int32_t* chunk_len;   // [nc_max]
+  int32_t* nc;          // [1]
+};
+
+inline Tables tables_at(void* base, int N, int nc_max) {
+  int32_t* p = reinterpret_cast<int32_t*>(base);
+  Tables t;
+  t.seq_chunk0 = p;
+  t.chunk_seq = p + (N + 1);
+  t.chunk_tok0 = t.chunk_seq + nc_max;
+  t.chunk_len = t.chunk_tok0 + nc_max;
+  t.nc = t.chunk_len + nc_max;
+  return t;
+}
+
+inline size_t tables_bytes(int N, int nc_max) { return sizeof(int32_t) * ((size_t)N + 1 + 3 * (size_t)nc_max + 1); }
+
+inline int nc_max_of(const gdn_problem& p, int C) {
+  return p.varlen ? (int)(ceil_div(p.T, C) + p.N) : (int)(p.B * ceil_div(p.T, C));
+}
+
+// Launch the prepare kernel: chunk tables for chunk length C, validation of
+// cu_seqlens (status word + nc = -1 on error).
+cudaError_t launch_prepare(const gdn_problem& p, int C, const int32_t* cu_seqlens, Tables t, int nc_max,
+                           int32_t* status, cudaStream_t s);
+
+// Staged path (gdn_staged.cu).
+gdn_status staged_layout(const gdn_problem& p, gdn_staged_layout_t* out);
+gdn_status run_staged(const gdn_problem& p, int stop_after, const void* q, const void* k, const void* v,
+                      const float* g, const float* beta, float scale, const float* h0, const int32_t* cu,
+                      void* o, float* ht, void* ws, cudaStream_t s);
+
+// Fused path (gdn_fused.cu).
+bool fused_supported(const gdn_problem& p);
+size_t fused_workspace_bytes(const gdn_problem& p);
+size_t fused_status_offset(const gdn_problem& p);
+gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                     void* ws, cudaStream_t s);
+
+}  // namespace gdn

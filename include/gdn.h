@@ -1,0 +1,165 @@
+/*
+ * gdn.h -- C ABI of libgdn.so: the Gated DeltaNet chunked forward pass on one
+ * GB300 (sm_103a).
+ *
+ * Operator (MegaGDN-PTO walkthrough, section 1.1, the seven-stage chunk
+ * pipeline; TileLang x xLLM page, Step 1, chunk_gated_delta_rule_fwd_h):
+ *
+ *   S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T     (S is [K][V])
+ *   o_t = scale * S_t^T q_t
+ *
+ * evaluated chunk-wise (cumsum -> scaled_dot_kkt -> solve_tril -> wy_fast ->
+ * chunk_h -> chunk_o).  Inputs with GQA: value head h reads q/k head
+ * h / (Hv / Hqk) (MegaGDN-PTO walkthrough, section 5.2).  Packed variable-length
+ * batches use cu_seqlens (section 5.3).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays,
+ *    owned by the caller; the library allocates nothing.
+ *  - q, k, v and o must be 16-byte aligned (they are read/written by TMA).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Host-side argument checks run before any launch; a
+ *    failed check returns an error and launches nothing.  Errors found on the
+ *    device (malformed cu_seqlens, a bounded wait that timed out) are written
+ *    to a status word inside the workspace; read it with
+ *    gdn_get_device_status().
+ *  - No exception or C++ type crosses this boundary.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or workspace too small */
+  GDN_ERR_UNSUPPORTED = 2,   /* valid request that this build does not implement */
+  GDN_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute, ...) */
+  GDN_ERR_DEVICE = 4         /* the device reported an error through the status word */
+} gdn_status;
+
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+/* Device status word values (read by gdn_get_device_status). */
+#define GDN_DEV_OK 0
+#define GDN_DEV_BAD_CU_SEQLENS 1   /* cu[0] != 0, decreasing, or cu[N] != T */
+#define GDN_DEV_WAIT_TIMEOUT 2     /* a bounded spin-wait inside a kernel gave up */
+
+/* Execution path. */
+typedef enum {
+  GDN_PATH_AUTO = 0,    /* fused when supported, else staged */
+  GDN_PATH_STAGED = 1,  /* one kernel per stage, intermediates in the workspace */
+  GDN_PATH_FUSED = 2    /* single persistent tcgen05 kernel (bf16, K = V = 128) */
+} gdn_path;
+
+/*
+ * Problem description.
+ *   B, T      : fixed-length batch [B, T] (cu_seqlens == NULL, N = B), or the
+ *               packed batch [1, T] of N sequences (cu_seqlens != NULL, B = 1,
+ *               T = total tokens, may be 0).
+ *   Hqk, Hv   : q/k heads and value heads; Hv % Hqk == 0.
+ *   K, V      : key and value head dims, each in {64, 128, 256}.
+ *   C         : chunk length, 64 or 128.
+ *   dt        : dtype of q, k, v and o (fp32 or bf16); g, beta, h0, ht are fp32.
+ */
+typedef struct {
+  int B, T, N, Hqk, Hv, K, V, C;
+  gdn_dtype dt;
+  int varlen;   /* 1 when cu_seqlens is given */
+} gdn_problem;
+
+/*
+ * Bytes of workspace that gdn_chunk_fwd needs for `path` (AUTO resolves as in
+ * gdn_chunk_fwd).  Returns 0 for an invalid problem.  The varlen bound assumes
+ * at most ceil(T / C) + N chunks, so cu_seqlens need not be read on the host.
+ */
+size_t gdn_chunk_fwd_workspace_size(const gdn_problem* p, gdn_path path);
+
+/*
+ * The chunked forward pass.
+ *   q, k    : [B, T, Hqk, K]  dtype p->dt
+ *   v       : [B, T, Hv, V]   dtype p->dt
+ *   g       : [B, T, Hv] fp32, log-decay (used as given; no activation)
+ *   beta    : [B, T, Hv] fp32
+ *   scale   : multiplies o only (never the state); callers usually pass K^-0.5
+ *   h0      : [N, Hv, K, V] fp32 initial state, or NULL for zeros
+ *   cu_seqlens : [N + 1] int32 device array of token offsets, or NULL
+ *   o       : out [B, T, Hv, V] dtype p->dt (round-to-nearest-even for bf16)
+ *   ht      : out [N, Hv, K, V] fp32 final state, or NULL to skip it
+ *   workspace / workspace_bytes : device scratch of at least
+ *             gdn_chunk_fwd_workspace_size(p, path) bytes, 256-byte aligned
+ * Returns GDN_OK once everything is enqueued on `stream`.
+ */
+gdn_status gdn_chunk_fwd(const gdn_problem* p, gdn_path path,
+                         const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, float scale,
+                         const float* h0, const int32_t* cu_seqlens,
+                         void* o, float* ht,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Staged path with a stop point (the pages' staged mode and MEGA_STOP_AFTER_*
+ * hooks, MegaGDN-PTO walkthrough, section 7.4).  Runs stages 0..stop_after:
+ *   0 prepare (chunk tables), 1 cumsum, 2 scaled_dot_kkt, 3 solve_tril,
+ *   4 wy_fast, 5 chunk_h, 6 chunk_o (6 = full forward; o/ht written only by
+ *   stages 6 and 5 respectively).
+ * Intermediates stay in the workspace at the offsets of gdn_staged_layout.
+ */
+gdn_status gdn_chunk_fwd_staged(const gdn_problem* p, int stop_after,
+                                 const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta, float scale,
+                                 const float* h0, const int32_t* cu_seqlens,
+                                 void* o, float* ht,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Byte offsets of the staged path's intermediates inside its workspace.
+ * nc_max = B * ceil(T / C) (fixed length) or ceil(T / C) + N (varlen).
+ *   tables : int32 seq_chunk0[N + 1] | chunk_seq[nc_max] | chunk_tok0[nc_max] |
+ *            chunk_len[nc_max] | nc[1]   (chunk c of the packed token stream
+ *            covers tokens chunk_tok0[c] .. + chunk_len[c] of sequence chunk_seq[c])
+ *   status : int32 device status word
+ *   gamma  : f32 [nc_max][Hv][C]      in-chunk cumsum of g
+ *   A      : f32 [nc_max][Hv][C][C]   strictly lower, beta_i exp(g_i - g_j) k_i.k_j
+ *   Tinv   : f32 [nc_max][Hv][C][C]   (I + A)^{-1}
+ *   W, U   : f32 [nc_max][Hv][C][K] and [nc_max][Hv][C][V]
+ *   S0     : f32 [nc_max][Hv][K][V]   state at each chunk's start
+ *   Vn     : f32 [nc_max][Hv][C][V]   v_new = U - W S0
+ * Rows past a chunk's length hold zeros, except Tinv, which holds the
+ * identity there (the inverse of I + A with A zero-padded).
+ */
+typedef struct {
+  size_t tables, status, gamma, A, Tinv, W, U, S0, Vn, total;
+  int nc_max;
+} gdn_staged_layout_t;
+
+gdn_status gdn_staged_layout(const gdn_problem* p, gdn_staged_layout_t* out);
+
+/*
+ * Waits for `stream`, then reads the device status word that the last call
+ * using `workspace` left (GDN_DEV_*) into *dev_status and clears it.
+ * `path` must be the path that call ran with (it locates the status word).
+ * Returns GDN_ERR_CUDA if the synchronisation or the copy fails.
+ */
+gdn_status gdn_get_device_status(const gdn_problem* p, gdn_path path, void* workspace,
+                                 void* stream, int* dev_status);
+
+/* Path that GDN_PATH_AUTO selects for this problem (STAGED or FUSED). */
+gdn_path gdn_resolve_path(const gdn_problem* p);
+
+/* Human-readable name of a status code (static string). */
+const char* gdn_status_string(gdn_status s);
+
+/* Library version string, e.g. "gdn 0.1 sm_103a". */
+const char* gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,173 @@
+"""GPU parity: the CUDA library against the fp64 oracle on the same seeded
+inputs, through the C ABI (the Python binding only marshals arguments).
+
+Bar (spec tolerances): relative Frobenius error on both o and ht of at
+most 1e-4 for fp32 inputs and 5e-3 for bf16 inputs (fp32 state); chunk
+tables bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from conftest import rel_fro
+from gated_deltanet_chunked_gdn_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 5e-3}
+
+
+@pytest.fixture(scope="module")
+def gdn():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_chunked_gdn_gb300 import binding
+    binding.load()
+    return binding
+
+
+# Reduced versions of the five workloads: several chunks, a ragged tail, GQA,
+# empty and sub-chunk sequences, both head dims, both dtypes.
+SMALL = {
+    "tiny_fp32": (I.WORKLOADS[0], None),
+    "gqa_prefill": (I.WORKLOADS[1].with_(T=300, Hqk=2, Hv=4), None),
+    "batched_C128": (I.WORKLOADS[2].with_(B=2, T=333, Hqk=2, Hv=2), None),
+    "varlen": (I.WORKLOADS[3].with_(Hqk=2, Hv=4), [5, 64, 200, 1, 0, 129, 63]),
+    "long_d256": (I.WORKLOADS[4].with_(B=1, T=200, Hqk=1, Hv=4), None),
+    "fp32_C128_gqa": (I.WORKLOADS[0].with_(B=2, T=150, Hqk=1, Hv=3, K=128, V=64, C=128), None),
+}
+
+
+def run_case(gdn, w, lens, path, device="cuda"):
+    x = I.make_inputs(w, "cpu", lengths=lens)
+    d = {k_: (v_.to(device) if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
+    o, ht = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
+                              cu_seqlens=d["cu_seqlens"], C=w.C, path=path)
+    torch.cuda.synchronize()
+    return x, o.float().cpu().numpy(), ht.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("path", ["staged", "auto"])
+def test_parity_small(gdn, oracle_mod, name, path):
+    w, lens = SMALL[name]
+    x, o, ht = run_case(gdn, w, lens, path)
+    o_ref, ht_ref = oracle_mod.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                                         cu_seqlens=x["cu_seqlens"])
+    tol = TOL[w.dtype]
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(ht))
+    assert rel_fro(o, o_ref) <= tol, rel_fro(o, o_ref)
+    assert rel_fro(ht, ht_ref) <= tol, rel_fro(ht, ht_ref)
+
+
+def test_h0_none_and_ht_skipped(gdn, oracle_mod):
+    w = I.WORKLOADS[1].with_(T=130, Hqk=1, Hv=2)
+    x = I.make_inputs(w, "cpu")
+    d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
+    o, ht = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], C=w.C,
+                              output_final_state=False)
+    assert ht is None
+    o_ref, _ = oracle_mod.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"])
+    assert rel_fro(o.float().cpu().numpy(), o_ref) <= TOL["bf16"]
+
+
+def test_state_passing_on_gpu(gdn, oracle_mod):
+    """run(T1) then run(T2, h0=ht) on the GPU equals the oracle on T1+T2."""
+    w = I.WORKLOADS[2].with_(B=1, T=400, Hqk=2, Hv=2, C=128, dtype="f32")
+    x = I.make_inputs(w, "cpu")
+    d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
+    T1 = 150
+    sl = lambda t, a, b_: t[:, a:b_].contiguous()
+    o1, ht1 = gdn.gdn_chunk_fwd(*(sl(d[n], 0, T1) for n in ("q", "k", "v", "g", "beta")), d["scale"], h0=d["h0"],
+                                C=w.C)
+    o2, ht2 = gdn.gdn_chunk_fwd(*(sl(d[n], T1, 400) for n in ("q", "k", "v", "g", "beta")), d["scale"], h0=ht1,
+                                C=w.C)
+    o_ref, ht_ref = oracle_mod.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"])
+    o = torch.cat([o1, o2], dim=1).cpu().numpy()
+    assert rel_fro(o, o_ref) <= TOL["f32"]
+    assert rel_fro(ht2.cpu().numpy(), ht_ref) <= TOL["f32"]
+
+
+def test_chunk_tables_bit_exact(gdn):
+    """The prepare stage's chunk tables equal a host computation exactly."""
+    lens = [5, 0, 64, 65, 1, 128, 300, 0, 63]
+    C = 64
+    w = I.WORKLOADS[3].with_(Hqk=1, Hv=1, K=64, V=64, dtype="f32")
+    x = I.make_inputs(w, "cuda", lengths=lens)
+    _, _, ws, layout = gdn.gdn_chunk_fwd_staged(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"],
+                                                cu_seqlens=x["cu_seqlens"], C=C, stop_after="prepare")
+    torch.cuda.synchronize()
+    p = gdn.problem_of(x["q"], x["v"], C, x["cu_seqlens"])
+    t = {k_: v_.cpu().numpy() for k_, v_ in gdn.staged_view(ws, layout, p, "tables").items()}
+    seq_chunk0, seqs, tok0, ln = [0], [], [], []
+    off = 0
+    for n, L in enumerate(lens):
+        nch = -(-L // C)
+        for j in range(nch):
+            seqs.append(n)
+            tok0.append(off + j * C)
+            ln.append(min(C, L - j * C))
+        seq_chunk0.append(seq_chunk0[-1] + nch)
+        off += L
+    nc = seq_chunk0[-1]
+    assert int(t["nc"][0]) == nc
+    assert t["seq_chunk0"].tolist() == seq_chunk0
+    assert t["chunk_seq"][:nc].tolist() == seqs
+    assert t["chunk_tok0"][:nc].tolist() == tok0
+    assert t["chunk_len"][:nc].tolist() == ln
+
+
+def test_malformed_cu_seqlens_sets_device_status(gdn):
+    """Decreasing offsets are caught by the prepare kernel: the device status
+    word reports it and no stage runs (the output stays untouched)."""
+    w = I.WORKLOADS[3].with_(Hqk=1, Hv=2, K=64, V=64, dtype="f32")
+    x = I.make_inputs(w, "cuda", lengths=[10, 20, 30])
+    bad = torch.tensor([0, 25, 20, 60], dtype=torch.int32, device="cuda")
+    o = torch.full_like(x["v"], 7.0)
+    p = gdn.problem_of(x["q"], x["v"], 64, bad)
+    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, "staged"), dtype=torch.uint8, device="cuda")
+    gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], cu_seqlens=bad, C=64, path="staged",
+                      o=o, workspace=ws)
+    assert gdn.gdn_get_device_status(p, "staged", ws) == gdn.DEV_BAD_CU_SEQLENS
+    assert torch.all(o == 7.0)
+    # a good call on the same workspace clears it
+    gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], cu_seqlens=x["cu_seqlens"], C=64,
+                      path="staged", o=o, workspace=ws)
+    assert gdn.gdn_get_device_status(p, "staged", ws) == gdn.DEV_OK
+
+
+STAGE_KEYS = [("gamma", "gamma", 1), ("A", "A", 2), ("Tinv", "T", 3), ("W", "W", 4), ("U", "U", 4),
+              ("S0", "S0", 5), ("Vn", "Vn", 5)]
+
+
+@pytest.mark.parametrize("C", [64, 128])
+def test_stage_intermediates_match_oracle(gdn, oracle_mod, C):
+    """Each stage of the staged path, stopped right after it, against the
+    chunked oracle's intermediates for every chain (fp32 inputs)."""
+    lens = [C + 37, 2, 2 * C]
+    w = I.WORKLOADS[3].with_(Hqk=1, Hv=2, K=64, V=64, C=C, dtype="f32")
+    x = I.make_inputs(w, "cpu", lengths=lens)
+    d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
+    p = gdn.problem_of(d["q"], d["v"], C, d["cu_seqlens"])
+    for key, okey, stop in STAGE_KEYS:
+        _, _, ws, layout = gdn.gdn_chunk_fwd_staged(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"],
+                                                    h0=d["h0"], cu_seqlens=d["cu_seqlens"], C=C, stop_after=stop)
+        torch.cuda.synchronize()
+        got = gdn.staged_view(ws, layout, p, key).cpu().numpy()
+        c0 = 0
+        for n, L in enumerate(lens):
+            nt = -(-L // C)
+            for h in range(w.Hv):
+                ref = oracle_mod.chunked_stages(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], C, n, h,
+                                                h0=x["h0"], cu_seqlens=x["cu_seqlens"])[okey]
+                g_ = got[c0:c0 + nt, h].copy()
+                if key == "Tinv":
+                    # past a tail chunk's length (I + A) is the identity, so
+                    # its inverse holds 1 on the diagonal there
+                    tail = L - (nt - 1) * C
+                    diag = np.arange(tail, C)
+                    assert np.all(g_[-1, diag, diag] == 1.0)
+                    g_[-1, diag, diag] = 0.0
+                err = rel_fro(g_, ref) if np.linalg.norm(ref) > 0 else np.abs(g_).max()
+                assert err < 1e-4, (key, n, h, err)
+            c0 += nt
