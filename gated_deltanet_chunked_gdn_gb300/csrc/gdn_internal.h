@@ -1,6 +1,7 @@
 // gdn_internal.h -- shared host/device helpers of libgdn (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -52,6 +53,12 @@ inline int nc_max_of(const gdn_problem& p, int C) {
 // cu_seqlens (status word + nc = -1 on error).
 cudaError_t launch_prepare(const gdn_problem& p, int C, const int32_t* cu_seqlens, Tables t, int nc_max,
                            int32_t* status, cudaStream_t s);
+
+// TMA tensor map over a bf16 tensor, 128-byte swizzle, zero fill out of
+// bounds (gdn_tmap.cu).  dims / box innermost first; strides_bytes has
+// rank - 1 entries (dims 1..rank-1).
+bool make_tmap_bf16(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                    const uint64_t* strides_bytes, const uint32_t* box);
 
 // Staged path (gdn_staged.cu).
 gdn_status staged_layout(const gdn_problem& p, gdn_staged_layout_t* out);

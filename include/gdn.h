@@ -149,6 +149,20 @@ gdn_status gdn_staged_layout(const gdn_problem* p, gdn_staged_layout_t* out);
 gdn_status gdn_get_device_status(const gdn_problem* p, gdn_path path, void* workspace,
                                  void* stream, int* dev_status);
 
+/*
+ * Self-test of the tensor-core operand layouts used by the fused kernel (no
+ * counterpart on the pages; a test hook).  Computes D = A B (or -A B) with one
+ * CTA through tcgen05.mma over 128-byte-swizzled shared-memory tiles.
+ *   A : bf16 [128][Kd] row-major, B : bf16 [Kd][N] row-major, D : fp32 [128][N]
+ *   variant bits: 1 = A staged MN-major (else K-major), 2 = B staged MN-major,
+ *                 4 = N 128 (else 64), 8 = Kd 128 (else 64), 16 = negate A,
+ *                 32 = stage A with a TMA tiled load (needs bit 1 clear,
+ *                 A 16-byte aligned)
+ *   workspace : >= 4 bytes of device memory for the status word
+ */
+gdn_status gdn_selftest_umma(int variant, const void* A, const void* B, float* D, void* workspace,
+                             void* stream);
+
 /* Path that GDN_PATH_AUTO selects for this problem (STAGED or FUSED). */
 gdn_path gdn_resolve_path(const gdn_problem* p);
 
