@@ -147,6 +147,7 @@ const char* gdn_status_string(gdn_status s) {
     case GDN_ERR_UNSUPPORTED: return "unsupported problem for this path";
     case GDN_ERR_CUDA: return "CUDA runtime error";
     case GDN_ERR_DEVICE: return "device reported an error";
+    case GDN_ERR_SCRATCH_LIMIT: return "problem needs more than the built-in 32 MiB static scratch";
   }
   return "unknown status";
 }
@@ -154,3 +155,63 @@ const char* gdn_status_string(gdn_status s) {
 const char* gdn_version(void) { return "gdn 0.1 sm_103a"; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward pass without any caller-provided or library-allocated device memory
+// beyond the caller's inputs and outputs.
+//
+// Some callers cannot allocate device memory in the call path: an op embedded
+// in a host framework that owns every device buffer and hands the op only its
+// inputs and outputs (no workspace), or a caller that cannot afford the
+// implicit device-wide synchronisation of cudaMalloc/cudaFree between its
+// launches.  For them the staged forward pass runs with its intermediates in
+// one file-scope device array, kStaticScratchBytes (32 MiB) per GPU, which
+// every GPU that loads this library holds until the process exits.
+#include <mutex>
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device.  The host-side
+// name of the array is only a stand-in, so the address is fetched once per
+// device with cudaGetSymbolAddress (with that device current) and cached.
+gdn_status static_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* pp, const void* q, const void* k, const void* v,
+                                            const float* g, const float* beta, float scale, const float* h0,
+                                            const int32_t* cu_seqlens, void* o, float* ht, void* stream) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
+  const size_t need = workspace_for(p, GDN_PATH_STAGED);
+  if (need > kStaticScratchBytes) return GDN_ERR_SCRATCH_LIMIT;
+  void* scratch = nullptr;
+  gdn_status st = static_scratch(&scratch);
+  if (st != GDN_OK) return st;
+  st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, scratch, kStaticScratchBytes, need);
+  if (st != GDN_OK) return st;
+  // run_staged clears the status word it uses; every other intermediate is
+  // rewritten before it is read, so stale contents of earlier calls are harmless.
+  return run_staged(p, 6, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, scratch,
+                    static_cast<cudaStream_t>(stream));
+}

@@ -40,7 +40,8 @@ typedef enum {
   GDN_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or workspace too small */
   GDN_ERR_UNSUPPORTED = 2,   /* valid request that this build does not implement */
   GDN_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch, attribute, ...) */
-  GDN_ERR_DEVICE = 4         /* the device reported an error through the status word */
+  GDN_ERR_DEVICE = 4,        /* the device reported an error through the status word */
+  GDN_ERR_SCRATCH_LIMIT = 5  /* gdn_chunk_fwd_noalloc: problem larger than its static scratch */
 } gdn_status;
 
 typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
@@ -162,6 +163,33 @@ gdn_status gdn_get_device_status(const gdn_problem* p, gdn_path path, void* work
  */
 gdn_status gdn_selftest_umma(int variant, const void* A, const void* B, float* D, void* workspace,
                              void* stream);
+
+/*
+ * Forward pass for callers that cannot allocate device memory (no counterpart
+ * on the pages).  Some callers cannot call cudaMalloc in their call path: an
+ * op inside a host framework that owns every device buffer and passes the op
+ * only its inputs and outputs, or a caller that cannot accept the implicit
+ * device-wide synchronisation of cudaMalloc/cudaFree.  This entry point
+ * allocates nothing and takes no workspace: it runs the staged path with its
+ * intermediates in a file-scope device array of 32 MiB that every GPU which
+ * loads libgdn.so holds until the process exits.
+ *   Arguments as gdn_chunk_fwd (the caller still passes inputs and outputs).
+ *   Returns GDN_ERR_SCRATCH_LIMIT, launching nothing, when the problem's
+ *   staged workspace (gdn_chunk_fwd_workspace_size with GDN_PATH_STAGED)
+ *   exceeds 32 MiB.
+ *   The first call on a device looks up the array's device address with
+ *   cudaGetSymbolAddress (with that device current); make that first call
+ *   before any stream capture.
+ *   All calls share the one array: calls whose executions overlap on the GPU
+ *   (other streams, other host threads) race on it and must be serialised by
+ *   the caller.  The device status word lives in the array too and is not
+ *   exposed.
+ */
+gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* p,
+                                 const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta, float scale,
+                                 const float* h0, const int32_t* cu_seqlens,
+                                 void* o, float* ht, void* stream);
 
 /* Path that GDN_PATH_AUTO selects for this problem (STAGED or FUSED). */
 gdn_path gdn_resolve_path(const gdn_problem* p);
