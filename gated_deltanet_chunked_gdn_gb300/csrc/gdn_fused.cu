@@ -1,14 +1,606 @@
-// gdn_fused.cu -- single-launch fused path (tcgen05 / TMEM / TMA on sm_103a).
-#include "gdn_internal.h"
+// gdn_fused.cu -- the fused path: the whole chunk pipeline (cumsum,
+// scaled_dot_kkt, solve_tril, wy_fast, chunk_h, chunk_o; MegaGDN-PTO
+// walkthrough, sections 1.1 and 4.5) in ONE sm_103a launch.
+//
+// One CTA per (sequence, value head) chain walks the chain's chunks in order;
+// the fp32 state never leaves the SM (TMEM) between chunks, and no
+// intermediate goes through HBM.  Two CTAs share an SM (their shared memory
+// and TMEM halves), so one chain's SIMT phases overlap the other's tensor
+// phases.  Chunks are 64 tokens; a C = 128 request is processed as two
+// 64-token chunks (the chunked form is exact for any chunk length).
+//
+// Layout: everything is transposed so that every tcgen05.mma has M = 128 on
+// the key/value dimension (TMEM lane = value column e or key column d):
+//
+//   M1  [K;Q] K^T          D[0:64]   = K K^T, D[64:128] = Q K^T   (M128 N64 K128)
+//   S1  A = strict-lower(beta_i e^{g_i - g_j} K K^T)  -> smem fp32
+//       P = lower(e^{g_i - g_j} Q K^T)                 -> smem bf16
+//   S2  T = (I + A)^{-1}: 16x16 diagonal blocks by forward substitution, then
+//       merges T21 = -T22 A21 T11 (MegaGDN-PTO walkthrough, section 4.4)
+//   M2  W^T = K^T (T diag(beta e^g))^T,  U^T = V^T (T diag(beta))^T (section 4.3)
+//   S4  S^T (fp32, TMEM) -> bf16 operand; S^T *= e^{g_last}
+//   M3  V'^T = U^T - S^T W^T;  OQ^T = S^T Q^T      (chunk_h first half)
+//   S5  V'^T -> bf16, V''^T = V'^T diag(e^{g_last - g}) -> bf16
+//   M4  OP^T = V'^T P^T;  S^T += V''^T K          (chunk_h second half)
+//   S6  o_i = scale (e^{g_i} OQ_i + OP_i)         (chunk_o)
+//
+// Rows past a sequence's end (tail chunk) get beta = 0 and g = 0, which zeroes
+// their rows of A, W, U and V' exactly; they are never stored.
+#include <string.h>
+
+#include "gdn_sm100.cuh"
 
 namespace gdn {
+namespace {
 
-bool fused_supported(const gdn_problem&) { return false; }
-size_t fused_workspace_bytes(const gdn_problem&) { return 0; }
+using namespace sm100;
+
+constexpr int kChunk = 64;      // tokens per chunk
+constexpr int kD = 128;         // K = V
+constexpr int kThreads = 256;
+constexpr int kTmemCols = 256;
+
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_KQ = 0;         // [k rows 0..63 ; q rows 64..127] x 128 d, 2 atom columns of 16 KB
+constexpr uint32_t OFF_V = 32768;      // v rows 0..63 x 128 e, 2 atom columns of 8 KB
+constexpr uint32_t OFF_Y = 49152;      // T diag(beta) | T diag(beta e^g)  (8 KB each), later W^T (16 KB)
+constexpr uint32_t OFF_TB = OFF_Y;
+constexpr uint32_t OFF_TBE = OFF_Y + 8192;
+constexpr uint32_t OFF_W = OFF_Y;
+constexpr uint32_t OFF_P = 65536;      // P [i][j] bf16, 8 KB
+constexpr uint32_t OFF_X = 73728;      // 32 KB, reused: A/T fp32 + scratch | S^T bf16 | V'^T, V''^T | o staging
+constexpr uint32_t OFF_AS = OFF_X;     // fp32 [64][68]
+constexpr uint32_t OFF_TMP = OFF_X + 64 * 68 * 4;  // fp32 scratch for the solve merges (1024 floats)
+constexpr uint32_t OFF_ST = OFF_X;     // S^T bf16 [e][d], 2 atom columns of 16 KB
+constexpr uint32_t OFF_VP = OFF_X;     // V'^T bf16 [e][j], 16 KB
+constexpr uint32_t OFF_VPP = OFF_X + 16384;
+constexpr uint32_t OFF_OS = OFF_X;     // o staging bf16 [64][128]
+constexpr uint32_t OFF_MISC = 106496;
+constexpr uint32_t OFF_GAM = OFF_MISC;         // float[64] gamma (in-chunk cumsum of g)
+constexpr uint32_t OFF_BET = OFF_MISC + 256;   // float[64] beta (0 past the end)
+constexpr uint32_t OFF_BE = OFF_MISC + 512;    // float[64] beta e^gamma
+constexpr uint32_t OFF_DL = OFF_MISC + 768;    // float[64] e^{gamma_last - gamma}
+constexpr uint32_t OFF_EG = OFF_MISC + 1024;   // float[64] e^gamma
+constexpr uint32_t OFF_BAR = OFF_MISC + 1280;  // 3 mbarriers
+constexpr uint32_t OFF_FLAGS = OFF_MISC + 1312;  // [0] tmem base, [1] abort
+constexpr uint32_t kSmemUsed = OFF_MISC + 1344;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
+constexpr int kAsLd = 68;
+
+static_assert(OFF_TMP + 1024 * 4 <= OFF_X + 32768, "solve scratch overflows region X");
+static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs must fit one SM");
+
+struct FusedParams {
+  const float* g;
+  const float* beta;
+  const float* h0;
+  const int32_t* cu;
+  __nv_bfloat16* o;
+  float* ht;
+  int32_t* status;
+  int N, Tseq, Ttot, Hqk, Hv, varlen;
+  float scale;
+};
+
+// T = (I + A)^{-1} for a 64x64 strictly lower A held in place in As (fp32,
+// leading dimension kAsLd, zeros on and above the diagonal).
+//  1. Diagonal 16x16 blocks by forward substitution: a half-warp per block,
+//     lane l keeps column l of the block's inverse in registers.
+//  2. Merge neighbouring blocks, [[T11, 0], [A21-block, T22]] ->
+//     T21 = -T22 (A21 T11), first for the 16-blocks (two pairs), then for the
+//     32-blocks (one pair).  The upper triangles hold zeros, so the products
+//     run over full square blocks.
+template <int S>
+__device__ __forceinline__ void merge_level(float* As, float* tmp, int tid) {
+  // every thread owns R consecutive columns of one row of the merged pairs
+  constexpr int NP = kChunk / (2 * S);          // pairs at this level
+  constexpr int R = (NP * S * S) / kThreads;    // outputs per thread (2 or 4)
+  constexpr int CPR = S / R;                    // threads per row
+  static_assert(R * kThreads == NP * S * S && (R == 2 || R == 4), "merge tiling");
+  const int p = tid / (S * CPR);
+  const int i = (tid / CPR) % S;
+  const int m0 = (tid % CPR) * R;
+  const int o = 2 * S * p;
+  float acc[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+  // tmp = A21 T11
+#pragma unroll 8
+  for (int j = 0; j < S; ++j) {
+    const float a = As[(o + S + i) * kAsLd + o + j];
+    const float* t = As + (o + j) * kAsLd + o + m0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = fmaf(a, t[r], acc[r]);
+  }
+  float* tp = tmp + p * S * S + i * S + m0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) tp[r] = acc[r];
+  __syncthreads();
+  // T21 = -T22 tmp
+#pragma unroll
+  for (int r = 0; r < R; ++r) acc[r] = 0.f;
+#pragma unroll 8
+  for (int j = 0; j < S; ++j) {
+    const float a = As[(o + S + i) * kAsLd + o + S + j];
+    const float* t = tmp + p * S * S + j * S + m0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) acc[r] = fmaf(a, t[r], acc[r]);
+  }
+  float* dst = As + (o + S + i) * kAsLd + o + m0;
+#pragma unroll
+  for (int r = 0; r < R; ++r) dst[r] = -acc[r];
+  __syncthreads();
+}
+
+__device__ __forceinline__ void solve64(float* As, float* tmp, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < 2) {
+    const int b = 16 * (2 * warp + (lane >> 4));
+    const int l = lane & 15;
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float* arow = As + (b + i) * kAsLd + b;
+      float x = (i == l) ? 1.f : 0.f;
+#pragma unroll
+      for (int j = 0; j < i; ++j) x = fmaf(-arow[j], t[j], x);
+      t[i] = x;
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) As[(b + i) * kAsLd + b + l] = t[i];
+  }
+  __syncthreads();
+  merge_level<16>(As, tmp, tid);
+  merge_level<32>(As, tmp, tid);
+}
+
+__device__ __forceinline__ void store8_bf16(uint32_t saddr, const float* v) {
+  st_shared_v4(saddr, pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+}
+
+__global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                const __grid_constant__ CUtensorMap tm_k,
+                                                                const __grid_constant__ CUtensorMap tm_v,
+                                                                const FusedParams prm) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  float* As = reinterpret_cast<float*>(sm + OFF_AS);
+  float* tmp = reinterpret_cast<float*>(sm + OFF_TMP);
+  float* gam = reinterpret_cast<float*>(sm + OFF_GAM);
+  float* bet = reinterpret_cast<float*>(sm + OFF_BET);
+  float* be = reinterpret_cast<float*>(sm + OFF_BE);
+  float* dl = reinterpret_cast<float*>(sm + OFF_DL);
+  float* eg = reinterpret_cast<float*>(sm + OFF_EG);
+  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* bar_v = bar_kq + 1;
+  uint64_t* bar_mma = bar_kq + 2;
+  volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sm + OFF_FLAGS);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, hf = warp >> 2;   // TMEM lane quadrant, column half
+  const int chain = blockIdx.x;
+  const int n = chain / prm.Hv, h = chain % prm.Hv;
+  const int hq = h / (prm.Hv / prm.Hqk);
+
+  // sequence bounds (validated: a malformed cu_seqlens touches no memory)
+  int64_t tok0, L;
+  if (prm.varlen) {
+    const int64_t a = prm.cu[n], b = prm.cu[n + 1];
+    bool ok = (0 <= a) && (a <= b) && (b <= prm.Ttot);
+    if (chain == 0 && (prm.cu[0] != 0 || prm.cu[prm.N] != prm.Ttot)) ok = false;
+    if (!ok) {
+      if (tid == 0) atomicExch(prm.status, GDN_DEV_BAD_CU_SEQLENS);
+      return;
+    }
+    tok0 = a;
+    L = b - a;
+  } else {
+    tok0 = (int64_t)n * prm.Tseq;
+    L = prm.Tseq;
+  }
+  const int nchunks = (int)((L + kChunk - 1) / kChunk);
+
+  if (tid == 0) {
+    mbar_init(bar_kq, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_mma, 1);
+    mbar_fence_init();
+    flags[1] = 0;
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  if (warp == 0) tmem_alloc(const_cast<uint32_t*>(flags), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = flags[0];
+  const uint32_t R_S = tmem, R_a = tmem + 128, R_b = tmem + 192;
+  const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+  const int row = 32 * qd + lane;   // this thread's TMEM lane (e or d or chunk row)
+
+  // state S^T[e][d] = h0[d][e]
+  {
+    const float* h0p = prm.h0 ? prm.h0 + ((int64_t)n * prm.Hv + h) * kD * kD : nullptr;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      float v[32];
+      const int d0 = 64 * hf + 32 * half;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = h0p ? h0p[(int64_t)(d0 + i) * kD + row] : 0.f;
+      tmem_st32(R_S + lane_off + d0, v);
+    }
+    tmem_wait_st();
+  }
+
+  uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0;
+  bool kq_pending = false, v_pending = false, mma_pending = false;   // meaningful in thread 0
+  auto issue_kq = [&](int c) {
+    const int t = (int)(tok0 + (int64_t)kChunk * c);
+    mbar_arrive_expect_tx(bar_kq, 32768);
+    tma_load_3d(sm + OFF_KQ, &tm_k, bar_kq, 0, hq, t);
+    tma_load_3d(sm + OFF_KQ + 8192, &tm_q, bar_kq, 0, hq, t);
+    tma_load_3d(sm + OFF_KQ + 16384, &tm_k, bar_kq, 64, hq, t);
+    tma_load_3d(sm + OFF_KQ + 24576, &tm_q, bar_kq, 64, hq, t);
+    kq_pending = true;
+  };
+  auto issue_v = [&](int c) {
+    const int t = (int)(tok0 + (int64_t)kChunk * c);
+    mbar_arrive_expect_tx(bar_v, 16384);
+    tma_load_3d(sm + OFF_V, &tm_v, bar_v, 0, h, t);
+    tma_load_3d(sm + OFF_V + 8192, &tm_v, bar_v, 64, h, t);
+    v_pending = true;
+  };
+  // all threads: wait for the MMA batch just committed; false on abort
+  auto wait_mma = [&]() -> bool {
+    __syncthreads();
+    if (flags[1]) return false;
+    const bool ok = mbar_wait(bar_mma, ph_mma, prm.status);
+    ph_mma ^= 1;
+    if (!ok) flags[1] = 1;
+    __syncthreads();
+    if (tid == 0) mma_pending = false;
+    tc_fence_after();
+    return flags[1] == 0;
+  };
+  const uint32_t kq = sbase + OFF_KQ;
+
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && nchunks > 0) {
+    issue_kq(0);
+    issue_v(0);
+  }
+  float g_next = 0.f, b_next = 0.f;   // threads < 64: g and beta of the next chunk's row tid
+  if (tid < kChunk && tid < L) {
+    g_next = prm.g[(tok0 + tid) * prm.Hv + h];
+    b_next = prm.beta[(tok0 + tid) * prm.Hv + h];
+  }
+
+#pragma unroll 1
+  for (int c = 0; c < nchunks; ++c) {
+    const int64_t t0 = tok0 + (int64_t)kChunk * c;
+    const int Lc = (int)((L - (int64_t)kChunk * c) < kChunk ? (L - (int64_t)kChunk * c) : kChunk);
+
+    // ---- S0: g, beta (loaded one chunk ahead), gamma = in-chunk cumsum of g
+    if (tid < kChunk) {
+      gam[tid] = g_next;
+      bet[tid] = b_next;
+      if (c + 1 < nchunks) {
+        const int64_t tn = t0 + kChunk + tid;
+        const bool valid = tn < tok0 + L;
+        g_next = valid ? prm.g[tn * prm.Hv + h] : 0.f;
+        b_next = valid ? prm.beta[tn * prm.Hv + h] : 0.f;
+      }
+    }
+    __syncthreads();
+    if (warp == 0) {
+      const float a = gam[2 * lane], b = gam[2 * lane + 1];
+      float s = a + b;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float t = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += t;
+      }
+      gam[2 * lane] = s - b;
+      gam[2 * lane + 1] = s;
+    }
+    __syncthreads();
+    const float glast = gam[kChunk - 1];
+    if (tid < kChunk) {
+      const float gi = gam[tid];
+      be[tid] = bet[tid] * __expf(gi);
+      dl[tid] = __expf(glast - gi);
+      eg[tid] = __expf(gi);
+    }
+
+    // ---- M1: [K;Q] K^T -> R_a
+    if (tid == 0) {
+      if (!mbar_wait(bar_kq, ph_kq, prm.status)) {
+        flags[1] = 1;
+      } else {
+        ph_kq ^= 1;
+        kq_pending = false;
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t a = kq + (s >> 2) * 16384 + (s & 3) * 32;
+          mma_bf16(R_a, desc_sw128(a, 16, 1024), desc_sw128(a, 16, 1024), id, s > 0);
+        }
+        mma_commit(bar_mma);
+        mma_pending = true;
+      }
+    }
+    if (!wait_mma()) break;
+
+    // ---- S1: A rows (lanes 0..63) and P rows (lanes 64..127)
+    {
+      float v[32];
+      tmem_ld32(R_a + lane_off + 32 * hf, v);
+      // warps whose whole 32x32 block lies above the diagonal only write zeros
+      const bool upper = (qd & 1) == 0 && hf == 1;
+      if (qd < 2) {
+        const int i = row;
+        const float bi = bet[i], gi = gam[i];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * hf + jj;
+          v[jj] = (!upper && j < i) ? bi * __expf(gi - gam[j]) * v[jj] : 0.f;
+        }
+        float4* dst = reinterpret_cast<float4*>(As + i * kAsLd + 32 * hf);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      } else {
+        const int i = row - 64;
+        const float gi = gam[i];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = 32 * hf + jj;
+          v[jj] = (!upper && j <= i) ? __expf(gi - gam[j]) * v[jj] : 0.f;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sbase + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- S2: solve_tril in place, then T diag(beta) and T diag(beta e^g) as bf16
+    solve64(As, tmp, tid);
+    for (int u = tid; u < 512; u += kThreads) {
+      const int i = u >> 3, cc = u & 7;
+      const float4 x0 = *reinterpret_cast<const float4*>(As + i * kAsLd + 8 * cc);
+      const float4 x1 = *reinterpret_cast<const float4*>(As + i * kAsLd + 8 * cc + 4);
+      const float t[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      float a[8], b[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        a[q] = t[q] * bet[8 * cc + q];
+        b[q] = t[q] * be[8 * cc + q];
+      }
+      store8_bf16(sbase + OFF_TB + sw128_chunk(i, cc), a);
+      store8_bf16(sbase + OFF_TBE + sw128_chunk(i, cc), b);
+    }
+    fence_proxy_async();
+    __syncthreads();
+
+    // ---- M2: W^T = K^T (T diag(beta e^g))^T -> R_a ; U^T = V^T (T diag(beta))^T -> R_b
+    if (tid == 0) {
+      if (!mbar_wait(bar_v, ph_v, prm.status)) {
+        flags[1] = 1;
+      } else {
+        ph_v ^= 1;
+        v_pending = false;
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(R_a, desc_sw128(kq + s * 2048, 16384, 1024), desc_sw128(sbase + OFF_TBE + s * 32, 16, 1024), id,
+                   s > 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(R_b, desc_sw128(sbase + OFF_V + s * 2048, 8192, 1024),
+                   desc_sw128(sbase + OFF_TB + s * 32, 16, 1024), id, s > 0);
+        mma_commit(bar_mma);
+        mma_pending = true;
+      }
+    }
+    if (!wait_mma()) break;
+    if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);   // v tile consumed
+
+    // ---- S3: W^T -> bf16 [d][i] (MN-major B);  S4: S^T -> bf16 [e][d] (K-major A), S^T *= e^{g_last}
+    {
+      float v[32];
+      tmem_ld32(R_a + lane_off + 32 * hf, v);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) store8_bf16(sbase + OFF_W + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+      const float dec = __expf(glast);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t col = 64 * hf + 32 * half;
+        tmem_ld32(R_S + lane_off + col, v);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc)
+          store8_bf16(sbase + OFF_ST + hf * 16384 + sw128_chunk(row, 4 * half + cc), v + 8 * cc);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= dec;
+        tmem_st32(R_S + lane_off + col, v);
+      }
+      tmem_wait_st();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- M3: V'^T = U^T - S^T W^T (R_b) ; OQ^T = S^T Q^T (R_a)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idv = idesc_bf16(128, 64, 0, 1, 1);
+      const uint32_t ido = idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t a = sbase + OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+        mma_bf16(R_b, desc_sw128(a, 16, 1024), desc_sw128(sbase + OFF_W + s * 2048, 16384, 1024), idv, 1);
+      }
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t a = sbase + OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+        const uint32_t b = kq + 8192 + (s >> 2) * 16384 + (s & 3) * 32;
+        mma_bf16(R_a, desc_sw128(a, 16, 1024), desc_sw128(b, 16, 1024), ido, s > 0);
+      }
+      mma_commit(bar_mma);
+      mma_pending = true;
+    }
+    if (!wait_mma()) break;
+
+    // ---- S5: V'^T -> bf16 [e][j] ; V''^T = V'^T diag(e^{g_last - g}) -> bf16
+    {
+      float v[32], w[32];
+      tmem_ld32(R_b + lane_off + 32 * hf, v);
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) w[jj] = v[jj] * dl[32 * hf + jj];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        store8_bf16(sbase + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+        store8_bf16(sbase + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- M4: OP^T = V'^T P^T (R_b) ; S^T += V''^T K (R_S)
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t idp = idesc_bf16(128, 64, 0, 0, 0);
+      const uint32_t ids = idesc_bf16(128, 128, 0, 1, 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma_bf16(R_b, desc_sw128(sbase + OFF_VP + s * 32, 16, 1024), desc_sw128(sbase + OFF_P + s * 32, 16, 1024),
+                 idp, s > 0);
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma_bf16(R_S, desc_sw128(sbase + OFF_VPP + s * 32, 16, 1024), desc_sw128(kq + s * 2048, 16384, 1024), ids,
+                 1);
+      mma_commit(bar_mma);
+      mma_pending = true;
+    }
+    if (!wait_mma()) break;
+    if (tid == 0 && c + 1 < nchunks) issue_kq(c + 1);   // k / q tiles consumed
+
+    // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
+    {
+      float a[32], b[32];
+      tmem_ld32(R_a + lane_off + 32 * hf, a);
+      tmem_ld32(R_b + lane_off + 32 * hf, b);
+      __nv_bfloat16* os = reinterpret_cast<__nv_bfloat16*>(sm + OFF_OS);
+#pragma unroll
+      for (int ii = 0; ii < 32; ++ii) {
+        const int i = 32 * hf + ii;
+        os[i * kD + row] = __float2bfloat16_rn(prm.scale * (eg[i] * a[ii] + b[ii]));
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    for (int u = tid; u < kChunk * 16; u += kThreads) {
+      const int i = u >> 4, cc = u & 15;
+      if (i < Lc) {
+        const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OS + i * 256 + cc * 16);
+        *reinterpret_cast<uint4*>(prm.o + ((t0 + i) * prm.Hv + h) * kD + cc * 8) = val;
+      }
+    }
+    __syncthreads();
+  }
+
+  if (flags[1]) {
+    // abort: let copies and MMAs already in flight finish (bounded) before
+    // the shared memory and TMEM are released
+    if (tid == 0) {
+      if (kq_pending) mbar_wait(bar_kq, ph_kq, prm.status, 100000000ull);
+      if (v_pending) mbar_wait(bar_v, ph_v, prm.status, 100000000ull);
+      if (mma_pending) mbar_wait(bar_mma, ph_mma, prm.status, 100000000ull);
+    }
+  } else if (prm.ht) {
+    // final state ht[d][e] = S^T[e][d]
+    float* htp = prm.ht + ((int64_t)n * prm.Hv + h) * kD * kD;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      float v[32];
+      const int d0 = 64 * hf + 32 * half;
+      tmem_ld32(R_S + lane_off + d0, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) htp[(int64_t)(d0 + i) * kD + row] = v[i];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+bool fused_supported(const gdn_problem& p) {
+  return p.dt == GDN_BF16 && p.K == kD && p.V == kD && (p.C == 64 || p.C == 128);
+}
+
+size_t fused_workspace_bytes(const gdn_problem&) { return kAlign; }   // the status word
 size_t fused_status_offset(const gdn_problem&) { return 0; }
-gdn_status run_fused(const gdn_problem&, const void*, const void*, const void*, const float*, const float*, float,
-                     const float*, const int32_t*, void*, float*, void*, cudaStream_t) {
-  return GDN_ERR_UNSUPPORTED;
+
+gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                     void* ws, cudaStream_t s) {
+  if (!fused_supported(p)) return GDN_ERR_UNSUPPORTED;
+  int32_t* status = static_cast<int32_t*>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+  const int64_t Ttot = (int64_t)p.B * p.T;
+  if (Ttot == 0 || (int64_t)p.N * p.Hv == 0) {
+    // no tokens: ht = h0 (or zeros)
+    if (ht) {
+      const size_t bytes = sizeof(float) * (size_t)p.N * p.Hv * p.K * p.V;
+      cudaError_t e = h0 ? cudaMemcpyAsync(ht, h0, bytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(ht, 0, bytes, s);
+      if (e != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+  }
+  CUtensorMap tq, tk, tv;
+  memset(&tq, 0, sizeof(tq));
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  const uint32_t box[3] = {64, 1, kChunk};
+  {
+    const uint64_t dims[3] = {(uint64_t)p.K, (uint64_t)p.Hqk, (uint64_t)Ttot};
+    const uint64_t str[2] = {(uint64_t)p.K * 2, (uint64_t)p.Hqk * p.K * 2};
+    if (!make_tmap_bf16(&tq, q, 3, dims, str, box) || !make_tmap_bf16(&tk, k, 3, dims, str, box)) return GDN_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)p.V, (uint64_t)p.Hv, (uint64_t)Ttot};
+    const uint64_t str[2] = {(uint64_t)p.V * 2, (uint64_t)p.Hv * p.V * 2};
+    if (!make_tmap_bf16(&tv, v, 3, dims, str, box)) return GDN_ERR_CUDA;
+  }
+  FusedParams prm;
+  prm.g = g;
+  prm.beta = beta;
+  prm.h0 = h0;
+  prm.cu = p.varlen ? cu : nullptr;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.ht = ht;
+  prm.status = status;
+  prm.N = p.N;
+  prm.Tseq = p.T;
+  prm.Ttot = (int)Ttot;
+  prm.Hqk = p.Hqk;
+  prm.Hv = p.Hv;
+  prm.varlen = p.varlen;
+  prm.scale = scale;
+  if (cudaFuncSetAttribute(gdn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+      cudaSuccess)
+    return GDN_ERR_CUDA;
+  const unsigned grid = (unsigned)((int64_t)p.N * p.Hv);
+  gdn_fused_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, prm);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace gdn

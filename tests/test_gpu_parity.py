@@ -171,3 +171,81 @@ def test_stage_intermediates_match_oracle(gdn, oracle_mod, C):
                 err = rel_fro(g_, ref) if np.linalg.norm(ref) > 0 else np.abs(g_).max()
                 assert err < 1e-4, (key, n, h, err)
             c0 += nt
+
+
+# ------------------------------------------------------------- fused path
+
+FUSED_CASES = {
+    "fixed_C64_ragged": (I.WORKLOADS[1].with_(B=2, T=333, Hqk=2, Hv=4), None),
+    "fixed_C128_request": (I.WORKLOADS[2].with_(B=2, T=300, Hqk=2, Hv=2), None),
+    "varlen_short_and_empty": (I.WORKLOADS[3].with_(Hqk=1, Hv=2), [5, 64, 200, 1, 0, 129, 63, 65]),
+    "single_token": (I.WORKLOADS[2].with_(B=3, T=1, Hqk=1, Hv=1), None),
+    "gqa4_h0": (I.WORKLOADS[2].with_(B=1, T=130, Hqk=1, Hv=4, C=64), None),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FUSED_CASES))
+def test_fused_parity(gdn, oracle_mod, name):
+    w, lens = FUSED_CASES[name]
+    x = I.make_inputs(w, "cpu", lengths=lens)
+    d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
+    p = gdn.problem_of(d["q"], d["v"], w.C, d["cu_seqlens"])
+    assert gdn.gdn_resolve_path(p) == "fused"
+    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, "fused"), dtype=torch.uint8, device="cuda")
+    o, ht = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
+                              cu_seqlens=d["cu_seqlens"], C=w.C, path="fused", workspace=ws)
+    assert gdn.gdn_get_device_status(p, "fused", ws) == gdn.DEV_OK
+    o_ref, ht_ref = oracle_mod.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                                         cu_seqlens=x["cu_seqlens"])
+    o, ht = o.float().cpu().numpy(), ht.cpu().numpy()
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(ht))
+    assert rel_fro(o, o_ref) <= TOL["bf16"], rel_fro(o, o_ref)
+    assert rel_fro(ht, ht_ref) <= TOL["bf16"], rel_fro(ht, ht_ref)
+
+
+def test_fused_leaves_rows_of_other_sequences_untouched(gdn):
+    """A tail chunk's padding rows belong to the next sequence: the fused
+    kernel must not store them.  Sequence 1 is empty-output-checked by giving
+    the call an o prefilled with a sentinel and zero-length sequences."""
+    w = I.WORKLOADS[3].with_(Hqk=1, Hv=2)
+    lens = [70, 0, 10]
+    x = I.make_inputs(w, "cuda", lengths=lens)
+    o = torch.full_like(x["v"], 3.0)
+    gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                      cu_seqlens=x["cu_seqlens"], C=64, path="fused", o=o)
+    torch.cuda.synchronize()
+    assert torch.all(o != 3.0)   # every row of the packed batch written exactly by its own sequence
+    # sequence 0 alone reproduces its rows: rows 64..69 were not clobbered by chunk padding
+    o0, _ = gdn.gdn_chunk_fwd(x["q"][:, :70].contiguous(), x["k"][:, :70].contiguous(), x["v"][:, :70].contiguous(),
+                              x["g"][:, :70].contiguous(), x["beta"][:, :70].contiguous(), x["scale"],
+                              h0=x["h0"][:1].contiguous(), C=64, path="fused")
+    assert torch.equal(o0, o[:, :70])
+
+
+def test_fused_malformed_cu_seqlens(gdn):
+    w = I.WORKLOADS[3].with_(Hqk=1, Hv=2)
+    x = I.make_inputs(w, "cuda", lengths=[10, 20, 30])
+    # sequence 1 runs past the end of the batch, sequence 2 has a negative length
+    bad = torch.tensor([0, 10, 70, 60], dtype=torch.int32, device="cuda")
+    p = gdn.problem_of(x["q"], x["v"], 64, bad)
+    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, "fused"), dtype=torch.uint8, device="cuda")
+    o = torch.full_like(x["v"], 7.0)
+    gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], cu_seqlens=bad, C=64, path="fused",
+                      o=o, workspace=ws)
+    assert gdn.gdn_get_device_status(p, "fused", ws) == gdn.DEV_BAD_CU_SEQLENS
+    # the malformed sequences wrote nothing; the valid one wrote its rows
+    assert torch.all(o[:, 10:] == 7.0)
+    assert not torch.any(o[:, :10] == 7.0)
+
+
+def test_fused_matches_staged(gdn):
+    """Fused and staged paths agree with each other (both against the same
+    seeded inputs) -- a cross-check independent of the oracle."""
+    w = I.WORKLOADS[1].with_(T=500, Hqk=2, Hv=4)
+    x = I.make_inputs(w, "cuda")
+    args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"])
+    of, hf = gdn.gdn_chunk_fwd(*args, C=64, path="fused")
+    os_, hs = gdn.gdn_chunk_fwd(*args, C=64, path="staged")
+    torch.cuda.synchronize()
+    assert rel_fro(of.float().cpu().numpy(), os_.float().cpu().numpy()) < 5e-3
+    assert rel_fro(hf.cpu().numpy(), hs.cpu().numpy()) < 5e-3
