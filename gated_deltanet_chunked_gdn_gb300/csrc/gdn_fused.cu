@@ -50,7 +50,7 @@ constexpr uint32_t OFF_W = OFF_Y;
 constexpr uint32_t OFF_P = 65536;      // P [i][j] bf16, 8 KB
 constexpr uint32_t OFF_X = 73728;      // 32 KB, reused: A/T fp32 + scratch | S^T bf16 | V'^T, V''^T | o staging
 constexpr uint32_t OFF_AS = OFF_X;     // fp32 [64][68]
-constexpr uint32_t OFF_TMP = OFF_X + 64 * 68 * 4;  // fp32 scratch for the solve merges (1024 floats)
+constexpr uint32_t OFF_TMP = OFF_X + 64 * 68 * 4;  // fp32 scratch for the solve merges (32 x 40 floats)
 constexpr uint32_t OFF_ST = OFF_X;     // S^T bf16 [e][d], 2 atom columns of 16 KB
 constexpr uint32_t OFF_VP = OFF_X;     // V'^T bf16 [e][j], 16 KB
 constexpr uint32_t OFF_VPP = OFF_X + 16384;
@@ -67,7 +67,7 @@ constexpr uint32_t kSmemUsed = OFF_MISC + 1344;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 constexpr int kAsLd = 68;
 
-static_assert(OFF_TMP + 1024 * 4 <= OFF_X + 32768, "solve scratch overflows region X");
+static_assert(OFF_TMP + 32 * 40 * 4 <= OFF_X + 32768, "solve scratch overflows region X");
 static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs must fit one SM");
 
 struct FusedParams {
@@ -86,49 +86,70 @@ struct FusedParams {
 // leading dimension kAsLd, zeros on and above the diagonal).
 //  1. Diagonal 16x16 blocks by forward substitution: a half-warp per block,
 //     lane l keeps column l of the block's inverse in registers.
-//  2. Merge neighbouring blocks, [[T11, 0], [A21-block, T22]] ->
-//     T21 = -T22 (A21 T11), first for the 16-blocks (two pairs), then for the
-//     32-blocks (one pair).  The upper triangles hold zeros, so the products
-//     run over full square blocks.
+//  2. Merge neighbouring blocks, [[T11, 0], [A21, T22]] -> T21 = -T22 (A21 T11),
+//     first the 16-blocks (two pairs), then the 32-blocks (one pair).  The
+//     merge products run on the tensor cores (mma.sync m16n8k8, tf32 inputs,
+//     fp32 accumulation); the upper triangles hold zeros, so they are plain
+//     square products.  tf32 rounding here stays two orders of magnitude below
+//     the bf16 rounding T receives as an MMA operand afterwards.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// d[16x8] += A[16 x KK] B[KK x 8]; A(r, c) = A[r * lda + c], B(r, c) = B[r * ldb + c].
+template <int KK>
+__device__ __forceinline__ void tile_mma_tf32(float (&d)[4], const float* A, int lda, const float* B, int ldb,
+                                              int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int k0 = 0; k0 < KK; k0 += 8) {
+    const uint32_t a0 = to_tf32(A[g * lda + k0 + t]), a1 = to_tf32(A[(g + 8) * lda + k0 + t]);
+    const uint32_t a2 = to_tf32(A[g * lda + k0 + t + 4]), a3 = to_tf32(A[(g + 8) * lda + k0 + t + 4]);
+    const uint32_t b0 = to_tf32(B[(k0 + t) * ldb + g]), b1 = to_tf32(B[(k0 + t + 4) * ldb + g]);
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+// Store a 16x8 accumulator tile (times `sign`) at D(r, c) = D[r * ldd + c].
+__device__ __forceinline__ void tile_store(const float (&d)[4], float* D, int ldd, int lane, float sign) {
+  const int g = lane >> 2, t = lane & 3;
+  D[g * ldd + 2 * t] = sign * d[0];
+  D[g * ldd + 2 * t + 1] = sign * d[1];
+  D[(g + 8) * ldd + 2 * t] = sign * d[2];
+  D[(g + 8) * ldd + 2 * t + 1] = sign * d[3];
+}
+
+// One merge level: pairs of S x S blocks along the diagonal of the 64x64 tile.
+// Output tiles (pair, 16-row tile, 8-column tile) are dealt to warps.
 template <int S>
-__device__ __forceinline__ void merge_level(float* As, float* tmp, int tid) {
-  // every thread owns R consecutive columns of one row of the merged pairs
-  constexpr int NP = kChunk / (2 * S);          // pairs at this level
-  constexpr int R = (NP * S * S) / kThreads;    // outputs per thread (2 or 4)
-  constexpr int CPR = S / R;                    // threads per row
-  static_assert(R * kThreads == NP * S * S && (R == 2 || R == 4), "merge tiling");
-  const int p = tid / (S * CPR);
-  const int i = (tid / CPR) % S;
-  const int m0 = (tid % CPR) * R;
-  const int o = 2 * S * p;
-  float acc[R];
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = 0.f;
-  // tmp = A21 T11
-#pragma unroll 8
-  for (int j = 0; j < S; ++j) {
-    const float a = As[(o + S + i) * kAsLd + o + j];
-    const float* t = As + (o + j) * kAsLd + o + m0;
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = fmaf(a, t[r], acc[r]);
+__device__ __forceinline__ void merge_level(float* As, float* tmp, int warp, int lane) {
+  constexpr int NP = kChunk / (2 * S);
+  constexpr int MT = S / 16, NT = S / 8;
+  constexpr int TLD = S + 8;                  // padded leading dimension of tmp (no bank conflicts)
+  constexpr int TILES = NP * MT * NT;
+  // tmp_p = A21 T11
+  for (int tile = warp; tile < TILES; tile += kThreads / 32) {
+    const int p = tile / (MT * NT), mt = (tile / NT) % MT, nt = tile % NT;
+    const int o = 2 * S * p;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mma_tf32<S>(d, As + (o + S + 16 * mt) * kAsLd + o, kAsLd, As + o * kAsLd + o + 8 * nt, kAsLd, lane);
+    tile_store(d, tmp + p * S * TLD + 16 * mt * TLD + 8 * nt, TLD, lane, 1.f);
   }
-  float* tp = tmp + p * S * S + i * S + m0;
-#pragma unroll
-  for (int r = 0; r < R; ++r) tp[r] = acc[r];
   __syncthreads();
-  // T21 = -T22 tmp
-#pragma unroll
-  for (int r = 0; r < R; ++r) acc[r] = 0.f;
-#pragma unroll 8
-  for (int j = 0; j < S; ++j) {
-    const float a = As[(o + S + i) * kAsLd + o + S + j];
-    const float* t = tmp + p * S * S + j * S + m0;
-#pragma unroll
-    for (int r = 0; r < R; ++r) acc[r] = fmaf(a, t[r], acc[r]);
+  // T21 = -T22 tmp_p
+  for (int tile = warp; tile < TILES; tile += kThreads / 32) {
+    const int p = tile / (MT * NT), mt = (tile / NT) % MT, nt = tile % NT;
+    const int o = 2 * S * p;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mma_tf32<S>(d, As + (o + S + 16 * mt) * kAsLd + o + S, kAsLd, tmp + p * S * TLD + 8 * nt, TLD, lane);
+    tile_store(d, As + (o + S + 16 * mt) * kAsLd + o + 8 * nt, kAsLd, lane, -1.f);
   }
-  float* dst = As + (o + S + i) * kAsLd + o + m0;
-#pragma unroll
-  for (int r = 0; r < R; ++r) dst[r] = -acc[r];
   __syncthreads();
 }
 
@@ -151,8 +172,8 @@ __device__ __forceinline__ void solve64(float* As, float* tmp, int tid) {
     for (int i = 0; i < 16; ++i) As[(b + i) * kAsLd + b + l] = t[i];
   }
   __syncthreads();
-  merge_level<16>(As, tmp, tid);
-  merge_level<32>(As, tmp, tid);
+  merge_level<16>(As, tmp, warp, lane);
+  merge_level<32>(As, tmp, warp, lane);
 }
 
 __device__ __forceinline__ void store8_bf16(uint32_t saddr, const float* v) {
@@ -408,15 +429,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         mma_pending = true;
       }
     }
-    if (!wait_mma()) break;
-    if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);   // v tile consumed
-
-    // ---- S3: W^T -> bf16 [d][i] (MN-major B);  S4: S^T -> bf16 [e][d] (K-major A), S^T *= e^{g_last}
+    // ---- S4 (while M2 runs): S^T -> bf16 [e][d] (K-major A), S^T *= e^{g_last}
     {
       float v[32];
-      tmem_ld32(R_a + lane_off + 32 * hf, v);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) store8_bf16(sbase + OFF_W + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
       const float dec = __expf(glast);
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -430,6 +445,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         tmem_st32(R_S + lane_off + col, v);
       }
       tmem_wait_st();
+      tc_fence_before();
+    }
+    if (!wait_mma()) break;
+    if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);   // v tile consumed
+
+    // ---- S3: W^T -> bf16 [d][i] (MN-major B)
+    {
+      float v[32];
+      tmem_ld32(R_a + lane_off + 32 * hf, v);
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) store8_bf16(sbase + OFF_W + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -493,14 +519,18 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
 
     // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
     {
-      float a[32], b[32];
-      tmem_ld32(R_a + lane_off + 32 * hf, a);
-      tmem_ld32(R_b + lane_off + 32 * hf, b);
       __nv_bfloat16* os = reinterpret_cast<__nv_bfloat16*>(sm + OFF_OS);
+#pragma unroll 1
+      for (int q = 0; q < 2; ++q) {
+        float a[16], b[16];
+        const uint32_t col = 32 * hf + 16 * q;
+        tmem_ld16(R_a + lane_off + col, a);
+        tmem_ld16(R_b + lane_off + col, b);
 #pragma unroll
-      for (int ii = 0; ii < 32; ++ii) {
-        const int i = 32 * hf + ii;
-        os[i * kD + row] = __float2bfloat16_rn(prm.scale * (eg[i] * a[ii] + b[ii]));
+        for (int ii = 0; ii < 16; ++ii) {
+          const int i = col + ii;
+          os[i * kD + row] = __float2bfloat16_rn(prm.scale * (eg[i] * a[ii] + b[ii]));
+        }
       }
     }
     tc_fence_before();
