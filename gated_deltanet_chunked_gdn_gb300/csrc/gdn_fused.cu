@@ -184,8 +184,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
                                                                 const __grid_constant__ CUtensorMap tm_k,
                                                                 const __grid_constant__ CUtensorMap tm_v,
                                                                 const FusedParams prm) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned base, derived by pointer arithmetic on the __shared__
+  // array so that every access below stays a shared-memory access
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(sm);
   float* As = reinterpret_cast<float*>(sm + OFF_AS);
   float* tmp = reinterpret_cast<float*>(sm + OFF_TMP);

@@ -20,8 +20,8 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const __nv_bfloat16*
                                                             float* __restrict__ D, int variant,
                                                             const __grid_constant__ CUtensorMap tmapA,
                                                             int32_t* status) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* As = base;
   uint8_t* Bs = base + 32768;
   uint64_t* bar = reinterpret_cast<uint64_t*>(base + 65536);
