@@ -22,7 +22,7 @@
 //   M3  V'^T = U^T - S^T W^T;  OQ^T = S^T Q^T      (chunk_h first half)
 //   S5  V'^T -> bf16, V''^T = V'^T diag(e^{g_last - g}) -> bf16
 //   M4  OP^T = V'^T P^T;  S^T += V''^T K          (chunk_h second half)
-//   S6  o_i = scale (e^{g_i} OQ_i + OP_i)         (chunk_o)
+//   S6  o_i = scale e^{g_i} OQ_i + OP_i           (chunk_o; P carries scale)
 //
 // Rows past a sequence's end (tail chunk) get beta = 0 and g = 0, which zeroes
 // their rows of A, W, U and V' exactly; they are never stored.
@@ -54,15 +54,15 @@ constexpr uint32_t OFF_TMP = OFF_X + 64 * 68 * 4;  // fp32 scratch for the solve
 constexpr uint32_t OFF_ST = OFF_X;     // S^T bf16 [e][d], 2 atom columns of 16 KB
 constexpr uint32_t OFF_VP = OFF_X;     // V'^T bf16 [e][j], 16 KB
 constexpr uint32_t OFF_VPP = OFF_X + 16384;
-constexpr uint32_t OFF_OS = OFF_X;     // o staging bf16 [64][128]
+constexpr uint32_t OFF_OS = OFF_X;     // o staging bf16: 2 boxes [64 rows][64], 128-byte swizzle (TMA store)
 constexpr uint32_t OFF_MISC = 106496;
 constexpr uint32_t OFF_GAM = OFF_MISC;         // float[64] gamma (in-chunk cumsum of g)
 constexpr uint32_t OFF_BET = OFF_MISC + 256;   // float[64] beta (0 past the end)
 constexpr uint32_t OFF_BE = OFF_MISC + 512;    // float[64] beta e^gamma
 constexpr uint32_t OFF_DL = OFF_MISC + 768;    // float[64] e^{gamma_last - gamma}
 constexpr uint32_t OFF_EG = OFF_MISC + 1024;   // float[64] e^gamma
-constexpr uint32_t OFF_BAR = OFF_MISC + 1280;  // 3 mbarriers
-constexpr uint32_t OFF_FLAGS = OFF_MISC + 1312;  // [0] tmem base, [1] abort
+constexpr uint32_t OFF_BAR = OFF_MISC + 1280;    // 5 mbarriers: k/q tiles, v tile, three MMA commit groups
+constexpr uint32_t OFF_FLAGS = OFF_MISC + 1320;  // [0] tmem base, [1] abort
 constexpr uint32_t kSmemUsed = OFF_MISC + 1344;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 constexpr int kAsLd = 68;
@@ -126,9 +126,12 @@ __device__ __forceinline__ void tile_store(const float (&d)[4], float* D, int ld
 }
 
 // One merge level: pairs of S x S blocks along the diagonal of the 64x64 tile.
-// Output tiles (pair, 16-row tile, 8-column tile) are dealt to warps.
+// Output tiles (pair, 16-row tile, 8-column tile) are dealt to warps.  The
+// final T21 tiles also go out as the two bf16 MMA operands T diag(beta) and
+// T diag(beta e^g) (tb, tbe: 64 x 64 K-major tiles, 128-byte swizzle).
 template <int S>
-__device__ __forceinline__ void merge_level(float* As, float* tmp, int warp, int lane) {
+__device__ __forceinline__ void merge_level(float* As, float* tmp, int warp, int lane, uint8_t* tb, uint8_t* tbe,
+                                            const float* bet, const float* be) {
   constexpr int NP = kChunk / (2 * S);
   constexpr int MT = S / 16, NT = S / 8;
   constexpr int TLD = S + 8;                  // padded leading dimension of tmp (no bank conflicts)
@@ -143,17 +146,28 @@ __device__ __forceinline__ void merge_level(float* As, float* tmp, int warp, int
   }
   __syncthreads();
   // T21 = -T22 tmp_p
+  const int g = lane >> 2, t = lane & 3;
   for (int tile = warp; tile < TILES; tile += kThreads / 32) {
     const int p = tile / (MT * NT), mt = (tile / NT) % MT, nt = tile % NT;
     const int o = 2 * S * p;
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mma_tf32<S>(d, As + (o + S + 16 * mt) * kAsLd + o + S, kAsLd, tmp + p * S * TLD + 8 * nt, TLD, lane);
-    tile_store(d, As + (o + S + 16 * mt) * kAsLd + o + 8 * nt, kAsLd, lane, -1.f);
+    const int r0 = o + S + 16 * mt, c0 = o + 8 * nt + 2 * t;
+    tile_store(d, As + r0 * kAsLd + o + 8 * nt, kAsLd, lane, -1.f);
+    const float b0 = bet[c0], b1 = bet[c0 + 1], e0 = be[c0], e1 = be[c0 + 1];
+    *reinterpret_cast<uint32_t*>(tb + sw128_offset(r0 + g, c0)) = pack_bf16(-d[0] * b0, -d[1] * b1);
+    *reinterpret_cast<uint32_t*>(tb + sw128_offset(r0 + g + 8, c0)) = pack_bf16(-d[2] * b0, -d[3] * b1);
+    *reinterpret_cast<uint32_t*>(tbe + sw128_offset(r0 + g, c0)) = pack_bf16(-d[0] * e0, -d[1] * e1);
+    *reinterpret_cast<uint32_t*>(tbe + sw128_offset(r0 + g + 8, c0)) = pack_bf16(-d[2] * e0, -d[3] * e1);
   }
+  fence_proxy_async();   // the bf16 tiles feed tcgen05.mma
   __syncthreads();
 }
 
-__device__ __forceinline__ void solve64(float* As, float* tmp, int tid) {
+// T = (I + A)^{-1} (see above); also writes T diag(beta) and T diag(beta e^g)
+// as bf16 K-major operands (tb, tbe), including their zero upper blocks.
+__device__ __forceinline__ void solve64(float* As, float* tmp, int tid, uint8_t* tb, uint8_t* tbe, const float* bet,
+                                        const float* be) {
   const int warp = tid >> 5, lane = tid & 31;
   if (warp < 2) {
     const int b = 16 * (2 * warp + (lane >> 4));
@@ -168,21 +182,39 @@ __device__ __forceinline__ void solve64(float* As, float* tmp, int tid) {
       t[i] = x;
     }
     __syncwarp();
+    const float bl = bet[b + l], el = be[b + l];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) As[(b + i) * kAsLd + b + l] = t[i];
+    for (int i = 0; i < 16; ++i) {
+      As[(b + i) * kAsLd + b + l] = t[i];
+      *reinterpret_cast<__nv_bfloat16*>(tb + sw128_offset(b + i, b + l)) = __float2bfloat16_rn(t[i] * bl);
+      *reinterpret_cast<__nv_bfloat16*>(tbe + sw128_offset(b + i, b + l)) = __float2bfloat16_rn(t[i] * el);
+    }
+  } else {
+    // warps 2..7: zero the six strictly-upper 16x16 blocks of both operands
+    // (one 16-byte chunk per thread and operand: 6 blocks x 16 rows x 2 chunks)
+    const int u = tid - 64;                        // 0..191
+    const int blk = u >> 5, r = (u >> 1) & 15, half = u & 1;
+    const int rb = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+    const int cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+    const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
+    *reinterpret_cast<uint4*>(tb + off) = make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(tbe + off) = make_uint4(0u, 0u, 0u, 0u);
   }
   __syncthreads();
-  merge_level<16>(As, tmp, warp, lane);
-  merge_level<32>(As, tmp, warp, lane);
+  merge_level<16>(As, tmp, warp, lane, tb, tbe, bet, be);
+  merge_level<32>(As, tmp, warp, lane, tb, tbe, bet, be);
 }
 
-__device__ __forceinline__ void store8_bf16(uint32_t saddr, const float* v) {
-  st_shared_v4(saddr, pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
+// Eight floats as bf16 into one 16-byte chunk of shared memory.
+__device__ __forceinline__ void store8_bf16(uint8_t* p, const float* v) {
+  *reinterpret_cast<uint4*>(p) =
+      make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
 }
 
 __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 const __grid_constant__ CUtensorMap tm_k,
                                                                 const __grid_constant__ CUtensorMap tm_v,
+                                                                const __grid_constant__ CUtensorMap tm_o,
                                                                 const FusedParams prm) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned base, derived by pointer arithmetic on the __shared__
@@ -198,7 +230,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
   float* eg = reinterpret_cast<float*>(sm + OFF_EG);
   uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* bar_v = bar_kq + 1;
-  uint64_t* bar_mma = bar_kq + 2;
+  // MMA commit groups.  Every commit is waited for (by every thread, in
+  // order) before the next commit to the same barrier, so a waiter can never
+  // miss a phase.
+  uint64_t* bar_mma = bar_kq + 2;   // M1, M2, then the S^T Q^T product of M3
+  uint64_t* bar_x = bar_kq + 3;     // V' (M3), then the state update (M4)
+  uint64_t* bar_q = bar_kq + 4;     // V'^T P^T (M4)
   volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sm + OFF_FLAGS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -229,11 +266,14 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     mbar_init(bar_kq, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_x, 1);
+    mbar_init(bar_q, 1);
     mbar_fence_init();
     flags[1] = 0;
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_o);
   }
   if (warp == 0) tmem_alloc(const_cast<uint32_t*>(flags), kTmemCols);
   tc_fence_before();
@@ -258,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     tmem_wait_st();
   }
 
-  uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0;
-  bool kq_pending = false, v_pending = false, mma_pending = false;   // meaningful in thread 0
+  uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_x = 0, ph_q = 0;
+  bool kq_pending = false, v_pending = false;   // meaningful in thread 0
+  int mma_pending = 0, x_pending = 0, q_pending = 0;   // commits not yet waited for (thread 0)
   auto issue_kq = [&](int c) {
     const int t = (int)(tok0 + (int64_t)kChunk * c);
     mbar_arrive_expect_tx(bar_kq, 32768);
@@ -276,17 +317,22 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     tma_load_3d(sm + OFF_V + 8192, &tm_v, bar_v, 64, h, t);
     v_pending = true;
   };
-  // all threads: wait for the MMA batch just committed; false on abort
-  auto wait_mma = [&]() -> bool {
+  // Every thread waits for every MMA commit, in commit order, so that all
+  // threads track the same barrier phases.  A wait that times out raises the
+  // abort flag; sync_ok() makes the flag visible to all threads.
+  auto wait_commit = [&](uint64_t* bar, uint32_t& ph, int& pending) {
+    if (!mbar_wait(bar, ph, prm.status)) flags[1] = 1;
+    ph ^= 1;
+    if (tid == 0) --pending;
+  };
+  auto sync_ok = [&]() -> bool {
     __syncthreads();
-    if (flags[1]) return false;
-    const bool ok = mbar_wait(bar_mma, ph_mma, prm.status);
-    ph_mma ^= 1;
-    if (!ok) flags[1] = 1;
-    __syncthreads();
-    if (tid == 0) mma_pending = false;
     tc_fence_after();
     return flags[1] == 0;
+  };
+  auto wait_mma = [&]() -> bool {
+    wait_commit(bar_mma, ph_mma, mma_pending);
+    return sync_ok();
   };
   const uint32_t kq = sbase + OFF_KQ;
 
@@ -296,10 +342,14 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     issue_kq(0);
     issue_v(0);
   }
-  float g_next = 0.f, b_next = 0.f;   // threads < 64: g and beta of the next chunk's row tid
-  if (tid < kChunk && tid < L) {
-    g_next = prm.g[(tok0 + tid) * prm.Hv + h];
-    b_next = prm.beta[(tok0 + tid) * prm.Hv + h];
+  float g_nx[2] = {0.f, 0.f}, b_nx[2] = {0.f, 0.f};   // warp 0: g, beta of rows 2 lane, 2 lane + 1
+  if (warp == 0) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      if (2 * lane + r < L) {
+        g_nx[r] = prm.g[(tok0 + 2 * lane + r) * prm.Hv + h];
+        b_nx[r] = prm.beta[(tok0 + 2 * lane + r) * prm.Hv + h];
+      }
   }
 
 #pragma unroll 1
@@ -307,36 +357,32 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     const int64_t t0 = tok0 + (int64_t)kChunk * c;
     const int Lc = (int)((L - (int64_t)kChunk * c) < kChunk ? (L - (int64_t)kChunk * c) : kChunk);
 
-    // ---- S0: g, beta (loaded one chunk ahead), gamma = in-chunk cumsum of g
-    if (tid < kChunk) {
-      gam[tid] = g_next;
-      bet[tid] = b_next;
-      if (c + 1 < nchunks) {
-        const int64_t tn = t0 + kChunk + tid;
-        const bool valid = tn < tok0 + L;
-        g_next = valid ? prm.g[tn * prm.Hv + h] : 0.f;
-        b_next = valid ? prm.beta[tn * prm.Hv + h] : 0.f;
-      }
-    }
-    __syncthreads();
+    // ---- S0 (warp 0): gamma = in-chunk cumsum of g, from g / beta loaded one
+    // chunk ahead (lane l holds rows 2l and 2l + 1); the next sync comes
+    // before any reader.
     if (warp == 0) {
-      const float a = gam[2 * lane], b = gam[2 * lane + 1];
-      float s = a + b;
+      const float ga = g_nx[0], gb = g_nx[1], ba = b_nx[0], bb = b_nx[1];
+      if (c + 1 < nchunks) {
+        const int64_t tn = t0 + kChunk + 2 * lane, end = tok0 + L;
+        g_nx[0] = tn < end ? prm.g[tn * prm.Hv + h] : 0.f;
+        b_nx[0] = tn < end ? prm.beta[tn * prm.Hv + h] : 0.f;
+        g_nx[1] = tn + 1 < end ? prm.g[(tn + 1) * prm.Hv + h] : 0.f;
+        b_nx[1] = tn + 1 < end ? prm.beta[(tn + 1) * prm.Hv + h] : 0.f;
+      }
+      float sum = ga + gb;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
-        const float t = __shfl_up_sync(0xffffffffu, s, off);
-        if (lane >= off) s += t;
+        const float t = __shfl_up_sync(0xffffffffu, sum, off);
+        if (lane >= off) sum += t;
       }
-      gam[2 * lane] = s - b;
-      gam[2 * lane + 1] = s;
-    }
-    __syncthreads();
-    const float glast = gam[kChunk - 1];
-    if (tid < kChunk) {
-      const float gi = gam[tid];
-      be[tid] = bet[tid] * __expf(gi);
-      dl[tid] = __expf(glast - gi);
-      eg[tid] = __expf(gi);
+      // gam <- log2(e) * cumsum: e^{gamma_i - gamma_j} is then one subtraction and one ex2
+      const float g0 = (sum - gb) * kLog2e, g1 = sum * kLog2e;
+      const float gl = __shfl_sync(0xffffffffu, sum, 31) * kLog2e;
+      *reinterpret_cast<float2*>(gam + 2 * lane) = make_float2(g0, g1);
+      *reinterpret_cast<float2*>(bet + 2 * lane) = make_float2(ba, bb);
+      *reinterpret_cast<float2*>(be + 2 * lane) = make_float2(ba * ex2_fast(g0), bb * ex2_fast(g1));
+      *reinterpret_cast<float2*>(dl + 2 * lane) = make_float2(ex2_fast(gl - g0), ex2_fast(gl - g1));
+      *reinterpret_cast<float2*>(eg + 2 * lane) = make_float2(prm.scale * ex2_fast(g0), prm.scale * ex2_fast(g1));
     }
 
     // ---- M1: [K;Q] K^T -> R_a
@@ -354,8 +400,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
           mma_bf16(R_a, desc_sw128(a, 16, 1024), desc_sw128(a, 16, 1024), id, s > 0);
         }
         mma_commit(bar_mma);
-        mma_pending = true;
+        ++mma_pending;
       }
+      bulk_wait_read();   // the previous chunk's o staging (region X) has been read by its TMA store
     }
     if (!wait_mma()) break;
 
@@ -371,44 +418,29 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = 32 * hf + jj;
-          v[jj] = (!upper && j < i) ? bi * __expf(gi - gam[j]) * v[jj] : 0.f;
+          v[jj] = (!upper && j < i) ? bi * ex2_fast(gi - gam[j]) * v[jj] : 0.f;
         }
         float4* dst = reinterpret_cast<float4*>(As + i * kAsLd + 32 * hf);
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       } else {
+        // P carries the output scale: OP = scale * V'^T P^T
         const int i = row - 64;
-        const float gi = gam[i];
+        const float gi = gam[i], sc = prm.scale;
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) {
           const int j = 32 * hf + jj;
-          v[jj] = (!upper && j <= i) ? __expf(gi - gam[j]) * v[jj] : 0.f;
+          v[jj] = (!upper && j <= i) ? sc * ex2_fast(gi - gam[j]) * v[jj] : 0.f;
         }
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) store8_bf16(sbase + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
       }
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- S2: solve_tril in place, then T diag(beta) and T diag(beta e^g) as bf16
-    solve64(As, tmp, tid);
-    for (int u = tid; u < 512; u += kThreads) {
-      const int i = u >> 3, cc = u & 7;
-      const float4 x0 = *reinterpret_cast<const float4*>(As + i * kAsLd + 8 * cc);
-      const float4 x1 = *reinterpret_cast<const float4*>(As + i * kAsLd + 8 * cc + 4);
-      const float t[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-      float a[8], b[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        a[q] = t[q] * bet[8 * cc + q];
-        b[q] = t[q] * be[8 * cc + q];
-      }
-      store8_bf16(sbase + OFF_TB + sw128_chunk(i, cc), a);
-      store8_bf16(sbase + OFF_TBE + sw128_chunk(i, cc), b);
-    }
-    fence_proxy_async();
-    __syncthreads();
+    // ---- S2: solve_tril in place; T diag(beta) and T diag(beta e^g) go out as bf16 operands
+    solve64(As, tmp, tid, sm + OFF_TB, sm + OFF_TBE, bet, be);
 
     // ---- M2: W^T = K^T (T diag(beta e^g))^T -> R_a ; U^T = V^T (T diag(beta))^T -> R_b
     if (tid == 0) {
@@ -428,20 +460,20 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
           mma_bf16(R_b, desc_sw128(sbase + OFF_V + s * 2048, 8192, 1024),
                    desc_sw128(sbase + OFF_TB + s * 32, 16, 1024), id, s > 0);
         mma_commit(bar_mma);
-        mma_pending = true;
+        ++mma_pending;
       }
     }
     // ---- S4 (while M2 runs): S^T -> bf16 [e][d] (K-major A), S^T *= e^{g_last}
     {
       float v[32];
-      const float dec = __expf(glast);
+      const float dec = ex2_fast(gam[kChunk - 1]);
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
         const uint32_t col = 64 * hf + 32 * half;
         tmem_ld32(R_S + lane_off + col, v);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
-          store8_bf16(sbase + OFF_ST + hf * 16384 + sw128_chunk(row, 4 * half + cc), v + 8 * cc);
+          store8_bf16(sm + OFF_ST + hf * 16384 + sw128_chunk(row, 4 * half + cc), v + 8 * cc);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= dec;
         tmem_st32(R_S + lane_off + col, v);
@@ -457,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       float v[32];
       tmem_ld32(R_a + lane_off + 32 * hf, v);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) store8_bf16(sbase + OFF_W + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+      for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_W + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -473,6 +505,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         const uint32_t a = sbase + OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
         mma_bf16(R_b, desc_sw128(a, 16, 1024), desc_sw128(sbase + OFF_W + s * 2048, 16384, 1024), idv, 1);
       }
+      mma_commit(bar_x);    // V' ready: S5 starts while Q S runs
+      ++x_pending;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const uint32_t a = sbase + OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
@@ -480,9 +514,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         mma_bf16(R_a, desc_sw128(a, 16, 1024), desc_sw128(b, 16, 1024), ido, s > 0);
       }
       mma_commit(bar_mma);
-      mma_pending = true;
+      ++mma_pending;
     }
-    if (!wait_mma()) break;
+    wait_commit(bar_x, ph_x, x_pending);
+    if (!sync_ok()) break;
 
     // ---- S5: V'^T -> bf16 [e][j] ; V''^T = V'^T diag(e^{g_last - g}) -> bf16
     {
@@ -492,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       for (int jj = 0; jj < 32; ++jj) w[jj] = v[jj] * dl[32 * hf + jj];
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
-        store8_bf16(sbase + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
-        store8_bf16(sbase + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
+        store8_bf16(sm + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+        store8_bf16(sm + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
       }
     }
     fence_proxy_async();
@@ -507,21 +542,30 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       const uint32_t ids = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma_bf16(R_b, desc_sw128(sbase + OFF_VP + s * 32, 16, 1024), desc_sw128(sbase + OFF_P + s * 32, 16, 1024),
-                 idp, s > 0);
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
         mma_bf16(R_S, desc_sw128(sbase + OFF_VPP + s * 32, 16, 1024), desc_sw128(kq + s * 2048, 16384, 1024), ids,
                  1);
-      mma_commit(bar_mma);
-      mma_pending = true;
+      mma_commit(bar_x);    // state updated: the k / q tiles are free
+      ++x_pending;
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma_bf16(R_b, desc_sw128(sbase + OFF_VP + s * 32, 16, 1024), desc_sw128(sbase + OFF_P + s * 32, 16, 1024),
+                 idp, s > 0);
+      mma_commit(bar_q);
+      ++q_pending;
     }
-    if (!wait_mma()) break;
-    if (tid == 0 && c + 1 < nchunks) issue_kq(c + 1);   // k / q tiles consumed
+    wait_commit(bar_mma, ph_mma, mma_pending);   // S^T Q^T (committed in M3)
+    wait_commit(bar_x, ph_x, x_pending);         // state update
+    if (tid == 0 && c + 1 < nchunks && !flags[1]) issue_kq(c + 1);
+    wait_commit(bar_q, ph_q, q_pending);         // V'^T P^T
+    if (!sync_ok()) break;
 
     // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
     {
-      __nv_bfloat16* os = reinterpret_cast<__nv_bfloat16*>(sm + OFF_OS);
+      // this thread holds column e = row of o for 32 rows i; neighbouring
+      // lanes exchange values so that each writes bf16 pairs (e, e + 1)
+      uint8_t* box = sm + OFF_OS + (row >> 6) * 8192;
+      const int ecol = (row & 63) & ~1;
+      const bool odd = lane & 1;
 #pragma unroll 1
       for (int q = 0; q < 2; ++q) {
         float a[16], b[16];
@@ -529,23 +573,38 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         tmem_ld16(R_a + lane_off + col, a);
         tmem_ld16(R_b + lane_off + col, b);
 #pragma unroll
-        for (int ii = 0; ii < 16; ++ii) {
-          const int i = col + ii;
-          os[i * kD + row] = __float2bfloat16_rn(prm.scale * (eg[i] * a[ii] + b[ii]));
+        for (int pp = 0; pp < 8; ++pp) {
+          const float v0 = fmaf(eg[col + 2 * pp], a[2 * pp], b[2 * pp]);
+          const float v1 = fmaf(eg[col + 2 * pp + 1], a[2 * pp + 1], b[2 * pp + 1]);
+          const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+          const int i = col + 2 * pp + (odd ? 1 : 0);
+          const uint32_t word = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
+          *reinterpret_cast<uint32_t*>(box + sw128_offset(i, ecol)) = word;
         }
       }
     }
+    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-    for (int u = tid; u < kChunk * 16; u += kThreads) {
-      const int i = u >> 4, cc = u & 15;
-      if (i < Lc) {
-        const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OS + i * 256 + cc * 16);
-        *reinterpret_cast<uint4*>(prm.o + ((t0 + i) * prm.Hv + h) * kD + cc * 8) = val;
+    if (Lc == kChunk) {
+      if (tid == 0) {
+        tma_store_3d(&tm_o, sm + OFF_OS, 0, h, (int)t0);
+        tma_store_3d(&tm_o, sm + OFF_OS + 8192, 64, h, (int)t0);
+        bulk_commit();
       }
+    } else {
+      // tail chunk: only rows of this sequence are stored
+      for (int u = tid; u < kChunk * 16; u += kThreads) {
+        const int i = u >> 4, cc = u & 15;
+        if (i < Lc) {
+          const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OS + (cc >> 3) * 8192 + sw128_chunk(i, cc & 7));
+          *reinterpret_cast<uint4*>(prm.o + ((t0 + i) * prm.Hv + h) * kD + cc * 8) = val;
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
+  if (tid == 0) bulk_wait_read();   // staging reads done before shared memory is released
 
   if (flags[1]) {
     // abort: let copies and MMAs already in flight finish (bounded) before
@@ -553,7 +612,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     if (tid == 0) {
       if (kq_pending) mbar_wait(bar_kq, ph_kq, prm.status, 100000000ull);
       if (v_pending) mbar_wait(bar_v, ph_v, prm.status, 100000000ull);
-      if (mma_pending) mbar_wait(bar_mma, ph_mma, prm.status, 100000000ull);
+      for (; mma_pending > 0; --mma_pending, ph_mma ^= 1) mbar_wait(bar_mma, ph_mma, prm.status, 100000000ull);
+      for (; x_pending > 0; --x_pending, ph_x ^= 1) mbar_wait(bar_x, ph_x, prm.status, 100000000ull);
+      for (; q_pending > 0; --q_pending, ph_q ^= 1) mbar_wait(bar_q, ph_q, prm.status, 100000000ull);
     }
   } else if (prm.ht) {
     // final state ht[d][e] = S^T[e][d]
@@ -597,7 +658,8 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
     }
     return GDN_OK;
   }
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
+  memset(&to, 0, sizeof(to));
   memset(&tq, 0, sizeof(tq));
   memset(&tk, 0, sizeof(tk));
   memset(&tv, 0, sizeof(tv));
@@ -611,6 +673,7 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
     const uint64_t dims[3] = {(uint64_t)p.V, (uint64_t)p.Hv, (uint64_t)Ttot};
     const uint64_t str[2] = {(uint64_t)p.V * 2, (uint64_t)p.Hv * p.V * 2};
     if (!make_tmap_bf16(&tv, v, 3, dims, str, box)) return GDN_ERR_CUDA;
+    if (!make_tmap_bf16(&to, o, 3, dims, str, box)) return GDN_ERR_CUDA;
   }
   FusedParams prm;
   prm.g = g;
@@ -631,7 +694,7 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
       cudaSuccess)
     return GDN_ERR_CUDA;
   const unsigned grid = (unsigned)((int64_t)p.N * p.Hv);
-  gdn_fused_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, prm);
+  gdn_fused_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 

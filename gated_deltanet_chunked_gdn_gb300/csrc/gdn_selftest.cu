@@ -89,10 +89,22 @@ __global__ void __launch_bounds__(128) umma_selftest_kernel(const __nv_bfloat16*
   if (warp == 0) tmem_dealloc(tmem, 128);
 }
 
+__global__ void exp_selftest_kernel(const float* __restrict__ x, float* __restrict__ y, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = exp_fast(x[i]);
+}
+
 }  // namespace
 }  // namespace gdn
 
 using namespace gdn;
+
+extern "C" gdn_status gdn_selftest_exp(const float* x, float* y, int n, void* stream) {
+  if (!x || !y || n < 0) return GDN_ERR_INVALID_ARG;
+  if (n == 0) return GDN_OK;
+  exp_selftest_kernel<<<(n + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, y, n);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
 
 extern "C" gdn_status gdn_selftest_umma(int variant, const void* A, const void* B, float* D, void* workspace,
                                         void* stream) {

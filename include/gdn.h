@@ -191,6 +191,14 @@ gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* p,
                                  const float* h0, const int32_t* cu_seqlens,
                                  void* o, float* ht, void* stream);
 
+/*
+ * Test hook (no counterpart on the pages): y[i] = e^{x[i]} computed the way
+ * the fused kernel computes its decay factors (2^{x log2 e} on the MUFU ex2
+ * unit), so tests can bound its error against CUDA's expf.  x, y device
+ * arrays of n floats.
+ */
+gdn_status gdn_selftest_exp(const float* x, float* y, int n, void* stream);
+
 /* Path that GDN_PATH_AUTO selects for this problem (STAGED or FUSED). */
 gdn_path gdn_resolve_path(const gdn_problem* p);
 
