@@ -46,6 +46,25 @@ def peaks() -> dict:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def measured_traffic(path: str, B: int):
+    """DRAM bytes per launch of the fused kernel from the committed ncu
+    summary (profiles/fused_traffic.json), scaled to a batch of B sequences;
+    None when the kernel source changed since that capture."""
+    import hashlib
+    if path != "fused":
+        return None
+    try:
+        with open(os.path.join(ROOT, "profiles", "fused_traffic.json")) as f:
+            rec = json.load(f)
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except (OSError, KeyError, ValueError):
+        return None
+    if sha != rec.get("source_sha256"):
+        return None
+    return rec["dram_bytes_per_bench_launch"] * B / 16
+
+
 def algorithmic(B, T, Hqk, Hv, K, V, C, elem=2, h0=True):
     """Compulsory bytes and algorithmic FLOPs of one forward pass.
 
@@ -78,7 +97,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "25"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError as e:
             self.error = str(e)
@@ -327,8 +346,9 @@ def main():
                    "l2": "inputs larger than L2 (4.4 GB compulsory traffic per step)"},
         "tflops_alg": flops / sec / 1e12,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": None, "peak_source": pk["source"],
-                     "kernel": "gdn_chunk_fwd call (all launches of one step)",
+                     "traffic": measured_traffic(path, w.B), "peak_source": pk["source"],
+                     "kernel": "gdn_fused_kernel (the step's only launch)" if path == "fused"
+                     else "gdn_chunk_fwd call (all launches of one step)",
                      "alg_bytes": nbytes, "alg_flops": flops,
                      "t_hbm_ms": 1e3 * t_hbm, "t_tensor_ms": 1e3 * t_tc},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
