@@ -23,7 +23,7 @@ DEV_OK, DEV_BAD_CU_SEQLENS, DEV_WAIT_TIMEOUT = 0, 1, 2
 STAGES = {"prepare": 0, "cumsum": 1, "kkt": 2, "solve_tril": 3, "wy_fast": 4, "chunk_h": 5, "chunk_o": 6}
 
 EXPORTED = ["gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_staged", "gdn_staged_layout",
-            "gdn_get_device_status", "gdn_resolve_path", "gdn_status_string", "gdn_version"]
+            "gdn_get_device_status", "gdn_resolve_path", "gdn_status_string", "gdn_version", "gdn_recurrent_fwd"]
 
 
 class Problem(ctypes.Structure):
@@ -81,6 +81,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdn_resolve_path.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
         lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_recurrent_fwd.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, ctypes.c_float, fp, i32p, ctypes.c_int,
+                                          i32p, vp, vp]
+        lib.gdn_recurrent_fwd.restype = ctypes.c_int
         lib.gdn_version.argtypes = []
         lib.gdn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -252,3 +255,30 @@ def chunk_gated_delta_rule(q, k, v, g, beta, scale=None, initial_state=None, out
     """Framework-style entry: (o, final_state) like the pages' integration call."""
     return gdn_chunk_fwd(q, k, v, g, beta, scale=scale, h0=initial_state, cu_seqlens=cu_seqlens, C=chunk_size,
                          output_final_state=output_final_state)
+
+
+def gdn_recurrent_fwd(q, k, v, a, b, A_log, state, dt_bias=None, scale: Optional[float] = None,
+                      state_indices=None, cu_seqlens=None, o=None, stream=None):
+    """Fused gated recurrent (decode) step.  ``state`` [slots, Hv, K, V] fp32 is
+    updated in place; returns o.  g = -exp(A_log) softplus(a + dt_bias),
+    beta = sigmoid(b), then the gated delta rule token by token."""
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("a", a), ("b", b), ("A_log", A_log), ("state", state),
+                    ("dt_bias", dt_bias), ("state_indices", state_indices), ("cu_seqlens", cu_seqlens)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    for name, t in (("a", a), ("b", b), ("A_log", A_log), ("state", state), ("dt_bias", dt_bias)):
+        if t is not None and t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
+    p = problem_of(q, v, 64, cu_seqlens)
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    if o is None:
+        o = torch.empty_like(v)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    st = lib.gdn_recurrent_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log),
+                               _ptr(dt_bias), ctypes.c_float(scale), _ptr(state), _ptr(state_indices),
+                               int(state.shape[0]), _ptr(cu_seqlens), _ptr(o), ctypes.c_void_p(s))
+    if st:
+        raise GDNError(st, "gdn_recurrent_fwd")
+    return o

@@ -140,6 +140,27 @@ gdn_status gdn_get_device_status(const gdn_problem* pp, gdn_path path, void* wor
   return GDN_OK;
 }
 
+gdn_status gdn_recurrent_fwd(const gdn_problem* pp, const void* q, const void* k, const void* v, const float* a,
+                             const float* b, const float* A_log, const float* dt_bias, float scale, float* state,
+                             const int32_t* state_indices, int state_slots, const int32_t* cu_seqlens, void* o,
+                             void* stream) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
+  if (p.V % 64 != 0 || state_slots <= 0 || !state || !A_log) return GDN_ERR_INVALID_ARG;
+  if (!state_indices && state_slots < p.N) return GDN_ERR_INVALID_ARG;
+  const bool any_tokens = (int64_t)p.B * p.T > 0;
+  if (any_tokens && (!q || !k || !v || !a || !b || !o)) return GDN_ERR_INVALID_ARG;
+  if (p.varlen != (cu_seqlens != nullptr)) return GDN_ERR_INVALID_ARG;
+  const void* a16[] = {q, k, v, o, state};
+  for (const void* x : a16)
+    if (x && !aligned(x, 16)) return GDN_ERR_INVALID_ARG;
+  const void* a4[] = {a, b, A_log, dt_bias, state_indices, cu_seqlens};
+  for (const void* x : a4)
+    if (x && !aligned(x, 4)) return GDN_ERR_INVALID_ARG;
+  return run_recurrent(p, q, k, v, a, b, A_log, dt_bias, scale, state, state_indices, state_slots, cu_seqlens, o,
+                       static_cast<cudaStream_t>(stream));
+}
+
 const char* gdn_status_string(gdn_status s) {
   switch (s) {
     case GDN_OK: return "ok";

@@ -66,6 +66,12 @@ gdn_status run_staged(const gdn_problem& p, int stop_after, const void* q, const
                       const float* g, const float* beta, float scale, const float* h0, const int32_t* cu,
                       void* o, float* ht, void* ws, cudaStream_t s);
 
+// Fused recurrent (decode) step (gdn_decode.cu).
+gdn_status run_recurrent(const gdn_problem& p, const void* q, const void* k, const void* v, const float* a,
+                         const float* b, const float* A_log, const float* dt_bias, float scale, float* state,
+                         const int32_t* state_indices, int state_slots, const int32_t* cu, void* o,
+                         cudaStream_t s);
+
 // Fused path (gdn_fused.cu).
 bool fused_supported(const gdn_problem& p);
 size_t fused_workspace_bytes(const gdn_problem& p);

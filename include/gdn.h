@@ -192,6 +192,34 @@ gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* p,
                                  void* o, float* ht, void* stream);
 
 /*
+ * Fused recurrent (decode) step with sigmoid gating (TileLang x xLLM page,
+ * fused_sigmoid_gating_delta_rule: the decode-phase operator that fuses the
+ * sigmoid activation, the gate computation from the decay rate A_log and the
+ * delta-rule update of the fp32 state, with per-sequence state offsets).
+ * For every token t of every sequence, value head h:
+ *     g_t    = -exp(A_log[h]) * softplus(a_t + dt_bias[h])
+ *     beta_t = sigmoid(b_t)
+ *     S <- e^{g_t} (I - beta_t k_t k_t^T) S + beta_t k_t v_t^T,   o_t = scale * S^T q_t
+ * Tokens of a sequence are processed in order (one token per sequence is the
+ * decode case; several run the plain recurrence).
+ *   p           : as for gdn_chunk_fwd (C is ignored; V a multiple of 64)
+ *   q, k        : [B, T, Hqk, K];  v : [B, T, Hv, V];  o : out [B, T, Hv, V]  (dtype p->dt)
+ *   a, b        : [B, T, Hv] fp32 gate and beta pre-activations
+ *   A_log       : [Hv] fp32;  dt_bias : [Hv] fp32 or NULL (= 0)
+ *   state       : [state_slots, Hv, K, V] fp32 pool, read and updated in place
+ *   state_indices : [N] int32 slot of each sequence, or NULL (slot n); a
+ *                 sequence whose slot is negative or >= state_slots gets zero
+ *                 outputs and no state update
+ *   cu_seqlens  : [N + 1] int32 or NULL, as for gdn_chunk_fwd; sequences whose
+ *                 offsets fall outside [0, T] are skipped
+ * No workspace; asynchronous on `stream`.
+ */
+gdn_status gdn_recurrent_fwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                             const float* a, const float* b, const float* A_log, const float* dt_bias,
+                             float scale, float* state, const int32_t* state_indices, int state_slots,
+                             const int32_t* cu_seqlens, void* o, void* stream);
+
+/*
  * Test hook (no counterpart on the pages): y[i] = e^{x[i]} computed the way
  * the fused kernel computes its decay factors (2^{x log2 e} on the MUFU ex2
  * unit), so tests can bound its error against CUDA's expf.  x, y device

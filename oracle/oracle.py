@@ -189,3 +189,35 @@ def chunked_stages(q, k, v, g, beta, scale, C, n, h, h0=None, cu_seqlens=None):
         raise RuntimeError(f"oracle_chunked_stages failed: {rc}")
     out["o"], out["ht"] = o, ht
     return out
+
+
+def gated_recurrent(q, k, v, a, b, A_log, dt_bias, scale, state, state_indices=None, cu_seqlens=None):
+    """Decode-phase gated delta rule (the fused sigmoid-gating recurrent step of
+    the TileLang x xLLM page): per token and value head
+        g = -exp(A_log[h]) * softplus(a + dt_bias[h]),  beta = sigmoid(b),
+    then the token recurrence from each sequence's slot of ``state``
+    ([slots, Hv, K, V]).  Sequences whose slot is negative or out of range get
+    zero outputs and leave the state untouched.  Returns (o, new_state), fp64.
+    """
+    a64, b64, A64 = _f64(a), _f64(b), _f64(A_log)
+    d64 = _f64(dt_bias) if dt_bias is not None else np.zeros_like(A64)
+    st = _f64(state)
+    x = a64 + d64[None, None, :]
+    g = -np.exp(A64)[None, None, :] * np.logaddexp(0.0, x)      # softplus(x) = log(1 + e^x)
+    beta = 1.0 / (1.0 + np.exp(-b64))                            # sigmoid
+    Bq = _f64(q).shape[0]
+    N = (len(_i64(cu_seqlens)) - 1) if cu_seqlens is not None else Bq
+    slots = _i64(state_indices) if state_indices is not None else np.arange(N)
+    valid = (slots >= 0) & (slots < st.shape[0])
+    h0 = np.zeros((N,) + st.shape[1:])
+    h0[valid] = st[slots[valid]]
+    o, ht = recurrent(q, k, v, g, beta, scale, h0=h0, cu_seqlens=cu_seqlens)
+    new_state = st.copy()
+    new_state[slots[valid]] = ht[valid]
+    cu = _i64(cu_seqlens) if cu_seqlens is not None else None
+    for n in np.nonzero(~valid)[0]:
+        if cu is None:
+            o[n] = 0.0
+        else:
+            o[0, cu[n]:cu[n + 1]] = 0.0
+    return o, new_state

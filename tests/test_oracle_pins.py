@@ -292,3 +292,50 @@ def test_stage_intermediates(oracle_mod):
             np.testing.assert_array_equal(st["S0"][0], h0[0, 1])
     tail = T - (NT - 1) * C
     assert np.all(st["W"][-1, tail:] == 0) and np.all(st["Vn"][-1, tail:] == 0)
+
+
+# -------------------------------------------------------- decode (gated) step
+
+def test_gated_decode_hand_example(oracle_mod):
+    case = json.load(open(GOLDEN))["decode_cases"][0]
+    K, V = case["K"], case["V"]
+    q = np.array(case["q"]).reshape(1, 1, 1, K)
+    k = np.array(case["k"]).reshape(1, 1, 1, K)
+    v = np.array(case["v"]).reshape(1, 1, 1, V)
+    a = np.array(case["a"]).reshape(1, 1, 1)
+    b = np.array(case["b"]).reshape(1, 1, 1)
+    st = np.array(case["state"]).reshape(1, 1, K, V)
+    o, new = oracle_mod.gated_recurrent(q, k, v, a, b, np.array(case["A_log"]), np.array(case["dt_bias"]),
+                                        case["scale"], st)
+    np.testing.assert_allclose(o.reshape(V), np.array(case["o"]).reshape(V), atol=1e-12, rtol=0)
+    np.testing.assert_allclose(new.reshape(K, V), np.array(case["new_state"]), atol=1e-12, rtol=0)
+
+
+def test_gated_decode_continues_prefill(oracle_mod):
+    """Prefill of T tokens (chunked form) followed by one gated decode step on
+    the resulting state equals the recurrence over T + 1 tokens whose last
+    gate / beta come from the gating formula; state slots are honoured and an
+    out-of-range slot leaves its state untouched with zero output."""
+    rng = np.random.default_rng(41)
+    T, K, V, Hv = 40, 8, 6, 2
+    q, k, v, g, beta, _ = rand_inputs(rng, 3, T + 1, 1, Hv, K, V, h0=False)
+    a = rng.standard_normal((3, 1, Hv))
+    b = rng.standard_normal((3, 1, Hv))
+    A_log = rng.standard_normal(Hv) * 0.5
+    dt_bias = rng.standard_normal(Hv) * 0.1
+    _, ht = oracle_mod.chunked(q[:, :T], k[:, :T], v[:, :T], g[:, :T], beta[:, :T], 0.3, 16)
+    pool = rng.standard_normal((5, Hv, K, V))
+    slots = np.array([4, 1, 7])            # sequence 2 has no slot
+    pool[4], pool[1] = ht[0], ht[1]
+    o1, new = oracle_mod.gated_recurrent(q[:, T:], k[:, T:], v[:, T:], a, b, A_log, dt_bias, 0.3, pool,
+                                         state_indices=slots)
+    g_last = -np.exp(A_log)[None, None, :] * np.logaddexp(0.0, a + dt_bias[None, None, :])
+    beta_last = 1.0 / (1.0 + np.exp(-b))
+    g_full = np.concatenate([g[:, :T], g_last], axis=1)
+    b_full = np.concatenate([beta[:, :T], beta_last], axis=1)
+    o_ref, ht_ref = oracle_mod.recurrent(q, k, v, g_full, b_full, 0.3)
+    assert rel_fro(o1[:2], o_ref[:2, T:]) < TOL
+    assert rel_fro(new[4], ht_ref[0]) < TOL and rel_fro(new[1], ht_ref[1]) < TOL
+    assert np.all(o1[2] == 0.0)
+    untouched = [0, 2, 3]
+    np.testing.assert_array_equal(new[untouched], pool[untouched])
