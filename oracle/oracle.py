@@ -221,3 +221,61 @@ def gated_recurrent(q, k, v, a, b, A_log, dt_bias, scale, state, state_indices=N
         else:
             o[0, cu[n]:cu[n + 1]] = 0.0
     return o, new_state
+
+
+def causal_conv1d(x, weight, bias=None, activation="silu", conv_state=None, cache_indices=None,
+                  has_initial_state=None, cu_seqlens=None):
+    """Causal depthwise 1-D convolution with a carried convolution state (the
+    causal_conv1d operator of the TileLang x xLLM page: each output token
+    depends on the current and earlier tokens of its own sequence only; the
+    last W-1 inputs are kept per sequence in ``conv_state`` for incremental
+    decode; ``cache_indices`` picks each sequence's slot of the state pool).
+
+    Shapes: x ``[B, T, D]`` (packed with ``cu_seqlens`` when B == 1),
+    weight ``[D, W]``, bias ``[D]`` or None, conv_state ``[slots, W-1, D]``.
+    For a sequence with inputs x_0..x_{L-1}, prepend its W-1 initial inputs
+    (the slot's state when the sequence has one, zeros otherwise) to get
+    ext_0..ext_{L+W-2}; then
+
+        y_p[d] = act(bias[d] + sum_{w<W} weight[d, w] ext_{p+w}[d]),
+        new state = ext_L .. ext_{L+W-2}   (the last W-1 inputs),
+
+    with act = identity or SiLU (u * sigmoid(u)).  A sequence whose slot is
+    negative has no state: zeros are prepended and no state is written.
+    ``has_initial_state[n] == 0`` prepends zeros but still writes the slot.
+    Returns (y fp64 [B, T, D], new conv_state fp64 or None).
+    """
+    xs, w = _f64(x), _f64(weight)
+    B, T, D = xs.shape
+    W = w.shape[1]
+    b = _f64(bias) if bias is not None else np.zeros(D)
+    if cu_seqlens is None:
+        seqs = [(n, 0, T) for n in range(B)]
+    else:
+        if B != 1:
+            raise ValueError("cu_seqlens requires B == 1")
+        cu = _i64(cu_seqlens)
+        seqs = [(0, int(cu[n]), int(cu[n + 1])) for n in range(len(cu) - 1)]
+    st = _f64(conv_state) if conv_state is not None else None
+    new_state = st.copy() if st is not None else None
+    slots = _i64(cache_indices) if cache_indices is not None else np.arange(len(seqs))
+    init_flag = _i64(has_initial_state) if has_initial_state is not None else np.ones(len(seqs), dtype=np.int64)
+    y = np.zeros_like(xs)
+    for n, (bi, s, e) in enumerate(seqs):
+        L = e - s
+        slot = int(slots[n]) if st is not None else -1
+        init = np.zeros((W - 1, D))
+        if slot >= 0 and init_flag[n] != 0:
+            init = st[slot]
+        ext = np.concatenate([init, xs[bi, s:e]], axis=0)
+        acc = np.tile(b, (L, 1))
+        for j in range(W):
+            acc += w[:, j][None, :] * ext[j:j + L]
+        if activation == "silu":
+            acc = acc / (1.0 + np.exp(-acc))
+        elif activation not in (None, "none"):
+            raise ValueError(activation)
+        y[bi, s:e] = acc
+        if slot >= 0:
+            new_state[slot] = ext[L:L + W - 1]
+    return y, new_state
