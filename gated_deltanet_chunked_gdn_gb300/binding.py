@@ -23,7 +23,8 @@ DEV_OK, DEV_BAD_CU_SEQLENS, DEV_WAIT_TIMEOUT = 0, 1, 2
 STAGES = {"prepare": 0, "cumsum": 1, "kkt": 2, "solve_tril": 3, "wy_fast": 4, "chunk_h": 5, "chunk_o": 6}
 
 EXPORTED = ["gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_staged", "gdn_staged_layout",
-            "gdn_get_device_status", "gdn_resolve_path", "gdn_status_string", "gdn_version", "gdn_recurrent_fwd"]
+            "gdn_get_device_status", "gdn_resolve_path", "gdn_status_string", "gdn_version", "gdn_recurrent_fwd",
+            "gdn_causal_conv1d_fwd"]
 
 
 class Problem(ctypes.Structure):
@@ -84,6 +85,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdn_recurrent_fwd.argtypes = [P, vp, vp, vp, fp, fp, fp, fp, ctypes.c_float, fp, i32p, ctypes.c_int,
                                           i32p, vp, vp]
         lib.gdn_recurrent_fwd.restype = ctypes.c_int
+        lib.gdn_causal_conv1d_fwd.argtypes = [vp, fp, fp, ctypes.c_int, vp, ctypes.c_int, i32p, i32p, i32p,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, vp, vp]
+        lib.gdn_causal_conv1d_fwd.restype = ctypes.c_int
         lib.gdn_version.argtypes = []
         lib.gdn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -282,3 +287,45 @@ def gdn_recurrent_fwd(q, k, v, a, b, A_log, state, dt_bias=None, scale: Optional
     if st:
         raise GDNError(st, "gdn_recurrent_fwd")
     return o
+
+
+ACTIVATIONS = {None: 0, "none": 0, "silu": 1}
+DTYPES = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}
+
+
+def gdn_causal_conv1d_fwd(x, weight, bias=None, activation="silu", conv_state=None, cache_indices=None,
+                          has_initial_state=None, cu_seqlens=None, y=None, stream=None):
+    """Causal depthwise convolution with a carried state.  x [B, T, D] (bf16
+    or fp32; packed with cu_seqlens when B == 1), weight [D, W] fp32, bias [D]
+    fp32.  ``conv_state`` [slots, W-1, D] (dtype of x) is read and then
+    updated in place; returns y (shape and dtype of x)."""
+    lib = load()
+    for name, t in (("x", x), ("weight", weight), ("bias", bias), ("conv_state", conv_state),
+                    ("cache_indices", cache_indices), ("has_initial_state", has_initial_state),
+                    ("cu_seqlens", cu_seqlens)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    for name, t in (("weight", weight), ("bias", bias)):
+        if t is not None and t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
+    for name, t in (("cache_indices", cache_indices), ("has_initial_state", has_initial_state),
+                    ("cu_seqlens", cu_seqlens)):
+        if t is not None and t.dtype != torch.int32:
+            raise ValueError(f"{name} must be int32")
+    if x.dtype not in DTYPES:
+        raise ValueError("x must be float32 or bfloat16")
+    if conv_state is not None and conv_state.dtype != x.dtype:
+        raise ValueError("conv_state must have the dtype of x")
+    B, T, D = x.shape
+    W = int(weight.shape[1])
+    N = int(cu_seqlens.numel()) - 1 if cu_seqlens is not None else B
+    if y is None:
+        y = torch.empty_like(x)
+    slots = int(conv_state.shape[0]) if conv_state is not None else 0
+    s = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+    st = lib.gdn_causal_conv1d_fwd(_ptr(x), _ptr(weight), _ptr(bias), W, _ptr(conv_state), slots,
+                                   _ptr(cache_indices), _ptr(has_initial_state), _ptr(cu_seqlens), N, B, T, D,
+                                   DTYPES[x.dtype], ACTIVATIONS[activation], _ptr(y), ctypes.c_void_p(s))
+    if st:
+        raise GDNError(st, "gdn_causal_conv1d_fwd")
+    return y

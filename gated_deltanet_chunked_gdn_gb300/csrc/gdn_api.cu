@@ -161,6 +161,27 @@ gdn_status gdn_recurrent_fwd(const gdn_problem* pp, const void* q, const void* k
                        static_cast<cudaStream_t>(stream));
 }
 
+gdn_status gdn_causal_conv1d_fwd(const void* x, const float* weight, const float* bias, int W, void* conv_state,
+                                 int state_slots, const int32_t* cache_indices, const int32_t* has_initial_state,
+                                 const int32_t* cu_seqlens, int N, int B, int T, int D, gdn_dtype dt,
+                                 gdn_activation act, void* y, void* stream) {
+  if (W < 1 || W > 4 || D <= 0 || D % 8 != 0 || B < 0 || T < 0 || N < 0) return GDN_ERR_INVALID_ARG;
+  if (dt != GDN_F32 && dt != GDN_BF16) return GDN_ERR_INVALID_ARG;
+  if (act != GDN_ACT_NONE && act != GDN_ACT_SILU) return GDN_ERR_INVALID_ARG;
+  if (cu_seqlens ? B != 1 : N != B) return GDN_ERR_INVALID_ARG;
+  if ((int64_t)B * T > 0 && (!x || !y)) return GDN_ERR_INVALID_ARG;
+  if (!weight) return GDN_ERR_INVALID_ARG;
+  if (W > 1 && conv_state && (state_slots <= 0 || (!cache_indices && state_slots < N))) return GDN_ERR_INVALID_ARG;
+  const void* a16[] = {x, y, W > 1 ? conv_state : nullptr};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return GDN_ERR_INVALID_ARG;
+  const void* a4[] = {weight, bias, cache_indices, has_initial_state, cu_seqlens};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return GDN_ERR_INVALID_ARG;
+  return run_causal_conv1d(x, weight, bias, W, conv_state, state_slots, cache_indices, has_initial_state, cu_seqlens,
+                           N, B, T, D, dt, act == GDN_ACT_SILU, y, static_cast<cudaStream_t>(stream));
+}
+
 const char* gdn_status_string(gdn_status s) {
   switch (s) {
     case GDN_OK: return "ok";

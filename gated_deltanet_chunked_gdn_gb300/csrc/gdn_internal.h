@@ -67,6 +67,11 @@ gdn_status run_staged(const gdn_problem& p, int stop_after, const void* q, const
                       void* o, float* ht, void* ws, cudaStream_t s);
 
 // Fused recurrent (decode) step (gdn_decode.cu).
+gdn_status run_causal_conv1d(const void* x, const float* weight, const float* bias, int W, void* conv_state,
+                             int state_slots, const int32_t* cache_indices, const int32_t* has_initial_state,
+                             const int32_t* cu_seqlens, int N, int B, int T, int D, gdn_dtype dt, bool silu_act,
+                             void* y, cudaStream_t s);
+
 gdn_status run_recurrent(const gdn_problem& p, const void* q, const void* k, const void* v, const float* a,
                          const float* b, const float* A_log, const float* dt_bias, float scale, float* state,
                          const int32_t* state_indices, int state_slots, const int32_t* cu, void* o,

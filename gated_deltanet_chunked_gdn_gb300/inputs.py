@@ -124,3 +124,35 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu", lengths: Option
         "cu_seqlens": cu.to(device) if cu is not None else None,
         "scale": w.K ** -0.5, "C": w.C, "N": N,
     }
+
+
+def conv_channels(Hqk: int, Hv: int, K: int, V: int) -> int:
+    """Channels of the convolution in front of a GDN layer: the q, k and v
+    projections side by side (2 Hqk K + Hv V)."""
+    return 2 * Hqk * K + Hv * V
+
+
+def make_conv_inputs(B: int, T: int, D: int, W: int, dtype: str, device="cpu", seed: int = 0,
+                     lengths: Optional[list[int]] = None, slots: Optional[int] = None) -> dict:
+    """Inputs of the causal convolution with a carried state: x ~ N(0, 1)
+    [B, T, D] (or packed [1, sum(lengths), D] with cu_seqlens), weight ~
+    N(0, 1/W) [D, W] fp32, bias ~ N(0, 0.1) [D] fp32, conv_state ~ N(0, 1)
+    [slots, W-1, D] (slots defaults to the number of sequences), x and the
+    state rounded to ``dtype``."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device).manual_seed(seed)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    cu = None
+    if lengths is not None:
+        B, T, N = 1, int(sum(lengths)), len(lengths)
+        cu = torch.zeros(N + 1, dtype=torch.int32)
+        cu[1:] = torch.cumsum(torch.tensor(lengths, dtype=torch.int64), 0).to(torch.int32)
+    else:
+        N = B
+    S = N if slots is None else slots
+    x = _normal((B, T, D), gen, device).to(dt)
+    weight = _normal((D, W), gen, device, std=W ** -0.5)
+    bias = _normal((D,), gen, device, std=0.1)
+    state = _normal((S, max(W - 1, 0), D), gen, device).to(dt)
+    return {"x": x.contiguous(), "weight": weight.contiguous(), "bias": bias.contiguous(),
+            "conv_state": state.contiguous(), "cu_seqlens": cu.to(device) if cu is not None else None, "N": N}

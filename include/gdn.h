@@ -219,6 +219,49 @@ gdn_status gdn_recurrent_fwd(const gdn_problem* p, const void* q, const void* k,
                              float scale, float* state, const int32_t* state_indices, int state_slots,
                              const int32_t* cu_seqlens, void* o, void* stream);
 
+/* Activation applied after the convolution of gdn_causal_conv1d_fwd. */
+typedef enum { GDN_ACT_NONE = 0, GDN_ACT_SILU = 1 } gdn_activation;
+
+/*
+ * Causal depthwise convolution with a carried state (TileLang x xLLM page,
+ * causal_conv1d: each output token depends on the current and earlier inputs
+ * of its own sequence only; the convolution state keeps the last W-1 inputs of
+ * every sequence for incremental decode, in the state-pool slot that
+ * cache_indices gives it).  For a sequence with inputs x_0..x_{L-1}, let
+ * ext = [the W-1 initial inputs ; x_0 .. x_{L-1}]; then for every channel d
+ *     y_p[d]    = act(bias[d] + sum_{w<W} weight[d*W + w] * ext_{p+w}[d])
+ *     new state = ext_L .. ext_{L+W-2}
+ * so weight[d*W + W-1] multiplies the current token.  act is the identity or
+ * SiLU, u * sigmoid(u).  The initial inputs are the slot's state, or zeros
+ * when the sequence has no slot or has_initial_state[n] == 0.
+ *   x, y        : [B, T, D] of dtype dt, 16-byte aligned, D % 8 == 0; with
+ *                 cu_seqlens, B == 1 and T is the packed total.  y must not
+ *                 overlap x or conv_state.
+ *   weight      : [D, W] fp32, 1 <= W <= 4;  bias : [D] fp32 or NULL (= 0)
+ *   conv_state  : [state_slots, W-1, D] of dtype dt (16-byte aligned), or NULL
+ *                 (zero initial inputs, nothing kept).  Read by the
+ *                 convolution, then rewritten in place with the new state.
+ *                 Ignored when W == 1.
+ *   cache_indices : [N] int32 slot per sequence, or NULL (slot n; then
+ *                 state_slots >= N).  A slot outside [0, state_slots) means
+ *                 "no state": zero initial inputs, nothing written.  Distinct
+ *                 sequences must use distinct slots.
+ *   has_initial_state : [N] int32 or NULL (all 1); 0 starts the sequence from
+ *                 zeros but still writes its slot.
+ *   cu_seqlens  : [N + 1] int32 or NULL (then N == B and sequence n is row n
+ *                 of x).  A sequence whose offsets fall outside [0, T] or
+ *                 decrease is skipped (outputs and state); tokens that no
+ *                 well-formed sequence covers are not written.
+ * States are exact copies of inputs.  Two launches (convolution, then state
+ * update), asynchronous on `stream`; no workspace.  Returns
+ * GDN_ERR_INVALID_ARG for a failed host-side check (nothing launched).
+ */
+gdn_status gdn_causal_conv1d_fwd(const void* x, const float* weight, const float* bias, int W,
+                                 void* conv_state, int state_slots, const int32_t* cache_indices,
+                                 const int32_t* has_initial_state, const int32_t* cu_seqlens, int N,
+                                 int B, int T, int D, gdn_dtype dt, gdn_activation act, void* y,
+                                 void* stream);
+
 /*
  * Test hook (no counterpart on the pages): y[i] = e^{x[i]} computed the way
  * the fused kernel computes its decay factors (2^{x log2 e} on the MUFU ex2

@@ -109,3 +109,28 @@ def test_fused_path_reports_unsupported_problems():
     assert b.gdn_chunk_fwd_workspace_size(p, "fused") == 0
     assert b.gdn_resolve_path(p) == "staged"
     assert call(p, path=2) == b.GDN_ERR_UNSUPPORTED
+
+
+def conv_call(x=1 << 12, weight=2 << 12, bias=0, W=4, state=3 << 12, slots=2, idx=0, init=0, cu=0, N=2, B=2, T=16,
+              D=64, dt=1, act=1, y=4 << 12):
+    """gdn_causal_conv1d_fwd with fake (never dereferenced) device addresses;
+    every case below must fail host validation before any CUDA call."""
+    lib = b.load()
+    v = ctypes.c_void_p
+    return lib.gdn_causal_conv1d_fwd(v(x), v(weight), v(bias), W, v(state), slots, v(idx), v(init), v(cu), N, B, T,
+                                     D, dt, act, v(y), v(0))
+
+
+def test_conv1d_rejects_bad_arguments():
+    bad = b.GDN_ERR_INVALID_ARG
+    assert conv_call(D=12) == bad                    # channels must come in 16-byte vectors of bf16
+    assert conv_call(W=0) == bad and conv_call(W=5) == bad
+    assert conv_call(weight=0) == bad
+    assert conv_call(x=0) == bad and conv_call(y=0) == bad
+    assert conv_call(x=(1 << 12) + 8) == bad         # 16-byte alignment
+    assert conv_call(state=(3 << 12) + 4) == bad
+    assert conv_call(bias=(5 << 12) + 2) == bad
+    assert conv_call(slots=1) == bad                 # identity slot map needs a slot per sequence
+    assert conv_call(N=3) == bad                     # fixed length: N == B
+    assert conv_call(cu=6 << 12, B=2) == bad         # packed batches have B == 1
+    assert conv_call(dt=7) == bad and conv_call(act=2) == bad
