@@ -203,6 +203,41 @@ def test_fused_parity(gdn, oracle_mod, name):
     assert rel_fro(ht, ht_ref) <= TOL["bf16"], rel_fro(ht, ht_ref)
 
 
+def _gate_pattern(kind, B, T, H, gen):
+    """Per-token log-decays g (<= 0) that put the fused kernel's gating into
+    each of its regimes: a 32-row block whose exponents span little (row x
+    column factors), one that spans a lot (an exponential per element), and
+    a mix of the two inside one chunk."""
+    r = torch.arange(T) % 64
+    if kind == "strong":
+        return -(1.0 + 5.0 * torch.rand(B, T, H, generator=gen))
+    if kind == "weak_then_strong":
+        return torch.where((r < 32)[None, :, None], -0.02 * torch.ones(B, T, H), -3.0 * torch.ones(B, T, H))
+    if kind == "strong_then_weak":
+        return torch.where((r < 32)[None, :, None], -3.0 * torch.ones(B, T, H), -0.02 * torch.ones(B, T, H))
+    if kind == "no_decay":
+        return torch.zeros(B, T, H)
+    if kind == "near_span_limit":
+        # about 60 binary orders of magnitude across each 32-row block
+        return -(1.3 + 0.1 * torch.rand(B, T, H, generator=gen))
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("kind", ["strong", "weak_then_strong", "strong_then_weak", "no_decay", "near_span_limit"])
+def test_fused_gate_regimes(gdn, oracle_mod, kind):
+    w = I.WORKLOADS[2].with_(B=2, T=200, Hqk=2, Hv=2, C=64)
+    x = I.make_inputs(w, "cpu")
+    x["g"] = _gate_pattern(kind, w.B, w.T, w.Hv, torch.Generator().manual_seed(7)).float().contiguous()
+    d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
+    o, ht = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"], C=64,
+                              path="fused")
+    o_ref, ht_ref = oracle_mod.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"])
+    o, ht = o.float().cpu().numpy(), ht.cpu().numpy()
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(ht))
+    assert rel_fro(o, o_ref) <= TOL["bf16"], rel_fro(o, o_ref)
+    assert rel_fro(ht, ht_ref) <= TOL["bf16"], rel_fro(ht, ht_ref)
+
+
 def test_fused_leaves_rows_of_other_sequences_untouched(gdn):
     """A tail chunk's padding rows belong to the next sequence: the fused
     kernel must not store them.  Sequence 1 is empty-output-checked by giving
