@@ -223,6 +223,152 @@ def run_reference(args, rank: int, world: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def timed(step, steps, world, dev, stream):
+    """Time `steps` calls of step() with CUDA events on `stream`, clocks
+    sampled meanwhile; returns (seconds over all steps, max over ranks, clocks)."""
+    import torch
+    import torch.distributed as dist
+    sampler = ClockSampler(gpu_uuid(dev.index or 0))
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    return ev0.elapsed_time(ev1) / 1000.0, sampler.summary(t_wall0, t_wall1)
+
+
+def hbm_roofline(nbytes: float, sec_per_launch: float, kernel: str, traffic=None) -> dict:
+    pk = peaks()
+    achieved = nbytes / sec_per_launch / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk["source"], "kernel": kernel,
+            "alg_bytes": nbytes, "t_hbm_ms": 1e3 * nbytes / (pk["hbm_gbs"] * 1e9)}
+
+
+def run_conv1d(args, rank, world, dev):
+    """Causal conv1d in front of a 32-head GDN layer: 16 x 8192 tokens,
+    D = 2*32*128 + 32*128 channels, W = 4, SiLU, bf16, a 16-slot state pool.
+    One step = one gdn_causal_conv1d_fwd call (convolution + state update)."""
+    import torch
+    from gated_deltanet_chunked_gdn_gb300 import binding
+    from gated_deltanet_chunked_gdn_gb300 import inputs as I
+    B, T, W = args.B, 8192, 4
+    D = I.conv_channels(32, 32, 128, 128)
+    d = I.make_conv_inputs(B, T, D, W, "bf16", device=dev, seed=2 + rank)
+    y = torch.empty_like(d["x"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x=d["x"]):
+        binding.gdn_causal_conv1d_fwd(x, d["weight"], d["bias"], "silu", conv_state=d["conv_state"], y=y,
+                                      stream=stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sec, clocks = timed(step, args.steps, world, dev, stream)
+    value, sec_total = aggregate(sec, B * T, args.steps, world, dev)
+    sec_step = sec_total / args.steps
+    nbytes = 2 * (B * T * D * 2) + D * W * 4 + D * 4 + 2 * B * (W - 1) * D * 2
+    x_host = d["x"].cpu().pin_memory()
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    x_dev = torch.empty_like(d["x"])
+
+    def e2e_step():
+        x_dev.copy_(x_host, non_blocking=True)
+        step(x_dev)
+        y_host.copy_(y, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_value, _ = aggregate(time.perf_counter() - t0, B * T, args.e2e_steps, world, dev)
+    line = {
+        "metric": "causal conv1d tokens/s (16x8192, D=12288, W=4, SiLU, bf16); % roofline", "value": value,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"conv1d_{B}x{T}_D{D}_W{W}", "B": B, "T": T, "D": D, "W": W, "activation": "silu",
+                   "parallelism": f"dp{world} (independent batches)",
+                   "l2": f"inputs larger than L2 ({nbytes / 1e9:.1f} GB compulsory traffic per step)"},
+        "roofline": hbm_roofline(nbytes, sec_step, "conv1d_kernel + conv1d_state_kernel (one step)"),
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x_host.numel() * 2,
+                "d2h_bytes_per_step": y_host.numel() * 2, "steps": args.e2e_steps},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import oracle as O
+        xs, ws_, bs_, st_ = d["x"][0].cpu(), d["weight"].cpu(), d["bias"].cpu(), d["conv_state"][:1].cpu()
+        Ds, done, t0 = 512, 0, time.perf_counter()
+        while time.perf_counter() - t0 < args.cpu_seconds:
+            c = (done * Ds) % D
+            O.causal_conv1d(xs[None, :, c:c + Ds], ws_[c:c + Ds], bs_[c:c + Ds], "silu", conv_state=st_[:, :, c:c + Ds])
+            done += 1
+        el = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": done * T * Ds / D / el, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{done} blocks of {T} tokens x {Ds} channels of sequence 0"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_decode(args, rank, world, dev):
+    """Gated decode step: 512 sequences x 1 token, Hqk = Hv = 32, K = V = 128,
+    bf16 q/k/v/o, fp32 state pool (2 GB read + written per step, larger than
+    L2).  One step = one gdn_recurrent_fwd call."""
+    import torch
+    from gated_deltanet_chunked_gdn_gb300 import binding
+    N, H, K = 512, 32, 128
+    gen = torch.Generator(device=dev).manual_seed(2 + rank)
+    rn = lambda *s_, dt=torch.float32: torch.randn(*s_, generator=gen, device=dev, dtype=torch.float32).to(dt)
+    q = torch.nn.functional.normalize(rn(N, 1, H, K), dim=-1).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(rn(N, 1, H, K), dim=-1).to(torch.bfloat16)
+    v = rn(N, 1, H, K, dt=torch.bfloat16)
+    a, b_ = rn(N, 1, H), rn(N, 1, H)
+    A_log, dt_bias = rn(H) * 0.5, rn(H) * 0.1
+    state = rn(N, H, K, K) * 0.1
+    o = torch.empty_like(v)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.gdn_recurrent_fwd(q, k, v, a, b_, A_log, state, dt_bias=dt_bias, o=o, stream=stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sec, clocks = timed(step, args.steps, world, dev, stream)
+    value, sec_total = aggregate(sec, N, args.steps, world, dev)
+    sec_step = sec_total / args.steps
+    nbytes = 2 * N * H * K * K * 4 + 4 * N * H * K * 2 + 2 * N * H * 4 + 2 * H * 4
+    line = {
+        "metric": "gated decode step tokens/s (512 seqs x 1 token, H=32, K=V=128, fp32 state); % roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode_{N}x1_H{H}", "N": N, "H": H, "K": K, "V": K,
+                   "parallelism": f"dp{world} (independent batches)",
+                   "l2": f"state pool larger than L2 ({nbytes / 1e9:.2f} GB per step)"},
+        "roofline": hbm_roofline(nbytes, sec_step, "gdn_recurrent_kernel (the step's only launch)"),
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -235,6 +381,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--B", type=int, default=16, help="batch override (profiling runs only; the metric is B=16)")
+    ap.add_argument("--op", default="chunk_fwd", choices=["chunk_fwd", "conv1d", "decode"],
+                    help="chunk_fwd: the GDN chunked forward (the headline); conv1d / decode: the neighbouring "
+                         "ops of the same layer, each with its own JSON line")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -256,6 +405,11 @@ def main():
     from gated_deltanet_chunked_gdn_gb300 import inputs as I
 
     binding.load()
+    if args.op != "chunk_fwd":
+        {"conv1d": run_conv1d, "decode": run_decode}[args.op](args, rank, world, dev)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     w = I.WORKLOADS[2].with_(B=args.B, Hqk=args.H, Hv=args.H, seed=2 + rank)
     x = I.make_inputs(w, dev)
     p = binding.problem_of(x["q"], x["v"], w.C)
