@@ -107,7 +107,17 @@ __device__ __forceinline__ int seq_slot(const ConvArgs& a, int n) {
   return (slot >= 0 && slot < a.slots) ? slot : -1;
 }
 
-__device__ __forceinline__ float silu(float u) { return u / (1.f + sm100::exp_fast(-u)); }
+// 1/y on the MUFU unit (rcp.approx.ftz.f32: about 1 ulp; 1/+inf = +0).
+__device__ __forceinline__ float rcp_approx(float y) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+  return r;
+}
+
+// SiLU u sigmoid(u) = u / (1 + e^{-u}) with two MUFU operations (ex2 and rcp)
+// instead of an IEEE division; for very negative u, e^{-u} overflows to +inf
+// and the result is -0.
+__device__ __forceinline__ float silu(float u) { return u * rcp_approx(1.f + sm100::exp_fast(-u)); }
 
 template <typename T, int W, bool SILU>
 __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const ConvArgs a) {

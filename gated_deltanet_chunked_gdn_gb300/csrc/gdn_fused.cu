@@ -387,6 +387,15 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
 
     // ---- M1: [K;Q] K^T -> R_a
     if (tid == 0) {
+      // the next chunk's k / q boxes go to L2 now; their TMA load (issued
+      // once M4 frees the tile) then waits on L2 instead of HBM
+      if (c + 1 < nchunks) {
+        const int tn = (int)(t0 + kChunk);
+        tma_prefetch_3d(&tm_k, 0, hq, tn);
+        tma_prefetch_3d(&tm_k, 64, hq, tn);
+        tma_prefetch_3d(&tm_q, 0, hq, tn);
+        tma_prefetch_3d(&tm_q, 64, hq, tn);
+      }
       if (!mbar_wait(bar_kq, ph_kq, prm.status)) {
         flags[1] = 1;
       } else {
