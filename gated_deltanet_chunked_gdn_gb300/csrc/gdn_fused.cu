@@ -63,7 +63,8 @@ constexpr uint32_t OFF_DL = OFF_MISC + 768;    // float[64] e^{gamma_last - gamm
 constexpr uint32_t OFF_EG = OFF_MISC + 1024;   // float[64] e^gamma
 constexpr uint32_t OFF_BAR = OFF_MISC + 1280;    // 5 mbarriers: k/q tiles, v tile, three MMA commit groups
 constexpr uint32_t OFF_FLAGS = OFF_MISC + 1320;  // [0] tmem base, [1] abort
-constexpr uint32_t kSmemUsed = OFF_MISC + 1344;
+constexpr uint32_t OFF_GRAW = OFF_MISC + 1344;   // float[2][2][64]: raw g, beta of two chunks
+constexpr uint32_t kSmemUsed = OFF_MISC + 2368;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 constexpr int kAsLd = 68;
 
@@ -342,33 +343,40 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     issue_kq(0);
     issue_v(0);
   }
-  float g_nx[2] = {0.f, 0.f}, b_nx[2] = {0.f, 0.f};   // warp 0: g, beta of rows 2 lane, 2 lane + 1
-  if (warp == 0) {
+  // warp 0 stages chunk cc's g and beta rows in graw[cc & 1] (lane l: rows
+  // 2 l and 2 l + 1, zeros past the sequence) with asynchronous copies
+  float* graw = reinterpret_cast<float*>(sm + OFF_GRAW);
+  auto fetch_gb = [&](int cc) {
+    float* dst = graw + (cc & 1) * 128;
 #pragma unroll
-    for (int r = 0; r < 2; ++r)
-      if (2 * lane + r < L) {
-        g_nx[r] = prm.g[(tok0 + 2 * lane + r) * prm.Hv + h];
-        b_nx[r] = prm.beta[(tok0 + 2 * lane + r) * prm.Hv + h];
+    for (int r = 0; r < 2; ++r) {
+      const int rr = 2 * lane + r;
+      const int64_t tn = tok0 + (int64_t)kChunk * cc + rr;
+      if (tn < tok0 + L) {
+        cp_async4(dst + rr, prm.g + tn * prm.Hv + h);
+        cp_async4(dst + 64 + rr, prm.beta + tn * prm.Hv + h);
+      } else {
+        dst[rr] = 0.f;
+        dst[64 + rr] = 0.f;
       }
-  }
+    }
+    cp_async_commit();
+  };
+  if (warp == 0 && nchunks > 0) fetch_gb(0);
 
 #pragma unroll 1
   for (int c = 0; c < nchunks; ++c) {
     const int64_t t0 = tok0 + (int64_t)kChunk * c;
     const int Lc = (int)((L - (int64_t)kChunk * c) < kChunk ? (L - (int64_t)kChunk * c) : kChunk);
 
-    // ---- S0 (warp 0): gamma = in-chunk cumsum of g, from g / beta loaded one
-    // chunk ahead (lane l holds rows 2l and 2l + 1); the next sync comes
-    // before any reader.
+    // ---- S0 (warp 0): gamma = in-chunk cumsum of g, from the g / beta rows
+    // copied to shared memory one chunk ahead (lane l copied and reads rows
+    // 2l and 2l + 1); the next sync comes before any other reader.
     if (warp == 0) {
-      const float ga = g_nx[0], gb = g_nx[1], ba = b_nx[0], bb = b_nx[1];
-      if (c + 1 < nchunks) {
-        const int64_t tn = t0 + kChunk + 2 * lane, end = tok0 + L;
-        g_nx[0] = tn < end ? prm.g[tn * prm.Hv + h] : 0.f;
-        b_nx[0] = tn < end ? prm.beta[tn * prm.Hv + h] : 0.f;
-        g_nx[1] = tn + 1 < end ? prm.g[(tn + 1) * prm.Hv + h] : 0.f;
-        b_nx[1] = tn + 1 < end ? prm.beta[(tn + 1) * prm.Hv + h] : 0.f;
-      }
+      cp_async_wait_all();   // this lane's copies of chunk c (issued one chunk ago)
+      const float* cur = graw + (c & 1) * 128;
+      const float ga = cur[2 * lane], gb = cur[2 * lane + 1], ba = cur[64 + 2 * lane], bb = cur[64 + 2 * lane + 1];
+      if (c + 1 < nchunks) fetch_gb(c + 1);
       float sum = ga + gb;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -418,29 +426,33 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     // ---- S1: A rows (lanes 0..63) and P rows (lanes 64..127)
     {
       float v[32];
-      tmem_ld32(R_a + lane_off + 32 * hf, v);
       // warps whose whole 32x32 block lies above the diagonal only write zeros
       const bool upper = (qd & 1) == 0 && hf == 1;
-      if (qd < 2) {
-        const int i = row;
-        const float bi = bet[i], gi = gam[i];
+      const int i = qd < 2 ? row : row - 64;
+      if (upper) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * hf + jj;
-          v[jj] = (!upper && j < i) ? bi * ex2_fast(gi - gam[j]) * v[jj] : 0.f;
+        for (int jj = 0; jj < 32; ++jj) v[jj] = 0.f;
+      } else {
+        tmem_ld32(R_a + lane_off + 32 * hf, v);
+        const float ri = qd < 2 ? bet[i] : prm.scale;   // P carries the output scale: OP = scale V'^T P^T
+        const float gi = gam[i];
+        const int lim = qd < 2 ? i : i + 1;              // A: j < i (strict); P: j <= i
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const float4 gj = *reinterpret_cast<const float4*>(gam + 32 * hf + 4 * k4);
+          const float gjs[4] = {gj.x, gj.y, gj.z, gj.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int j = 32 * hf + 4 * k4 + u;
+            v[4 * k4 + u] = j < lim ? ri * ex2_fast(gi - gjs[u]) * v[4 * k4 + u] : 0.f;
+          }
         }
+      }
+      if (qd < 2) {
         float4* dst = reinterpret_cast<float4*>(As + i * kAsLd + 32 * hf);
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       } else {
-        // P carries the output scale: OP = scale * V'^T P^T
-        const int i = row - 64;
-        const float gi = gam[i], sc = prm.scale;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = 32 * hf + jj;
-          v[jj] = (!upper && j <= i) ? sc * ex2_fast(gi - gam[j]) * v[jj] : 0.f;
-        }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
       }
@@ -572,23 +584,33 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     {
       // this thread holds column e = row of o for 32 rows i; neighbouring
       // lanes exchange values so that each writes bf16 pairs (e, e + 1)
-      uint8_t* box = sm + OFF_OS + (row >> 6) * 8192;
+      // staging row i, bf16 pair (e, e + 1): byte i*128 + ((e/8 ^ i%8) << 4) + (e%8)*2.
+      // With i = col + 2 pp + odd (col a multiple of 16), i%8 = (2 pp)%8 | odd.
       const int ecol = (row & 63) & ~1;
       const bool odd = lane & 1;
+      uint8_t* lbase = sm + OFF_OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
+      const uint32_t xsw = (static_cast<uint32_t>((ecol >> 3) ^ (odd ? 1 : 0))) << 4;
 #pragma unroll 1
       for (int q = 0; q < 2; ++q) {
         float a[16], b[16];
         const uint32_t col = 32 * hf + 16 * q;
         tmem_ld16(R_a + lane_off + col, a);
         tmem_ld16(R_b + lane_off + col, b);
+        float e[16];
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float4 x = *reinterpret_cast<const float4*>(eg + col + 4 * k4);
+          e[4 * k4] = x.x, e[4 * k4 + 1] = x.y, e[4 * k4 + 2] = x.z, e[4 * k4 + 3] = x.w;
+        }
+        uint8_t* qb = lbase + col * 128;
 #pragma unroll
         for (int pp = 0; pp < 8; ++pp) {
-          const float v0 = fmaf(eg[col + 2 * pp], a[2 * pp], b[2 * pp]);
-          const float v1 = fmaf(eg[col + 2 * pp + 1], a[2 * pp + 1], b[2 * pp + 1]);
+          const float v0 = fmaf(e[2 * pp], a[2 * pp], b[2 * pp]);
+          const float v1 = fmaf(e[2 * pp + 1], a[2 * pp + 1], b[2 * pp + 1]);
           const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-          const int i = col + 2 * pp + (odd ? 1 : 0);
           const uint32_t word = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
-          *reinterpret_cast<uint32_t*>(box + sw128_offset(i, ecol)) = word;
+          const uint32_t off = (2 * pp) * 128 + (xsw ^ (static_cast<uint32_t>((2 * pp) & 7) << 4));
+          *reinterpret_cast<uint32_t*>(qb + off) = word;
         }
       }
     }
@@ -614,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     }
   }
   if (tid == 0) bulk_wait_read();   // staging reads done before shared memory is released
+  if (warp == 0) cp_async_wait_all();   // g / beta copies of a chunk the loop did not reach
 
   if (flags[1]) {
     // abort: let copies and MMAs already in flight finish (bounded) before
