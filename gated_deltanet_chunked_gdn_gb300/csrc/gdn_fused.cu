@@ -43,17 +43,17 @@ constexpr int kTmemCols = 256;
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_KQ = 0;         // [k rows 0..63 ; q rows 64..127] x 128 d, 2 atom columns of 16 KB
 constexpr uint32_t OFF_V = 32768;      // v rows 0..63 x 128 e, 2 atom columns of 8 KB
-constexpr uint32_t OFF_Y = 49152;      // T diag(beta) | T diag(beta e^g)  (8 KB each), later W^T (16 KB)
+constexpr uint32_t OFF_Y = 49152;      // T diag(beta) | T diag(beta e^g)  (8 KB each), then W^T, then V''^T (16 KB)
 constexpr uint32_t OFF_TB = OFF_Y;
 constexpr uint32_t OFF_TBE = OFF_Y + 8192;
 constexpr uint32_t OFF_W = OFF_Y;
 constexpr uint32_t OFF_P = 65536;      // P [i][j] bf16, 8 KB
-constexpr uint32_t OFF_X = 73728;      // 32 KB, reused: A/T fp32 + scratch | S^T bf16 | V'^T, V''^T | o staging
+constexpr uint32_t OFF_X = 73728;      // 32 KB, reused: A/T fp32 + scratch | S^T bf16 | V'^T | o staging
 constexpr uint32_t OFF_AS = OFF_X;     // fp32 [64][68]
 constexpr uint32_t OFF_TMP = OFF_X + 64 * 68 * 4;  // fp32 scratch for the solve merges (32 x 40 floats)
 constexpr uint32_t OFF_ST = OFF_X;     // S^T bf16 [e][d], 2 atom columns of 16 KB
-constexpr uint32_t OFF_VP = OFF_X;     // V'^T bf16 [e][j], 16 KB
-constexpr uint32_t OFF_VPP = OFF_X + 16384;
+constexpr uint32_t OFF_VP = OFF_X;     // V'^T bf16 [e][j], 16 KB (the S^T half that M3 reads first)
+constexpr uint32_t OFF_VPP = OFF_Y;    // V''^T bf16 [e][j], 16 KB (W^T is dead once V' is complete)
 constexpr uint32_t OFF_OS = OFF_X;     // o staging bf16: 2 boxes [64 rows][64], 128-byte swizzle (TMA store)
 constexpr uint32_t OFF_MISC = 106496;
 constexpr uint32_t OFF_GAM = OFF_MISC;         // float[64] gamma (in-chunk cumsum of g)
@@ -91,24 +91,28 @@ struct FusedParams {
 //     first the 16-blocks (two pairs), then the 32-blocks (one pair).  The
 //     merge products run on the tensor cores (mma.sync m16n8k8, tf32 inputs,
 //     fp32 accumulation); the upper triangles hold zeros, so they are plain
-//     square products.  tf32 rounding here stays two orders of magnitude below
-//     the bf16 rounding T receives as an MMA operand afterwards.
-__device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
-}
+//     square products.  The fp32 values enter the tf32 MMA unrounded (the unit
+//     reads their upper 19 bits, i.e. truncates to tf32: at most 2^-10
+//     relative per operand); measured end to end against the fp64 oracle,
+//     this leaves the error of o and ht where rounding to tf32 puts it, far
+//     below the bf16 rounding T receives as an MMA operand afterwards.
 
-// d[16x8] += A[16 x KK] B[KK x 8]; A(r, c) = A[r * lda + c], B(r, c) = B[r * ldb + c].
+// d[16x8] += A[16 x KK] B[KK x 8]; A(r, c) = A[r * lda + c], B(r, c) = B[r * ldb + c]
+// (shared memory).  A's fragments come from one ldmatrix.x4 per k-step (four
+// 8 x 4 fp32 sub-tiles, rows 16-byte aligned); the fp32 values go to the tf32
+// MMA as they are (the unit reads their upper 19 bits).
 template <int KK>
 __device__ __forceinline__ void tile_mma_tf32(float (&d)[4], const float* A, int lda, const float* B, int ldb,
                                               int lane) {
   const int g = lane >> 2, t = lane & 3;
+  const uint32_t pa = smem_u32(A + ((lane & 7) + 8 * ((lane >> 3) & 1)) * lda + 4 * (lane >> 4));
 #pragma unroll
   for (int k0 = 0; k0 < KK; k0 += 8) {
-    const uint32_t a0 = to_tf32(A[g * lda + k0 + t]), a1 = to_tf32(A[(g + 8) * lda + k0 + t]);
-    const uint32_t a2 = to_tf32(A[g * lda + k0 + t + 4]), a3 = to_tf32(A[(g + 8) * lda + k0 + t + 4]);
-    const uint32_t b0 = to_tf32(B[(k0 + t) * ldb + g]), b1 = to_tf32(B[(k0 + t + 4) * ldb + g]);
+    uint32_t a0, a1, a2, a3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(pa + 4u * k0));
+    const uint32_t b0 = __float_as_uint(B[(k0 + t) * ldb + g]), b1 = __float_as_uint(B[(k0 + t + 4) * ldb + g]);
     asm volatile(
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
@@ -163,6 +167,15 @@ __device__ __forceinline__ void merge_level(float* As, float* tmp, int warp, int
   }
   fence_proxy_async();   // the bf16 tiles feed tcgen05.mma
   __syncthreads();
+}
+
+// Shared-memory descriptor of the 128-byte-swizzled tile at byte offset `off`
+// from the 1024-aligned base whose shared address / 16 is s4 (the same fields
+// as desc_sw128 with SBO = 1024; no carry out of the address field, the
+// shared window being below 256 KB): one add per descriptor in the issue loops.
+__device__ __forceinline__ uint64_t dsw(uint32_t s4, uint32_t off, uint32_t lbo) {
+  constexpr uint32_t hi = (1024u >> 4) | (1u << 14) | (2u << 29);
+  return (static_cast<uint64_t>(hi) << 32) | (s4 + ((off >> 4) + ((lbo >> 4) << 16)));
 }
 
 // T = (I + A)^{-1} (see above); also writes T diag(beta) and T diag(beta e^g)
@@ -335,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     wait_commit(bar_mma, ph_mma, mma_pending);
     return sync_ok();
   };
-  const uint32_t kq = sbase + OFF_KQ;
+  const uint32_t s4 = (sbase & 0x3FFFFu) >> 4;   // descriptor address field of the tile base
 
   tc_fence_before();
   __syncthreads();
@@ -413,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t a = kq + (s >> 2) * 16384 + (s & 3) * 32;
-          mma_bf16(R_a, desc_sw128(a, 16, 1024), desc_sw128(a, 16, 1024), id, s > 0);
+          const uint32_t a = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
+          mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, a, 16), id, s > 0);
         }
         mma_commit(bar_mma);
         ++mma_pending;
@@ -474,12 +487,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma_bf16(R_a, desc_sw128(kq + s * 2048, 16384, 1024), desc_sw128(sbase + OFF_TBE + s * 32, 16, 1024), id,
-                   s > 0);
+          mma_bf16(R_a, dsw(s4, OFF_KQ + s * 2048, 16384), dsw(s4, OFF_TBE + s * 32, 16), id, s > 0);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma_bf16(R_b, desc_sw128(sbase + OFF_V + s * 2048, 8192, 1024),
-                   desc_sw128(sbase + OFF_TB + s * 32, 16, 1024), id, s > 0);
+          mma_bf16(R_b, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), id, s > 0);
         mma_commit(bar_mma);
         ++mma_pending;
       }
@@ -516,23 +527,33 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     tc_fence_before();
     __syncthreads();
 
-    // ---- M3: V'^T = U^T - S^T W^T (R_b) ; OQ^T = S^T Q^T (R_a)
+    // ---- M3: V'^T = U^T - S^T W^T (R_b) ; OQ^T = S^T Q^T (R_a).  S5 overwrites
+    // the first half of S^T (k-steps 0..3) with V'^T as soon as bar_x fires, so
+    // the k-steps of S^T Q^T that read that half are issued before V'; a
+    // commit tracks every earlier MMA of the thread, so bar_x covers them too.
+    // The second half of S^T is left alone until the last commit (bar_mma).
     if (tid == 0) {
       tc_fence_after();
       const uint32_t idv = idesc_bf16(128, 64, 0, 1, 1);
       const uint32_t ido = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t a = sbase + OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-        mma_bf16(R_b, desc_sw128(a, 16, 1024), desc_sw128(sbase + OFF_W + s * 2048, 16384, 1024), idv, 1);
+      for (int s = 0; s < 4; ++s) {
+        const uint32_t a = OFF_ST + (s & 3) * 32;
+        const uint32_t b = OFF_KQ + 8192 + (s & 3) * 32;
+        mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, b, 16), ido, s > 0);
       }
-      mma_commit(bar_x);    // V' ready: S5 starts while Q S runs
-      ++x_pending;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const uint32_t a = sbase + OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-        const uint32_t b = kq + 8192 + (s >> 2) * 16384 + (s & 3) * 32;
-        mma_bf16(R_a, desc_sw128(a, 16, 1024), desc_sw128(b, 16, 1024), ido, s > 0);
+        const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+        mma_bf16(R_b, dsw(s4, a, 16), dsw(s4, OFF_W + s * 2048, 16384), idv, 1);
+      }
+      mma_commit(bar_x);    // V' ready (and S^T's first half read): S5 starts while Q S finishes
+      ++x_pending;
+#pragma unroll
+      for (int s = 4; s < 8; ++s) {
+        const uint32_t a = OFF_ST + 16384 + (s & 3) * 32;
+        const uint32_t b = OFF_KQ + 8192 + 16384 + (s & 3) * 32;
+        mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, b, 16), ido, 1);
       }
       mma_commit(bar_mma);
       ++mma_pending;
@@ -563,14 +584,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       const uint32_t ids = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma_bf16(R_S, desc_sw128(sbase + OFF_VPP + s * 32, 16, 1024), desc_sw128(kq + s * 2048, 16384, 1024), ids,
-                 1);
+        mma_bf16(R_S, dsw(s4, OFF_VPP + s * 32, 16), dsw(s4, OFF_KQ + s * 2048, 16384), ids, 1);
       mma_commit(bar_x);    // state updated: the k / q tiles are free
       ++x_pending;
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma_bf16(R_b, desc_sw128(sbase + OFF_VP + s * 32, 16, 1024), desc_sw128(sbase + OFF_P + s * 32, 16, 1024),
-                 idp, s > 0);
+        mma_bf16(R_b, dsw(s4, OFF_VP + s * 32, 16), dsw(s4, OFF_P + s * 32, 16), idp, s > 0);
       mma_commit(bar_q);
       ++q_pending;
     }
