@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     issue_kq(0);
     issue_v(0);
   }
-  // warp 0 stages chunk cc's g and beta rows in graw[cc & 1] (lane l: rows
+  // warp 1 stages chunk cc's g and beta rows in graw[cc & 1] (lane l: rows
   // 2 l and 2 l + 1, zeros past the sequence) with asynchronous copies
   float* graw = reinterpret_cast<float*>(sm + OFF_GRAW);
   auto fetch_gb = [&](int cc) {
@@ -375,17 +375,18 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     }
     cp_async_commit();
   };
-  if (warp == 0 && nchunks > 0) fetch_gb(0);
+  if (warp == 1 && nchunks > 0) fetch_gb(0);
 
 #pragma unroll 1
   for (int c = 0; c < nchunks; ++c) {
     const int64_t t0 = tok0 + (int64_t)kChunk * c;
     const int Lc = (int)((L - (int64_t)kChunk * c) < kChunk ? (L - (int64_t)kChunk * c) : kChunk);
 
-    // ---- S0 (warp 0): gamma = in-chunk cumsum of g, from the g / beta rows
-    // copied to shared memory one chunk ahead (lane l copied and reads rows
-    // 2l and 2l + 1); the next sync comes before any other reader.
-    if (warp == 0) {
+    // ---- S0 (warp 1, while thread 0 issues M1): gamma = in-chunk cumsum of g,
+    // from the g / beta rows copied to shared memory one chunk ahead (lane l
+    // copied and reads rows 2l and 2l + 1); the next sync comes before any
+    // other reader.
+    if (warp == 1) {
       cp_async_wait_all();   // this lane's copies of chunk c (issued one chunk ago)
       const float* cur = graw + (c & 1) * 128;
       const float ga = cur[2 * lane], gb = cur[2 * lane + 1], ba = cur[64 + 2 * lane], bb = cur[64 + 2 * lane + 1];
@@ -410,13 +411,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     if (tid == 0) {
       // the next chunk's k / q boxes go to L2 now; their TMA load (issued
       // once M4 frees the tile) then waits on L2 instead of HBM
-      if (c + 1 < nchunks) {
-        const int tn = (int)(t0 + kChunk);
-        tma_prefetch_3d(&tm_k, 0, hq, tn);
-        tma_prefetch_3d(&tm_k, 64, hq, tn);
-        tma_prefetch_3d(&tm_q, 0, hq, tn);
-        tma_prefetch_3d(&tm_q, 64, hq, tn);
-      }
       if (!mbar_wait(bar_kq, ph_kq, prm.status)) {
         flags[1] = 1;
       } else {
@@ -431,6 +425,13 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         }
         mma_commit(bar_mma);
         ++mma_pending;
+      }
+      if (c + 1 < nchunks) {
+        const int tn = (int)(t0 + kChunk);
+        tma_prefetch_3d(&tm_k, 0, hq, tn);
+        tma_prefetch_3d(&tm_k, 64, hq, tn);
+        tma_prefetch_3d(&tm_q, 0, hq, tn);
+        tma_prefetch_3d(&tm_q, 64, hq, tn);
       }
       bulk_wait_read();   // the previous chunk's o staging (region X) has been read by its TMA store
     }
@@ -584,18 +585,16 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       const uint32_t ids = idesc_bf16(128, 128, 0, 1, 0);
 #pragma unroll
       for (int s = 0; s < 4; ++s)
-        mma_bf16(R_S, dsw(s4, OFF_VPP + s * 32, 16), dsw(s4, OFF_KQ + s * 2048, 16384), ids, 1);
-      mma_commit(bar_x);    // state updated: the k / q tiles are free
-      ++x_pending;
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
         mma_bf16(R_b, dsw(s4, OFF_VP + s * 32, 16), dsw(s4, OFF_P + s * 32, 16), idp, s > 0);
       mma_commit(bar_q);
       ++q_pending;
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        mma_bf16(R_S, dsw(s4, OFF_VPP + s * 32, 16), dsw(s4, OFF_KQ + s * 2048, 16384), ids, 1);
+      mma_commit(bar_x);    // state updated: the k / q tiles are free
+      ++x_pending;
     }
     wait_commit(bar_mma, ph_mma, mma_pending);   // S^T Q^T (committed in M3)
-    wait_commit(bar_x, ph_x, x_pending);         // state update
-    if (tid == 0 && c + 1 < nchunks && !flags[1]) issue_kq(c + 1);
     wait_commit(bar_q, ph_q, q_pending);         // V'^T P^T
     if (!sync_ok()) break;
 
@@ -633,6 +632,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         }
       }
     }
+    // the state update ran under S6; its completion frees the k / q tile
+    wait_commit(bar_x, ph_x, x_pending);
+    if (tid == 0 && c + 1 < nchunks && !flags[1]) issue_kq(c + 1);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -655,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     }
   }
   if (tid == 0) bulk_wait_read();   // staging reads done before shared memory is released
-  if (warp == 0) cp_async_wait_all();   // g / beta copies of a chunk the loop did not reach
+  if (warp == 1) cp_async_wait_all();   // g / beta copies of a chunk the loop did not reach
 
   if (flags[1]) {
     // abort: let copies and MMAs already in flight finish (bounded) before
