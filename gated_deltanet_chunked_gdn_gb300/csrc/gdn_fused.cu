@@ -88,7 +88,9 @@ struct FusedParams {
 //  1. Diagonal 16x16 blocks by forward substitution: a half-warp per block,
 //     lane l keeps column l of the block's inverse in registers.
 //  2. Merge neighbouring blocks, [[T11, 0], [A21, T22]] -> T21 = -T22 (A21 T11),
-//     first the 16-blocks (two pairs), then the 32-blocks (one pair).  The
+//     first the 16-blocks (two pairs, each inside the one warp that wrote
+//     that 32x32 diagonal block of A in the gating step, so steps 1 and 2a
+//     need no block barrier), then the 32-blocks (one pair, all warps).  The
 //     merge products run on the tensor cores (mma.sync m16n8k8, tf32 inputs,
 //     fp32 accumulation); the upper triangles hold zeros, so they are plain
 //     square products.  The fp32 values enter the tf32 MMA unrounded (the unit
@@ -178,45 +180,58 @@ __device__ __forceinline__ uint64_t dsw(uint32_t s4, uint32_t off, uint32_t lbo)
   return (static_cast<uint64_t>(hi) << 32) | (s4 + ((off >> 4) + ((lbo >> 4) << 16)));
 }
 
-// T = (I + A)^{-1} (see above); also writes T diag(beta) and T diag(beta e^g)
-// as bf16 K-major operands (tb, tbe), including their zero upper blocks.
-__device__ __forceinline__ void solve64(float* As, float* tmp, int tid, uint8_t* tb, uint8_t* tbe, const float* bet,
-                                        const float* be) {
-  const int warp = tid >> 5, lane = tid & 31;
-  if (warp < 2) {
-    const int b = 16 * (2 * warp + (lane >> 4));
-    const int l = lane & 15;
-    float t[16];
+// Diagonal 16x16 blocks b and b + 16 of T = (I + A)^{-1} by forward
+// substitution, one half-warp per block (lane l keeps column l of the block's
+// inverse), written to As (fp32) and to tb / tbe (bf16, times beta and beta e^g).
+__device__ __forceinline__ void diag_pair(float* As, int b0, int lane, uint8_t* tb, uint8_t* tbe, const float* bet,
+                                          const float* be) {
+  const int b = b0 + 16 * (lane >> 4);
+  const int l = lane & 15;
+  float t[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float* arow = As + (b + i) * kAsLd + b;
-      float x = (i == l) ? 1.f : 0.f;
+  for (int i = 0; i < 16; ++i) {
+    const float* arow = As + (b + i) * kAsLd + b;
+    float x = (i == l) ? 1.f : 0.f;
 #pragma unroll
-      for (int j = 0; j < i; ++j) x = fmaf(-arow[j], t[j], x);
-      t[i] = x;
-    }
-    __syncwarp();
-    const float bl = bet[b + l], el = be[b + l];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      As[(b + i) * kAsLd + b + l] = t[i];
-      *reinterpret_cast<__nv_bfloat16*>(tb + sw128_offset(b + i, b + l)) = __float2bfloat16_rn(t[i] * bl);
-      *reinterpret_cast<__nv_bfloat16*>(tbe + sw128_offset(b + i, b + l)) = __float2bfloat16_rn(t[i] * el);
-    }
-  } else {
-    // warps 2..7: zero the six strictly-upper 16x16 blocks of both operands
-    // (one 16-byte chunk per thread and operand: 6 blocks x 16 rows x 2 chunks)
-    const int u = tid - 64;                        // 0..191
-    const int blk = u >> 5, r = (u >> 1) & 15, half = u & 1;
-    const int rb = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-    const int cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-    const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
-    *reinterpret_cast<uint4*>(tb + off) = make_uint4(0u, 0u, 0u, 0u);
-    *reinterpret_cast<uint4*>(tbe + off) = make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < i; ++j) x = fmaf(-arow[j], t[j], x);
+    t[i] = x;
   }
-  __syncthreads();
-  merge_level<16>(As, tmp, warp, lane, tb, tbe, bet, be);
-  merge_level<32>(As, tmp, warp, lane, tb, tbe, bet, be);
+  __syncwarp();
+  const float bl = bet[b + l], el = be[b + l];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    As[(b + i) * kAsLd + b + l] = t[i];
+    *reinterpret_cast<__nv_bfloat16*>(tb + sw128_offset(b + i, b + l)) = __float2bfloat16_rn(t[i] * bl);
+    *reinterpret_cast<__nv_bfloat16*>(tbe + sw128_offset(b + i, b + l)) = __float2bfloat16_rn(t[i] * el);
+  }
+}
+
+// 16-level merge inside one warp for the 32x32 diagonal block at o:
+// T21 = -T22 (A21 T11), the product A21 T11 passing through a warp-private
+// scratch (16 x 16, leading dimension 24).
+__device__ __forceinline__ void merge16_warp(float* As, float* scr, int o, int lane, uint8_t* tb, uint8_t* tbe,
+                                             const float* bet, const float* be) {
+  constexpr int SLD = 24;
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mma_tf32<16>(d, As + (o + 16) * kAsLd + o, kAsLd, As + o * kAsLd + o + 8 * nt, kAsLd, lane);
+    tile_store(d, scr + 8 * nt, SLD, lane, 1.f);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    tile_mma_tf32<16>(d, As + (o + 16) * kAsLd + o + 16, kAsLd, scr + 8 * nt, SLD, lane);
+    const int r0 = o + 16, c0 = o + 8 * nt + 2 * t;
+    tile_store(d, As + r0 * kAsLd + o + 8 * nt, kAsLd, lane, -1.f);
+    const float b0 = bet[c0], b1 = bet[c0 + 1], e0 = be[c0], e1 = be[c0 + 1];
+    *reinterpret_cast<uint32_t*>(tb + sw128_offset(r0 + g, c0)) = pack_bf16(-d[0] * b0, -d[1] * b1);
+    *reinterpret_cast<uint32_t*>(tb + sw128_offset(r0 + g + 8, c0)) = pack_bf16(-d[2] * b0, -d[3] * b1);
+    *reinterpret_cast<uint32_t*>(tbe + sw128_offset(r0 + g, c0)) = pack_bf16(-d[0] * e0, -d[1] * e1);
+    *reinterpret_cast<uint32_t*>(tbe + sw128_offset(r0 + g + 8, c0)) = pack_bf16(-d[2] * e0, -d[3] * e1);
+  }
 }
 
 // Eight floats as bf16 into one 16-byte chunk of shared memory.
@@ -471,11 +486,31 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
       }
     }
+
+    // ---- S2: solve_tril in place; T diag(beta) and T diag(beta e^g) go out as
+    // bf16 operands.  Warps 0 and 5 wrote rows 0..31 x cols 0..31 and rows
+    // 32..63 x cols 32..63 of A: each solves its two diagonal 16x16 blocks and
+    // merges them into its 32x32 diagonal block of T without waiting for the
+    // other warps, which meanwhile zero the upper 16x16 blocks of both
+    // operands (one 16-byte chunk per thread and operand).
+    if (warp == 0 || warp == 5) {
+      const int o = warp == 5 ? 32 : 0;
+      __syncwarp();
+      diag_pair(As, o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+      __syncwarp();
+      merge16_warp(As, tmp + (warp == 5 ? 16 * 24 : 0), o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+    } else {
+      const int u = 32 * (warp - 1 - (warp > 5 ? 1 : 0)) + lane;   // 0..191 over warps 1-4, 6, 7
+      const int blk = u >> 5, r = (u >> 1) & 15, half = u & 1;
+      const int rb = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
+      *reinterpret_cast<uint4*>(sm + OFF_TB + off) = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(sm + OFF_TBE + off) = make_uint4(0u, 0u, 0u, 0u);
+    }
     tc_fence_before();
     __syncthreads();
-
-    // ---- S2: solve_tril in place; T diag(beta) and T diag(beta e^g) go out as bf16 operands
-    solve64(As, tmp, tid, sm + OFF_TB, sm + OFF_TBE, bet, be);
+    merge_level<32>(As, tmp, warp, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
 
     // ---- M2: W^T = K^T (T diag(beta e^g))^T -> R_a ; U^T = V^T (T diag(beta))^T -> R_b
     if (tid == 0) {
