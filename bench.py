@@ -32,6 +32,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "GDN chunk-fwd tokens/s (16x8192, H=32, K=V=128, bf16); % roofline"
+L2_BYTES = 129 * 1000 * 1000   # GB300 L2
 
 
 def peaks() -> dict:
@@ -381,6 +382,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--B", type=int, default=16, help="batch override (profiling runs only; the metric is B=16)")
+    ap.add_argument("--workload", default="batched_16x8192",
+                    choices=["batched_16x8192", "gqa_prefill_1x4096", "long_1x32768"],
+                    help="chunk_fwd shape: the headline 16 x 8192 batch, or one long GQA sequence (1 x 4096 or "
+                         "1 x 32768 tokens, 16 qk / 32 value heads), where AUTO takes the chunk-parallel path")
     ap.add_argument("--op", default="chunk_fwd", choices=["chunk_fwd", "conv1d", "decode"],
                     help="chunk_fwd: the GDN chunked forward (the headline); conv1d / decode: the neighbouring "
                          "ops of the same layer, each with its own JSON line")
@@ -410,7 +415,13 @@ def main():
         if world > 1:
             dist.destroy_process_group()
         return
-    w = I.WORKLOADS[2].with_(B=args.B, Hqk=args.H, Hv=args.H, seed=2 + rank)
+    if args.workload == "batched_16x8192":
+        w = I.WORKLOADS[2].with_(B=args.B, Hqk=args.H, Hv=args.H, seed=2 + rank)
+        wname = f"batched_{w.B}x8192_H{args.H}"
+    else:
+        T = 4096 if args.workload == "gqa_prefill_1x4096" else 32768
+        w = I.WORKLOADS[1].with_(T=T, seed=1 + rank)
+        wname = f"gqa_prefill_1x{T}_Hqk{w.Hqk}_Hv{w.Hv}"
     x = I.make_inputs(w, dev)
     p = binding.problem_of(x["q"], x["v"], w.C)
     path = args.path if args.path != "auto" else binding.gdn_resolve_path(p)
@@ -433,20 +444,32 @@ def main():
     sampler = ClockSampler(gpu_uuid(local))
     sampler.start()
     time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # inputs smaller than about twice the L2 are timed step by step with the
+    # L2 flushed (a 512 MB write) between steps, outside the timed spans
+    in_bytes, _ = algorithmic(w.B, w.T, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if in_bytes < 2 * L2_BYTES else None
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps if flush is not None else 1)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
+    if flush is None:
+        evs[0][0].record(stream)
+        for _ in range(args.steps):
+            step()
+        evs[0][1].record(stream)
+    else:
+        for e_a, e_b in evs:
+            flush.zero_()
+            e_a.record(stream)
+            step()
+            e_b.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1)
+    ms = sum(e_a.elapsed_time(e_b) for e_a, e_b in evs)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
     tokens_step = w.B * w.T
@@ -456,8 +479,9 @@ def main():
     # End to end through the public API: inputs from pinned host memory, o and
     # ht read back, every step.
     host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
-    host["h0"] = x["h0"].cpu().pin_memory()
-    dev_in = {k: torch.empty_like(x[k]) for k in ("q", "k", "v", "g", "beta", "h0")}
+    if x["h0"] is not None:
+        host["h0"] = x["h0"].cpu().pin_memory()
+    dev_in = {k: torch.empty_like(x[k]) for k in host}
     o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     ht_host = torch.empty(ht.shape, dtype=ht.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
@@ -466,7 +490,7 @@ def main():
     def e2e_step():
         for k_ in dev_in:
             dev_in[k_].copy_(host[k_], non_blocking=True)
-        step(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["h0"])
+        step(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in.get("h0"))
         o_host.copy_(o, non_blocking=True)
         ht_host.copy_(ht, non_blocking=True)
 
@@ -481,7 +505,7 @@ def main():
     e2e_value, _ = aggregate(time.perf_counter() - t0, tokens_step, args.e2e_steps, world, dev)
 
     pk = peaks()
-    nbytes, flops = algorithmic(w.B, w.T, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=True)
+    nbytes, flops = algorithmic(w.B, w.T, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None)
     t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
     t_tc = flops / (pk["bf16_tflops"] * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
@@ -490,17 +514,19 @@ def main():
         achieved, peak, unit = nbytes / sec / 1e9, pk["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = flops / sec / 1e12, pk["bf16_tflops"], "TFLOP/s"
-    launches = {"staged": 7, "fused": 1}[path]
+    launches = {"staged": 7, "fused": 1, "cp": 4}[path]
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if args.workload == "batched_16x8192" else f"GDN chunk-fwd tokens/s ({wname}, bf16); % roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"batched_{w.B}x8192_H{args.H}", "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv,
+        "config": {"workload": wname, "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv,
                    "K": w.K, "V": w.V, "C": w.C, "path": path, "parallelism": f"dp{world} (independent batches)",
-                   "l2": "inputs larger than L2 (4.4 GB compulsory traffic per step)"},
+                   "l2": (f"inputs larger than L2 ({nbytes / 1e9:.2f} GB compulsory traffic per step)"
+                          if flush is None else "L2 flushed (512 MB write) before every timed step")},
         "tflops_alg": flops / sec / 1e12,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": measured_traffic(path, w.B), "peak_source": pk["source"],
+                     "traffic": measured_traffic(path, w.B) if args.workload == "batched_16x8192" else None, "peak_source": pk["source"],
                      "kernel": "gdn_fused_kernel (the step's only launch)" if path == "fused"
                      else "gdn_chunk_fwd call (all launches of one step)",
                      "alg_bytes": nbytes, "alg_flops": flops,

@@ -34,12 +34,20 @@ bool problem_ok(const gdn_problem* pp, gdn_problem* out) {
 }
 
 gdn_path resolve(const gdn_problem& p, gdn_path path) {
-  if (path == GDN_PATH_AUTO) return fused_supported(p) ? GDN_PATH_FUSED : GDN_PATH_STAGED;
+  if (path == GDN_PATH_AUTO) {
+    if (!fused_supported(p)) return GDN_PATH_STAGED;
+    return cp_preferred(p) ? GDN_PATH_CP : GDN_PATH_FUSED;
+  }
   return path;
+}
+
+bool path_ok(gdn_path path) {
+  return path == GDN_PATH_AUTO || path == GDN_PATH_STAGED || path == GDN_PATH_FUSED || path == GDN_PATH_CP;
 }
 
 size_t workspace_for(const gdn_problem& p, gdn_path path) {
   if (path == GDN_PATH_FUSED) return fused_workspace_bytes(p);
+  if (path == GDN_PATH_CP) return cp_workspace_bytes(p);
   gdn_staged_layout_t L;
   staged_layout(p, &L);
   return L.total;
@@ -47,6 +55,7 @@ size_t workspace_for(const gdn_problem& p, gdn_path path) {
 
 size_t status_offset(const gdn_problem& p, gdn_path path) {
   if (path == GDN_PATH_FUSED) return fused_status_offset(p);
+  if (path == GDN_PATH_CP) return 0;
   gdn_staged_layout_t L;
   staged_layout(p, &L);
   return L.status;
@@ -76,8 +85,9 @@ extern "C" {
 size_t gdn_chunk_fwd_workspace_size(const gdn_problem* pp, gdn_path path) {
   gdn_problem p;
   if (!problem_ok(pp, &p)) return 0;
+  if (!path_ok(path)) return 0;
   path = resolve(p, path);
-  if (path == GDN_PATH_FUSED && !fused_supported(p)) return 0;
+  if ((path == GDN_PATH_FUSED || path == GDN_PATH_CP) && !fused_supported(p)) return 0;
   return workspace_for(p, path);
 }
 
@@ -93,14 +103,16 @@ gdn_status gdn_chunk_fwd(const gdn_problem* pp, gdn_path path, const void* q, co
                          void* stream) {
   gdn_problem p;
   if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
-  if (path != GDN_PATH_AUTO && path != GDN_PATH_STAGED && path != GDN_PATH_FUSED) return GDN_ERR_INVALID_ARG;
+  if (!path_ok(path)) return GDN_ERR_INVALID_ARG;
   path = resolve(p, path);
-  if (path == GDN_PATH_FUSED && !fused_supported(p)) return GDN_ERR_UNSUPPORTED;
+  if ((path == GDN_PATH_FUSED || path == GDN_PATH_CP) && !fused_supported(p)) return GDN_ERR_UNSUPPORTED;
   gdn_status st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, workspace, workspace_bytes,
                              workspace_for(p, path));
   if (st != GDN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (path == GDN_PATH_FUSED) return run_fused(p, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, s);
+  if (path == GDN_PATH_CP)
+    return run_cp(p, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, workspace_bytes, s);
   return run_staged(p, 6, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, s);
 }
 
@@ -128,7 +140,7 @@ gdn_status gdn_get_device_status(const gdn_problem* pp, gdn_path path, void* wor
                                  int* dev_status) {
   gdn_problem p;
   if (!problem_ok(pp, &p) || !workspace || !dev_status) return GDN_ERR_INVALID_ARG;
-  if (path != GDN_PATH_AUTO && path != GDN_PATH_STAGED && path != GDN_PATH_FUSED) return GDN_ERR_INVALID_ARG;
+  if (!path_ok(path)) return GDN_ERR_INVALID_ARG;
   path = resolve(p, path);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int32_t* word = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + status_offset(p, path));

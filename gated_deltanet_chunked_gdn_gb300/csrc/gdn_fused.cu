@@ -63,6 +63,7 @@ constexpr uint32_t OFF_DL = OFF_MISC + 768;    // float[64] e^{gamma_last - gamm
 constexpr uint32_t OFF_EG = OFF_MISC + 1024;   // float[64] e^gamma
 constexpr uint32_t OFF_BAR = OFF_MISC + 1280;    // 5 mbarriers: k/q tiles, v tile, three MMA commit groups
 constexpr uint32_t OFF_FLAGS = OFF_MISC + 1320;  // [0] tmem base, [1] abort
+constexpr uint32_t OFF_BAR1 = OFF_MISC + 1336;   // sixth mbarrier: first half of S^T Q^T
 constexpr uint32_t OFF_GRAW = OFF_MISC + 1344;   // float[2][2][64]: raw g, beta of two chunks
 constexpr uint32_t kSmemUsed = OFF_MISC + 2368;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
@@ -81,7 +82,17 @@ struct FusedParams {
   int32_t* status;
   int N, Tseq, Ttot, Hqk, Hv, varlen;
   float scale;
+  // kStates launches only: blocks [0, split) are the chains of a problem started
+  // from a zero state (final state -> ht); blocks [split, 2 split) the same
+  // chains started from the identity with v = 0 (final state = the chain's
+  // state-transition matrix -> ht2)
+  float* ht2;
+  int split;
 };
+
+// Kernel modes: the full forward pass, or final states only (no q, no o).
+constexpr int kFull = 0;
+constexpr int kStates = 1;
 
 // T = (I + A)^{-1} for a 64x64 strictly lower A held in place in As (fp32,
 // leading dimension kAsLd, zeros on and above the diagonal).
@@ -240,6 +251,7 @@ __device__ __forceinline__ void store8_bf16(uint8_t* p, const float* v) {
       make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
 }
 
+template <int MODE>
 __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 const __grid_constant__ CUtensorMap tm_k,
                                                                 const __grid_constant__ CUtensorMap tm_v,
@@ -265,11 +277,14 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
   uint64_t* bar_mma = bar_kq + 2;   // M1, M2, then the S^T Q^T product of M3
   uint64_t* bar_x = bar_kq + 3;     // V' (M3), then the state update (M4)
   uint64_t* bar_q = bar_kq + 4;     // V'^T P^T (M4)
+  uint64_t* bar_o1 = reinterpret_cast<uint64_t*>(sm + OFF_BAR1);   // first half of S^T Q^T (M3)
   volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sm + OFF_FLAGS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, hf = warp >> 2;   // TMEM lane quadrant, column half
-  const int chain = blockIdx.x;
+  // kStates: the upper half of the grid computes transition matrices
+  const bool trans = MODE == kStates && (int)blockIdx.x >= prm.split;
+  const int chain = trans ? (int)blockIdx.x - prm.split : (int)blockIdx.x;
   const int n = chain / prm.Hv, h = chain % prm.Hv;
   const int hq = h / (prm.Hv / prm.Hqk);
 
@@ -297,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     mbar_init(bar_mma, 1);
     mbar_init(bar_x, 1);
     mbar_init(bar_q, 1);
+    mbar_init(bar_o1, 1);
     mbar_fence_init();
     flags[1] = 0;
     prefetch_tmap(&tm_q);
@@ -313,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
   const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
   const int row = 32 * qd + lane;   // this thread's TMEM lane (e or d or chunk row)
 
-  // state S^T[e][d] = h0[d][e]
+  // state S^T[e][d] = h0[d][e] (the identity for a transition chain)
   {
     const float* h0p = prm.h0 ? prm.h0 + ((int64_t)n * prm.Hv + h) * kD * kD : nullptr;
 #pragma unroll 1
@@ -321,22 +337,26 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       float v[32];
       const int d0 = 64 * hf + 32 * half;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = h0p ? h0p[(int64_t)(d0 + i) * kD + row] : 0.f;
+      for (int i = 0; i < 32; ++i) v[i] = trans ? (d0 + i == row ? 1.f : 0.f) : (h0p ? h0p[(int64_t)(d0 + i) * kD + row] : 0.f);
       tmem_st32(R_S + lane_off + d0, v);
     }
     tmem_wait_st();
   }
 
-  uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_x = 0, ph_q = 0;
+  uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_x = 0, ph_q = 0, ph_o1 = 0;
   bool kq_pending = false, v_pending = false;   // meaningful in thread 0
-  int mma_pending = 0, x_pending = 0, q_pending = 0;   // commits not yet waited for (thread 0)
+  int mma_pending = 0, x_pending = 0, q_pending = 0, o1_pending = 0;   // commits not yet waited for (thread 0)
   auto issue_kq = [&](int c) {
     const int t = (int)(tok0 + (int64_t)kChunk * c);
-    mbar_arrive_expect_tx(bar_kq, 32768);
+    // kStates needs no q: its rows of the [k; q] tile are left as they are
+    // (their products are computed but never used)
+    mbar_arrive_expect_tx(bar_kq, MODE == kFull ? 32768 : 16384);
     tma_load_3d(sm + OFF_KQ, &tm_k, bar_kq, 0, hq, t);
-    tma_load_3d(sm + OFF_KQ + 8192, &tm_q, bar_kq, 0, hq, t);
     tma_load_3d(sm + OFF_KQ + 16384, &tm_k, bar_kq, 64, hq, t);
-    tma_load_3d(sm + OFF_KQ + 24576, &tm_q, bar_kq, 64, hq, t);
+    if (MODE == kFull) {
+      tma_load_3d(sm + OFF_KQ + 8192, &tm_q, bar_kq, 0, hq, t);
+      tma_load_3d(sm + OFF_KQ + 24576, &tm_q, bar_kq, 64, hq, t);
+    }
     kq_pending = true;
   };
   auto issue_v = [&](int c) {
@@ -369,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
   __syncthreads();
   if (tid == 0 && nchunks > 0) {
     issue_kq(0);
-    issue_v(0);
+    if (!trans) issue_v(0);   // a transition chain has v = 0: U = 0 and no v tile
   }
   // warp 1 stages chunk cc's g and beta rows in graw[cc & 1] (lane l: rows
   // 2 l and 2 l + 1, zeros past the sequence) with asynchronous copies
@@ -445,8 +465,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         const int tn = (int)(t0 + kChunk);
         tma_prefetch_3d(&tm_k, 0, hq, tn);
         tma_prefetch_3d(&tm_k, 64, hq, tn);
-        tma_prefetch_3d(&tm_q, 0, hq, tn);
-        tma_prefetch_3d(&tm_q, 64, hq, tn);
+        if (MODE == kFull) {
+          tma_prefetch_3d(&tm_q, 0, hq, tn);
+          tma_prefetch_3d(&tm_q, 64, hq, tn);
+        }
       }
       bulk_wait_read();   // the previous chunk's o staging (region X) has been read by its TMA store
     }
@@ -514,19 +536,23 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
 
     // ---- M2: W^T = K^T (T diag(beta e^g))^T -> R_a ; U^T = V^T (T diag(beta))^T -> R_b
     if (tid == 0) {
-      if (!mbar_wait(bar_v, ph_v, prm.status)) {
+      if (!trans && !mbar_wait(bar_v, ph_v, prm.status)) {
         flags[1] = 1;
       } else {
-        ph_v ^= 1;
-        v_pending = false;
+        if (!trans) {
+          ph_v ^= 1;
+          v_pending = false;
+        }
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
           mma_bf16(R_a, dsw(s4, OFF_KQ + s * 2048, 16384), dsw(s4, OFF_TBE + s * 32, 16), id, s > 0);
+        if (!trans) {
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-          mma_bf16(R_b, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), id, s > 0);
+          for (int s = 0; s < 4; ++s)
+            mma_bf16(R_b, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), id, s > 0);
+        }
         mma_commit(bar_mma);
         ++mma_pending;
       }
@@ -550,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       tc_fence_before();
     }
     if (!wait_mma()) break;
-    if (tid == 0 && c + 1 < nchunks) issue_v(c + 1);   // v tile consumed
+    if (tid == 0 && c + 1 < nchunks && !trans) issue_v(c + 1);   // v tile consumed
 
     // ---- S3: W^T -> bf16 [d][i] (MN-major B)
     {
@@ -564,35 +590,33 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     __syncthreads();
 
     // ---- M3: V'^T = U^T - S^T W^T (R_b) ; OQ^T = S^T Q^T (R_a).  S5 overwrites
-    // the first half of S^T (k-steps 0..3) with V'^T as soon as bar_x fires, so
-    // the k-steps of S^T Q^T that read that half are issued before V'; a
-    // commit tracks every earlier MMA of the thread, so bar_x covers them too.
-    // The second half of S^T is left alone until the last commit (bar_mma).
+    // the first half of S^T (k-steps 0..3) with V'^T: the S^T Q^T k-steps that
+    // read it commit to bar_o1, which S5 waits for before that store.
     if (tid == 0) {
       tc_fence_after();
       const uint32_t idv = idesc_bf16(128, 64, 0, 1, 1);
       const uint32_t ido = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const uint32_t a = OFF_ST + (s & 3) * 32;
-        const uint32_t b = OFF_KQ + 8192 + (s & 3) * 32;
-        mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, b, 16), ido, s > 0);
-      }
-#pragma unroll
       for (int s = 0; s < 8; ++s) {
         const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-        mma_bf16(R_b, dsw(s4, a, 16), dsw(s4, OFF_W + s * 2048, 16384), idv, 1);
+        mma_bf16(R_b, dsw(s4, a, 16), dsw(s4, OFF_W + s * 2048, 16384), idv, (trans && s == 0) ? 0u : 1u);
       }
-      mma_commit(bar_x);    // V' ready (and S^T's first half read): S5 starts while Q S finishes
+      mma_commit(bar_x);    // V' ready: S5 starts while Q S runs
       ++x_pending;
 #pragma unroll
-      for (int s = 4; s < 8; ++s) {
-        const uint32_t a = OFF_ST + 16384 + (s & 3) * 32;
-        const uint32_t b = OFF_KQ + 8192 + 16384 + (s & 3) * 32;
-        mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, b, 16), ido, 1);
+      for (int s = 0; s < (MODE == kFull ? 8 : 0); ++s) {
+        const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+        const uint32_t b = OFF_KQ + 8192 + (s >> 2) * 16384 + (s & 3) * 32;
+        mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, b, 16), ido, s > 0);
+        if (s == 3) {
+          mma_commit(bar_o1);   // S^T's first half read
+          ++o1_pending;
+        }
       }
-      mma_commit(bar_mma);
-      ++mma_pending;
+      if (MODE == kFull) {
+        mma_commit(bar_mma);
+        ++mma_pending;
+      }
     }
     wait_commit(bar_x, ph_x, x_pending);
     if (!sync_ok()) break;
@@ -604,10 +628,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) w[jj] = v[jj] * dl[32 * hf + jj];
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        store8_bf16(sm + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
-        store8_bf16(sm + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
-      }
+      for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
+      if (MODE == kFull) wait_commit(bar_o1, ph_o1, o1_pending);   // S^T Q^T no longer reads the first half of S^T
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -618,16 +642,25 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       tc_fence_after();
       const uint32_t idp = idesc_bf16(128, 64, 0, 0, 0);
       const uint32_t ids = idesc_bf16(128, 128, 0, 1, 0);
+      if (MODE == kFull) {
 #pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_bf16(R_b, dsw(s4, OFF_VP + s * 32, 16), dsw(s4, OFF_P + s * 32, 16), idp, s > 0);
-      mma_commit(bar_q);
-      ++q_pending;
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(R_b, dsw(s4, OFF_VP + s * 32, 16), dsw(s4, OFF_P + s * 32, 16), idp, s > 0);
+        mma_commit(bar_q);
+        ++q_pending;
+      }
 #pragma unroll
       for (int s = 0; s < 4; ++s)
         mma_bf16(R_S, dsw(s4, OFF_VPP + s * 32, 16), dsw(s4, OFF_KQ + s * 2048, 16384), ids, 1);
       mma_commit(bar_x);    // state updated: the k / q tiles are free
       ++x_pending;
+    }
+    if (MODE == kStates) {
+      // final states only: wait for the state update, release the k tile
+      wait_commit(bar_x, ph_x, x_pending);
+      if (tid == 0 && c + 1 < nchunks && !flags[1]) issue_kq(c + 1);
+      if (!sync_ok()) break;
+      continue;
     }
     wait_commit(bar_mma, ph_mma, mma_pending);   // S^T Q^T (committed in M3)
     wait_commit(bar_q, ph_q, q_pending);         // V'^T P^T
@@ -703,10 +736,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       for (; mma_pending > 0; --mma_pending, ph_mma ^= 1) mbar_wait(bar_mma, ph_mma, prm.status, 100000000ull);
       for (; x_pending > 0; --x_pending, ph_x ^= 1) mbar_wait(bar_x, ph_x, prm.status, 100000000ull);
       for (; q_pending > 0; --q_pending, ph_q ^= 1) mbar_wait(bar_q, ph_q, prm.status, 100000000ull);
+      for (; o1_pending > 0; --o1_pending, ph_o1 ^= 1) mbar_wait(bar_o1, ph_o1, prm.status, 100000000ull);
     }
-  } else if (prm.ht) {
+  } else if (trans ? prm.ht2 != nullptr : prm.ht != nullptr) {
     // final state ht[d][e] = S^T[e][d]
-    float* htp = prm.ht + ((int64_t)n * prm.Hv + h) * kD * kD;
+    float* htp = (trans ? prm.ht2 : prm.ht) + ((int64_t)n * prm.Hv + h) * kD * kD;
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
       float v[32];
@@ -730,22 +764,12 @@ bool fused_supported(const gdn_problem& p) {
 size_t fused_workspace_bytes(const gdn_problem&) { return kAlign; }   // the status word
 size_t fused_status_offset(const gdn_problem&) { return 0; }
 
-gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
-                     const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
-                     void* ws, cudaStream_t s) {
-  if (!fused_supported(p)) return GDN_ERR_UNSUPPORTED;
-  int32_t* status = static_cast<int32_t*>(ws);
-  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+// One launch of the fused kernel over the chains of `p` (N x Hv, or twice
+// that for kStates).  status: the device status word.
+gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                        float* ht2, int32_t* status, cudaStream_t s) {
   const int64_t Ttot = (int64_t)p.B * p.T;
-  if (Ttot == 0 || (int64_t)p.N * p.Hv == 0) {
-    // no tokens: ht = h0 (or zeros)
-    if (ht) {
-      const size_t bytes = sizeof(float) * (size_t)p.N * p.Hv * p.K * p.V;
-      cudaError_t e = h0 ? cudaMemcpyAsync(ht, h0, bytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(ht, 0, bytes, s);
-      if (e != cudaSuccess) return GDN_ERR_CUDA;
-    }
-    return GDN_OK;
-  }
   CUtensorMap tq, tk, tv, to;
   memset(&to, 0, sizeof(to));
   memset(&tq, 0, sizeof(tq));
@@ -778,12 +802,47 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
   prm.Hv = p.Hv;
   prm.varlen = p.varlen;
   prm.scale = scale;
-  if (cudaFuncSetAttribute(gdn_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-      cudaSuccess)
-    return GDN_ERR_CUDA;
-  const unsigned grid = (unsigned)((int64_t)p.N * p.Hv);
-  gdn_fused_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
+  prm.ht2 = ht2;
+  prm.split = p.N * p.Hv;
+  const unsigned chains = (unsigned)((int64_t)p.N * p.Hv);
+  if (mode == kFull) {
+    if (cudaFuncSetAttribute(gdn_fused_kernel<kFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    gdn_fused_kernel<kFull><<<chains, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
+  } else {
+    if (cudaFuncSetAttribute(gdn_fused_kernel<kStates>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
+      return GDN_ERR_CUDA;
+    gdn_fused_kernel<kStates><<<2 * chains, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
+  }
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                     const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                     void* ws, cudaStream_t s) {
+  if (!fused_supported(p)) return GDN_ERR_UNSUPPORTED;
+  int32_t* status = static_cast<int32_t*>(ws);
+  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+  const int64_t Ttot = (int64_t)p.B * p.T;
+  if (Ttot == 0 || (int64_t)p.N * p.Hv == 0) {
+    // no tokens: ht = h0 (or zeros)
+    if (ht) {
+      const size_t bytes = sizeof(float) * (size_t)p.N * p.Hv * p.K * p.V;
+      cudaError_t e = h0 ? cudaMemcpyAsync(ht, h0, bytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(ht, 0, bytes, s);
+      if (e != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+  }
+  return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s);
+}
+
+gdn_status run_fused_states(const gdn_problem& p, const void* k, const void* v, const float* g, const float* beta,
+                            const int32_t* cu, float* ht_zero, float* ht_trans, int32_t* status, cudaStream_t s) {
+  // q and o are never touched in this mode; k / v stand in for their maps
+  return launch_fused(p, kStates, k, k, v, g, beta, 1.f, nullptr, cu, const_cast<void*>(v), ht_zero, ht_trans,
+                      status, s);
 }
 
 }  // namespace gdn

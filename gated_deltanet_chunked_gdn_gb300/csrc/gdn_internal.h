@@ -84,5 +84,24 @@ size_t fused_status_offset(const gdn_problem& p);
 gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
                      const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
                      void* ws, cudaStream_t s);
+// States-only launch over the chains of p (p.varlen with cu): chains started
+// from a zero state write their final states to ht_zero, the same chains
+// started from the identity with v = 0 write their transition matrices to
+// ht_trans.
+gdn_status run_fused_states(const gdn_problem& p, const void* k, const void* v, const float* g, const float* beta,
+                            const int32_t* cu, float* ht_zero, float* ht_trans, int32_t* status, cudaStream_t s);
+
+// Chunk-parallel path (gdn_cp.cu): sequences cut into segments run in parallel.
+size_t cp_workspace_bytes(const gdn_problem& p);
+gdn_status run_cp(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                  const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht, void* ws,
+                  size_t ws_bytes, cudaStream_t s);
+int cp_segment_length(const gdn_problem& p);
+// AUTO takes the chunk-parallel path for long sequences with few chains.
+bool cp_preferred(const gdn_problem& p);
+// One fused-kernel launch (mode 0: the full pass; 1: final states only).
+gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                        float* ht2, int32_t* status, cudaStream_t s);
 
 }  // namespace gdn

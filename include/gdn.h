@@ -53,9 +53,12 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 
 /* Execution path. */
 typedef enum {
-  GDN_PATH_AUTO = 0,    /* fused when supported, else staged */
+  GDN_PATH_AUTO = 0,    /* cp or fused when supported, else staged */
   GDN_PATH_STAGED = 1,  /* one kernel per stage, intermediates in the workspace */
-  GDN_PATH_FUSED = 2    /* single persistent tcgen05 kernel (bf16, K = V = 128) */
+  GDN_PATH_FUSED = 2,   /* single persistent tcgen05 kernel (bf16, K = V = 128) */
+  GDN_PATH_CP = 3       /* chunk-parallel: each sequence cut into segments run on separate SMs
+                           (bf16, K = V = 128); AUTO takes it for sequences of >= 2048 tokens
+                           when the (sequence, value head) chains number at most half the SMs */
 } gdn_path;
 
 /*
@@ -270,7 +273,7 @@ gdn_status gdn_causal_conv1d_fwd(const void* x, const float* weight, const float
  */
 gdn_status gdn_selftest_exp(const float* x, float* y, int n, void* stream);
 
-/* Path that GDN_PATH_AUTO selects for this problem (STAGED or FUSED). */
+/* Path that GDN_PATH_AUTO selects for this problem (STAGED, FUSED or CP). */
 gdn_path gdn_resolve_path(const gdn_problem* p);
 
 /* Human-readable name of a status code (static string). */
