@@ -126,6 +126,148 @@ int oracle_recurrent(int64_t Ttot, int N, const int64_t* cu, int Hqk, int Hv, in
   return err ? ORACLE_ENOMEM : ORACLE_OK;
 }
 
+/* ------------------------------------------------------- form 1, backward */
+
+/*
+ * Gradients of the token recurrence (reverse mode, written out by hand from
+ * the forward above; the FlashQLA notes list a backward of the chunk form
+ * among the variants, section 4.3).  For upstream gradients dout = dL/do and
+ * dht = dL/dht, with a_t = exp(g_t), b_t = beta_t, P_t = I - b_t k_t k_t^T
+ * (symmetric) and S_t the state after token t (S_0 = h0):
+ *
+ *   G     <- G + scale q_t dout_t^T            (G = dL/dS_t, starts at dht)
+ *   dq_t   = scale S_t dout_t
+ *   u      = S_{t-1}^T k_t,   w = G^T k_t      (V-vectors)
+ *   dv_t   = b_t w
+ *   dg_t   = a_t (<G, S_{t-1}> - b_t w.u)      (<,> = sum of elementwise products)
+ *   dbeta_t= -a_t w.u + w.v_t
+ *   dk_t   = -a_t b_t (G u + S_{t-1} w) + b_t G v_t
+ *   G     <- a_t (G - b_t k_t w^T)             (= a_t P_t G, the gradient w.r.t. S_{t-1})
+ *
+ * and dh0 = the final G.  With GQA, dq and dk of a q/k head sum over the
+ * value heads that read it.  Chains keep every state of the sequence (tests
+ * use small sizes).
+ */
+static void recurrent_chain_bwd(int64_t t0, int64_t L, int Hqk, int Hv, int K, int V, int h,
+                                const double* q, const double* k, const double* v, const double* g,
+                                const double* beta, double scale, const double* h0c, const double* dout,
+                                const double* dhtc, double* dq, double* dk, double* dv, double* dg,
+                                double* dbeta, double* dh0c, double* St /* [(L+1)][K][V] */,
+                                double* G /* [K][V] */, double* u /* [V] */, double* w /* [V] */) {
+  const int hq = h / (Hv / Hqk);
+  const int64_t KV = (int64_t)K * V;
+  /* forward, keeping every state */
+  if (h0c) memcpy(St, h0c, sizeof(double) * (size_t)KV);
+  else memset(St, 0, sizeof(double) * (size_t)KV);
+  for (int64_t i = 0; i < L; ++i) {
+    const int64_t t = t0 + i;
+    const double* kt = k + (t * Hqk + hq) * (int64_t)K;
+    const double* vt = v + (t * Hv + h) * (int64_t)V;
+    const double a = exp(g[t * Hv + h]), b = beta[t * Hv + h];
+    const double* Sp = St + i * KV;
+    double* Sn = St + (i + 1) * KV;
+    for (int e = 0; e < V; ++e) {
+      u[e] = 0.0;
+      for (int d = 0; d < K; ++d) u[e] += kt[d] * Sp[(int64_t)d * V + e];
+    }
+    for (int d = 0; d < K; ++d)
+      for (int e = 0; e < V; ++e)
+        Sn[(int64_t)d * V + e] = a * (Sp[(int64_t)d * V + e] - b * kt[d] * u[e]) + b * kt[d] * vt[e];
+  }
+  /* backward */
+  if (dhtc) memcpy(G, dhtc, sizeof(double) * (size_t)KV);
+  else memset(G, 0, sizeof(double) * (size_t)KV);
+  for (int64_t i = L - 1; i >= 0; --i) {
+    const int64_t t = t0 + i;
+    const double* kt = k + (t * Hqk + hq) * (int64_t)K;
+    const double* qt = q + (t * Hqk + hq) * (int64_t)K;
+    const double* vt = v + (t * Hv + h) * (int64_t)V;
+    const double* dot = dout + (t * Hv + h) * (int64_t)V;
+    const double a = exp(g[t * Hv + h]), b = beta[t * Hv + h];
+    const double* Sp = St + i * KV;        /* S_{t-1} */
+    const double* Sc = St + (i + 1) * KV;  /* S_t */
+    double* dqt = dq + (t * Hqk + hq) * (int64_t)K;
+    double* dkt = dk + (t * Hqk + hq) * (int64_t)K;
+    for (int d = 0; d < K; ++d)
+      for (int e = 0; e < V; ++e) G[(int64_t)d * V + e] += scale * qt[d] * dot[e];
+    for (int d = 0; d < K; ++d) {
+      double acc = 0.0;
+      for (int e = 0; e < V; ++e) acc += Sc[(int64_t)d * V + e] * dot[e];
+      dqt[d] += scale * acc;
+    }
+    for (int e = 0; e < V; ++e) {
+      u[e] = 0.0;
+      w[e] = 0.0;
+      for (int d = 0; d < K; ++d) {
+        u[e] += Sp[(int64_t)d * V + e] * kt[d];
+        w[e] += G[(int64_t)d * V + e] * kt[d];
+      }
+    }
+    double wu = 0.0, wv = 0.0, gs = 0.0;
+    for (int e = 0; e < V; ++e) {
+      wu += w[e] * u[e];
+      wv += w[e] * vt[e];
+    }
+    for (int64_t x = 0; x < KV; ++x) gs += G[x] * Sp[x];
+    double* dvt = dv + (t * Hv + h) * (int64_t)V;
+    for (int e = 0; e < V; ++e) dvt[e] = b * w[e];
+    dg[t * Hv + h] = a * (gs - b * wu);
+    dbeta[t * Hv + h] = -a * wu + wv;
+    for (int d = 0; d < K; ++d) {
+      double gu = 0.0, sw = 0.0, gv = 0.0;
+      for (int e = 0; e < V; ++e) {
+        gu += G[(int64_t)d * V + e] * u[e];
+        sw += Sp[(int64_t)d * V + e] * w[e];
+        gv += G[(int64_t)d * V + e] * vt[e];
+      }
+      dkt[d] += -a * b * (gu + sw) + b * gv;
+    }
+    for (int d = 0; d < K; ++d)
+      for (int e = 0; e < V; ++e) G[(int64_t)d * V + e] = a * (G[(int64_t)d * V + e] - b * kt[d] * w[e]);
+  }
+  memcpy(dh0c, G, sizeof(double) * (size_t)KV);
+}
+
+/* dq, dk [Ttot][Hqk][K] are overwritten (accumulated over the value heads of
+ * each q/k head); dv [Ttot][Hv][V], dg, dbeta [Ttot][Hv], dh0 [N][Hv][K][V].
+ * dht may be NULL (zero). */
+int oracle_recurrent_bwd(int64_t Ttot, int N, const int64_t* cu, int Hqk, int Hv, int K, int V,
+                         const double* q, const double* k, const double* v, const double* g,
+                         const double* beta, double scale, const double* h0, const double* dout,
+                         const double* dht, double* dq, double* dk, double* dv, double* dg, double* dbeta,
+                         double* dh0, int nthreads) {
+  int rc = check_args(Ttot, N, cu, Hqk, Hv, K, V);
+  if (rc) return rc;
+  memset(dq, 0, sizeof(double) * (size_t)Ttot * Hqk * K);
+  memset(dk, 0, sizeof(double) * (size_t)Ttot * Hqk * K);
+  const int G_ = Hv / Hqk;
+  int err = 0;
+#ifdef _OPENMP
+  if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+  for (int c = 0; c < N * Hqk; ++c) {   /* one q/k head group per task: dq / dk have one writer */
+    const int n = c / Hqk, hq = c % Hqk;
+    const int64_t L = cu[n + 1] - cu[n];
+    const int64_t KV = (int64_t)K * V;
+    double* buf = (double*)malloc(sizeof(double) * ((size_t)(L + 2) * KV + 2 * (size_t)V));
+    if (!buf) { err = 1; continue; }
+    double* St = buf;
+    double* G = buf + (L + 1) * KV;
+    double* u = G + KV;
+    double* w = u + V;
+    for (int j = 0; j < G_; ++j) {
+      const int h = hq * G_ + j;
+      const int64_t off = ((int64_t)n * Hv + h) * KV;
+      recurrent_chain_bwd(cu[n], L, Hqk, Hv, K, V, h, q, k, v, g, beta, scale, h0 ? h0 + off : NULL, dout,
+                          dht ? dht + off : NULL, dq, dk, dv, dg, dbeta, dh0 + off, St, G, u, w);
+    }
+    free(buf);
+  }
+  (void)nthreads;
+  return err ? ORACLE_ENOMEM : ORACLE_OK;
+}
+
 /* ---------------------------------------------------------------- form 2 */
 
 /* Generic Gauss-Jordan inverse with partial pivoting: Minv = M^{-1}, n x n.

@@ -12,6 +12,7 @@ marshals numpy arrays.  Forms:
 * :func:`chunked` -- the chunked form with an explicit Gauss-Jordan inverse.
 * :func:`chunked_stages` -- the chunked form of one chain, returning every
   per-chunk intermediate (gamma, A, T, W, U, S0, V').
+* :func:`recurrent_bwd` -- gradients of the token recurrence (reverse mode).
 
 Tensor conventions (same as the library): q, k ``[B, T, Hqk, K]``;
 v ``[B, T, Hv, V]``; g, beta ``[B, T, Hv]``; h0 / ht ``[N, Hv, K, V]``;
@@ -57,6 +58,8 @@ def _bind(lib):
     lib.oracle_chunked_stages.argtypes = (common + [ctypes.c_int] + [dp] * 5 + [ctypes.c_double, dp, ctypes.c_int, ctypes.c_int]
                                           + [dp] * 9)
     lib.oracle_chunked_stages.restype = ctypes.c_int
+    lib.oracle_recurrent_bwd.argtypes = common + [dp] * 5 + [ctypes.c_double] + [dp] * 9 + [ctypes.c_int]
+    lib.oracle_recurrent_bwd.restype = ctypes.c_int
     return lib
 
 
@@ -80,6 +83,9 @@ class Oracle:
 
     def chunked(self, *a, **kw):
         return chunked(*a, _lib=self._lib, **kw)
+
+    def recurrent_bwd(self, *a, **kw):
+        return recurrent_bwd(*a, _lib=self._lib, **kw)
 
 
 def _f64(x):
@@ -116,7 +122,7 @@ def _prep(q, k, v, g, beta, h0, cu_seqlens):
     Hv, V = v.shape[2], v.shape[3]
     if cu_seqlens is None:
         N = B
-        cu = np.arange(0, (B + 1) * T, T, dtype=np.int64)[: B + 1]
+        cu = np.arange(B + 1, dtype=np.int64) * T
     else:
         cu = _i64(cu_seqlens)
         if B != 1:
@@ -148,6 +154,27 @@ def recurrent(q, k, v, g, beta, scale, h0=None, cu_seqlens=None, chains=None, nt
     if rc:
         raise RuntimeError(f"oracle_recurrent failed: {rc}")
     return o, ht
+
+
+def recurrent_bwd(q, k, v, g, beta, scale, dout, h0=None, dht=None, cu_seqlens=None, nthreads=0, _lib=None):
+    """Gradients of the token recurrence for upstream gradients ``dout``
+    (dL/do, [B,T,Hv,V]) and ``dht`` (dL/dht, [N,Hv,K,V] or None).  Returns a
+    dict of float64 arrays: dq, dk [B,T,Hqk,K]; dv [B,T,Hv,V]; dg, dbeta
+    [B,T,Hv]; dh0 [N,Hv,K,V] (the gradient w.r.t. the initial state, zero
+    state when h0 is None)."""
+    q, k, v, g, beta, h0, cu, B, T, Hqk, K, Hv, V, N = _prep(q, k, v, g, beta, h0, cu_seqlens)
+    do = _f64(dout)
+    dh = _f64(dht)
+    out = {"dq": np.zeros((B, T, Hqk, K)), "dk": np.zeros((B, T, Hqk, K)), "dv": np.zeros((B, T, Hv, V)),
+           "dg": np.zeros((B, T, Hv)), "dbeta": np.zeros((B, T, Hv)), "dh0": np.zeros((N, Hv, K, V))}
+    rc = (_lib or _load()).oracle_recurrent_bwd(B * T, N, cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)), Hqk, Hv,
+                                                K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                                _ptr(h0), _ptr(do), _ptr(dh), _ptr(out["dq"]), _ptr(out["dk"]),
+                                                _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
+                                                _ptr(out["dh0"]), int(nthreads))
+    if rc:
+        raise RuntimeError(f"oracle_recurrent_bwd failed ({rc})")
+    return out
 
 
 def chunked(q, k, v, g, beta, scale, C, h0=None, cu_seqlens=None, chains=None, nthreads=0, _lib=None):
