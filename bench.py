@@ -370,6 +370,59 @@ def run_decode(args, rank, world, dev):
         print(json.dumps(line), flush=True)
 
 
+# fp32 SIMT peak of this GB300 from its unit counts: 152 SMs x 128 FP32 lanes
+# x 2 FLOP (FMA) x 2.07 GHz boost clock
+FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def run_bwd(args, rank, world, dev):
+    """Backward pass on the 16 x 8192, 32-head batch (bf16 inputs, fp32
+    gradients).  One step = one gdn_chunk_bwd call (checkpoint pass +
+    backward).  Algorithmic FLOPs per (token, value head): one forward step of
+    the recurrence (4 K V) and one reverse step (16 K V)."""
+    import torch
+    from gated_deltanet_chunked_gdn_gb300 import binding
+    from gated_deltanet_chunked_gdn_gb300 import inputs as I
+    w = I.WORKLOADS[2].with_(B=args.B, Hqk=args.H, Hv=args.H, seed=2 + rank)
+    x = I.make_inputs(w, dev)
+    gen = torch.Generator(device=dev).manual_seed(7 + rank)
+    do = torch.randn(x["v"].shape, generator=gen, device=dev).to(x["v"].dtype)
+    dht = torch.randn((w.B, w.Hv, w.K, w.V), generator=gen, device=dev)
+    p = binding.problem_of(x["q"], x["v"], 64)
+    ws = torch.empty(binding.gdn_chunk_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.gdn_chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], do, scale=x["scale"], h0=x["h0"], dht=dht,
+                              workspace=ws, stream=stream.cuda_stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sec, clocks = timed(step, args.steps, world, dev, stream)
+    tokens = w.B * w.T
+    value, sec_total = aggregate(sec, tokens, args.steps, world, dev)
+    sec_step = sec_total / args.steps
+    flops = 20.0 * w.K * w.V * tokens * w.Hv
+    achieved = flops / sec_step / 1e12
+    line = {
+        "metric": "GDN backward tokens/s (16x8192, H=32, K=V=128, bf16 inputs, fp32 gradients)", "value": value,
+        "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sec_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"bwd_{w.B}x{w.T}_H{w.Hv}", "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv, "K": w.K,
+                   "V": w.V, "parallelism": f"dp{world} (independent batches)",
+                   "l2": "inputs larger than L2 (4.4 GB of inputs and upstream gradients per step)"},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_SIMT_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / FP32_SIMT_TFLOPS, "traffic": None, "peak_source": "derived (unit counts x clock)",
+                     "kernel": "gdn_bwd_ckpt_kernel + gdn_bwd_kernel (one step)", "alg_flops": flops},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -386,7 +439,7 @@ def main():
                     choices=["batched_16x8192", "gqa_prefill_1x4096", "long_1x32768"],
                     help="chunk_fwd shape: the headline 16 x 8192 batch, or one long GQA sequence (1 x 4096 or "
                          "1 x 32768 tokens, 16 qk / 32 value heads), where AUTO takes the chunk-parallel path")
-    ap.add_argument("--op", default="chunk_fwd", choices=["chunk_fwd", "conv1d", "decode"],
+    ap.add_argument("--op", default="chunk_fwd", choices=["chunk_fwd", "conv1d", "decode", "bwd"],
                     help="chunk_fwd: the GDN chunked forward (the headline); conv1d / decode: the neighbouring "
                          "ops of the same layer, each with its own JSON line")
     args = ap.parse_args()
@@ -411,7 +464,7 @@ def main():
 
     binding.load()
     if args.op != "chunk_fwd":
-        {"conv1d": run_conv1d, "decode": run_decode}[args.op](args, rank, world, dev)
+        {"conv1d": run_conv1d, "decode": run_decode, "bwd": run_bwd}[args.op](args, rank, world, dev)
         if world > 1:
             dist.destroy_process_group()
         return

@@ -24,7 +24,8 @@ STAGES = {"prepare": 0, "cumsum": 1, "kkt": 2, "solve_tril": 3, "wy_fast": 4, "c
 
 EXPORTED = ["gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_staged", "gdn_staged_layout",
             "gdn_get_device_status", "gdn_resolve_path", "gdn_status_string", "gdn_version", "gdn_recurrent_fwd",
-            "gdn_causal_conv1d_fwd"]
+            "gdn_causal_conv1d_fwd", "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd",
+            "gdn_chunk_bwd_get_device_status"]
 
 
 class Problem(ctypes.Structure):
@@ -89,6 +90,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                               ctypes.c_int, vp, vp]
         lib.gdn_causal_conv1d_fwd.restype = ctypes.c_int
+        lib.gdn_chunk_bwd_workspace_size.argtypes = [P]
+        lib.gdn_chunk_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.gdn_chunk_bwd.argtypes = [P, vp, vp, vp, fp, fp, ctypes.c_float, fp, i32p, vp, fp, fp, fp, fp, fp, fp, fp,
+                                      vp, ctypes.c_size_t, vp]
+        lib.gdn_chunk_bwd.restype = ctypes.c_int
+        lib.gdn_chunk_bwd_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+        lib.gdn_chunk_bwd_get_device_status.restype = ctypes.c_int
         lib.gdn_version.argtypes = []
         lib.gdn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -329,3 +337,54 @@ def gdn_causal_conv1d_fwd(x, weight, bias=None, activation="silu", conv_state=No
     if st:
         raise GDNError(st, "gdn_causal_conv1d_fwd")
     return y
+
+
+def gdn_chunk_bwd_workspace_size(p: Problem) -> int:
+    return int(load().gdn_chunk_bwd_workspace_size(ctypes.byref(p)))
+
+
+def gdn_chunk_bwd(q, k, v, g, beta, dout, scale: Optional[float] = None, h0=None, dht=None, cu_seqlens=None,
+                  want_dh0: bool = True, workspace=None, stream=None) -> dict:
+    """Backward of gdn_chunk_fwd for upstream gradients ``dout`` (dL/do, dtype of v)
+    and ``dht`` (dL/dht, fp32 or None).  Returns fp32 gradients dq, dk
+    [B,T,Hqk,K], dv [B,T,Hv,V], dg, dbeta [B,T,Hv] and dh0 [N,Hv,K,V] (None
+    unless ``want_dh0``), plus the workspace under "workspace"."""
+    lib = load()
+    _check_inputs(q, k, v, g, beta, h0, cu_seqlens)
+    for name, t in (("dout", dout), ("dht", dht)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if dout.dtype != v.dtype or dout.shape != v.shape:
+        raise ValueError("dout must match v in shape and dtype")
+    if dht is not None and dht.dtype != torch.float32:
+        raise ValueError("dht must be float32")
+    p = problem_of(q, v, 64, cu_seqlens)
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    need = gdn_chunk_bwd_workspace_size(p)
+    if need == 0:
+        raise GDNError(GDN_ERR_UNSUPPORTED, "gdn_chunk_bwd_workspace_size")
+    if workspace is None:
+        workspace = _alloc_ws(need, q.device)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    out = {"dq": torch.empty(q.shape, **f32), "dk": torch.empty(k.shape, **f32), "dv": torch.empty(v.shape, **f32),
+           "dg": torch.empty(g.shape, **f32), "dbeta": torch.empty(beta.shape, **f32),
+           "dh0": torch.empty((p.N, p.Hv, p.K, p.V), **f32) if want_dh0 else None}
+    s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    st = lib.gdn_chunk_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), ctypes.c_float(scale),
+                           _ptr(h0), _ptr(cu_seqlens), _ptr(dout), _ptr(dht), _ptr(out["dq"]), _ptr(out["dk"]),
+                           _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dh0"]),
+                           _ptr(workspace), ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(s))
+    if st:
+        raise GDNError(st, "gdn_chunk_bwd")
+    out["workspace"] = workspace
+    return out
+
+
+def gdn_chunk_bwd_get_device_status(workspace, stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device).cuda_stream
+    v = ctypes.c_int(0)
+    st = load().gdn_chunk_bwd_get_device_status(_ptr(workspace), ctypes.c_void_p(s), ctypes.byref(v))
+    if st:
+        raise GDNError(st, "gdn_chunk_bwd_get_device_status")
+    return int(v.value)

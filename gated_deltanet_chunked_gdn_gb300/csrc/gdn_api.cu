@@ -194,6 +194,45 @@ gdn_status gdn_causal_conv1d_fwd(const void* x, const float* weight, const float
                            N, B, T, D, dt, act == GDN_ACT_SILU, y, static_cast<cudaStream_t>(stream));
 }
 
+size_t gdn_chunk_bwd_workspace_size(const gdn_problem* pp) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p) || !bwd_supported(p)) return 0;
+  return bwd_workspace_bytes(p);
+}
+
+gdn_status gdn_chunk_bwd(const gdn_problem* pp, const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, float scale, const float* h0, const int32_t* cu_seqlens,
+                         const void* dout, const float* dht, float* dq, float* dk, float* dv, float* dg,
+                         float* dbeta, float* dh0, void* workspace, size_t workspace_bytes, void* stream) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
+  if (!bwd_supported(p)) return GDN_ERR_UNSUPPORTED;
+  const bool any_tokens = (int64_t)p.B * p.T > 0;
+  if (any_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
+    return GDN_ERR_INVALID_ARG;
+  if (p.varlen != (cu_seqlens != nullptr)) return GDN_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < bwd_workspace_bytes(p) || !aligned(workspace, kAlign)) return GDN_ERR_INVALID_ARG;
+  const void* a16[] = {dh0, dht, h0};
+  for (const void* x : a16)
+    if (x && !aligned(x, 16)) return GDN_ERR_INVALID_ARG;
+  const void* a4[] = {q, k, v, g, beta, cu_seqlens, dout, dq, dk, dv, dg, dbeta};
+  for (const void* x : a4)
+    if (x && !aligned(x, 4)) return GDN_ERR_INVALID_ARG;
+  return run_bwd(p, q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
+                 static_cast<cudaStream_t>(stream));
+}
+
+gdn_status gdn_chunk_bwd_get_device_status(void* workspace, void* stream, int* dev_status) {
+  if (!workspace || !dev_status) return GDN_ERR_INVALID_ARG;
+  int32_t* word = static_cast<int32_t*>(workspace);
+  int32_t host = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemcpy(&host, word, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemset(word, 0, sizeof(int32_t)) != cudaSuccess) return GDN_ERR_CUDA;
+  *dev_status = host;
+  return GDN_OK;
+}
+
 const char* gdn_status_string(gdn_status s) {
   switch (s) {
     case GDN_OK: return "ok";

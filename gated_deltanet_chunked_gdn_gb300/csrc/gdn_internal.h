@@ -91,6 +91,14 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
 gdn_status run_fused_states(const gdn_problem& p, const void* k, const void* v, const float* g, const float* beta,
                             const int32_t* cu, float* ht_zero, float* ht_trans, int32_t* status, cudaStream_t s);
 
+// Backward pass (gdn_bwd.cu).
+bool bwd_supported(const gdn_problem& p);
+size_t bwd_workspace_bytes(const gdn_problem& p);
+gdn_status run_bwd(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                   const float* beta, float scale, const float* h0, const int32_t* cu, const void* dout,
+                   const float* dht, float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws,
+                   cudaStream_t s);
+
 // Chunk-parallel path (gdn_cp.cu): sequences cut into segments run in parallel.
 size_t cp_workspace_bytes(const gdn_problem& p);
 gdn_status run_cp(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,

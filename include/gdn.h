@@ -222,6 +222,41 @@ gdn_status gdn_recurrent_fwd(const gdn_problem* p, const void* q, const void* k,
                              float scale, float* state, const int32_t* state_indices, int state_slots,
                              const int32_t* cu_seqlens, void* o, void* stream);
 
+/*
+ * Backward pass of gdn_chunk_fwd (the FlashQLA notes list a backward of the
+ * chunk kernel among its variants, section 4.3): for upstream gradients
+ * dout = dL/do and dht = dL/dht, the gradients of L with respect to q, k, v,
+ * g, beta and h0, by reverse mode of the token recurrence
+ *     G <- G + scale q_t dout_t^T;  dq_t = scale S_t dout_t
+ *     u = S_{t-1}^T k_t, w = G^T k_t;  dv_t = beta_t w
+ *     dg_t = e^{g_t} (<G, S_{t-1}> - beta_t w.u);  dbeta_t = -e^{g_t} w.u + w.v_t
+ *     dk_t = -e^{g_t} beta_t (G u + S_{t-1} w) + beta_t G v_t
+ *     G <- e^{g_t} (G - beta_t k_t w^T)
+ * from G = dht down to dh0 = G (S_t the state after token t, S_0 = h0).  The
+ * states are recomputed in fp32 from checkpoints at every 64th token.
+ *   p, q, k, v, g, beta, scale, h0, cu_seqlens : as for gdn_chunk_fwd (K in
+ *                 {64, 128}, V a multiple of 16; any C)
+ *   dout        : [B, T, Hv, V], dtype p->dt;  dht : [N, Hv, K, V] fp32 or NULL (= 0)
+ *   dq, dk      : out [B, T, Hqk, K] fp32 (summed over the value heads of each
+ *                 q/k head);  dv : out [B, T, Hv, V] fp32
+ *   dg, dbeta   : out [B, T, Hv] fp32;  dh0 : out [N, Hv, K, V] fp32 or NULL
+ *   workspace   : gdn_chunk_bwd_workspace_size(p) bytes, 256-byte aligned
+ *                 (state checkpoints and the device status word)
+ * dq, dk, dg and dbeta are sums of fp32 atomic additions (their rounding may
+ * differ between runs).  Malformed cu_seqlens set the status word (read it
+ * with gdn_chunk_bwd_get_device_status) and leave the gradients incomplete.
+ * Asynchronous on `stream`.
+ */
+size_t gdn_chunk_bwd_workspace_size(const gdn_problem* p);
+gdn_status gdn_chunk_bwd(const gdn_problem* p, const void* q, const void* k, const void* v,
+                         const float* g, const float* beta, float scale, const float* h0,
+                         const int32_t* cu_seqlens, const void* dout, const float* dht,
+                         float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dh0,
+                         void* workspace, size_t workspace_bytes, void* stream);
+/* Status word of a gdn_chunk_bwd workspace (synchronises `stream`, then
+ * clears the word).  GDN_DEV_OK or GDN_DEV_BAD_CU_SEQLENS. */
+gdn_status gdn_chunk_bwd_get_device_status(void* workspace, void* stream, int* dev_status);
+
 /* Activation applied after the convolution of gdn_causal_conv1d_fwd. */
 typedef enum { GDN_ACT_NONE = 0, GDN_ACT_SILU = 1 } gdn_activation;
 
