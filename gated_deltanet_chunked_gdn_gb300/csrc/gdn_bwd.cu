@@ -32,28 +32,73 @@ namespace {
 constexpr int kCols = 16;   // V columns per CTA
 constexpr int kChunkB = 64;  // checkpoint interval
 constexpr int kSub = 16;     // tokens per recomputed block
-constexpr int kRow = 20;     // padded row length of the state tiles in shared memory (floats)
+constexpr int kRow = kCols;  // row length of the state tiles in shared memory (floats)
+
+// One 16-token block of the inputs, converted to fp32 (k, q: full rows; v,
+// dout: this CTA's 16 columns; e^g and beta).
+template <int K>
+struct TokBlock {
+  float k[kSub][K];
+  float q[kSub][K];
+  float v[kSub][kCols];
+  float dout[kSub][kCols];
+  float a[kSub];
+  float b[kSub];
+};
 
 template <int K>
 struct BwdSmem {
   float st[kSub + 1][K][kRow];        // states before each token of a block, and after its last
   float lvl[kChunkB / kSub][K][kRow];  // block-start states of a chunk
   float u[kSub][kCols];                // S_{t-1}^T k_t of the block's tokens
+  TokBlock<K> tb;
   float red[K / 32][kCols + 1];
   float sum[kCols + 1];
 };
 
-// Sum of NV values over the K threads of the block; the total lands in out[].
+// Warp sum of 16 values by reduce-scatter: at each of the first four levels a
+// lane keeps half of its values and adds its partner's copy of that half (8,
+// 4, 2, 1 exchanges), the fifth level adds the last pair; lanes 2j and 2j + 1
+// end with the total of value j.  16 shuffles instead of 80.
+__device__ __forceinline__ float warp_sum16(float (&x)[16], int lane) {
+#pragma unroll
+  for (int lvl = 0; lvl < 4; ++lvl) {
+    const int half = 8 >> lvl;              // values kept after this level
+    const int off = 16 >> lvl;              // partner lane distance
+    const bool upper = (lane & off) != 0;   // keep the upper half of the live values
+#pragma unroll
+    for (int j = 0; j < half; ++j) {
+      const float send = upper ? x[j] : x[j + half];
+      const float keep = upper ? x[j + half] : x[j];
+      x[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
+}
+
+// Index (0..15) of the value whose total lane `lane` holds after warp_sum16.
+__device__ __forceinline__ int warp_sum16_index(int lane) {
+  // level l kept the upper half when bit (16 >> l) of the lane was set; the
+  // kept half's offset adds 8 >> l
+  return ((lane & 16) ? 8 : 0) + ((lane & 8) ? 4 : 0) + ((lane & 4) ? 2 : 0) + ((lane & 2) ? 1 : 0);
+}
+
+// Sum of NV (16 or 17) values over the K threads of the block; the totals
+// land in out[].
 template <int K, int NV>
 __device__ __forceinline__ void block_sum(float (&x)[NV], float (*red)[kCols + 1], float* out, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
+  float y[16];
 #pragma unroll
-  for (int j = 0; j < NV; ++j)
+  for (int j = 0; j < 16; ++j) y[j] = x[j];
+  const float tot = warp_sum16(y, lane);
+  if ((lane & 1) == 0) red[warp][warp_sum16_index(lane)] = tot;
+  if (NV > 16) {
+    float z = x[NV - 1];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) x[j] += __shfl_xor_sync(0xffffffffu, x[j], off);
-  if (lane == 0)
-#pragma unroll
-    for (int j = 0; j < NV; ++j) red[warp][j] = x[j];
+    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+    if (lane == 0) red[warp][16] = z;
+  }
   __syncthreads();
   if (tid < NV) {
     float s = 0.f;
@@ -110,24 +155,46 @@ __device__ __forceinline__ bool bwd_bounds(const BwdArgs& a, int n, int64_t& tok
 // for all chunks of all sequences, below ceil(Ttot / 64) + N.
 __device__ __forceinline__ int64_t ckpt_slot(int64_t t0, int n) { return t0 / kChunkB + n; }
 
-// One forward token: S <- a (S - b k (k^T S)) + b k v^T for this thread's row.
+// Token block [t0, t0 + n) into shared memory (fp32), all threads.
 template <typename T, int K>
-__device__ __forceinline__ void fwd_token(const BwdArgs& a, BwdSmem<K>& s, int tid, int64_t t, int hq, int h, int e0,
+__device__ __forceinline__ void stage_block(const BwdArgs& a, TokBlock<K>& tb, int64_t t0, int n, int hq, int h,
+                                            int e0, bool with_q, int tid) {
+  const T* kp = static_cast<const T*>(a.k);
+  const T* qp = static_cast<const T*>(a.q);
+  for (int i = tid; i < n * K; i += K) {
+    const int r = i / K, d = i % K;
+    const int64_t off = ((t0 + r) * a.Hqk + hq) * (int64_t)K + d;
+    tb.k[r][d] = to_f(kp[off]);
+    if (with_q) tb.q[r][d] = to_f(qp[off]);
+  }
+  for (int i = tid; i < n * kCols; i += K) {
+    const int r = i / kCols, e = i % kCols;
+    const int64_t off = ((t0 + r) * a.Hv + h) * (int64_t)a.V + e0 + e;
+    tb.v[r][e] = to_f(static_cast<const T*>(a.v)[off]);
+    if (with_q) tb.dout[r][e] = to_f(static_cast<const T*>(a.dout)[off]);
+  }
+  if (tid < n) {
+    tb.a[tid] = expf(a.g[(t0 + tid) * a.Hv + h]);
+    tb.b[tid] = a.beta[(t0 + tid) * a.Hv + h];
+  }
+  __syncthreads();
+}
+
+// One forward token (row i of the staged block): S <- a (S - b k (k^T S)) + b k v^T
+// for this thread's row of the state.
+template <int K>
+__device__ __forceinline__ void fwd_token(const TokBlock<K>& tb, int i, float (*red)[kCols + 1], float* sum, int tid,
                                           float (&S)[kCols], float* u_out) {
-  const float kd = to_f(static_cast<const T*>(a.k)[(t * a.Hqk + hq) * (int64_t)K + tid]);
+  const float kd = tb.k[i][tid];
   float x[kCols];
 #pragma unroll
   for (int e = 0; e < kCols; ++e) x[e] = S[e] * kd;
-  block_sum<K, kCols>(x, s.red, s.sum, tid);
-  const float ag = expf(a.g[t * a.Hv + h]), b = a.beta[t * a.Hv + h];
-  const T* vt = static_cast<const T*>(a.v) + (t * a.Hv + h) * (int64_t)a.V + e0;
+  block_sum<K, kCols>(x, red, sum, tid);
+  const float ag = tb.a[i], b = tb.b[i];
 #pragma unroll
-  for (int e = 0; e < kCols; ++e) {
-    const float ue = s.sum[e];
-    S[e] = ag * (S[e] - b * kd * ue) + b * kd * to_f(vt[e]);
-  }
-  if (u_out && tid < kCols) u_out[tid] = s.sum[tid];
-  __syncthreads();   // s.sum is reused by the next reduction
+  for (int e = 0; e < kCols; ++e) S[e] = ag * (S[e] - b * kd * sum[e]) + b * kd * tb.v[i][e];
+  if (u_out && tid < kCols) u_out[tid] = sum[tid];
+  __syncthreads();   // sum is reused by the next reduction
 }
 
 // Checkpoints: the forward recurrence of every chain, the state slice saved at
@@ -136,6 +203,7 @@ template <typename T, int K>
 __global__ void __launch_bounds__(K) gdn_bwd_ckpt_kernel(const BwdArgs a) {
   __shared__ float red[K / 32][kCols + 1];
   __shared__ float sum[kCols + 1];
+  __shared__ TokBlock<K> tb;
   const int n = blockIdx.x, h = blockIdx.y, e0 = kCols * blockIdx.z, tid = threadIdx.x;
   const int hq = h / (a.Hv / a.Hqk);
   int64_t tok0, L;
@@ -145,23 +213,16 @@ __global__ void __launch_bounds__(K) gdn_bwd_ckpt_kernel(const BwdArgs a) {
   const float* h0p = a.h0 ? a.h0 + ((size_t)n * a.Hv + h) * KV + (size_t)tid * a.V + e0 : nullptr;
 #pragma unroll
   for (int e = 0; e < kCols; ++e) S[e] = h0p ? h0p[e] : 0.f;
-  for (int64_t i = 0; i < L; ++i) {
-    const int64_t t = tok0 + i;
-    if (i % kChunkB == 0) {
-      float* cp = a.ckpt + ((size_t)ckpt_slot(t, n) * a.Hv + h) * KV + (size_t)tid * a.V + e0;
+  for (int64_t i0 = 0; i0 < L; i0 += kSub) {
+    const int64_t t0 = tok0 + i0;
+    if (i0 % kChunkB == 0) {
+      float* cp = a.ckpt + ((size_t)ckpt_slot(t0, n) * a.Hv + h) * KV + (size_t)tid * a.V + e0;
 #pragma unroll
       for (int e = 0; e < kCols; e += 4) *reinterpret_cast<float4*>(cp + e) = make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
     }
-    const float kd = to_f(static_cast<const T*>(a.k)[(t * a.Hqk + hq) * (int64_t)K + tid]);
-    float x[kCols];
-#pragma unroll
-    for (int e = 0; e < kCols; ++e) x[e] = S[e] * kd;
-    block_sum<K, kCols>(x, red, sum, tid);
-    const float ag = expf(a.g[t * a.Hv + h]), b = a.beta[t * a.Hv + h];
-    const T* vt = static_cast<const T*>(a.v) + (t * a.Hv + h) * (int64_t)a.V + e0;
-#pragma unroll
-    for (int e = 0; e < kCols; ++e) S[e] = ag * (S[e] - b * kd * sum[e]) + b * kd * to_f(vt[e]);
-    __syncthreads();
+    const int nb = L - i0 < kSub ? (int)(L - i0) : kSub;
+    stage_block<T, K>(a, tb, t0, nb, hq, h, e0, false, tid);
+    for (int i = 0; i < nb; ++i) fwd_token<K>(tb, i, red, sum, tid, S, nullptr);
   }
 }
 
@@ -196,9 +257,11 @@ __global__ void __launch_bounds__(K) gdn_bwd_kernel(const BwdArgs a) {
     float S[kCols];
     get(a.ckpt + ((size_t)ckpt_slot(t0, n) * a.Hv + h) * KV + (size_t)tid * a.V + e0, S);
     // block-start states of the chunk
-    for (int i = 0; i < Lc; ++i) {
-      if (i % kSub == 0) put(&s.lvl[i / kSub][tid][0], S);
-      fwd_token<T, K>(a, s, tid, t0 + i, hq, h, e0, S, nullptr);
+    for (int i0 = 0; i0 < Lc; i0 += kSub) {
+      put(&s.lvl[i0 / kSub][tid][0], S);
+      const int nb = Lc - i0 < kSub ? Lc - i0 : kSub;
+      stage_block<T, K>(a, s.tb, t0 + i0, nb, hq, h, e0, false, tid);
+      for (int i = 0; i < nb; ++i) fwd_token<K>(s.tb, i, s.red, s.sum, tid, S, nullptr);
     }
     const int nsub = (Lc + kSub - 1) / kSub;
     for (int sb = nsub - 1; sb >= 0; --sb) {
@@ -206,23 +269,21 @@ __global__ void __launch_bounds__(K) gdn_bwd_kernel(const BwdArgs a) {
       const int nb = Lc - kSub * sb < kSub ? Lc - kSub * sb : kSub;
       get(&s.lvl[sb][tid][0], S);
       put(&s.st[0][tid][0], S);
+      stage_block<T, K>(a, s.tb, tb, nb, hq, h, e0, true, tid);
       for (int i = 0; i < nb; ++i) {
-        fwd_token<T, K>(a, s, tid, tb + i, hq, h, e0, S, &s.u[i][0]);
+        fwd_token<K>(s.tb, i, s.red, s.sum, tid, S, &s.u[i][0]);
         put(&s.st[i + 1][tid][0], S);
       }
       __syncthreads();   // u of the block visible to every thread
       for (int i = nb - 1; i >= 0; --i) {
         const int64_t t = tb + i;
-        const float qd = to_f(static_cast<const T*>(a.q)[(t * a.Hqk + hq) * (int64_t)K + tid]);
-        const float kd = to_f(static_cast<const T*>(a.k)[(t * a.Hqk + hq) * (int64_t)K + tid]);
-        const T* dot = static_cast<const T*>(a.dout) + (t * a.Hv + h) * (int64_t)a.V + e0;
-        const T* vt = static_cast<const T*>(a.v) + (t * a.Hv + h) * (int64_t)a.V + e0;
-        const float ag = expf(a.g[t * a.Hv + h]), b = a.beta[t * a.Hv + h];
+        const float qd = s.tb.q[i][tid], kd = s.tb.k[i][tid];
+        const float ag = s.tb.a[i], b = s.tb.b[i];
         float dov[kCols], vv[kCols], Sn[kCols], Sp[kCols], uu[kCols];
 #pragma unroll
         for (int e = 0; e < kCols; ++e) {
-          dov[e] = to_f(dot[e]);
-          vv[e] = to_f(vt[e]);
+          dov[e] = s.tb.dout[i][e];
+          vv[e] = s.tb.v[i][e];
           uu[e] = s.u[i][e];
         }
         get(&s.st[i + 1][tid][0], Sn);
