@@ -47,23 +47,22 @@ def peaks() -> dict:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def measured_traffic(path: str, B: int):
-    """DRAM bytes per launch of the fused kernel from the committed ncu
-    summary (profiles/fused_traffic.json), scaled to a batch of B sequences;
-    None when the kernel source changed since that capture."""
+def measured_traffic(op: str, units: float):
+    """DRAM bytes (read + write) per launch of op's kernels, from the committed
+    ncu summary table (profiles/traffic.json), scaled linearly from the
+    captured case to `units` (sequences, or pool entries for decode); None
+    when any of the kernels' sources changed since that capture."""
     import hashlib
-    if path != "fused":
-        return None
     try:
-        with open(os.path.join(ROOT, "profiles", "fused_traffic.json")) as f:
-            rec = json.load(f)
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[op]
+        for src, want in rec["sources"].items():
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != want:
+                    return None
     except (OSError, KeyError, ValueError):
         return None
-    if sha != rec.get("source_sha256"):
-        return None
-    return rec["dram_bytes_per_bench_launch"] * B / 16
+    return rec["dram_bytes_per_launch"] * units / rec["units"]
 
 
 def algorithmic(B, T, Hqk, Hv, K, V, C, elem=2, h0=True):
@@ -305,7 +304,8 @@ def run_conv1d(args, rank, world, dev):
         "config": {"workload": f"conv1d_{B}x{T}_D{D}_W{W}", "B": B, "T": T, "D": D, "W": W, "activation": "silu",
                    "parallelism": f"dp{world} (independent batches)",
                    "l2": f"inputs larger than L2 ({nbytes / 1e9:.1f} GB compulsory traffic per step)"},
-        "roofline": hbm_roofline(nbytes, sec_step, "conv1d_kernel + conv1d_state_kernel (one step)"),
+        "roofline": hbm_roofline(nbytes, sec_step, "conv1d_kernel + conv1d_state_kernel (one step)",
+                                 traffic=measured_traffic("conv1d", B * T / 8192)),
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": x_host.numel() * 2,
                 "d2h_bytes_per_step": y_host.numel() * 2, "steps": args.e2e_steps},
         "gpu_launches": 2 * args.steps,
@@ -362,7 +362,8 @@ def run_decode(args, rank, world, dev):
         "config": {"workload": f"decode_{N}x1_H{H}", "N": N, "H": H, "K": K, "V": K,
                    "parallelism": f"dp{world} (independent batches)",
                    "l2": f"state pool larger than L2 ({nbytes / 1e9:.2f} GB per step)"},
-        "roofline": hbm_roofline(nbytes, sec_step, "gdn_recurrent_kernel (the step's only launch)"),
+        "roofline": hbm_roofline(nbytes, sec_step, "gdn_recurrent_kernel (the step's only launch)",
+                                 traffic=measured_traffic("decode", N)),
         "gpu_launches": args.steps,
         "clocks": clocks,
     }
@@ -579,7 +580,7 @@ def main():
                           if flush is None else "L2 flushed (512 MB write) before every timed step")},
         "tflops_alg": flops / sec / 1e12,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": measured_traffic(path, w.B) if args.workload == "batched_16x8192" else None, "peak_source": pk["source"],
+                     "traffic": measured_traffic("fused", w.B) if path == "fused" and args.workload == "batched_16x8192" else None, "peak_source": pk["source"],
                      "kernel": "gdn_fused_kernel (the step's only launch)" if path == "fused"
                      else "gdn_chunk_fwd call (all launches of one step)",
                      "alg_bytes": nbytes, "alg_flops": flops,
