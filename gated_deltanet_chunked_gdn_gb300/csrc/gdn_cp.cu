@@ -172,14 +172,14 @@ __global__ void __launch_bounds__(256) cp_combine_kernel(const int32_t* __restri
   }
 }
 
+}  // namespace
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return 148;
   return n > 0 ? n : 148;
 }
-
-}  // namespace
 
 // Segment length (a multiple of the 64-token chunk, at least 512 tokens): aim
 // for about two (segment, head) chains per SM in the final pass, from the mean

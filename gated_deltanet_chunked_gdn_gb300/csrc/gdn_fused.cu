@@ -2,11 +2,13 @@
 // scaled_dot_kkt, solve_tril, wy_fast, chunk_h, chunk_o; MegaGDN-PTO
 // walkthrough, sections 1.1 and 4.5) in ONE sm_103a launch.
 //
-// One CTA per (sequence, value head) chain walks the chain's chunks in order;
-// the fp32 state never leaves the SM (TMEM) between chunks, and no
-// intermediate goes through HBM.  Two CTAs share an SM (their shared memory
-// and TMEM halves), so one chain's SIMT phases overlap the other's tensor
-// phases.  Chunks are 64 tokens; a C = 128 request is processed as two
+// A CTA walks a (sequence, value head) chain's chunks in order; the fp32
+// state stays on the SM (TMEM) between chunks, and no intermediate goes
+// through HBM.  Two CTAs share an SM (their shared memory and TMEM halves), so
+// one chain's SIMT phases overlap the other's tensor phases.  With more chains
+// than CTA slots, equal-length chains are dealt out as windows of an equal
+// number of chunks (one slot each, so the last wave leaves no SM half idle):
+// a chain cut at a window boundary hands its state over once through HBM.  Chunks are 64 tokens; a C = 128 request is processed as two
 // 64-token chunks (the chunked form is exact for any chunk length).
 //
 // Layout: everything is transposed so that every tcgen05.mma has M = 128 on
@@ -62,7 +64,7 @@ constexpr uint32_t OFF_BE = OFF_MISC + 512;    // float[64] beta e^gamma
 constexpr uint32_t OFF_DL = OFF_MISC + 768;    // float[64] e^{gamma_last - gamma}
 constexpr uint32_t OFF_EG = OFF_MISC + 1024;   // float[64] e^gamma
 constexpr uint32_t OFF_BAR = OFF_MISC + 1280;    // 5 mbarriers: k/q tiles, v tile, three MMA commit groups
-constexpr uint32_t OFF_FLAGS = OFF_MISC + 1320;  // [0] tmem base, [1] abort
+constexpr uint32_t OFF_FLAGS = OFF_MISC + 1320;  // [0] tmem base, [1] abort, [2] window
 constexpr uint32_t OFF_BAR1 = OFF_MISC + 1336;   // sixth mbarrier: first half of S^T Q^T
 constexpr uint32_t OFF_GRAW = OFF_MISC + 1344;   // float[2][2][64]: raw g, beta of two chunks
 constexpr uint32_t kSmemUsed = OFF_MISC + 2368;
@@ -88,6 +90,19 @@ struct FusedParams {
   // state-transition matrix -> ht2)
   float* ht2;
   int split;
+  // Window schedule (kFull, equal-length sequences; null sched = one chain per
+  // CTA).  The chains' chunks are laid end to end, each chain's in reverse
+  // order, and cut into nwin windows of W chunks; a CTA claims windows from
+  // the last down (sched[0] counts the claims) and runs a window's pieces in
+  // order.  A window starts with a prefix of a chain (or a whole chain) and
+  // ends with a suffix of one: a chain cut at a window boundary has its prefix
+  // run first thing by window m + 1, which hands its state over in slot m + 1
+  // of `hand` ([K][V] fp32 per slot) and sets sched[1 + m + 1]; window m waits
+  // for that flag before it runs the suffix, as its last piece.  W is at
+  // least the chunks of one chain, so no chain spans more than two windows.
+  int* sched;
+  float* hand;
+  int nwin, W;
 };
 
 // Kernel modes: the full forward pass, or final states only (no q, no o).
@@ -282,31 +297,40 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, hf = warp >> 2;   // TMEM lane quadrant, column half
+  const bool windowed = MODE == kFull && prm.sched != nullptr;
   // kStates: the upper half of the grid computes transition matrices
   const bool trans = MODE == kStates && (int)blockIdx.x >= prm.split;
-  const int chain = trans ? (int)blockIdx.x - prm.split : (int)blockIdx.x;
-  const int n = chain / prm.Hv, h = chain % prm.Hv;
-  const int hq = h / (prm.Hv / prm.Hqk);
+  // the chain of the current piece: sequence n, value head h, its qk head,
+  // first token, length and chunks
+  int n = 0, h = 0, hq = 0, nchunks = 0;
+  int64_t tok0 = 0, L = 0;
 
-  // sequence bounds (validated: a malformed cu_seqlens touches no memory)
-  int64_t tok0, L;
-  if (prm.varlen) {
-    const int64_t a = prm.cu[n], b = prm.cu[n + 1];
-    bool ok = (0 <= a) && (a <= b) && (b <= prm.Ttot);
-    if (chain == 0 && (prm.cu[0] != 0 || prm.cu[prm.N] != prm.Ttot)) ok = false;
-    if (!ok) {
-      if (tid == 0) atomicExch(prm.status, GDN_DEV_BAD_CU_SEQLENS);
-      return;
+  // one chain per CTA: sequence bounds (validated: a malformed cu_seqlens
+  // touches no memory)
+  if (!windowed) {
+    const int chain = trans ? (int)blockIdx.x - prm.split : (int)blockIdx.x;
+    n = chain / prm.Hv;
+    h = chain % prm.Hv;
+    hq = h / (prm.Hv / prm.Hqk);
+    if (prm.varlen) {
+      const int64_t a = prm.cu[n], b = prm.cu[n + 1];
+      bool ok = (0 <= a) && (a <= b) && (b <= prm.Ttot);
+      if (chain == 0 && (prm.cu[0] != 0 || prm.cu[prm.N] != prm.Ttot)) ok = false;
+      if (!ok) {
+        if (tid == 0) atomicExch(prm.status, GDN_DEV_BAD_CU_SEQLENS);
+        return;
+      }
+      tok0 = a;
+      L = b - a;
+    } else {
+      tok0 = (int64_t)n * prm.Tseq;
+      L = prm.Tseq;
     }
-    tok0 = a;
-    L = b - a;
-  } else {
-    tok0 = (int64_t)n * prm.Tseq;
-    L = prm.Tseq;
+    nchunks = (int)((L + kChunk - 1) / kChunk);
   }
-  const int nchunks = (int)((L + kChunk - 1) / kChunk);
 
   if (tid == 0) {
+    flags[2] = windowed ? prm.nwin - 1 - atomicAdd(prm.sched, 1) : 0;
     mbar_init(bar_kq, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
@@ -328,20 +352,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
   const uint32_t R_S = tmem, R_a = tmem + 128, R_b = tmem + 192;
   const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
   const int row = 32 * qd + lane;   // this thread's TMEM lane (e or d or chunk row)
-
-  // state S^T[e][d] = h0[d][e] (the identity for a transition chain)
-  {
-    const float* h0p = prm.h0 ? prm.h0 + ((int64_t)n * prm.Hv + h) * kD * kD : nullptr;
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      float v[32];
-      const int d0 = 64 * hf + 32 * half;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = trans ? (d0 + i == row ? 1.f : 0.f) : (h0p ? h0p[(int64_t)(d0 + i) * kD + row] : 0.f);
-      tmem_st32(R_S + lane_off + d0, v);
-    }
-    tmem_wait_st();
-  }
 
   uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_x = 0, ph_q = 0, ph_o1 = 0;
   bool kq_pending = false, v_pending = false;   // meaningful in thread 0
@@ -385,12 +395,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
   };
   const uint32_t s4 = (sbase & 0x3FFFFu) >> 4;   // descriptor address field of the tile base
 
-  tc_fence_before();
-  __syncthreads();
-  if (tid == 0 && nchunks > 0) {
-    issue_kq(0);
-    if (!trans) issue_v(0);   // a transition chain has v = 0: U = 0 and no v tile
-  }
   // warp 1 stages chunk cc's g and beta rows in graw[cc & 1] (lane l: rows
   // 2 l and 2 l + 1, zeros past the sequence) with asynchronous copies
   float* graw = reinterpret_cast<float*>(sm + OFF_GRAW);
@@ -410,320 +414,408 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
     }
     cp_async_commit();
   };
-  if (warp == 1 && nchunks > 0) fetch_gb(0);
+  // this CTA's window: positions [wpos, wend) of the reversed chunk order
+  const int nch = (prm.Tseq + kChunk - 1) / kChunk;   // chunks per chain (window schedule)
+  const int win = (int)flags[2];
+  int64_t wpos = 0, wend = 0;
+  if (windowed) {
+    const int64_t U = (int64_t)prm.N * prm.Hv * nch;
+    wpos = (int64_t)win * prm.W;
+    wend = wpos + prm.W < U ? wpos + prm.W : U;
+  }
+  int* hflag = windowed ? prm.sched + 1 : nullptr;   // hflag[m]: slot m of `hand` is ready
 
 #pragma unroll 1
-  for (int c = 0; c < nchunks; ++c) {
-    const int64_t t0 = tok0 + (int64_t)kChunk * c;
-    const int Lc = (int)((L - (int64_t)kChunk * c) < kChunk ? (L - (int64_t)kChunk * c) : kChunk);
-
-    // ---- S0 (warp 1, while thread 0 issues M1): gamma = in-chunk cumsum of g,
-    // from the g / beta rows copied to shared memory one chunk ahead (lane l
-    // copied and reads rows 2l and 2l + 1); the next sync comes before any
-    // other reader.
-    if (warp == 1) {
-      cp_async_wait_all();   // this lane's copies of chunk c (issued one chunk ago)
-      const float* cur = graw + (c & 1) * 128;
-      const float ga = cur[2 * lane], gb = cur[2 * lane + 1], ba = cur[64 + 2 * lane], bb = cur[64 + 2 * lane + 1];
-      if (c + 1 < nchunks) fetch_gb(c + 1);
-      float sum = ga + gb;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float t = __shfl_up_sync(0xffffffffu, sum, off);
-        if (lane >= off) sum += t;
-      }
-      // gam <- log2(e) * cumsum: e^{gamma_i - gamma_j} is then one subtraction and one ex2
-      const float g0 = (sum - gb) * kLog2e, g1 = sum * kLog2e;
-      const float gl = __shfl_sync(0xffffffffu, sum, 31) * kLog2e;
-      *reinterpret_cast<float2*>(gam + 2 * lane) = make_float2(g0, g1);
-      *reinterpret_cast<float2*>(bet + 2 * lane) = make_float2(ba, bb);
-      *reinterpret_cast<float2*>(be + 2 * lane) = make_float2(ba * ex2_fast(g0), bb * ex2_fast(g1));
-      *reinterpret_cast<float2*>(dl + 2 * lane) = make_float2(ex2_fast(gl - g0), ex2_fast(gl - g1));
-      *reinterpret_cast<float2*>(eg + 2 * lane) = make_float2(prm.scale * ex2_fast(g0), prm.scale * ex2_fast(g1));
+  for (bool first = true;; first = false) {
+    // ---- the next piece: chunks [c_begin, c_end) of one chain
+    int c_begin = 0, c_end = nchunks;
+    bool from_hand = false, to_hand = false;
+    if (windowed) {
+      if (wpos >= wend) break;
+      const int64_t j = wpos / nch, off = wpos - j * nch;
+      const int64_t len = (wend < (j + 1) * nch ? wend : (j + 1) * nch) - wpos;
+      n = (int)(j / prm.Hv);
+      h = (int)(j % prm.Hv);
+      hq = h / (prm.Hv / prm.Hqk);
+      tok0 = (int64_t)n * prm.Tseq;
+      L = prm.Tseq;
+      nchunks = nch;
+      c_begin = (int)(nch - off - len);
+      c_end = (int)(nch - off);
+      from_hand = c_begin > 0;   // the suffix of a chain whose prefix window win + 1 ran
+      to_hand = c_end < nch;     // the prefix of a chain whose suffix window win - 1 runs
+      wpos += len;
+    } else if (!first) {
+      break;
+    }
+    if (from_hand) {
+      if (tid == 0 && !flag_wait(hflag + win + 1, prm.status)) flags[1] = 1;
+      __syncthreads();
+      if (flags[1]) break;
     }
 
-    // ---- M1: [K;Q] K^T -> R_a
-    if (tid == 0) {
-      // the next chunk's k / q boxes go to L2 now; their TMA load (issued
-      // once M4 frees the tile) then waits on L2 instead of HBM
-      if (!mbar_wait(bar_kq, ph_kq, prm.status)) {
-        flags[1] = 1;
+    // state S^T[e][d] = h0[d][e] (the identity for a transition chain; the
+    // handed-over state for a chain's suffix, read past L1)
+    {
+      const float* h0p = from_hand ? prm.hand + (int64_t)(win + 1) * kD * kD
+                                   : (prm.h0 ? prm.h0 + ((int64_t)n * prm.Hv + h) * kD * kD : nullptr);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float v[32];
+        const int d0 = 64 * hf + 32 * half;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int64_t at = (int64_t)(d0 + i) * kD + row;
+          v[i] = trans ? (d0 + i == row ? 1.f : 0.f) : (!h0p ? 0.f : (from_hand ? __ldcg(h0p + at) : h0p[at]));
+        }
+        tmem_st32(R_S + lane_off + d0, v);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && c_begin < c_end) {
+      issue_kq(c_begin);
+      if (!trans) issue_v(c_begin);   // a transition chain has v = 0: U = 0 and no v tile
+    }
+    if (warp == 1 && c_begin < c_end) fetch_gb(c_begin);
+
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; ++c) {
+      const int64_t t0 = tok0 + (int64_t)kChunk * c;
+      const int Lc = (int)((L - (int64_t)kChunk * c) < kChunk ? (L - (int64_t)kChunk * c) : kChunk);
+
+      // ---- S0 (warp 1, while thread 0 issues M1): gamma = in-chunk cumsum of g,
+      // from the g / beta rows copied to shared memory one chunk ahead (lane l
+      // copied and reads rows 2l and 2l + 1); the next sync comes before any
+      // other reader.
+      if (warp == 1) {
+        cp_async_wait_all();   // this lane's copies of chunk c (issued one chunk ago)
+        const float* cur = graw + (c & 1) * 128;
+        const float ga = cur[2 * lane], gb = cur[2 * lane + 1], ba = cur[64 + 2 * lane], bb = cur[64 + 2 * lane + 1];
+        if (c + 1 < c_end) fetch_gb(c + 1);
+        float sum = ga + gb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float t = __shfl_up_sync(0xffffffffu, sum, off);
+          if (lane >= off) sum += t;
+        }
+        // gam <- log2(e) * cumsum: e^{gamma_i - gamma_j} is then one subtraction and one ex2
+        const float g0 = (sum - gb) * kLog2e, g1 = sum * kLog2e;
+        const float gl = __shfl_sync(0xffffffffu, sum, 31) * kLog2e;
+        *reinterpret_cast<float2*>(gam + 2 * lane) = make_float2(g0, g1);
+        *reinterpret_cast<float2*>(bet + 2 * lane) = make_float2(ba, bb);
+        *reinterpret_cast<float2*>(be + 2 * lane) = make_float2(ba * ex2_fast(g0), bb * ex2_fast(g1));
+        *reinterpret_cast<float2*>(dl + 2 * lane) = make_float2(ex2_fast(gl - g0), ex2_fast(gl - g1));
+        *reinterpret_cast<float2*>(eg + 2 * lane) = make_float2(prm.scale * ex2_fast(g0), prm.scale * ex2_fast(g1));
+      }
+
+      // ---- M1: [K;Q] K^T -> R_a
+      if (tid == 0) {
+        // the next chunk's k / q boxes go to L2 now; their TMA load (issued
+        // once M4 frees the tile) then waits on L2 instead of HBM
+        if (!mbar_wait(bar_kq, ph_kq, prm.status)) {
+          flags[1] = 1;
+        } else {
+          ph_kq ^= 1;
+          kq_pending = false;
+          tc_fence_after();
+          const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            const uint32_t a = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
+            mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, a, 16), id, s > 0);
+          }
+          mma_commit(bar_mma);
+          ++mma_pending;
+        }
+        if (c + 1 < c_end) {
+          const int tn = (int)(t0 + kChunk);
+          tma_prefetch_3d(&tm_k, 0, hq, tn);
+          tma_prefetch_3d(&tm_k, 64, hq, tn);
+          if (MODE == kFull) {
+            tma_prefetch_3d(&tm_q, 0, hq, tn);
+            tma_prefetch_3d(&tm_q, 64, hq, tn);
+          }
+        }
+        bulk_wait_read();   // the previous chunk's o staging (region X) has been read by its TMA store
+      }
+      if (!wait_mma()) break;
+
+      // ---- S1: A rows (lanes 0..63) and P rows (lanes 64..127)
+      {
+        float v[32];
+        // warps whose whole 32x32 block lies above the diagonal only write zeros
+        const bool upper = (qd & 1) == 0 && hf == 1;
+        const int i = qd < 2 ? row : row - 64;
+        if (upper) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) v[jj] = 0.f;
+        } else {
+          tmem_ld32(R_a + lane_off + 32 * hf, v);
+          const float ri = qd < 2 ? bet[i] : prm.scale;   // P carries the output scale: OP = scale V'^T P^T
+          const float gi = gam[i];
+          const int lim = qd < 2 ? i : i + 1;              // A: j < i (strict); P: j <= i
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 gj = *reinterpret_cast<const float4*>(gam + 32 * hf + 4 * k4);
+            const float gjs[4] = {gj.x, gj.y, gj.z, gj.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int j = 32 * hf + 4 * k4 + u;
+              v[4 * k4 + u] = j < lim ? ri * ex2_fast(gi - gjs[u]) * v[4 * k4 + u] : 0.f;
+            }
+          }
+        }
+        if (qd < 2) {
+          float4* dst = reinterpret_cast<float4*>(As + i * kAsLd + 32 * hf);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
+        }
+      }
+
+      // ---- S2: solve_tril in place; T diag(beta) and T diag(beta e^g) go out as
+      // bf16 operands.  Warps 0 and 5 wrote rows 0..31 x cols 0..31 and rows
+      // 32..63 x cols 32..63 of A: each solves its two diagonal 16x16 blocks and
+      // merges them into its 32x32 diagonal block of T without waiting for the
+      // other warps, which meanwhile zero the upper 16x16 blocks of both
+      // operands (one 16-byte chunk per thread and operand).
+      if (warp == 0 || warp == 5) {
+        const int o = warp == 5 ? 32 : 0;
+        __syncwarp();
+        diag_pair(As, o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+        __syncwarp();
+        merge16_warp(As, tmp + (warp == 5 ? 16 * 24 : 0), o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
       } else {
-        ph_kq ^= 1;
-        kq_pending = false;
+        const int u = 32 * (warp - 1 - (warp > 5 ? 1 : 0)) + lane;   // 0..191 over warps 1-4, 6, 7
+        const int blk = u >> 5, r = (u >> 1) & 15, half = u & 1;
+        const int rb = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
+        *reinterpret_cast<uint4*>(sm + OFF_TB + off) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sm + OFF_TBE + off) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      tc_fence_before();
+      __syncthreads();
+      merge_level<32>(As, tmp, warp, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+
+      // ---- M2: W^T = K^T (T diag(beta e^g))^T -> R_a ; U^T = V^T (T diag(beta))^T -> R_b
+      if (tid == 0) {
+        if (!trans && !mbar_wait(bar_v, ph_v, prm.status)) {
+          flags[1] = 1;
+        } else {
+          if (!trans) {
+            ph_v ^= 1;
+            v_pending = false;
+          }
+          tc_fence_after();
+          const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            mma_bf16(R_a, dsw(s4, OFF_KQ + s * 2048, 16384), dsw(s4, OFF_TBE + s * 32, 16), id, s > 0);
+          if (!trans) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              mma_bf16(R_b, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), id, s > 0);
+          }
+          mma_commit(bar_mma);
+          ++mma_pending;
+        }
+      }
+      // ---- S4 (while M2 runs): S^T -> bf16 [e][d] (K-major A), S^T *= e^{g_last}
+      {
+        float v[32];
+        const float dec = ex2_fast(gam[kChunk - 1]);
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+          const uint32_t col = 64 * hf + 32 * half;
+          tmem_ld32(R_S + lane_off + col, v);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            store8_bf16(sm + OFF_ST + hf * 16384 + sw128_chunk(row, 4 * half + cc), v + 8 * cc);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= dec;
+          tmem_st32(R_S + lane_off + col, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      if (!wait_mma()) break;
+      if (tid == 0 && c + 1 < c_end && !trans) issue_v(c + 1);   // v tile consumed
+
+      // ---- S3: W^T -> bf16 [d][i] (MN-major B)
+      {
+        float v[32];
+        tmem_ld32(R_a + lane_off + 32 * hf, v);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_W + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+
+      // ---- M3: V'^T = U^T - S^T W^T (R_b) ; OQ^T = S^T Q^T (R_a).  S5 overwrites
+      // the first half of S^T (k-steps 0..3) with V'^T: the S^T Q^T k-steps that
+      // read it commit to bar_o1, which S5 waits for before that store.
+      if (tid == 0) {
         tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
+        const uint32_t idv = idesc_bf16(128, 64, 0, 1, 1);
+        const uint32_t ido = idesc_bf16(128, 64, 0, 0, 0);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t a = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
-          mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, a, 16), id, s > 0);
+          const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+          mma_bf16(R_b, dsw(s4, a, 16), dsw(s4, OFF_W + s * 2048, 16384), idv, (trans && s == 0) ? 0u : 1u);
         }
-        mma_commit(bar_mma);
-        ++mma_pending;
-      }
-      if (c + 1 < nchunks) {
-        const int tn = (int)(t0 + kChunk);
-        tma_prefetch_3d(&tm_k, 0, hq, tn);
-        tma_prefetch_3d(&tm_k, 64, hq, tn);
+        mma_commit(bar_x);    // V' ready: S5 starts while Q S runs
+        ++x_pending;
+#pragma unroll
+        for (int s = 0; s < (MODE == kFull ? 8 : 0); ++s) {
+          const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+          const uint32_t b = OFF_KQ + 8192 + (s >> 2) * 16384 + (s & 3) * 32;
+          mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, b, 16), ido, s > 0);
+          if (s == 3) {
+            mma_commit(bar_o1);   // S^T's first half read
+            ++o1_pending;
+          }
+        }
         if (MODE == kFull) {
-          tma_prefetch_3d(&tm_q, 0, hq, tn);
-          tma_prefetch_3d(&tm_q, 64, hq, tn);
+          mma_commit(bar_mma);
+          ++mma_pending;
         }
       }
-      bulk_wait_read();   // the previous chunk's o staging (region X) has been read by its TMA store
-    }
-    if (!wait_mma()) break;
+      wait_commit(bar_x, ph_x, x_pending);
+      if (!sync_ok()) break;
 
-    // ---- S1: A rows (lanes 0..63) and P rows (lanes 64..127)
-    {
-      float v[32];
-      // warps whose whole 32x32 block lies above the diagonal only write zeros
-      const bool upper = (qd & 1) == 0 && hf == 1;
-      const int i = qd < 2 ? row : row - 64;
-      if (upper) {
+      // ---- S5: V'^T -> bf16 [e][j] ; V''^T = V'^T diag(e^{g_last - g}) -> bf16
+      {
+        float v[32], w[32];
+        tmem_ld32(R_b + lane_off + 32 * hf, v);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) v[jj] = 0.f;
-      } else {
-        tmem_ld32(R_a + lane_off + 32 * hf, v);
-        const float ri = qd < 2 ? bet[i] : prm.scale;   // P carries the output scale: OP = scale V'^T P^T
-        const float gi = gam[i];
-        const int lim = qd < 2 ? i : i + 1;              // A: j < i (strict); P: j <= i
+        for (int jj = 0; jj < 32; ++jj) w[jj] = v[jj] * dl[32 * hf + jj];
 #pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
-          const float4 gj = *reinterpret_cast<const float4*>(gam + 32 * hf + 4 * k4);
-          const float gjs[4] = {gj.x, gj.y, gj.z, gj.w};
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
+        if (MODE == kFull) wait_commit(bar_o1, ph_o1, o1_pending);   // S^T Q^T no longer reads the first half of S^T
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int j = 32 * hf + 4 * k4 + u;
-            v[4 * k4 + u] = j < lim ? ri * ex2_fast(gi - gjs[u]) * v[4 * k4 + u] : 0.f;
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+
+      // ---- M4: OP^T = V'^T P^T (R_b) ; S^T += V''^T K (R_S)
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idp = idesc_bf16(128, 64, 0, 0, 0);
+        const uint32_t ids = idesc_bf16(128, 128, 0, 1, 0);
+        if (MODE == kFull) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            mma_bf16(R_b, dsw(s4, OFF_VP + s * 32, 16), dsw(s4, OFF_P + s * 32, 16), idp, s > 0);
+          mma_commit(bar_q);
+          ++q_pending;
+        }
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(R_S, dsw(s4, OFF_VPP + s * 32, 16), dsw(s4, OFF_KQ + s * 2048, 16384), ids, 1);
+        mma_commit(bar_x);    // state updated: the k / q tiles are free
+        ++x_pending;
+      }
+      if (MODE == kStates) {
+        // final states only: wait for the state update, release the k tile
+        wait_commit(bar_x, ph_x, x_pending);
+        if (tid == 0 && c + 1 < c_end && !flags[1]) issue_kq(c + 1);
+        if (!sync_ok()) break;
+        continue;
+      }
+      wait_commit(bar_mma, ph_mma, mma_pending);   // S^T Q^T (committed in M3)
+      wait_commit(bar_q, ph_q, q_pending);         // V'^T P^T
+      if (!sync_ok()) break;
+
+      // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
+      {
+        // this thread holds column e = row of o for 32 rows i; neighbouring
+        // lanes exchange values so that each writes bf16 pairs (e, e + 1)
+        // staging row i, bf16 pair (e, e + 1): byte i*128 + ((e/8 ^ i%8) << 4) + (e%8)*2.
+        // With i = col + 2 pp + odd (col a multiple of 16), i%8 = (2 pp)%8 | odd.
+        const int ecol = (row & 63) & ~1;
+        const bool odd = lane & 1;
+        uint8_t* lbase = sm + OFF_OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
+        const uint32_t xsw = (static_cast<uint32_t>((ecol >> 3) ^ (odd ? 1 : 0))) << 4;
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+          float a[16], b[16];
+          const uint32_t col = 32 * hf + 16 * q;
+          tmem_ld16(R_a + lane_off + col, a);
+          tmem_ld16(R_b + lane_off + col, b);
+          float e[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 x = *reinterpret_cast<const float4*>(eg + col + 4 * k4);
+            e[4 * k4] = x.x, e[4 * k4 + 1] = x.y, e[4 * k4 + 2] = x.z, e[4 * k4 + 3] = x.w;
+          }
+          uint8_t* qb = lbase + col * 128;
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp) {
+            const float v0 = fmaf(e[2 * pp], a[2 * pp], b[2 * pp]);
+            const float v1 = fmaf(e[2 * pp + 1], a[2 * pp + 1], b[2 * pp + 1]);
+            const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+            const uint32_t word = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
+            const uint32_t off = (2 * pp) * 128 + (xsw ^ (static_cast<uint32_t>((2 * pp) & 7) << 4));
+            *reinterpret_cast<uint32_t*>(qb + off) = word;
           }
         }
       }
-      if (qd < 2) {
-        float4* dst = reinterpret_cast<float4*>(As + i * kAsLd + 32 * hf);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      // the state update ran under S6; its completion frees the k / q tile
+      wait_commit(bar_x, ph_x, x_pending);
+      if (tid == 0 && c + 1 < c_end && !flags[1]) issue_kq(c + 1);
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      if (Lc == kChunk) {
+        if (tid == 0) {
+          tma_store_3d(&tm_o, sm + OFF_OS, 0, h, (int)t0);
+          tma_store_3d(&tm_o, sm + OFF_OS + 8192, 64, h, (int)t0);
+          bulk_commit();
+        }
       } else {
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
+        // tail chunk: only rows of this sequence are stored
+        for (int u = tid; u < kChunk * 16; u += kThreads) {
+          const int i = u >> 4, cc = u & 15;
+          if (i < Lc) {
+            const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OS + (cc >> 3) * 8192 + sw128_chunk(i, cc & 7));
+            *reinterpret_cast<uint4*>(prm.o + ((t0 + i) * prm.Hv + h) * kD + cc * 8) = val;
+          }
+        }
+        __syncthreads();
       }
     }
-
-    // ---- S2: solve_tril in place; T diag(beta) and T diag(beta e^g) go out as
-    // bf16 operands.  Warps 0 and 5 wrote rows 0..31 x cols 0..31 and rows
-    // 32..63 x cols 32..63 of A: each solves its two diagonal 16x16 blocks and
-    // merges them into its 32x32 diagonal block of T without waiting for the
-    // other warps, which meanwhile zero the upper 16x16 blocks of both
-    // operands (one 16-byte chunk per thread and operand).
-    if (warp == 0 || warp == 5) {
-      const int o = warp == 5 ? 32 : 0;
-      __syncwarp();
-      diag_pair(As, o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
-      __syncwarp();
-      merge16_warp(As, tmp + (warp == 5 ? 16 * 24 : 0), o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
-    } else {
-      const int u = 32 * (warp - 1 - (warp > 5 ? 1 : 0)) + lane;   // 0..191 over warps 1-4, 6, 7
-      const int blk = u >> 5, r = (u >> 1) & 15, half = u & 1;
-      const int rb = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-      const int cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
-      *reinterpret_cast<uint4*>(sm + OFF_TB + off) = make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4*>(sm + OFF_TBE + off) = make_uint4(0u, 0u, 0u, 0u);
-    }
-    tc_fence_before();
-    __syncthreads();
-    merge_level<32>(As, tmp, warp, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
-
-    // ---- M2: W^T = K^T (T diag(beta e^g))^T -> R_a ; U^T = V^T (T diag(beta))^T -> R_b
-    if (tid == 0) {
-      if (!trans && !mbar_wait(bar_v, ph_v, prm.status)) {
-        flags[1] = 1;
-      } else {
-        if (!trans) {
-          ph_v ^= 1;
-          v_pending = false;
-        }
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          mma_bf16(R_a, dsw(s4, OFF_KQ + s * 2048, 16384), dsw(s4, OFF_TBE + s * 32, 16), id, s > 0);
-        if (!trans) {
-#pragma unroll
-          for (int s = 0; s < 4; ++s)
-            mma_bf16(R_b, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), id, s > 0);
-        }
-        mma_commit(bar_mma);
-        ++mma_pending;
-      }
-    }
-    // ---- S4 (while M2 runs): S^T -> bf16 [e][d] (K-major A), S^T *= e^{g_last}
-    {
-      float v[32];
-      const float dec = ex2_fast(gam[kChunk - 1]);
+    if (flags[1]) break;
+    if (to_hand || (trans ? prm.ht2 != nullptr : prm.ht != nullptr)) {
+      // final state ht[d][e] = S^T[e][d] (or the hand-over slot of this window)
+      float* htp = to_hand ? prm.hand + (int64_t)win * kD * kD
+                           : (trans ? prm.ht2 : prm.ht) + ((int64_t)n * prm.Hv + h) * kD * kD;
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
-        const uint32_t col = 64 * hf + 32 * half;
-        tmem_ld32(R_S + lane_off + col, v);
+        float v[32];
+        const int d0 = 64 * hf + 32 * half;
+        tmem_ld32(R_S + lane_off + d0, v);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc)
-          store8_bf16(sm + OFF_ST + hf * 16384 + sw128_chunk(row, 4 * half + cc), v + 8 * cc);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= dec;
-        tmem_st32(R_S + lane_off + col, v);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-    }
-    if (!wait_mma()) break;
-    if (tid == 0 && c + 1 < nchunks && !trans) issue_v(c + 1);   // v tile consumed
-
-    // ---- S3: W^T -> bf16 [d][i] (MN-major B)
-    {
-      float v[32];
-      tmem_ld32(R_a + lane_off + 32 * hf, v);
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_W + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- M3: V'^T = U^T - S^T W^T (R_b) ; OQ^T = S^T Q^T (R_a).  S5 overwrites
-    // the first half of S^T (k-steps 0..3) with V'^T: the S^T Q^T k-steps that
-    // read it commit to bar_o1, which S5 waits for before that store.
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idv = idesc_bf16(128, 64, 0, 1, 1);
-      const uint32_t ido = idesc_bf16(128, 64, 0, 0, 0);
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-        mma_bf16(R_b, dsw(s4, a, 16), dsw(s4, OFF_W + s * 2048, 16384), idv, (trans && s == 0) ? 0u : 1u);
-      }
-      mma_commit(bar_x);    // V' ready: S5 starts while Q S runs
-      ++x_pending;
-#pragma unroll
-      for (int s = 0; s < (MODE == kFull ? 8 : 0); ++s) {
-        const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-        const uint32_t b = OFF_KQ + 8192 + (s >> 2) * 16384 + (s & 3) * 32;
-        mma_bf16(R_a, dsw(s4, a, 16), dsw(s4, b, 16), ido, s > 0);
-        if (s == 3) {
-          mma_commit(bar_o1);   // S^T's first half read
-          ++o1_pending;
-        }
-      }
-      if (MODE == kFull) {
-        mma_commit(bar_mma);
-        ++mma_pending;
+        for (int i = 0; i < 32; ++i) htp[(int64_t)(d0 + i) * kD + row] = v[i];
       }
     }
-    wait_commit(bar_x, ph_x, x_pending);
-    if (!sync_ok()) break;
-
-    // ---- S5: V'^T -> bf16 [e][j] ; V''^T = V'^T diag(e^{g_last - g}) -> bf16
-    {
-      float v[32], w[32];
-      tmem_ld32(R_b + lane_off + 32 * hf, v);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) w[jj] = v[jj] * dl[32 * hf + jj];
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
-      if (MODE == kFull) wait_commit(bar_o1, ph_o1, o1_pending);   // S^T Q^T no longer reads the first half of S^T
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- M4: OP^T = V'^T P^T (R_b) ; S^T += V''^T K (R_S)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idp = idesc_bf16(128, 64, 0, 0, 0);
-      const uint32_t ids = idesc_bf16(128, 128, 0, 1, 0);
-      if (MODE == kFull) {
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          mma_bf16(R_b, dsw(s4, OFF_VP + s * 32, 16), dsw(s4, OFF_P + s * 32, 16), idp, s > 0);
-        mma_commit(bar_q);
-        ++q_pending;
-      }
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        mma_bf16(R_S, dsw(s4, OFF_VPP + s * 32, 16), dsw(s4, OFF_KQ + s * 2048, 16384), ids, 1);
-      mma_commit(bar_x);    // state updated: the k / q tiles are free
-      ++x_pending;
-    }
-    if (MODE == kStates) {
-      // final states only: wait for the state update, release the k tile
-      wait_commit(bar_x, ph_x, x_pending);
-      if (tid == 0 && c + 1 < nchunks && !flags[1]) issue_kq(c + 1);
-      if (!sync_ok()) break;
-      continue;
-    }
-    wait_commit(bar_mma, ph_mma, mma_pending);   // S^T Q^T (committed in M3)
-    wait_commit(bar_q, ph_q, q_pending);         // V'^T P^T
-    if (!sync_ok()) break;
-
-    // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
-    {
-      // this thread holds column e = row of o for 32 rows i; neighbouring
-      // lanes exchange values so that each writes bf16 pairs (e, e + 1)
-      // staging row i, bf16 pair (e, e + 1): byte i*128 + ((e/8 ^ i%8) << 4) + (e%8)*2.
-      // With i = col + 2 pp + odd (col a multiple of 16), i%8 = (2 pp)%8 | odd.
-      const int ecol = (row & 63) & ~1;
-      const bool odd = lane & 1;
-      uint8_t* lbase = sm + OFF_OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
-      const uint32_t xsw = (static_cast<uint32_t>((ecol >> 3) ^ (odd ? 1 : 0))) << 4;
-#pragma unroll 1
-      for (int q = 0; q < 2; ++q) {
-        float a[16], b[16];
-        const uint32_t col = 32 * hf + 16 * q;
-        tmem_ld16(R_a + lane_off + col, a);
-        tmem_ld16(R_b + lane_off + col, b);
-        float e[16];
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const float4 x = *reinterpret_cast<const float4*>(eg + col + 4 * k4);
-          e[4 * k4] = x.x, e[4 * k4 + 1] = x.y, e[4 * k4 + 2] = x.z, e[4 * k4 + 3] = x.w;
-        }
-        uint8_t* qb = lbase + col * 128;
-#pragma unroll
-        for (int pp = 0; pp < 8; ++pp) {
-          const float v0 = fmaf(e[2 * pp], a[2 * pp], b[2 * pp]);
-          const float v1 = fmaf(e[2 * pp + 1], a[2 * pp + 1], b[2 * pp + 1]);
-          const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-          const uint32_t word = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
-          const uint32_t off = (2 * pp) * 128 + (xsw ^ (static_cast<uint32_t>((2 * pp) & 7) << 4));
-          *reinterpret_cast<uint32_t*>(qb + off) = word;
-        }
-      }
-    }
-    // the state update ran under S6; its completion frees the k / q tile
-    wait_commit(bar_x, ph_x, x_pending);
-    if (tid == 0 && c + 1 < nchunks && !flags[1]) issue_kq(c + 1);
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (Lc == kChunk) {
-      if (tid == 0) {
-        tma_store_3d(&tm_o, sm + OFF_OS, 0, h, (int)t0);
-        tma_store_3d(&tm_o, sm + OFF_OS + 8192, 64, h, (int)t0);
-        bulk_commit();
-      }
-    } else {
-      // tail chunk: only rows of this sequence are stored
-      for (int u = tid; u < kChunk * 16; u += kThreads) {
-        const int i = u >> 4, cc = u & 15;
-        if (i < Lc) {
-          const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OS + (cc >> 3) * 8192 + sw128_chunk(i, cc & 7));
-          *reinterpret_cast<uint4*>(prm.o + ((t0 + i) * prm.Hv + h) * kD + cc * 8) = val;
-        }
-      }
+    if (to_hand) {
+      // every thread's part of the slot is written before the flag is raised
       __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        atomicExch(hflag + win, 1);
+      }
     }
-  }
+  }   // pieces
+
   if (tid == 0) bulk_wait_read();   // staging reads done before shared memory is released
   if (warp == 1) cp_async_wait_all();   // g / beta copies of a chunk the loop did not reach
 
@@ -738,17 +830,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       for (; q_pending > 0; --q_pending, ph_q ^= 1) mbar_wait(bar_q, ph_q, prm.status, 100000000ull);
       for (; o1_pending > 0; --o1_pending, ph_o1 ^= 1) mbar_wait(bar_o1, ph_o1, prm.status, 100000000ull);
     }
-  } else if (trans ? prm.ht2 != nullptr : prm.ht != nullptr) {
-    // final state ht[d][e] = S^T[e][d]
-    float* htp = (trans ? prm.ht2 : prm.ht) + ((int64_t)n * prm.Hv + h) * kD * kD;
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      float v[32];
-      const int d0 = 64 * hf + 32 * half;
-      tmem_ld32(R_S + lane_off + d0, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) htp[(int64_t)(d0 + i) * kD + row] = v[i];
-    }
   }
   tc_fence_before();
   __syncthreads();
@@ -761,14 +842,56 @@ bool fused_supported(const gdn_problem& p) {
   return p.dt == GDN_BF16 && p.K == kD && p.V == kD && (p.C == 64 || p.C == 128);
 }
 
-size_t fused_workspace_bytes(const gdn_problem&) { return kAlign; }   // the status word
+namespace {
+
+constexpr int kCtasPerSm = 2;   // resident fused CTAs per SM (shared memory and TMEM halves)
+
+// Window schedule of the full pass over equal-length sequences: W chunks per
+// window, at least one chain's chunks and about an equal share of the U chunks
+// for each of the CTAs the GPU holds at once; nwin = 0: one chain per CTA
+// (varying lengths).
+struct Windows {
+  int64_t W = 0, nwin = 0;
+  bool handover() const { return nwin > 0; }
+};
+
+Windows fused_windows(const gdn_problem& p) {
+  Windows w;
+  if (p.varlen) return w;
+  const int64_t nch = ((int64_t)p.T + kChunk - 1) / kChunk;
+  const int64_t U = (int64_t)p.N * p.Hv * nch;
+  if (U == 0) return w;
+  const int64_t G = (int64_t)kCtasPerSm * sm_count();
+  w.W = (U + G - 1) / G;
+  if (w.W < nch) w.W = nch;
+  w.nwin = (U + w.W - 1) / w.W;
+  return w;
+}
+
+// Workspace: [status, claim counter, nwin hand-over flags] (int32), then, when
+// a window boundary can cut a chain (W above one chain's chunks), nwin state
+// slots of K x V fp32.
+size_t sched_bytes(const Windows& w) { return ((sizeof(int32_t) * (2 + w.nwin) + kAlign - 1) / kAlign) * kAlign; }
+
+bool cuts_chains(const gdn_problem& p, const Windows& w) {
+  return w.nwin > 0 && w.W != ((int64_t)p.T + kChunk - 1) / kChunk;
+}
+
+}  // namespace
+
+size_t fused_workspace_bytes(const gdn_problem& p) {
+  const Windows w = fused_windows(p);
+  if (!w.handover()) return kAlign;   // the status word
+  return sched_bytes(w) + (cuts_chains(p, w) ? (size_t)w.nwin * kD * kD * sizeof(float) : 0);
+}
 size_t fused_status_offset(const gdn_problem&) { return 0; }
 
 // One launch of the fused kernel over the chains of `p` (N x Hv, or twice
 // that for kStates).  status: the device status word.
 gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const void* k, const void* v, const float* g,
                         const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
-                        float* ht2, int32_t* status, cudaStream_t s) {
+                        float* ht2, int32_t* status, cudaStream_t s, int* sched, float* hand, int64_t nwin,
+                        int64_t W) {
   const int64_t Ttot = (int64_t)p.B * p.T;
   CUtensorMap tq, tk, tv, to;
   memset(&to, 0, sizeof(to));
@@ -804,12 +927,17 @@ gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const voi
   prm.scale = scale;
   prm.ht2 = ht2;
   prm.split = p.N * p.Hv;
+  prm.sched = mode == kFull ? sched : nullptr;
+  prm.hand = hand;
+  prm.nwin = (int)nwin;
+  prm.W = (int)W;
   const unsigned chains = (unsigned)((int64_t)p.N * p.Hv);
   if (mode == kFull) {
     if (cudaFuncSetAttribute(gdn_fused_kernel<kFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
       return GDN_ERR_CUDA;
-    gdn_fused_kernel<kFull><<<chains, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
+    const unsigned grid = prm.sched ? (unsigned)nwin : chains;
+    gdn_fused_kernel<kFull><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
   } else {
     if (cudaFuncSetAttribute(gdn_fused_kernel<kStates>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
@@ -824,7 +952,9 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
                      void* ws, cudaStream_t s) {
   if (!fused_supported(p)) return GDN_ERR_UNSUPPORTED;
   int32_t* status = static_cast<int32_t*>(ws);
-  if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
+  const Windows w = fused_windows(p);
+  if (cudaMemsetAsync(status, 0, w.handover() ? sizeof(int32_t) * (2 + w.nwin) : sizeof(int32_t), s) != cudaSuccess)
+    return GDN_ERR_CUDA;
   const int64_t Ttot = (int64_t)p.B * p.T;
   if (Ttot == 0 || (int64_t)p.N * p.Hv == 0) {
     // no tokens: ht = h0 (or zeros)
@@ -835,7 +965,10 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
     }
     return GDN_OK;
   }
-  return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s);
+  if (!w.handover()) return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s);
+  float* hand = cuts_chains(p, w) ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sched_bytes(w)) : nullptr;
+  return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s, status + 1, hand, w.nwin,
+                      w.W);
 }
 
 gdn_status run_fused_states(const gdn_problem& p, const void* k, const void* v, const float* g, const float* beta,

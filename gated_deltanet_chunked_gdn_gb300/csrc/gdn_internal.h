@@ -108,8 +108,13 @@ int cp_segment_length(const gdn_problem& p);
 // AUTO takes the chunk-parallel path for long sequences with few chains.
 bool cp_preferred(const gdn_problem& p);
 // One fused-kernel launch (mode 0: the full pass; 1: final states only).
+// sched / hand / nwin / W: the window schedule of an equal-length full pass
+// (sched null: one chain per CTA).
 gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const void* k, const void* v, const float* g,
                         const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
-                        float* ht2, int32_t* status, cudaStream_t s);
+                        float* ht2, int32_t* status, cudaStream_t s, int* sched = nullptr, float* hand = nullptr,
+                        int64_t nwin = 0, int64_t W = 0);
+// Streaming multiprocessors of the current device (148 when none can be queried).
+int sm_count();
 
 }  // namespace gdn

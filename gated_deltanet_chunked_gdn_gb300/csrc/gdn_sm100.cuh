@@ -68,6 +68,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int32_
   }
 }
 
+// Bounded wait until *flag != 0, read with acquire semantics at GPU scope (a
+// flag another CTA raises after a __threadfence); false, with
+// GDN_DEV_WAIT_TIMEOUT in *status, once limit_ns has passed.
+__device__ __forceinline__ bool flag_wait(const int* flag, int32_t* status, uint64_t limit_ns = 2000000000ull) {
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v != 0) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      atomicExch(status, GDN_DEV_WAIT_TIMEOUT);
+      return false;
+    }
+    __nanosleep(256);
+  }
+}
+
 // ---------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
   asm volatile(

@@ -81,6 +81,11 @@ typedef struct {
  * Bytes of workspace that gdn_chunk_fwd needs for `path` (AUTO resolves as in
  * gdn_chunk_fwd).  Returns 0 for an invalid problem.  The varlen bound assumes
  * at most ceil(T / C) + N chunks, so cu_seqlens need not be read on the host.
+ * The fused path over equal-length sequences spreads the (sequence, head)
+ * chains' chunks evenly over the CTAs the current device holds at once (two
+ * per SM), cutting a chain in two where a share ends; its workspace then holds
+ * one K x V fp32 hand-over state per CTA (about 20 MB on 152 SMs), so query
+ * the size with the device that will run the call current.
  */
 size_t gdn_chunk_fwd_workspace_size(const gdn_problem* p, gdn_path path);
 

@@ -66,7 +66,8 @@ def test_full_gqa_prefill(gdn, oracle_mod):
 @pytest.mark.parametrize("H", [32, 16, 48, 64])
 def test_full_batched_16x8192(gdn, oracle_mod, H):
     w = I.WORKLOADS[2].with_(Hqk=H, Hv=H)
-    chains = [(0, 0), (7, H // 2 - 1), (15, H - 1)] if H == 32 else [(15, H - 1)]
+    # (0, 1) and (15, H - 1) straddle a window boundary of the fused schedule
+    chains = [(0, 0), (0, 1), (7, H // 2 - 1), (15, H - 1)] if H == 32 else [(15, H - 1)]
     check_chains(gdn, oracle_mod, w, chains)
 
 

@@ -181,6 +181,9 @@ FUSED_CASES = {
     "varlen_short_and_empty": (I.WORKLOADS[3].with_(Hqk=1, Hv=2), [5, 64, 200, 1, 0, 129, 63, 65]),
     "single_token": (I.WORKLOADS[2].with_(B=3, T=1, Hqk=1, Hv=1), None),
     "gqa4_h0": (I.WORKLOADS[2].with_(B=1, T=130, Hqk=1, Hv=4, C=64), None),
+    # 320 chains of 3 chunks (ragged last chunk) over more chains than the GPU
+    # holds CTAs: windows of 4 chunks, most chains cut in two and handed over
+    "windows_cut_chains": (I.WORKLOADS[2].with_(B=40, T=190, Hqk=4, Hv=8, C=64), None),
 }
 
 
