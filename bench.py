@@ -436,6 +436,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--B", type=int, default=16, help="batch override (profiling runs only; the metric is B=16)")
+    ap.add_argument("--T", type=int, default=8192,
+                    help="sequence length override of the batched workload (profiling runs only; the metric is T=8192)")
     ap.add_argument("--workload", default="batched_16x8192",
                     choices=["batched_16x8192", "gqa_prefill_1x4096", "long_1x32768"],
                     help="chunk_fwd shape: the headline 16 x 8192 batch, or one long GQA sequence (1 x 4096 or "
@@ -470,8 +472,8 @@ def main():
             dist.destroy_process_group()
         return
     if args.workload == "batched_16x8192":
-        w = I.WORKLOADS[2].with_(B=args.B, Hqk=args.H, Hv=args.H, seed=2 + rank)
-        wname = f"batched_{w.B}x8192_H{args.H}"
+        w = I.WORKLOADS[2].with_(B=args.B, T=args.T, Hqk=args.H, Hv=args.H, seed=2 + rank)
+        wname = f"batched_{w.B}x{w.T}_H{args.H}"
     else:
         T = 4096 if args.workload == "gqa_prefill_1x4096" else 32768
         w = I.WORKLOADS[1].with_(T=T, seed=1 + rank)
@@ -580,7 +582,8 @@ def main():
                           if flush is None else "L2 flushed (512 MB write) before every timed step")},
         "tflops_alg": flops / sec / 1e12,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": measured_traffic("fused", w.B) if path == "fused" and args.workload == "batched_16x8192" else None, "peak_source": pk["source"],
+                     "traffic": (measured_traffic("fused", w.B * w.T / 8192)
+                                 if path == "fused" and args.workload == "batched_16x8192" else None), "peak_source": pk["source"],
                      "kernel": "gdn_fused_kernel (the step's only launch)" if path == "fused"
                      else "gdn_chunk_fwd call (all launches of one step)",
                      "alg_bytes": nbytes, "alg_flops": flops,
