@@ -114,9 +114,11 @@ constexpr int kStates = 1;
 //  1. Diagonal 16x16 blocks by forward substitution: a half-warp per block,
 //     lane l keeps column l of the block's inverse in registers.
 //  2. Merge neighbouring blocks, [[T11, 0], [A21, T22]] -> T21 = -T22 (A21 T11),
-//     first the 16-blocks (two pairs, each inside the one warp that wrote
-//     that 32x32 diagonal block of A in the gating step, so steps 1 and 2a
-//     need no block barrier), then the 32-blocks (one pair, all warps).  The
+//     first the 16-blocks (two pairs; each pair's diagonal blocks are solved
+//     by the warp that wrote that 32x32 diagonal block of A in the gating
+//     step, which then merges one column tile while a partner warp merges
+//     the other, joined by a named barrier instead of a block barrier), then
+//     the 32-blocks (one pair, all warps).  The
 //     merge products run on the tensor cores (mma.sync m16n8k8, tf32 inputs,
 //     fp32 accumulation); the upper triangles hold zeros, so they are plain
 //     square products.  The fp32 values enter the tf32 MMA unrounded (the unit
@@ -232,22 +234,29 @@ __device__ __forceinline__ void diag_pair(float* As, int b0, int lane, uint8_t* 
   }
 }
 
-// 16-level merge inside one warp for the 32x32 diagonal block at o:
-// T21 = -T22 (A21 T11), the product A21 T11 passing through a warp-private
-// scratch (16 x 16, leading dimension 24).
-__device__ __forceinline__ void merge16_warp(float* As, float* scr, int o, int lane, uint8_t* tb, uint8_t* tbe,
-                                             const float* bet, const float* be) {
+// Named barrier ID over 64 threads (two warps).
+template <int ID>
+__device__ __forceinline__ void named_bar64() {
+  asm volatile("bar.sync %0, 64;" :: "n"(ID) : "memory");
+}
+
+// 16-level merge of the 32x32 diagonal block at o, T21 = -T22 (A21 T11),
+// split over two warps: this one computes the 8-column tile nt of T21, the
+// product A21 T11 passing through the pair's scratch (16 x 16, leading
+// dimension 24; each warp touches only its own columns).  Named barrier BAR
+// joins the pair between the two products, before A21 is overwritten by T21.
+template <int BAR>
+__device__ __forceinline__ void merge16_half(float* As, float* scr, int o, int nt, int lane, uint8_t* tb,
+                                             uint8_t* tbe, const float* bet, const float* be) {
   constexpr int SLD = 24;
   const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  {
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mma_tf32<16>(d, As + (o + 16) * kAsLd + o, kAsLd, As + o * kAsLd + o + 8 * nt, kAsLd, lane);
     tile_store(d, scr + 8 * nt, SLD, lane, 1.f);
   }
-  __syncwarp();
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
+  named_bar64<BAR>();   // both column tiles' A21 T11 done: A21 may be overwritten
+  {
     float d[4] = {0.f, 0.f, 0.f, 0.f};
     tile_mma_tf32<16>(d, As + (o + 16) * kAsLd + o + 16, kAsLd, scr + 8 * nt, SLD, lane);
     const int r0 = o + 16, c0 = o + 8 * nt + 2 * t;
@@ -266,7 +275,9 @@ __device__ __forceinline__ void store8_bf16(uint8_t* p, const float* v) {
       make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]), pack_bf16(v[6], v[7]));
 }
 
-template <int MODE>
+// WIN: the window schedule (kFull only); a separate instantiation, so that the
+// one-chain-per-CTA code carries none of its state through the chunk loop.
+template <int MODE, bool WIN>
 __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                 const __grid_constant__ CUtensorMap tm_k,
                                                                 const __grid_constant__ CUtensorMap tm_v,
@@ -297,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, hf = warp >> 2;   // TMEM lane quadrant, column half
-  const bool windowed = MODE == kFull && prm.sched != nullptr;
+  constexpr bool windowed = MODE == kFull && WIN;
   // kStates: the upper half of the grid computes transition matrices
   const bool trans = MODE == kStates && (int)blockIdx.x >= prm.split;
   // the chain of the current piece: sequence n, value head h, its qk head,
@@ -579,16 +590,22 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
 
       // ---- S2: solve_tril in place; T diag(beta) and T diag(beta e^g) go out as
       // bf16 operands.  Warps 0 and 5 wrote rows 0..31 x cols 0..31 and rows
-      // 32..63 x cols 32..63 of A: each solves its two diagonal 16x16 blocks and
-      // merges them into its 32x32 diagonal block of T without waiting for the
-      // other warps, which meanwhile zero the upper 16x16 blocks of both
-      // operands (one 16-byte chunk per thread and operand).
+      // 32..63 x cols 32..63 of A: each solves its two diagonal 16x16 blocks,
+      // then merges them into its 32x32 diagonal block of T together with a
+      // partner warp (2 for 0, 7 for 5: other SM sub-partitions) that takes
+      // the second column tile; the other warps meanwhile zero the upper 16x16
+      // blocks of both operands (one 16-byte chunk per thread and operand).
       if (warp == 0 || warp == 5) {
         const int o = warp == 5 ? 32 : 0;
         __syncwarp();
         diag_pair(As, o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
-        __syncwarp();
-        merge16_warp(As, tmp + (warp == 5 ? 16 * 24 : 0), o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+        if (warp == 5) {   // the partner warp may read this block's T11, T22 and A21
+          named_bar64<2>();
+          merge16_half<2>(As, tmp + 16 * 24, o, 0, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+        } else {
+          named_bar64<1>();
+          merge16_half<1>(As, tmp, o, 0, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+        }
       } else {
         const int u = 32 * (warp - 1 - (warp > 5 ? 1 : 0)) + lane;   // 0..191 over warps 1-4, 6, 7
         const int blk = u >> 5, r = (u >> 1) & 15, half = u & 1;
@@ -597,6 +614,15 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
         *reinterpret_cast<uint4*>(sm + OFF_TB + off) = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(sm + OFF_TBE + off) = make_uint4(0u, 0u, 0u, 0u);
+        if (warp == 2 || warp == 7) {
+          if (warp == 7) {
+            named_bar64<2>();
+            merge16_half<2>(As, tmp + 16 * 24, 32, 1, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+          } else {
+            named_bar64<1>();
+            merge16_half<1>(As, tmp, 0, 1, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+          }
+        }
       }
       tc_fence_before();
       __syncthreads();
@@ -932,18 +958,12 @@ gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const voi
   prm.nwin = (int)nwin;
   prm.W = (int)W;
   const unsigned chains = (unsigned)((int64_t)p.N * p.Hv);
-  if (mode == kFull) {
-    if (cudaFuncSetAttribute(gdn_fused_kernel<kFull>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return GDN_ERR_CUDA;
-    const unsigned grid = prm.sched ? (unsigned)nwin : chains;
-    gdn_fused_kernel<kFull><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
-  } else {
-    if (cudaFuncSetAttribute(gdn_fused_kernel<kStates>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
-      return GDN_ERR_CUDA;
-    gdn_fused_kernel<kStates><<<2 * chains, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
-  }
+  auto kernel = mode == kStates ? gdn_fused_kernel<kStates, false>
+               : (prm.sched ? gdn_fused_kernel<kFull, true> : gdn_fused_kernel<kFull, false>);
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  const unsigned grid = mode == kStates ? 2 * chains : (prm.sched ? (unsigned)nwin : chains);
+  kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
