@@ -65,15 +65,16 @@ def measured_traffic(op: str, units: float):
     return rec["dram_bytes_per_launch"] * units / rec["units"]
 
 
-def algorithmic(B, T, Hqk, Hv, K, V, C, elem=2, h0=True):
-    """Compulsory bytes and algorithmic FLOPs of one forward pass.
+def algorithmic(B, T, Hqk, Hv, K, V, C, elem=2, h0=True, N=None):
+    """Compulsory bytes and algorithmic FLOPs of one forward pass over B x T
+    tokens in N sequences (N = B unless packed).
 
     Bytes: q, k, v, o in the input dtype, g and beta fp32, h0 and ht fp32.
     FLOPs (triangular products counted as half, KK^T / QK^T once per qk head):
     per token Hqk*(C*K + C*K) + Hv*(C*V + C*K + C*V + 6*K*V + C*C/3).
     """
     tokens = B * T
-    N = B
+    N = B if N is None else N
     per_tok = 2 * Hqk * K * elem + 2 * Hv * V * elem + 8 * Hv
     state = N * Hv * K * V * 4 * (2 if h0 else 1)
     nbytes = tokens * per_tok + state
@@ -433,15 +434,18 @@ def main():
     ap.add_argument("--H", type=int, default=32, choices=[16, 32, 48, 64])
     ap.add_argument("--path", default="auto", choices=["auto", "staged", "fused"])
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-split", type=int, default=8,
+                    help="sub-batches of the end-to-end leg (host buffers streamed through the GPU)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--B", type=int, default=16, help="batch override (profiling runs only; the metric is B=16)")
     ap.add_argument("--T", type=int, default=8192,
                     help="sequence length override of the batched workload (profiling runs only; the metric is T=8192)")
     ap.add_argument("--workload", default="batched_16x8192",
-                    choices=["batched_16x8192", "gqa_prefill_1x4096", "long_1x32768"],
-                    help="chunk_fwd shape: the headline 16 x 8192 batch, or one long GQA sequence (1 x 4096 or "
-                         "1 x 32768 tokens, 16 qk / 32 value heads), where AUTO takes the chunk-parallel path")
+                    choices=["batched_16x8192", "gqa_prefill_1x4096", "long_1x32768", "varlen_64"],
+                    help="chunk_fwd shape: the headline 16 x 8192 batch, one long GQA sequence (1 x 4096 or "
+                         "1 x 32768 tokens, 16 qk / 32 value heads), where AUTO takes the chunk-parallel path, or "
+                         "64 packed sequences of log-uniform lengths in [1, 16384] (16 qk / 32 value heads)")
     ap.add_argument("--op", default="chunk_fwd", choices=["chunk_fwd", "conv1d", "decode", "bwd"],
                     help="chunk_fwd: the GDN chunked forward (the headline); conv1d / decode: the neighbouring "
                          "ops of the same layer, each with its own JSON line")
@@ -474,12 +478,17 @@ def main():
     if args.workload == "batched_16x8192":
         w = I.WORKLOADS[2].with_(B=args.B, T=args.T, Hqk=args.H, Hv=args.H, seed=2 + rank)
         wname = f"batched_{w.B}x{w.T}_H{args.H}"
+    elif args.workload == "varlen_64":
+        w = I.WORKLOADS[3].with_(seed=3 + rank)
     else:
         T = 4096 if args.workload == "gqa_prefill_1x4096" else 32768
         w = I.WORKLOADS[1].with_(T=T, seed=1 + rank)
         wname = f"gqa_prefill_1x{T}_Hqk{w.Hqk}_Hv{w.Hv}"
     x = I.make_inputs(w, dev)
-    p = binding.problem_of(x["q"], x["v"], w.C)
+    Bx, Tx = x["q"].shape[0], x["q"].shape[1]   # the packed batch is [1, total tokens]
+    if args.workload == "varlen_64":
+        wname = f"varlen_{x['N']}seqs_{Tx}tok_Hqk{w.Hqk}_Hv{w.Hv}"
+    p = binding.problem_of(x["q"], x["v"], w.C, x["cu_seqlens"])
     path = args.path if args.path != "auto" else binding.gdn_resolve_path(p)
     o = torch.empty_like(x["v"])
     ht = torch.empty((p.N, p.Hv, p.K, p.V), dtype=torch.float32, device=dev)
@@ -487,8 +496,8 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step(q=x["q"], k=x["k"], v=x["v"], g=x["g"], beta=x["beta"], h0=x["h0"]):
-        binding.gdn_chunk_fwd(q, k, v, g, beta, x["scale"], h0=h0, C=w.C, path=path, o=o, ht=ht, workspace=ws,
-                              stream=stream.cuda_stream)
+        binding.gdn_chunk_fwd(q, k, v, g, beta, x["scale"], h0=h0, cu_seqlens=x["cu_seqlens"], C=w.C, path=path,
+                              o=o, ht=ht, workspace=ws, stream=stream.cuda_stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -502,7 +511,7 @@ def main():
     time.sleep(0.3)
     # inputs smaller than about twice the L2 are timed step by step with the
     # L2 flushed (a 512 MB write) between steps, outside the timed spans
-    in_bytes, _ = algorithmic(w.B, w.T, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None)
+    in_bytes, _ = algorithmic(Bx, Tx, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None, N=x["N"])
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev) if in_bytes < 2 * L2_BYTES else None
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps if flush is not None else 1)]
@@ -528,27 +537,31 @@ def main():
     ms = sum(e_a.elapsed_time(e_b) for e_a, e_b in evs)
     sampler.stop()
     clocks = sampler.summary(t_wall0, t_wall1)
-    tokens_step = w.B * w.T
+    tokens_step = Bx * Tx
     value, sec_total = aggregate(ms / 1000.0, tokens_step, args.steps, world, dev)
     ms_step = 1000.0 * sec_total / args.steps
 
-    # End to end through the public API: inputs from pinned host memory, o and
-    # ht read back, every step.
+    # End to end through the public API: the C-ABI call on host buffers
+    # (gdn_chunk_fwd_host: inputs in pinned host memory, the batch streamed
+    # through the GPU in sub-batches whose copies overlap the compute, o and ht
+    # back in host memory), every step.
     host = {k: x[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
     if x["h0"] is not None:
         host["h0"] = x["h0"].cpu().pin_memory()
-    dev_in = {k: torch.empty_like(x[k]) for k in host}
+    cu_host = x["cu_seqlens"].cpu() if x["cu_seqlens"] is not None else None
     o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     ht_host = torch.empty(ht.shape, dtype=ht.dtype, pin_memory=True)
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = o_host.numel() * o_host.element_size() + ht_host.numel() * ht_host.element_size()
+    p_host = binding.problem_of(host["q"], host["v"], w.C, cu_host)
+    ws_host = torch.empty(binding.gdn_chunk_fwd_host_workspace_size(p_host, cu_host, args.e2e_split, path),
+                          dtype=torch.uint8, device=dev)
 
     def e2e_step():
-        for k_ in dev_in:
-            dev_in[k_].copy_(host[k_], non_blocking=True)
-        step(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in.get("h0"))
-        o_host.copy_(o, non_blocking=True)
-        ht_host.copy_(ht, non_blocking=True)
+        binding.gdn_chunk_fwd_host(host["q"], host["k"], host["v"], host["g"], host["beta"], x["scale"],
+                                   h0=host.get("h0"), cu_seqlens=cu_host, C=w.C, path=path, nsplit=args.e2e_split,
+                                   o=o_host, ht=ht_host, workspace=ws_host, device=dev,
+                                   stream=stream.cuda_stream)
 
     e2e_step()
     torch.cuda.synchronize()
@@ -561,7 +574,7 @@ def main():
     e2e_value, _ = aggregate(time.perf_counter() - t0, tokens_step, args.e2e_steps, world, dev)
 
     pk = peaks()
-    nbytes, flops = algorithmic(w.B, w.T, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None)
+    nbytes, flops = algorithmic(Bx, Tx, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None, N=x["N"])
     t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
     t_tc = flops / (pk["bf16_tflops"] * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
@@ -576,7 +589,7 @@ def main():
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wname, "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv,
+        "config": {"workload": wname, "B": Bx, "T": Tx, "N": x["N"], "Hqk": w.Hqk, "Hv": w.Hv,
                    "K": w.K, "V": w.V, "C": w.C, "path": path, "parallelism": f"dp{world} (independent batches)",
                    "l2": (f"inputs larger than L2 ({nbytes / 1e9:.2f} GB compulsory traffic per step)"
                           if flush is None else "L2 flushed (512 MB write) before every timed step")},
@@ -589,7 +602,7 @@ def main():
                      "alg_bytes": nbytes, "alg_flops": flops,
                      "t_hbm_ms": 1e3 * t_hbm, "t_tensor_ms": 1e3 * t_tc},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": args.e2e_steps},
+                "steps": args.e2e_steps, "call": f"gdn_chunk_fwd_host, {args.e2e_split} sub-batches"},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
     }

@@ -25,7 +25,8 @@ STAGES = {"prepare": 0, "cumsum": 1, "kkt": 2, "solve_tril": 3, "wy_fast": 4, "c
 EXPORTED = ["gdn_chunk_fwd_workspace_size", "gdn_chunk_fwd", "gdn_chunk_fwd_staged", "gdn_staged_layout",
             "gdn_get_device_status", "gdn_resolve_path", "gdn_status_string", "gdn_version", "gdn_recurrent_fwd",
             "gdn_causal_conv1d_fwd", "gdn_chunk_bwd_workspace_size", "gdn_chunk_bwd",
-            "gdn_chunk_bwd_get_device_status"]
+            "gdn_chunk_bwd_get_device_status", "gdn_chunk_fwd_host_workspace_size", "gdn_chunk_fwd_host",
+            "gdn_chunk_fwd_host_get_device_status"]
 
 
 class Problem(ctypes.Structure):
@@ -97,6 +98,13 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
         lib.gdn_chunk_bwd.restype = ctypes.c_int
         lib.gdn_chunk_bwd_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
         lib.gdn_chunk_bwd_get_device_status.restype = ctypes.c_int
+        lib.gdn_chunk_fwd_host_workspace_size.argtypes = [P, i32p, ctypes.c_int, ctypes.c_int]
+        lib.gdn_chunk_fwd_host_workspace_size.restype = ctypes.c_size_t
+        lib.gdn_chunk_fwd_host.argtypes = [P, ctypes.c_int, ctypes.c_int, vp, vp, vp, fp, fp, ctypes.c_float, fp, i32p,
+                                           vp, fp, vp, ctypes.c_size_t, vp]
+        lib.gdn_chunk_fwd_host.restype = ctypes.c_int
+        lib.gdn_chunk_fwd_host_get_device_status.argtypes = [vp, vp, ctypes.POINTER(ctypes.c_int)]
+        lib.gdn_chunk_fwd_host_get_device_status.restype = ctypes.c_int
         lib.gdn_version.argtypes = []
         lib.gdn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -209,6 +217,54 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale: Optional[float] = None, h0=None, cu_s
     if st:
         raise GDNError(st, "gdn_chunk_fwd")
     return o, ht
+
+
+def gdn_chunk_fwd_host_workspace_size(p: Problem, cu_seqlens=None, nsplit: int = 4, path: str = "auto") -> int:
+    return int(load().gdn_chunk_fwd_host_workspace_size(ctypes.byref(p), _ptr(cu_seqlens), int(nsplit), PATHS[path]))
+
+
+def gdn_chunk_fwd_host(q, k, v, g, beta, scale: Optional[float] = None, h0=None, cu_seqlens=None, C: int = 64,
+                       path: str = "auto", nsplit: int = 4, o=None, ht=None, output_final_state: bool = True,
+                       workspace=None, device=None, stream=None):
+    """The forward pass on host (CPU) tensors, streamed through the GPU in
+    ``nsplit`` sub-batches (pin the tensors for the copies to overlap the
+    compute).  Returns host (o, ht) after the call has finished; ht is None
+    when ``output_final_state`` is False."""
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("h0", h0), ("cu_seqlens", cu_seqlens)):
+        if t is not None and (t.device.type != "cpu" or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    p = problem_of(q, v, C, cu_seqlens)
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    pin = q.is_pinned()
+    if o is None:
+        o = torch.empty(v.shape, dtype=v.dtype, pin_memory=pin)
+    if ht is None and output_final_state:
+        ht = torch.empty((p.N, p.Hv, p.K, p.V), dtype=torch.float32, pin_memory=pin)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    need = gdn_chunk_fwd_host_workspace_size(p, cu_seqlens, nsplit, path)
+    if need == 0:
+        raise GDNError(GDN_ERR_INVALID_ARG, "gdn_chunk_fwd_host_workspace_size")
+    if workspace is None:
+        workspace = _alloc_ws(need, dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev).cuda_stream
+    st = lib.gdn_chunk_fwd_host(ctypes.byref(p), PATHS[path], int(nsplit), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                _ptr(beta), ctypes.c_float(scale), _ptr(h0), _ptr(cu_seqlens), _ptr(o), _ptr(ht),
+                                _ptr(workspace), ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(s))
+    if st:
+        raise GDNError(st, "gdn_chunk_fwd_host")
+    torch.cuda.synchronize(dev)
+    return o, ht
+
+
+def gdn_chunk_fwd_host_get_device_status(workspace, stream=None) -> int:
+    out = ctypes.c_int(0)
+    s = stream if stream is not None else torch.cuda.current_stream(workspace.device).cuda_stream
+    st = load().gdn_chunk_fwd_host_get_device_status(_ptr(workspace), ctypes.c_void_p(s), ctypes.byref(out))
+    if st:
+        raise GDNError(st, "gdn_chunk_fwd_host_get_device_status")
+    return out.value
 
 
 def gdn_chunk_fwd_staged(q, k, v, g, beta, scale: Optional[float] = None, h0=None, cu_seqlens=None, C: int = 64,

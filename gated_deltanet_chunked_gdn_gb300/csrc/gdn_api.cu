@@ -80,6 +80,8 @@ gdn_status check_call(const gdn_problem& p, const void* q, const void* k, const 
 
 }  // namespace
 
+size_t gdn::fwd_status_offset(const gdn_problem& p, gdn_path path) { return status_offset(p, resolve(p, path)); }
+
 extern "C" {
 
 size_t gdn_chunk_fwd_workspace_size(const gdn_problem* pp, gdn_path path) {

@@ -116,5 +116,8 @@ gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const voi
                         int64_t nwin = 0, int64_t W = 0);
 // Streaming multiprocessors of the current device (148 when none can be queried).
 int sm_count();
+// Byte offset of the device status word inside a forward workspace for `path`
+// (AUTO resolved as gdn_chunk_fwd resolves it).
+size_t fwd_status_offset(const gdn_problem& p, gdn_path path);
 
 }  // namespace gdn

@@ -159,6 +159,42 @@ gdn_status gdn_get_device_status(const gdn_problem* p, gdn_path path, void* work
                                  void* stream, int* dev_status);
 
 /*
+ * The forward pass on HOST tensors (no counterpart on the pages: the
+ * streaming form of gdn_chunk_fwd for callers whose q, k, v, g, beta, h0 and
+ * outputs live in host memory).  Same shapes and meaning as gdn_chunk_fwd,
+ * but q, k, v, g, beta, h0, cu_seqlens, o and ht are HOST pointers; page-locked
+ * memory (cudaHostAlloc) is needed for the copies to overlap the compute
+ * (pageable memory is copied synchronously by the driver, still correctly).
+ * The batch is cut into at most `nsplit` sub-batches of whole sequences (about
+ * equal token counts); sub-batch i's inputs are copied to the device while
+ * sub-batch i - 1 runs gdn_chunk_fwd(path) and sub-batch i - 2's o and ht are
+ * copied back, on three streams that the library creates once per device and
+ * orders after `stream`; `stream` resumes once every output is in host memory.
+ * Calls from several host threads are enqueued one at a time.
+ *   workspace : DEVICE memory of gdn_chunk_fwd_host_workspace_size(p,
+ *               cu_seqlens, nsplit, path) bytes, 256-byte aligned: two sets
+ *               of device buffers for the largest sub-batch and the inner
+ *               forward's workspace.
+ * Host-side checks: the ones of gdn_chunk_fwd and, for packed sequences,
+ * cu_seqlens[0] == 0, cu_seqlens[N] == T and non-decreasing offsets
+ * (GDN_ERR_INVALID_ARG otherwise, nothing enqueued).  Device-side errors of
+ * any sub-batch (the first one kept) are read with
+ * gdn_chunk_fwd_host_get_device_status.  The host buffers must stay valid and
+ * unmodified until `stream` has passed the call.
+ */
+size_t gdn_chunk_fwd_host_workspace_size(const gdn_problem* p, const int32_t* cu_seqlens, int nsplit,
+                                         gdn_path path);
+gdn_status gdn_chunk_fwd_host(const gdn_problem* p, gdn_path path, int nsplit,
+                              const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, float scale,
+                              const float* h0, const int32_t* cu_seqlens,
+                              void* o, float* ht,
+                              void* workspace, size_t workspace_bytes, void* stream);
+/* Waits for `stream`, reads and clears the status word of a
+ * gdn_chunk_fwd_host workspace (GDN_DEV_*). */
+gdn_status gdn_chunk_fwd_host_get_device_status(void* workspace, void* stream, int* dev_status);
+
+/*
  * Self-test of the tensor-core operand layouts used by the fused kernel (no
  * counterpart on the pages; a test hook).  Computes D = A B (or -A B) with one
  * CTA through tcgen05.mma over 128-byte-swizzled shared-memory tiles.

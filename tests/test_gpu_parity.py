@@ -184,6 +184,9 @@ FUSED_CASES = {
     # 320 chains of 3 chunks (ragged last chunk) over more chains than the GPU
     # holds CTAs: windows of 4 chunks, most chains cut in two and handed over
     "windows_cut_chains": (I.WORKLOADS[2].with_(B=40, T=190, Hqk=4, Hv=8, C=64), None),
+    # 150 packed sequences of 0..299 tokens (empty ones included), GQA 2 -> 4
+    "varlen_many_short": (I.WORKLOADS[3].with_(Hqk=2, Hv=4),
+                          [int(n) for n in np.random.default_rng(5).integers(0, 300, 150)]),
 }
 
 
