@@ -15,9 +15,12 @@
 // Work is about three times that of the serial pass, spread over
 // (segments x heads) CTAs instead of (sequences x heads).
 #include "gdn_internal.h"
+#include "gdn_sm100.cuh"
 
 namespace gdn {
 namespace {
+
+using namespace sm100;
 
 constexpr int kD = 128;
 constexpr int kPrepThreads = 1024;
@@ -108,65 +111,100 @@ __global__ void __launch_bounds__(kPrepThreads) cp_prepare_kernel(const int32_t*
   for (int i = total + tid; i <= ns_max; i += kPrepThreads) seg_cu[i] = (int32_t)Ttot;
 }
 
-// Chain the segments of (sequence n, value head h) for 32 state columns:
+// Chain the segments of (sequence n, value head h) for 16 state columns:
 // H0s[j] = S_j, S_{j+1} = M_j S_j + B_j from S_0 = h0, ht = the last S.
-// 256 threads, each owning a 4 x 4 tile of the 128 x 32 slice; M_j goes
-// through shared memory transposed, 32 columns at a time, so that every step
-// of the inner product is two 16-byte shared loads and 16 FMAs.
-__global__ void __launch_bounds__(256) cp_combine_kernel(const int32_t* __restrict__ seq_seg, int Hv,
+// 128 threads, thread t owning rows t/4 + 32 r (r < 4) and 4 columns of the
+// 128 x 16 slice.  M_j is row-major in 32-column k-blocks, staged into a
+// double-buffered shared tile by cp.async one block ahead of the FMAs; a
+// step of the inner product reads four rows of M and four rows of S as
+// 16-byte loads for 64 FMAs (row stride 36 floats: the eight rows a warp
+// reads fall on distinct banks).
+constexpr int kCSlice = 16;
+constexpr int kKb = 32;
+constexpr int kMld = kKb + 4;
+
+__global__ void __launch_bounds__(128) cp_combine_kernel(const int32_t* __restrict__ seq_seg, int Hv,
                                                          const float* __restrict__ h0, const float* __restrict__ Bst,
                                                          const float* __restrict__ Mst, float* __restrict__ H0s,
                                                          float* __restrict__ ht) {
-  __shared__ __align__(16) float S[kD][32];
-  __shared__ __align__(16) float Mt[32][kD + 4];
-  const int n = blockIdx.x, h = blockIdx.y, e0 = 32 * blockIdx.z;
-  const int tid = threadIdx.x, d0 = 4 * (tid >> 3), c0 = 4 * (tid & 7);
+  __shared__ __align__(16) float S[kD][kCSlice];
+  __shared__ __align__(16) float Mb[2][kD][kMld];
+  const int n = blockIdx.x, h = blockIdx.y, e0 = kCSlice * blockIdx.z;
+  const int tid = threadIdx.x, t = tid >> 2, c0 = 4 * (tid & 3);
   const size_t mat = (size_t)kD * kD;
   const float* h0p = h0 ? h0 + ((size_t)n * Hv + h) * mat : nullptr;
-  for (int i = tid; i < kD * 32; i += 256) {
-    const int r = i >> 5, c = i & 31;
+  for (int i = tid; i < kD * kCSlice; i += 128) {
+    const int r = i / kCSlice, c = i % kCSlice;
     S[r][c] = h0p ? h0p[(size_t)r * kD + e0 + c] : 0.f;
   }
-  __syncthreads();
   const int j0 = seq_seg[n], j1 = seq_seg[n + 1];
-  for (int j = j0; j < j1; ++j) {
+  const int nb = (j1 - j0) * (kD / kKb);   // k-blocks of all the segments, in order
+  auto stage = [&](int blk) {
+    const float* src = Mst + ((size_t)(j0 + blk / (kD / kKb)) * Hv + h) * mat + (blk % (kD / kKb)) * kKb;
+    float* dst = &Mb[blk & 1][0][0];
+    for (int i = tid; i < kD * (kKb / 4); i += 128) {
+      const int d = i / (kKb / 4), q = i % (kKb / 4);
+      cp_async16(dst + d * kMld + 4 * q, src + (size_t)d * kD + 4 * q);
+    }
+    cp_async_commit();
+  };
+  if (nb > 0) stage(0);
+  __syncthreads();
+  float acc[4][4];
+  for (int blk = 0; blk < nb; ++blk) {
+    const int j = j0 + blk / (kD / kKb), kbi = blk % (kD / kKb), kb = kbi * kKb;
     const size_t base = ((size_t)j * Hv + h) * mat;
-    float acc[4][4];
+    if (kbi == 0) {
+      // segment start: record S_j, start from B_j
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const float4 sv = *reinterpret_cast<const float4*>(&S[d0 + r][c0]);
-      *reinterpret_cast<float4*>(H0s + base + (size_t)(d0 + r) * kD + e0 + c0) = sv;
-      const float4 bv = *reinterpret_cast<const float4*>(Bst + base + (size_t)(d0 + r) * kD + e0 + c0);
-      acc[r][0] = bv.x, acc[r][1] = bv.y, acc[r][2] = bv.z, acc[r][3] = bv.w;
-    }
-    for (int kb = 0; kb < kD; kb += 32) {
-      __syncthreads();   // previous block of Mt consumed
-      for (int i = tid; i < kD * 32; i += 256) {
-        const int d = i >> 5, kk = i & 31;
-        Mt[kk][d] = Mst[base + (size_t)d * kD + kb + kk];
+      for (int r = 0; r < 4; ++r) {
+        const int d = t + 32 * r;
+        const float4 sv = *reinterpret_cast<const float4*>(&S[d][c0]);
+        *reinterpret_cast<float4*>(H0s + base + (size_t)d * kD + e0 + c0) = sv;
+        const float4 bv = *reinterpret_cast<const float4*>(Bst + base + (size_t)d * kD + e0 + c0);
+        acc[r][0] = bv.x, acc[r][1] = bv.y, acc[r][2] = bv.z, acc[r][3] = bv.w;
       }
+    }
+    if (blk + 1 < nb) {
+      stage(blk + 1);
+      cp_async_wait_prev();
+    } else {
+      cp_async_wait_all();
+    }
+    __syncthreads();   // block blk is in shared memory
+    const float* Mk = &Mb[blk & 1][0][0];
+#pragma unroll 2
+    for (int g = 0; g < kKb / 4; ++g) {
+      float m[4][4], x[4][4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 v = *reinterpret_cast<const float4*>(Mk + (t + 32 * r) * kMld + 4 * g);
+        m[r][0] = v.x, m[r][1] = v.y, m[r][2] = v.z, m[r][3] = v.w;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 v = *reinterpret_cast<const float4*>(&S[kb + 4 * g + u][c0]);
+        x[u][0] = v.x, x[u][1] = v.y, x[u][2] = v.z, x[u][3] = v.w;
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(m[r][u], x[u][c], acc[r][c]);
+    }
+    __syncthreads();   // this buffer and S read: the next stage and S's update may go ahead
+    if (kbi == kD / kKb - 1) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        *reinterpret_cast<float4*>(&S[t + 32 * r][c0]) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
       __syncthreads();
-#pragma unroll 8
-      for (int kk = 0; kk < 32; ++kk) {
-        const float4 m = *reinterpret_cast<const float4*>(&Mt[kk][d0]);
-        const float4 x = *reinterpret_cast<const float4*>(&S[kb + kk][c0]);
-        const float mr[4] = {m.x, m.y, m.z, m.w}, xs[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(mr[r], xs[c], acc[r][c]);
-      }
     }
-    __syncthreads();   // every thread done reading S
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-      *reinterpret_cast<float4*>(&S[d0 + r][c0]) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-    __syncthreads();
   }
   if (ht) {
     float* htp = ht + ((size_t)n * Hv + h) * mat;
-    for (int i = tid; i < kD * 32; i += 256) {
-      const int r = i >> 5, c = i & 31;
+    for (int i = tid; i < kD * kCSlice; i += 128) {
+      const int r = i / kCSlice, c = i % kCSlice;
       htp[(size_t)r * kD + e0 + c] = S[r][c];
     }
   }
@@ -244,7 +282,7 @@ gdn_status run_cp(const gdn_problem& p, const void* q, const void* k, const void
   ps.varlen = 1;
   gdn_status st = run_fused_states(ps, k, v, g, beta, seg_cu, Bst, Mst, status, s);
   if (st != GDN_OK) return st;
-  cp_combine_kernel<<<dim3(p.N, p.Hv, kD / 32), 256, 0, s>>>(seq_seg, p.Hv, h0, Bst, Mst, H0s, ht);
+  cp_combine_kernel<<<dim3(p.N, p.Hv, kD / kCSlice), 128, 0, s>>>(seq_seg, p.Hv, h0, Bst, Mst, H0s, ht);
   if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   return launch_fused(ps, 0, q, k, v, g, beta, scale, H0s, seg_cu, o, nullptr, nullptr, status, s);
 }
