@@ -11,9 +11,9 @@
 //   dk_t = -a_t b_t (G u + S_{t-1} w) + b_t G v_t;   G <- a_t (G - b_t k_t w^T)
 //
 // Columns of S (and of G) evolve independently, so a CTA owns one
-// (sequence, value head, 16-column slice of V); thread d holds row d of the
+// (sequence, value head, 8-column slice of V); thread d holds row d of the
 // slice of S and of G in registers.  Sums over d (u, w, <G, S>) are block
-// reductions; sums over the 16 columns are per thread, and the column slices
+// reductions; sums over the 8 columns are per thread, and the column slices
 // and the value heads of a GQA group meet in fp32 atomics on dq, dk, dg and
 // dbeta (order of addition not fixed).
 //
@@ -29,7 +29,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kCols = 16;   // V columns per CTA
+constexpr int kCols = 8;    // V columns per CTA
 constexpr int kChunkB = 64;  // checkpoint interval
 constexpr int kSub = 16;     // tokens per recomputed block
 constexpr int kRow = kCols;  // row length of the state tiles in shared memory (floats)
@@ -56,14 +56,17 @@ struct BwdSmem {
   float sum[kCols + 1];
 };
 
-// Warp sum of 16 values by reduce-scatter: at each of the first four levels a
-// lane keeps half of its values and adds its partner's copy of that half (8,
-// 4, 2, 1 exchanges), the fifth level adds the last pair; lanes 2j and 2j + 1
-// end with the total of value j.  16 shuffles instead of 80.
-__device__ __forceinline__ float warp_sum16(float (&x)[16], int lane) {
+// Warp sum of NC (8 or 16) values by reduce-scatter: at each of the first
+// log2(NC) levels a lane keeps half of its values and adds its partner's copy
+// of that half (NC / 2, NC / 4, ..., 1 exchanges), the remaining levels add
+// the last partials; lanes (32 / NC) j .. (32 / NC) (j + 1) - 1 end with the
+// total of value j.  2 NC - 1 + 5 - log2(NC) shuffles instead of 5 NC.
+template <int NC>
+__device__ __forceinline__ float warp_sum_rs(float (&x)[NC], int lane) {
+  constexpr int kLevels = NC == 16 ? 4 : 3;
 #pragma unroll
-  for (int lvl = 0; lvl < 4; ++lvl) {
-    const int half = 8 >> lvl;              // values kept after this level
+  for (int lvl = 0; lvl < kLevels; ++lvl) {
+    const int half = (NC / 2) >> lvl;       // values kept after this level
     const int off = 16 >> lvl;              // partner lane distance
     const bool upper = (lane & off) != 0;   // keep the upper half of the live values
 #pragma unroll
@@ -73,31 +76,39 @@ __device__ __forceinline__ float warp_sum16(float (&x)[16], int lane) {
       x[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
     }
   }
-  return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 1);
+  float r = x[0];
+#pragma unroll
+  for (int off = (16 >> kLevels); off > 0; off >>= 1) r += __shfl_xor_sync(0xffffffffu, r, off);
+  return r;
 }
 
-// Index (0..15) of the value whose total lane `lane` holds after warp_sum16.
-__device__ __forceinline__ int warp_sum16_index(int lane) {
+// Index (0..NC-1) of the value whose total lane `lane` holds after warp_sum_rs.
+template <int NC>
+__device__ __forceinline__ int warp_sum_rs_index(int lane) {
   // level l kept the upper half when bit (16 >> l) of the lane was set; the
-  // kept half's offset adds 8 >> l
-  return ((lane & 16) ? 8 : 0) + ((lane & 8) ? 4 : 0) + ((lane & 4) ? 2 : 0) + ((lane & 2) ? 1 : 0);
+  // kept half's offset adds (NC / 2) >> l
+  int i = 0;
+#pragma unroll
+  for (int lvl = 0; lvl < (NC == 16 ? 4 : 3); ++lvl)
+    if (lane & (16 >> lvl)) i += (NC / 2) >> lvl;
+  return i;
 }
 
-// Sum of NV (16 or 17) values over the K threads of the block; the totals
-// land in out[].
+// Sum of NV (kCols or kCols + 1) values over the K threads of the block; the
+// totals land in out[].
 template <int K, int NV>
 __device__ __forceinline__ void block_sum(float (&x)[NV], float (*red)[kCols + 1], float* out, int tid) {
   const int lane = tid & 31, warp = tid >> 5;
-  float y[16];
+  float y[kCols];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) y[j] = x[j];
-  const float tot = warp_sum16(y, lane);
-  if ((lane & 1) == 0) red[warp][warp_sum16_index(lane)] = tot;
-  if (NV > 16) {
+  for (int j = 0; j < kCols; ++j) y[j] = x[j];
+  const float tot = warp_sum_rs<kCols>(y, lane);
+  if ((lane & (32 / kCols - 1)) == 0) red[warp][warp_sum_rs_index<kCols>(lane)] = tot;
+  if (NV > kCols) {
     float z = x[NV - 1];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-    if (lane == 0) red[warp][16] = z;
+    if (lane == 0) red[warp][kCols] = z;
   }
   __syncthreads();
   if (tid < NV) {
