@@ -199,7 +199,7 @@ gdn_status gdn_causal_conv1d_fwd(const void* x, const float* weight, const float
 size_t gdn_chunk_bwd_workspace_size(const gdn_problem* pp) {
   gdn_problem p;
   if (!problem_ok(pp, &p) || !bwd_supported(p)) return 0;
-  return bwd_workspace_bytes(p);
+  return bwdc_supported(p) ? bwdc_workspace_bytes(p) : bwd_workspace_bytes(p);
 }
 
 gdn_status gdn_chunk_bwd(const gdn_problem* pp, const void* q, const void* k, const void* v, const float* g,
@@ -213,13 +213,18 @@ gdn_status gdn_chunk_bwd(const gdn_problem* pp, const void* q, const void* k, co
   if (any_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
     return GDN_ERR_INVALID_ARG;
   if (p.varlen != (cu_seqlens != nullptr)) return GDN_ERR_INVALID_ARG;
-  if (!workspace || workspace_bytes < bwd_workspace_bytes(p) || !aligned(workspace, kAlign)) return GDN_ERR_INVALID_ARG;
+  const bool chunked = bwdc_supported(p) && (int64_t)p.N * p.Hv > 0;
+  const size_t need = chunked ? bwdc_workspace_bytes(p) : bwd_workspace_bytes(p);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, kAlign)) return GDN_ERR_INVALID_ARG;
   const void* a16[] = {dh0, dht, h0};
   for (const void* x : a16)
     if (x && !aligned(x, 16)) return GDN_ERR_INVALID_ARG;
   const void* a4[] = {q, k, v, g, beta, cu_seqlens, dout, dq, dk, dv, dg, dbeta};
   for (const void* x : a4)
     if (x && !aligned(x, 4)) return GDN_ERR_INVALID_ARG;
+  if (chunked)
+    return run_bwdc(p, q, k, v, g, beta, scale, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
+                    static_cast<cudaStream_t>(stream));
   return run_bwd(p, q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
                  static_cast<cudaStream_t>(stream));
 }

@@ -2,7 +2,8 @@
 the fp64 oracle's reverse-mode gradients on the same seeded inputs and
 upstream gradients.  The backward computes in fp32 from the stored inputs
 (bf16 or fp32), so the bar is a relative Frobenius error of at most 1e-4 on
-every gradient."""
+every gradient.  Equal-length batches with K = V = 128 take the chunked
+backward; packed sequences and K = 64 the token-recurrence one."""
 import numpy as np
 import pytest
 import torch
@@ -52,6 +53,12 @@ def check(gdn, oracle_mod, w, lens=None, with_h0=True, with_dht=True, seed=11):
 def test_bwd_fp32_gqa_ragged(gdn, oracle_mod):
     # 150 tokens: two full 64-token chunks and a tail, 16-token blocks and a tail; GQA 1 -> 2
     check(gdn, oracle_mod, I.WORKLOADS[0].with_(B=2, T=150, Hqk=1, Hv=2))
+
+
+def test_bwd_fp32_chunked_gqa_ragged(gdn, oracle_mod):
+    # equal lengths with K = V = 128: the chunked backward (150 tokens: two full
+    # chunks and a 22-token tail; GQA 1 -> 2)
+    check(gdn, oracle_mod, I.WORKLOADS[2].with_(B=2, T=150, Hqk=1, Hv=2, dtype="f32"))
 
 
 def test_bwd_bf16_varlen_gqa(gdn, oracle_mod):
