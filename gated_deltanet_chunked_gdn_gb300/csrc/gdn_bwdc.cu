@@ -23,9 +23,12 @@
 // from a serial reverse (one CTA per chain and 32-column slice of V); every
 // other product is a batched fp32 GEMM over all (chunk, head) pairs at once.
 #include "gdn_internal.h"
+#include "gdn_sm100.cuh"
 
 namespace gdn {
 namespace {
+
+using namespace sm100;
 
 constexpr int kC = 64;      // chunk length
 constexpr int kDh = 128;    // K = V
@@ -47,45 +50,71 @@ struct GemmArgs {
 };
 
 __global__ void __launch_bounds__(256) bgemm_kernel(const GemmArgs g) {
-  __shared__ __align__(16) float As[16][64 + 4];
-  __shared__ __align__(16) float Bs[16][64 + 4];
+  // k-tiles of 16 staged in two shared buffers; each thread fetches one float4
+  // of A and one of B per tile into registers one tile ahead
+  __shared__ __align__(16) float As[2][16][64 + 4];
+  __shared__ __align__(16) float Bs[2][16][64 + 4];
   const int64_t b = blockIdx.z;
   const int i0 = 64 * blockIdx.y, j0 = 64 * blockIdx.x;
   const float* A = g.A + b * g.sA;
   const float* B = g.B + b * g.sB;
   const int tid = threadIdx.x, ti = 4 * (tid >> 4), tj = 4 * (tid & 15);
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < g.Kd; k0 += 16) {
-    for (int u = tid; u < 16 * 64; u += 256) {
-      // A tile: (row i, k) -> As[k][i];  B tile: (k, col j) -> Bs[k][j]
-      int kk, i;
-      if (g.tA) { kk = u >> 6; i = u & 63; } else { i = u >> 4; kk = u & 15; }
-      As[kk][i] = g.tA ? A[(int64_t)(k0 + kk) * g.lda + i0 + i] : A[(int64_t)(i0 + i) * g.lda + k0 + kk];
-      int kb, j;
-      if (g.tB) { j = u >> 4; kb = u & 15; } else { kb = u >> 6; j = u & 63; }
-      Bs[kb][j] = g.tB ? B[(int64_t)(j0 + j) * g.ldb + k0 + kb] : B[(int64_t)(k0 + kb) * g.ldb + j0 + j];
+  // this thread's float4 of each tile: A (!tA) row ar, k 4 aq..; (tA) k ar, row 4 aq..
+  const int ar = g.tA ? tid >> 4 : tid >> 2, aq = g.tA ? 4 * (tid & 15) : 4 * (tid & 3);
+  const int br = g.tB ? tid >> 2 : tid >> 4, bq = g.tB ? 4 * (tid & 3) : 4 * (tid & 15);
+  auto fetch = [&](int k0, float4& ra, float4& rb) {
+    ra = g.tA ? *reinterpret_cast<const float4*>(A + (int64_t)(k0 + ar) * g.lda + i0 + aq)
+              : *reinterpret_cast<const float4*>(A + (int64_t)(i0 + ar) * g.lda + k0 + aq);
+    rb = g.tB ? *reinterpret_cast<const float4*>(B + (int64_t)(j0 + br) * g.ldb + k0 + bq)
+              : *reinterpret_cast<const float4*>(B + (int64_t)(k0 + br) * g.ldb + j0 + bq);
+  };
+  auto put = [&](int buf, const float4& ra, const float4& rb) {
+    if (g.tA) {
+      *reinterpret_cast<float4*>(&As[buf][ar][aq]) = ra;
+    } else {
+      As[buf][aq][ar] = ra.x; As[buf][aq + 1][ar] = ra.y; As[buf][aq + 2][ar] = ra.z; As[buf][aq + 3][ar] = ra.w;
     }
-    __syncthreads();
+    if (g.tB) {
+      Bs[buf][bq][br] = rb.x; Bs[buf][bq + 1][br] = rb.y; Bs[buf][bq + 2][br] = rb.z; Bs[buf][bq + 3][br] = rb.w;
+    } else {
+      *reinterpret_cast<float4*>(&Bs[buf][br][bq]) = rb;
+    }
+  };
+  float acc[4][4] = {};
+  float4 ra, rb;
+  fetch(0, ra, rb);
+  put(0, ra, rb);
+  __syncthreads();
+  int buf = 0;
+  for (int k0 = 0; k0 < g.Kd; k0 += 16) {
+    const bool more = k0 + 16 < g.Kd;
+    if (more) fetch(k0 + 16, ra, rb);
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[kk][ti]);
-      const float4 c = *reinterpret_cast<const float4*>(&Bs[kk][tj]);
+      const float4 a = *reinterpret_cast<const float4*>(&As[buf][kk][ti]);
+      const float4 c = *reinterpret_cast<const float4*>(&Bs[buf][kk][tj]);
       const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(av[r], bv[s], acc[r][s]);
     }
+    if (more) put(buf ^ 1, ra, rb);
     __syncthreads();
+    buf ^= 1;
   }
   float* C = g.C + b * g.sC;
 #pragma unroll
   for (int r = 0; r < 4; ++r) {
     const int i = i0 + ti + r;
     const float f = g.alpha * (g.rs ? g.rs[b * g.sR + i] : 1.f);
-    float* c = C + (int64_t)i * g.ldc + j0 + tj;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) c[s] = f * acc[r][s] + (g.beta != 0.f ? g.beta * c[s] : 0.f);
+    float4* c = reinterpret_cast<float4*>(C + (int64_t)i * g.ldc + j0 + tj);
+    float4 o = make_float4(f * acc[r][0], f * acc[r][1], f * acc[r][2], f * acc[r][3]);
+    if (g.beta != 0.f) {
+      const float4 x = *c;
+      o.x += g.beta * x.x; o.y += g.beta * x.y; o.z += g.beta * x.z; o.w += g.beta * x.w;
+    }
+    *c = o;
   }
 }
 
@@ -227,246 +256,384 @@ __global__ void __launch_bounds__(256) bwdc_scale_kv(const Lay L) {
   }
 }
 
+// Rows [0, rows) x [0, cols) floats of a row-major matrix (leading dimension
+// ld) into shared memory (leading dimension sld) by 16-byte cp.async copies;
+// cols, ld, sld and the column offset are multiples of 4.
+__device__ __forceinline__ void stage_rows(float* dst, int sld, const float* src, int64_t ld, int rows, int cols,
+                                           int tid, int nthreads) {
+  const int q = cols / 4;
+  for (int u = tid; u < rows * q; u += nthreads) {
+    const int r = u / q, c = 4 * (u % q);
+    cp_async16(dst + r * sld + c, src + r * ld + c);
+  }
+}
+
+// L2 prefetch of rows x (cols floats) of a row-major matrix.
+__device__ __forceinline__ void prefetch_rows(const float* src, int64_t ld, int rows, int cols, int tid, int nthreads) {
+  const int lines = (cols * 4 + 127) / 128;
+  for (int u = tid; u < rows * lines; u += nthreads) {
+    const float* p = src + (u / lines) * ld + 32 * (u % lines);
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+  }
+}
+
+constexpr int kLd = kDh + 4;   // padded row of the staged [64][128] tiles (no bank conflicts across rows)
+
 // Serial forward over a chain's chunks for 32 state columns: S0 of every
-// chunk and V' = U - W S0.  Grid (N Hv, 4), 256 threads.
+// chunk and V' = U - W S0.  Each chunk's W, K and U slice are staged in
+// shared memory (the next chunk's prefetched to L2 meanwhile).  Grid
+// (N Hv, 4), 256 threads, dynamic shared memory kFwdSmem.
+constexpr int kFwdSmem = (2 * kC * kLd + kC * kSl + kDh * kSl + kC * kSl) * 4;
 __global__ void __launch_bounds__(256) bwdc_fwd_states(const Lay L, const float* h0, int NC) {
-  __shared__ __align__(16) float S[kDh][kSl];
-  __shared__ __align__(16) float Vp[kC][kSl];
+  extern __shared__ __align__(16) float smf[];
+  float* Ws = smf;                    // [64][kLd]
+  float* Ks = Ws + kC * kLd;          // [64][kLd]
+  float* Us = Ks + kC * kLd;          // [64][32]
+  float* S = Us + kC * kSl;           // [128][32]
+  float* Vp = S + kDh * kSl;          // [64][32]
   const int64_t chain = blockIdx.x;
   const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
   for (int u = tid; u < kDh * kSl; u += 256) {
     const int d = u / kSl, e = u % kSl;
-    S[d][e] = h0 ? h0[(chain * kDh + d) * kDh + e0 + e] : 0.f;
+    S[d * kSl + e] = h0 ? h0[(chain * kDh + d) * kDh + e0 + e] : 0.f;
   }
-  __syncthreads();
   for (int c = 0; c < NC; ++c) {
     const int64_t b = chain * NC + c;
-    // S0 out
+    stage_rows(Ws, kLd, L.W + b * kC * kDh, kDh, kC, kDh, tid, 256);
+    stage_rows(Ks, kLd, L.K + b * kC * kDh, kDh, kC, kDh, tid, 256);
+    stage_rows(Us, kSl, L.U + b * kC * kDh + e0, kDh, kC, kSl, tid, 256);
+    cp_async_commit();
+    if (c + 1 < NC) {
+      prefetch_rows(L.W + (b + 1) * kC * kDh, kDh, kC, kDh, tid, 256);
+      prefetch_rows(L.K + (b + 1) * kC * kDh, kDh, kC, kDh, tid, 256);
+    }
+    __syncthreads();   // S of the previous step complete
     for (int u = tid; u < kDh * kSl; u += 256) {
       const int d = u / kSl, e = u % kSl;
-      L.S0[(b * kDh + d) * kDh + e0 + e] = S[d][e];
+      L.S0[(b * kDh + d) * kDh + e0 + e] = S[d * kSl + e];
     }
-    // V' = U - W S0 (64 x 32): thread -> rows 4 (tid / 8) .. + 3... (64 rows x 32 cols / 256 = 8 per thread)
+    cp_async_wait_all();
+    __syncthreads();
+    // V' = U - W S0 (64 x 32): thread -> row i, 8 columns
     {
       const int i = tid >> 2, c0 = 8 * (tid & 3);
-      const float* Wr = L.W + (b * kC + i) * kDh;
       float acc[8];
 #pragma unroll
-      for (int s = 0; s < 8; ++s) acc[s] = L.U[(b * kC + i) * kDh + e0 + c0 + s];
+      for (int s = 0; s < 8; ++s) acc[s] = Us[i * kSl + c0 + s];
+#pragma unroll 4
       for (int d = 0; d < kDh; ++d) {
-        const float w = Wr[d];
-#pragma unroll
-        for (int s = 0; s < 8; ++s) acc[s] = fmaf(-w, S[d][c0 + s], acc[s]);
+        const float w = Ws[i * kLd + d];
+        const float4 x0 = *reinterpret_cast<const float4*>(S + d * kSl + c0);
+        const float4 x1 = *reinterpret_cast<const float4*>(S + d * kSl + c0 + 4);
+        acc[0] = fmaf(-w, x0.x, acc[0]); acc[1] = fmaf(-w, x0.y, acc[1]);
+        acc[2] = fmaf(-w, x0.z, acc[2]); acc[3] = fmaf(-w, x0.w, acc[3]);
+        acc[4] = fmaf(-w, x1.x, acc[4]); acc[5] = fmaf(-w, x1.y, acc[5]);
+        acc[6] = fmaf(-w, x1.z, acc[6]); acc[7] = fmaf(-w, x1.w, acc[7]);
       }
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        Vp[i][c0 + s] = acc[s];
+        Vp[i * kSl + c0 + s] = acc[s];
         L.Vp[(b * kC + i) * kDh + e0 + c0 + s] = acc[s];
       }
     }
     __syncthreads();
-    // S <- e_l S + K^T diag(D) V'  (128 x 32: 16 per thread)
+    // S <- e_l S + K^T diag(D) V'  (128 x 32: row d, 16 columns per thread)
     {
       const float* Dv = vecp(L, b, kD);
       const float el = vecp(L, b, kE)[kC - 1];
       const int d = tid >> 1, c0 = 16 * (tid & 1);
       float acc[16];
 #pragma unroll
-      for (int s = 0; s < 16; ++s) acc[s] = el * S[d][c0 + s];
+      for (int s = 0; s < 16; ++s) acc[s] = el * S[d * kSl + c0 + s];
+#pragma unroll 2
       for (int i = 0; i < kC; ++i) {
-        const float kd = L.K[(b * kC + i) * kDh + d] * Dv[i];
+        const float kd = Ks[i * kLd + d] * Dv[i];
 #pragma unroll
-        for (int s = 0; s < 16; ++s) acc[s] = fmaf(kd, Vp[i][c0 + s], acc[s]);
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const float4 x = *reinterpret_cast<const float4*>(Vp + i * kSl + c0 + 4 * s4);
+          acc[4 * s4] = fmaf(kd, x.x, acc[4 * s4]);
+          acc[4 * s4 + 1] = fmaf(kd, x.y, acc[4 * s4 + 1]);
+          acc[4 * s4 + 2] = fmaf(kd, x.z, acc[4 * s4 + 2]);
+          acc[4 * s4 + 3] = fmaf(kd, x.w, acc[4 * s4 + 3]);
+        }
       }
-      __syncthreads();
+      __syncthreads();   // every thread done with this step's W, K, U tiles and S
 #pragma unroll
-      for (int s = 0; s < 16; ++s) S[d][c0 + s] = acc[s];
+      for (int s = 0; s < 16; ++s) S[d * kSl + c0 + s] = acc[s];
     }
-    __syncthreads();
   }
 }
 
 // Serial reverse over a chain's chunks for 32 columns of G = dL/dS1:
 // G of every chunk (before its update), dV' = D (K G) + scale P^T dO, then
-// G <- e_l G + scale Q^T diag(e) dO - W^T dV'.  dh0 = the last G.
-// Grid (N Hv, 4), 256 threads.
+// G <- e_l G + scale Q^T diag(e) dO - W^T dV'.  dh0 = the last G.  Each
+// chunk's K, Q, W, P and dO slice are staged in shared memory (the previous
+// chunk's prefetched to L2 meanwhile).  Grid (N Hv, 4), 256 threads, dynamic
+// shared memory kRevSmem.
+constexpr int kRevSmem = (3 * kC * kLd + kC * (kC + 4) + kC * kSl + kDh * kSl + 2 * kC * kSl) * 4;
 __global__ void __launch_bounds__(256) bwdc_rev(const Lay L, const float* dht, float* dh0, int NC, float scale) {
-  __shared__ __align__(16) float Gs[kDh][kSl];
-  __shared__ __align__(16) float dV[kC][kSl];
-  __shared__ __align__(16) float eD[kC][kSl];   // scale e_i dO_i
+  extern __shared__ __align__(16) float smr[];
+  float* Ks = smr;                    // [64][kLd]
+  float* Qs = Ks + kC * kLd;          // [64][kLd]
+  float* Ws = Qs + kC * kLd;          // [64][kLd]
+  float* Ps = Ws + kC * kLd;          // [64][68]
+  float* dOs = Ps + kC * (kC + 4);    // [64][32]
+  float* Gs = dOs + kC * kSl;         // [128][32]
+  float* dV = Gs + kDh * kSl;         // [64][32]
+  float* eD = dV + kC * kSl;          // [64][32]  scale e_i dO_i
   const int64_t chain = blockIdx.x;
   const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
   for (int u = tid; u < kDh * kSl; u += 256) {
     const int d = u / kSl, e = u % kSl;
-    Gs[d][e] = dht ? dht[(chain * kDh + d) * kDh + e0 + e] : 0.f;
+    Gs[d * kSl + e] = dht ? dht[(chain * kDh + d) * kDh + e0 + e] : 0.f;
   }
-  __syncthreads();
   for (int c = NC - 1; c >= 0; --c) {
     const int64_t b = chain * NC + c;
     const float* ev = vecp(L, b, kE);
     const float* Dv = vecp(L, b, kD);
+    stage_rows(Ks, kLd, L.K + b * kC * kDh, kDh, kC, kDh, tid, 256);
+    stage_rows(Qs, kLd, L.Q + b * kC * kDh, kDh, kC, kDh, tid, 256);
+    stage_rows(Ws, kLd, L.W + b * kC * kDh, kDh, kC, kDh, tid, 256);
+    stage_rows(Ps, kC + 4, L.P + b * kC * kC, kC, kC, kC, tid, 256);
+    stage_rows(dOs, kSl, L.dO + b * kC * kDh + e0, kDh, kC, kSl, tid, 256);
+    cp_async_commit();
+    if (c > 0) {
+      prefetch_rows(L.K + (b - 1) * kC * kDh, kDh, kC, kDh, tid, 256);
+      prefetch_rows(L.Q + (b - 1) * kC * kDh, kDh, kC, kDh, tid, 256);
+      prefetch_rows(L.W + (b - 1) * kC * kDh, kDh, kC, kDh, tid, 256);
+      prefetch_rows(L.P + (b - 1) * kC * kC, kC, kC, kC, tid, 256);
+    }
+    __syncthreads();   // G of the previous step complete
     for (int u = tid; u < kDh * kSl; u += 256) {
       const int d = u / kSl, e = u % kSl;
-      L.G[(b * kDh + d) * kDh + e0 + e] = Gs[d][e];
+      L.G[(b * kDh + d) * kDh + e0 + e] = Gs[d * kSl + e];
     }
-    for (int u = tid; u < kC * kSl; u += 256) {
-      const int i = u / kSl, e = u % kSl;
-      eD[i][e] = scale * ev[i] * L.dO[(b * kC + i) * kDh + e0 + e];
-    }
+    cp_async_wait_all();
     __syncthreads();
+    for (int u = tid; u < kC * kSl; u += 256) {
+      const int i = u / kSl;
+      eD[u] = scale * ev[i] * dOs[u];
+    }
     // dV' (64 x 32): D_i sum_d K_id G_de + scale sum_j P_ji dO_je
     {
       const int i = tid >> 2, c0 = 8 * (tid & 3);
       float acc[8] = {}, acc2[8] = {};
-      const float* Kr = L.K + (b * kC + i) * kDh;
+#pragma unroll 4
       for (int d = 0; d < kDh; ++d) {
-        const float kd = Kr[d];
-#pragma unroll
-        for (int s = 0; s < 8; ++s) acc[s] = fmaf(kd, Gs[d][c0 + s], acc[s]);
+        const float kd = Ks[i * kLd + d];
+        const float4 x0 = *reinterpret_cast<const float4*>(Gs + d * kSl + c0);
+        const float4 x1 = *reinterpret_cast<const float4*>(Gs + d * kSl + c0 + 4);
+        acc[0] = fmaf(kd, x0.x, acc[0]); acc[1] = fmaf(kd, x0.y, acc[1]);
+        acc[2] = fmaf(kd, x0.z, acc[2]); acc[3] = fmaf(kd, x0.w, acc[3]);
+        acc[4] = fmaf(kd, x1.x, acc[4]); acc[5] = fmaf(kd, x1.y, acc[5]);
+        acc[6] = fmaf(kd, x1.z, acc[6]); acc[7] = fmaf(kd, x1.w, acc[7]);
       }
+#pragma unroll 4
       for (int j = 0; j < kC; ++j) {
-        const float pj = L.P[(b * kC + j) * kC + i];   // P^T(i, j) = P(j, i)
-        const float* dOr = L.dO + (b * kC + j) * kDh + e0 + c0;
-#pragma unroll
-        for (int s = 0; s < 8; ++s) acc2[s] = fmaf(pj, dOr[s], acc2[s]);
+        const float pj = Ps[j * (kC + 4) + i];   // P^T(i, j) = P(j, i)
+        const float4 x0 = *reinterpret_cast<const float4*>(dOs + j * kSl + c0);
+        const float4 x1 = *reinterpret_cast<const float4*>(dOs + j * kSl + c0 + 4);
+        acc2[0] = fmaf(pj, x0.x, acc2[0]); acc2[1] = fmaf(pj, x0.y, acc2[1]);
+        acc2[2] = fmaf(pj, x0.z, acc2[2]); acc2[3] = fmaf(pj, x0.w, acc2[3]);
+        acc2[4] = fmaf(pj, x1.x, acc2[4]); acc2[5] = fmaf(pj, x1.y, acc2[5]);
+        acc2[6] = fmaf(pj, x1.z, acc2[6]); acc2[7] = fmaf(pj, x1.w, acc2[7]);
       }
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const float x = Dv[i] * acc[s] + scale * acc2[s];
-        dV[i][c0 + s] = x;
+        dV[i * kSl + c0 + s] = x;
         L.dVp[(b * kC + i) * kDh + e0 + c0 + s] = x;
       }
     }
     __syncthreads();
-    // G <- e_l G + Q^T (scale e dO) - W^T dV'   (128 x 32)
+    // G <- e_l G + Q^T (scale e dO) - W^T dV'   (128 x 32: row d, 16 columns per thread)
     {
       const float el = ev[kC - 1];
       const int d = tid >> 1, c0 = 16 * (tid & 1);
       float acc[16];
 #pragma unroll
-      for (int s = 0; s < 16; ++s) acc[s] = el * Gs[d][c0 + s];
+      for (int s = 0; s < 16; ++s) acc[s] = el * Gs[d * kSl + c0 + s];
+#pragma unroll 2
       for (int i = 0; i < kC; ++i) {
-        const float qd = L.Q[(b * kC + i) * kDh + d], wd = L.W[(b * kC + i) * kDh + d];
+        const float qd = Qs[i * kLd + d], wd = Ws[i * kLd + d];
 #pragma unroll
-        for (int s = 0; s < 16; ++s) acc[s] = fmaf(qd, eD[i][c0 + s], fmaf(-wd, dV[i][c0 + s], acc[s]));
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const float4 x = *reinterpret_cast<const float4*>(eD + i * kSl + c0 + 4 * s4);
+          const float4 y = *reinterpret_cast<const float4*>(dV + i * kSl + c0 + 4 * s4);
+          acc[4 * s4] = fmaf(qd, x.x, fmaf(-wd, y.x, acc[4 * s4]));
+          acc[4 * s4 + 1] = fmaf(qd, x.y, fmaf(-wd, y.y, acc[4 * s4 + 1]));
+          acc[4 * s4 + 2] = fmaf(qd, x.z, fmaf(-wd, y.z, acc[4 * s4 + 2]));
+          acc[4 * s4 + 3] = fmaf(qd, x.w, fmaf(-wd, y.w, acc[4 * s4 + 3]));
+        }
       }
-      __syncthreads();
+      __syncthreads();   // every thread done with this step's tiles and G
 #pragma unroll
-      for (int s = 0; s < 16; ++s) Gs[d][c0 + s] = acc[s];
+      for (int s = 0; s < 16; ++s) Gs[d * kSl + c0 + s] = acc[s];
     }
-    __syncthreads();
   }
+  __syncthreads();
   if (dh0)
     for (int u = tid; u < kDh * kSl; u += 256) {
       const int d = u / kSl, e = u % kSl;
-      dh0[(chain * kDh + d) * kDh + e0 + e] = Gs[d][e];
+      dh0[(chain * kDh + d) * kDh + e0 + e] = Gs[d * kSl + e];
     }
 }
 
-// Row sums over the 128 columns of products of two [64][128] matrices: out[i]
-// += f(i) sum_d X[i][d] Y[i][d].  mode 0: dgamma -= D_i (KG)_i . V'_i and
+// Row sums over the 128 columns of products of two [64][128] matrices (four
+// threads a row, 32 columns each).  mode 0: dgamma -= D_i (KG)_i . V'_i and
 // dgamma[last] += e_l <S0, G> + sum_i D_i (KG)_i . V'_i (the <S1, G> term);
-// mode 1: dgamma += scale e_i (Q S0)_i . dO_i.  Grid nb, 64 threads.
-__global__ void __launch_bounds__(64) bwdc_rowdots(const Lay L, int mode, float scale) {
+// mode 1: dgamma += scale e_i (Q S0)_i . dO_i.  Grid nb, 256 threads.
+__global__ void __launch_bounds__(256) bwdc_rowdots(const Lay L, int mode, float scale) {
   const int64_t b = blockIdx.x;
-  const int i = threadIdx.x;
-  const float* X = (mode == 0 ? L.X1 : L.X2) + (b * kC + i) * kDh;
-  const float* Y = (mode == 0 ? L.Vp : L.dO) + (b * kC + i) * kDh;
+  const int tid = threadIdx.x, i = tid >> 2, d0 = 32 * (tid & 3);
+  const float* X = (mode == 0 ? L.X1 : L.X2) + (b * kC + i) * kDh + d0;
+  const float* Y = (mode == 0 ? L.Vp : L.dO) + (b * kC + i) * kDh + d0;
   float s = 0.f;
-  for (int d = 0; d < kDh; ++d) s = fmaf(X[d], Y[d], s);
+#pragma unroll
+  for (int d = 0; d < 32; d += 4) {
+    const float4 x = *reinterpret_cast<const float4*>(X + d), y = *reinterpret_cast<const float4*>(Y + d);
+    s = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, s))));
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  s += __shfl_xor_sync(0xffffffffu, s, 2);
   float* dg = vecp(L, b, kDgam);
-  if (mode == 0) {
-    const float t = vecp(L, b, kD)[i] * s;
-    dg[i] -= t;
-    // <S1, G> = e_l <S0, G> + sum_i t_i
-    __shared__ float red[64], red2[64];
-    const float* S0 = L.S0 + b * kDh * kDh;
-    const float* G = L.G + b * kDh * kDh;
-    float sg = 0.f;
-    for (int x = i; x < kDh * kDh; x += 64) sg = fmaf(S0[x], G[x], sg);
-    red[i] = t;
-    red2[i] = sg;
-    __syncthreads();
-    if (i == 0) {
-      float tot = 0.f, sgt = 0.f;
-      for (int r = 0; r < 64; ++r) {
-        tot += red[r];
-        sgt += red2[r];
-      }
-      dg[kC - 1] += vecp(L, b, kE)[kC - 1] * sgt + tot;
+  if (mode == 1) {
+    if ((tid & 3) == 0) dg[i] += scale * vecp(L, b, kE)[i] * s;
+    return;
+  }
+  const float t = vecp(L, b, kD)[i] * s;
+  // <S1, G> = e_l <S0, G> + sum_i t_i
+  const float4* S0 = reinterpret_cast<const float4*>(L.S0 + b * kDh * kDh);
+  const float4* G = reinterpret_cast<const float4*>(L.G + b * kDh * kDh);
+  float sg = 0.f;
+  for (int x = tid; x < kDh * kDh / 4; x += 256) {
+    const float4 u = S0[x], v = G[x];
+    sg = fmaf(u.x, v.x, fmaf(u.y, v.y, fmaf(u.z, v.z, fmaf(u.w, v.w, sg))));
+  }
+  float tt = (tid & 3) == 0 ? t : 0.f;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sg += __shfl_xor_sync(0xffffffffu, sg, off);
+    tt += __shfl_xor_sync(0xffffffffu, tt, off);
+  }
+  __shared__ float red[8], red2[8];
+  if ((tid & 31) == 0) {
+    red[tid >> 5] = tt;
+    red2[tid >> 5] = sg;
+  }
+  if ((tid & 3) == 0) dg[i] -= t;
+  __syncthreads();
+  if (tid == 0) {
+    float tot = 0.f, sgt = 0.f;
+    for (int w = 0; w < 8; ++w) {
+      tot += red[w];
+      sgt += red2[w];
     }
-  } else {
-    dg[i] += scale * vecp(L, b, kE)[i] * s;
+    dg[kC - 1] += vecp(L, b, kE)[kC - 1] * sgt + tot;
   }
 }
 
 // dP = lower(M1) (M1 = scale dO V'^T): dgamma += rowsum(dP o P) - colsum(dP o P);
-// M1 <- dP o E (for dQ += M1 K, dK += M1^T Q).  Grid nb, 64 threads.
-__global__ void __launch_bounds__(64) bwdc_dp(const Lay L) {
+// M1 <- dP o E (for dQ += M1 K, dK += M1^T Q).  Four threads a row, 16
+// columns each.  Grid nb, 256 threads.
+__global__ void __launch_bounds__(256) bwdc_dp(const Lay L) {
   const int64_t b = blockIdx.x;
-  const int r = threadIdx.x;
+  const int tid = threadIdx.x, r = tid >> 2, j0 = 16 * (tid & 3);
   __shared__ float col[64][65];
   const float* gam = vecp(L, b, kGam);
+  const float gr = gam[r];
   float rs = 0.f;
-  for (int j = 0; j < kC; ++j) {
+#pragma unroll 4
+  for (int jj = 0; jj < 16; ++jj) {
+    const int j = j0 + jj;
     const int64_t x = b * kC * kC + r * kC + j;
     const float dp = r >= j ? L.M1[x] : 0.f;
     const float pp = dp * L.P[x];
     rs += pp;
     col[r][j] = pp;
-    L.M1[x] = r >= j ? dp * expf(gam[r] - gam[j]) : 0.f;
+    L.M1[x] = r >= j ? dp * expf(gr - gam[j]) : 0.f;
+  }
+  rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+  rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+  __syncthreads();
+  if (tid < kC) {
+    float cs = 0.f;
+    for (int i = 0; i < kC; ++i) cs += col[i][tid];
+    col[0][tid] = cs;   // column sums, read back below (row 0 of col is no longer needed)
   }
   __syncthreads();
-  float cs = 0.f;
-  for (int i = 0; i < kC; ++i) cs += col[i][r];
-  vecp(L, b, kDgam)[r] += rs - cs;
+  if ((tid & 3) == 0) vecp(L, b, kDgam)[r] += rs - col[0][r];
 }
 
 // From TdW = T^T dW and TdV = T^T dV': dK += diag(beta e) TdW, dbeta += e rowsum(K o TdW)
 // + rowsum(V o TdV), dgamma += beta e rowsum(K o TdW), TdV <- diag(beta) TdV (= dV).
-// Grid nb, 64 threads.
-__global__ void __launch_bounds__(64) bwdc_wy(const Lay L, const float* TdW, float* TdV) {
+// Four threads a row, 32 columns each.  Grid nb, 256 threads.
+__global__ void __launch_bounds__(256) bwdc_wy(const Lay L, const float* TdW, float* TdV) {
   const int64_t b = blockIdx.x;
-  const int i = threadIdx.x;
+  const int tid = threadIdx.x, i = tid >> 2, d0 = 32 * (tid & 3);
   const float be = vecp(L, b, kBe)[i], bt = vecp(L, b, kBeta)[i], e = vecp(L, b, kE)[i];
-  const int64_t r = (b * kC + i) * kDh;
+  const int64_t r = (b * kC + i) * kDh + d0;
   float kx = 0.f, vx = 0.f;
-  for (int d = 0; d < kDh; ++d) {
-    const float x3 = TdW[r + d], x4 = TdV[r + d];
-    kx = fmaf(L.K[r + d], x3, kx);
-    vx = fmaf(L.V[r + d], x4, vx);
-    L.dK[r + d] = fmaf(be, x3, L.dK[r + d]);
-    TdV[r + d] = bt * x4;
+#pragma unroll
+  for (int d = 0; d < 32; d += 4) {
+    const float4 x3 = *reinterpret_cast<const float4*>(TdW + r + d);
+    const float4 x4 = *reinterpret_cast<const float4*>(TdV + r + d);
+    const float4 k4 = *reinterpret_cast<const float4*>(L.K + r + d);
+    const float4 v4 = *reinterpret_cast<const float4*>(L.V + r + d);
+    float4 dk = *reinterpret_cast<const float4*>(L.dK + r + d);
+    kx = fmaf(k4.x, x3.x, fmaf(k4.y, x3.y, fmaf(k4.z, x3.z, fmaf(k4.w, x3.w, kx))));
+    vx = fmaf(v4.x, x4.x, fmaf(v4.y, x4.y, fmaf(v4.z, x4.z, fmaf(v4.w, x4.w, vx))));
+    dk.x = fmaf(be, x3.x, dk.x); dk.y = fmaf(be, x3.y, dk.y); dk.z = fmaf(be, x3.z, dk.z); dk.w = fmaf(be, x3.w, dk.w);
+    *reinterpret_cast<float4*>(L.dK + r + d) = dk;
+    *reinterpret_cast<float4*>(TdV + r + d) = make_float4(bt * x4.x, bt * x4.y, bt * x4.z, bt * x4.w);
   }
-  vecp(L, b, kDbeta)[i] += e * kx + vx;
-  vecp(L, b, kDgam)[i] += be * kx;
+  kx += __shfl_xor_sync(0xffffffffu, kx, 1);
+  kx += __shfl_xor_sync(0xffffffffu, kx, 2);
+  vx += __shfl_xor_sync(0xffffffffu, vx, 1);
+  vx += __shfl_xor_sync(0xffffffffu, vx, 2);
+  if ((tid & 3) == 0) {
+    vecp(L, b, kDbeta)[i] += e * kx + vx;
+    vecp(L, b, kDgam)[i] += be * kx;
+  }
 }
 
 // dA = strict-lower(M3) (M3 = -T^T dT T^T): dbeta += rowsum(dA o E o KK),
-// dgamma += rowsum(dA o A) - colsum(dA o A), M3 <- dKK = dA o beta_i E.
-// Grid nb, 64 threads.
-__global__ void __launch_bounds__(64) bwdc_da(const Lay L) {
+// dgamma += rowsum(dA o A) - colsum(dA o A), M3 <- dKK = dA o beta_i E.  Four
+// threads a row, 16 columns each.  Grid nb, 256 threads.
+__global__ void __launch_bounds__(256) bwdc_da(const Lay L) {
   const int64_t b = blockIdx.x;
-  const int r = threadIdx.x;
+  const int tid = threadIdx.x, r = tid >> 2, j0 = 16 * (tid & 3);
   __shared__ float col[64][65];
   const float* gam = vecp(L, b, kGam);
-  const float bt = vecp(L, b, kBeta)[r];
+  const float bt = vecp(L, b, kBeta)[r], gr = gam[r];
   float db = 0.f, rs = 0.f;
-  for (int j = 0; j < kC; ++j) {
+#pragma unroll 4
+  for (int jj = 0; jj < 16; ++jj) {
+    const int j = j0 + jj;
     const int64_t x = b * kC * kC + r * kC + j;
     const float da = r > j ? L.M3[x] : 0.f;
-    const float E = r > j ? expf(gam[r] - gam[j]) : 0.f;
+    const float E = r > j ? expf(gr - gam[j]) : 0.f;
     db = fmaf(da, E * L.KK[x], db);
     const float aa = da * L.A[x];
     rs += aa;
     col[r][j] = aa;
     L.M3[x] = da * bt * E;
   }
+  db += __shfl_xor_sync(0xffffffffu, db, 1);
+  db += __shfl_xor_sync(0xffffffffu, db, 2);
+  rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+  rs += __shfl_xor_sync(0xffffffffu, rs, 2);
   __syncthreads();
-  float cs = 0.f;
-  for (int i = 0; i < kC; ++i) cs += col[i][r];
-  vecp(L, b, kDgam)[r] += rs - cs;
-  vecp(L, b, kDbeta)[r] += db;
+  if (tid < kC) {
+    float cs = 0.f;
+    for (int i = 0; i < kC; ++i) cs += col[i][tid];
+    col[0][tid] = cs;
+  }
+  __syncthreads();
+  if ((tid & 3) == 0) {
+    vecp(L, b, kDgam)[r] += rs - col[0][r];
+    vecp(L, b, kDbeta)[r] += db;
+  }
 }
 
 // Scatter a pair's gradients: dq, dk (atomics across the value heads of a
@@ -548,8 +715,11 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, false, L.X1, B2, kDh, false, 0.f, L.W, B2, kDh);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, false, L.X2, B2, kDh, false, 0.f, L.U, B2, kDh);
   // the serial passes
-  bwdc_fwd_states<<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, h0, NC);
-  bwdc_rev<<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, dht, dh0, NC, scale);
+  if (cudaFuncSetAttribute(bwdc_fwd_states, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem) != cudaSuccess ||
+      cudaFuncSetAttribute(bwdc_rev, cudaFuncAttributeMaxDynamicSharedMemorySize, kRevSmem) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  bwdc_fwd_states<<<dim3((unsigned)chains, kDh / kSl), 256, kFwdSmem, s>>>(L, h0, NC);
+  bwdc_rev<<<dim3((unsigned)chains, kDh / kSl), 256, kRevSmem, s>>>(L, dht, dh0, NC, scale);
   // dQ = scale diag(e) dO S0^T ;  dK = diag(D) V' G^T
   ok = ok && gemm(s, nb, kC, kDh, kDh, scale, L.dO, B2, kDh, false, L.S0, S2, kDh, true, 0.f, L.dQ, B2, kDh,
                   L.vec + kE * kC, V8);
@@ -558,11 +728,11 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   // X1 = K G (the D (K G) . V' terms), X2 = Q S0 (the e (Q S0) . dO terms)
   ok = ok && gemm(s, nb, kC, kDh, kDh, 1.f, L.K, B2, kDh, false, L.G, S2, kDh, false, 0.f, L.X1, B2, kDh);
   ok = ok && gemm(s, nb, kC, kDh, kDh, 1.f, L.Q, B2, kDh, false, L.S0, S2, kDh, false, 0.f, L.X2, B2, kDh);
-  bwdc_rowdots<<<nbu, 64, 0, s>>>(L, 0, scale);
-  bwdc_rowdots<<<nbu, 64, 0, s>>>(L, 1, scale);
+  bwdc_rowdots<<<nbu, 256, 0, s>>>(L, 0, scale);
+  bwdc_rowdots<<<nbu, 256, 0, s>>>(L, 1, scale);
   // dP = lower(scale dO V'^T) -> (dP o E): dQ += . K, dK += .^T Q
   ok = ok && gemm(s, nb, kC, kC, kDh, scale, L.dO, B2, kDh, false, L.Vp, B2, kDh, true, 0.f, L.M1, Q2, kC);
-  bwdc_dp<<<nbu, 64, 0, s>>>(L);
+  bwdc_dp<<<nbu, 256, 0, s>>>(L);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, false, L.K, B2, kDh, false, 1.f, L.dQ, B2, kDh);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, true, L.Q, B2, kDh, false, 1.f, L.dK, B2, kDh);
   // dW = -dV' S0^T (X1); dT = dW (beta e K)^T + dV' (beta V)^T (M2)
@@ -573,11 +743,11 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   // X1 <- T^T dW, X4 = T^T dV'
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, true, L.X3, B2, kDh, false, 0.f, L.X1, B2, kDh);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, true, L.dVp, B2, kDh, false, 0.f, L.X4, B2, kDh);
-  bwdc_wy<<<nbu, 64, 0, s>>>(L, L.X1, L.X4);
+  bwdc_wy<<<nbu, 256, 0, s>>>(L, L.X1, L.X4);
   // dA = strict-lower(-T^T dT T^T): M1 = T^T dT, M3 = -M1 T^T
   ok = ok && gemm(s, nb, kC, kC, kC, 1.f, L.T, Q2, kC, true, L.M2, Q2, kC, false, 0.f, L.M1, Q2, kC);
   ok = ok && gemm(s, nb, kC, kC, kC, -1.f, L.M1, Q2, kC, false, L.T, Q2, kC, true, 0.f, L.M3, Q2, kC);
-  bwdc_da<<<nbu, 64, 0, s>>>(L);
+  bwdc_da<<<nbu, 256, 0, s>>>(L);
   // dK += dKK K + dKK^T K
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M3, Q2, kC, false, L.K, B2, kDh, false, 1.f, L.dK, B2, kDh);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M3, Q2, kC, true, L.K, B2, kDh, false, 1.f, L.dK, B2, kDh);
@@ -590,11 +760,32 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   return ok ? GDN_OK : GDN_ERR_CUDA;
 }
 
+// Sequences per group: the batch runs in groups of whole sequences whose
+// per-(chunk, head) data fits kGroupBytes (at least one sequence a group).
+constexpr size_t kGroupBytes = size_t(16) << 30;
+
+int group_seqs(const gdn_problem& p) {
+  gdn_problem one = p;
+  one.N = one.B = 1;
+  const size_t per = layout(one, nullptr).bytes;
+  int64_t g = (int64_t)(kGroupBytes / (per > 0 ? per : 1));
+  if (g < 1) g = 1;
+  return (int)(g < p.N ? g : p.N);
+}
+
+gdn_problem group_problem(const gdn_problem& p, int n) {
+  gdn_problem q = p;
+  q.N = q.B = n;
+  return q;
+}
+
 }  // namespace
 
 bool bwdc_supported(const gdn_problem& p) { return !p.varlen && p.K == kDh && p.V == kDh && p.T > 0; }
 
-size_t bwdc_workspace_bytes(const gdn_problem& p) { return kAlign + layout(p, nullptr).bytes; }
+size_t bwdc_workspace_bytes(const gdn_problem& p) {
+  return kAlign + layout(group_problem(p, group_seqs(p)), nullptr).bytes;
+}
 
 gdn_status run_bwdc(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
                     const float* beta, float scale, const float* h0, const void* dout, const float* dht, float* dq,
@@ -602,8 +793,30 @@ gdn_status run_bwdc(const gdn_problem& p, const void* q, const void* k, const vo
   int32_t* status = static_cast<int32_t*>(ws);
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
   void* w = static_cast<uint8_t*>(ws) + kAlign;
-  if (p.dt == GDN_F32) return run<float>(p, q, k, v, g, beta, scale, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, w, s);
-  return run<__nv_bfloat16>(p, q, k, v, g, beta, scale, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, w, s);
+  const int G = group_seqs(p);
+  const size_t e = p.dt == GDN_F32 ? 4 : 2;
+  const int64_t kv = (int64_t)p.K * p.V;
+  for (int n0 = 0; n0 < p.N; n0 += G) {
+    const int n = p.N - n0 < G ? p.N - n0 : G;
+    const gdn_problem gp = group_problem(p, n);
+    const int64_t t0 = (int64_t)n0 * p.T;   // first token of the group
+    auto off = [&](const void* x, int64_t elems) {
+      return x ? static_cast<const void*>(static_cast<const uint8_t*>(x) + elems * e) : nullptr;
+    };
+    auto offf = [&](const float* x, int64_t elems) { return x ? x + elems : nullptr; };
+    auto offw = [&](float* x, int64_t elems) { return x ? x + elems : nullptr; };
+    const int64_t tq = t0 * p.Hqk * p.K, tv = t0 * p.Hv * p.V, tg = t0 * p.Hv, ts = (int64_t)n0 * p.Hv * kv;
+    gdn_status st;
+    if (p.dt == GDN_F32)
+      st = run<float>(gp, off(q, tq), off(k, tq), off(v, tv), g + tg, beta + tg, scale, offf(h0, ts), off(dout, tv),
+                      offf(dht, ts), dq + tq, dk + tq, dv + tv, dg + tg, dbeta + tg, offw(dh0, ts), w, s);
+    else
+      st = run<__nv_bfloat16>(gp, off(q, tq), off(k, tq), off(v, tv), g + tg, beta + tg, scale, offf(h0, ts),
+                              off(dout, tv), offf(dht, ts), dq + tq, dk + tq, dv + tv, dg + tg, dbeta + tg,
+                              offw(dh0, ts), w, s);
+    if (st != GDN_OK) return st;
+  }
+  return GDN_OK;
 }
 
 }  // namespace gdn
