@@ -32,7 +32,7 @@ using namespace sm100;
 
 constexpr int kC = 64;      // chunk length
 constexpr int kDh = 128;    // K = V
-constexpr int kSl = 32;     // V columns per CTA of the serial kernels
+constexpr int kSl = 16;     // V columns per CTA of the serial kernels
 
 // ---------------------------------------------------------------- batched GEMM
 // C[b] = alpha diag(rs[b]) op(A[b]) op(B[b]) + beta C[b] for M, N multiples of
@@ -128,7 +128,7 @@ struct Lay {
   float *dQ, *dK;             // [nb][64][128]
   float *KK, *P, *A, *T;      // [nb][64][64]
   float *M1, *M2, *M3;        // [nb][64][64] scratch
-  float *S0, *G;              // [nb][128][128]
+  float *S0, *G, *H;          // [nb][128][128]
   float *vec;                 // [nb][8][64]: gamma, e, beta, D, beta e, dgamma, dbeta, spare
   size_t bytes;
 };
@@ -150,7 +150,7 @@ Lay layout(const gdn_problem& p, uint8_t* base) {
   L.dQ = take(big); L.dK = take(big);
   L.KK = take(sq); L.P = take(sq); L.A = take(sq); L.T = take(sq);
   L.M1 = take(sq); L.M2 = take(sq); L.M3 = take(sq);
-  L.S0 = take(st); L.G = take(st);
+  L.S0 = take(st); L.G = take(st); L.H = take(st);
   L.vec = take((size_t)L.nb * 8 * kC);
   L.bytes = off;
   return L;
@@ -279,18 +279,18 @@ __device__ __forceinline__ void prefetch_rows(const float* src, int64_t ld, int 
 
 constexpr int kLd = kDh + 4;   // padded row of the staged [64][128] tiles (no bank conflicts across rows)
 
-// Serial forward over a chain's chunks for 32 state columns: S0 of every
+// Serial forward over a chain's chunks for 16 state columns: S0 of every
 // chunk and V' = U - W S0.  Each chunk's W, K and U slice are staged in
 // shared memory (the next chunk's prefetched to L2 meanwhile).  Grid
-// (N Hv, 4), 256 threads, dynamic shared memory kFwdSmem.
+// (N Hv, 8), 256 threads, dynamic shared memory kFwdSmem (two CTAs an SM).
 constexpr int kFwdSmem = (2 * kC * kLd + kC * kSl + kDh * kSl + kC * kSl) * 4;
 __global__ void __launch_bounds__(256) bwdc_fwd_states(const Lay L, const float* h0, int NC) {
   extern __shared__ __align__(16) float smf[];
   float* Ws = smf;                    // [64][kLd]
   float* Ks = Ws + kC * kLd;          // [64][kLd]
-  float* Us = Ks + kC * kLd;          // [64][32]
-  float* S = Us + kC * kSl;           // [128][32]
-  float* Vp = S + kDh * kSl;          // [64][32]
+  float* Us = Ks + kC * kLd;          // [64][16]
+  float* S = Us + kC * kSl;           // [128][16]
+  float* Vp = S + kDh * kSl;          // [64][16]
   const int64_t chain = blockIdx.x;
   const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
   for (int u = tid; u < kDh * kSl; u += 256) {
@@ -314,73 +314,62 @@ __global__ void __launch_bounds__(256) bwdc_fwd_states(const Lay L, const float*
     }
     cp_async_wait_all();
     __syncthreads();
-    // V' = U - W S0 (64 x 32): thread -> row i, 8 columns
+    // V' = U - W S0 (64 x 16): thread -> row i, 4 columns
     {
-      const int i = tid >> 2, c0 = 8 * (tid & 3);
-      float acc[8];
-#pragma unroll
-      for (int s = 0; s < 8; ++s) acc[s] = Us[i * kSl + c0 + s];
-#pragma unroll 4
+      const int i = tid >> 2, c0 = 4 * (tid & 3);
+      float4 acc = *reinterpret_cast<const float4*>(Us + i * kSl + c0);
+#pragma unroll 8
       for (int d = 0; d < kDh; ++d) {
         const float w = Ws[i * kLd + d];
-        const float4 x0 = *reinterpret_cast<const float4*>(S + d * kSl + c0);
-        const float4 x1 = *reinterpret_cast<const float4*>(S + d * kSl + c0 + 4);
-        acc[0] = fmaf(-w, x0.x, acc[0]); acc[1] = fmaf(-w, x0.y, acc[1]);
-        acc[2] = fmaf(-w, x0.z, acc[2]); acc[3] = fmaf(-w, x0.w, acc[3]);
-        acc[4] = fmaf(-w, x1.x, acc[4]); acc[5] = fmaf(-w, x1.y, acc[5]);
-        acc[6] = fmaf(-w, x1.z, acc[6]); acc[7] = fmaf(-w, x1.w, acc[7]);
+        const float4 x = *reinterpret_cast<const float4*>(S + d * kSl + c0);
+        acc.x = fmaf(-w, x.x, acc.x); acc.y = fmaf(-w, x.y, acc.y);
+        acc.z = fmaf(-w, x.z, acc.z); acc.w = fmaf(-w, x.w, acc.w);
       }
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        Vp[i * kSl + c0 + s] = acc[s];
-        L.Vp[(b * kC + i) * kDh + e0 + c0 + s] = acc[s];
-      }
+      *reinterpret_cast<float4*>(Vp + i * kSl + c0) = acc;
+      *reinterpret_cast<float4*>(L.Vp + (b * kC + i) * kDh + e0 + c0) = acc;
     }
     __syncthreads();
-    // S <- e_l S + K^T diag(D) V'  (128 x 32: row d, 16 columns per thread)
+    // S <- e_l S + K^T diag(D) V'  (128 x 16: row d, 8 columns per thread)
     {
       const float* Dv = vecp(L, b, kD);
       const float el = vecp(L, b, kE)[kC - 1];
-      const int d = tid >> 1, c0 = 16 * (tid & 1);
-      float acc[16];
+      const int d = tid >> 1, c0 = 8 * (tid & 1);
+      float acc[8];
 #pragma unroll
-      for (int s = 0; s < 16; ++s) acc[s] = el * S[d * kSl + c0 + s];
-#pragma unroll 2
+      for (int s = 0; s < 8; ++s) acc[s] = el * S[d * kSl + c0 + s];
+#pragma unroll 4
       for (int i = 0; i < kC; ++i) {
         const float kd = Ks[i * kLd + d] * Dv[i];
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const float4 x = *reinterpret_cast<const float4*>(Vp + i * kSl + c0 + 4 * s4);
-          acc[4 * s4] = fmaf(kd, x.x, acc[4 * s4]);
-          acc[4 * s4 + 1] = fmaf(kd, x.y, acc[4 * s4 + 1]);
-          acc[4 * s4 + 2] = fmaf(kd, x.z, acc[4 * s4 + 2]);
-          acc[4 * s4 + 3] = fmaf(kd, x.w, acc[4 * s4 + 3]);
-        }
+        const float4 x0 = *reinterpret_cast<const float4*>(Vp + i * kSl + c0);
+        const float4 x1 = *reinterpret_cast<const float4*>(Vp + i * kSl + c0 + 4);
+        acc[0] = fmaf(kd, x0.x, acc[0]); acc[1] = fmaf(kd, x0.y, acc[1]);
+        acc[2] = fmaf(kd, x0.z, acc[2]); acc[3] = fmaf(kd, x0.w, acc[3]);
+        acc[4] = fmaf(kd, x1.x, acc[4]); acc[5] = fmaf(kd, x1.y, acc[5]);
+        acc[6] = fmaf(kd, x1.z, acc[6]); acc[7] = fmaf(kd, x1.w, acc[7]);
       }
-      __syncthreads();   // every thread done with this step's W, K, U tiles and S
+      __syncthreads();   // every thread done with this step's tiles and S
 #pragma unroll
-      for (int s = 0; s < 16; ++s) S[d * kSl + c0 + s] = acc[s];
+      for (int s = 0; s < 8; ++s) S[d * kSl + c0 + s] = acc[s];
     }
   }
 }
 
-// Serial reverse over a chain's chunks for 32 columns of G = dL/dS1:
-// G of every chunk (before its update), dV' = D (K G) + scale P^T dO, then
-// G <- e_l G + scale Q^T diag(e) dO - W^T dV'.  dh0 = the last G.  Each
-// chunk's K, Q, W, P and dO slice are staged in shared memory (the previous
-// chunk's prefetched to L2 meanwhile).  Grid (N Hv, 4), 256 threads, dynamic
-// shared memory kRevSmem.
-constexpr int kRevSmem = (3 * kC * kLd + kC * (kC + 4) + kC * kSl + kDh * kSl + 2 * kC * kSl) * 4;
-__global__ void __launch_bounds__(256) bwdc_rev(const Lay L, const float* dht, float* dh0, int NC, float scale) {
+// Serial reverse over a chain's chunks for 16 columns of G = dL/dS1, with the
+// G-independent terms computed beforehand by batched GEMMs (X = scale P^T dO
+// in dVp, H = scale Q^T diag(e) dO): G of every chunk (before its update),
+// dV' = D (K G) + X (over X in dVp), G <- e_l G + H - W^T dV'.  dh0 = the last
+// G.  Each chunk's K, W and the X, H slices are staged in shared memory (the
+// previous chunk's K and W prefetched to L2 meanwhile).  Grid (N Hv, 8), 256
+// threads, dynamic shared memory kRevSmem (two CTAs an SM).
+constexpr int kRevSmem = (2 * kC * kLd + kC * kSl + 2 * kDh * kSl + kC * kSl) * 4;
+__global__ void __launch_bounds__(256) bwdc_rev(const Lay L, const float* dht, float* dh0, int NC) {
   extern __shared__ __align__(16) float smr[];
   float* Ks = smr;                    // [64][kLd]
-  float* Qs = Ks + kC * kLd;          // [64][kLd]
-  float* Ws = Qs + kC * kLd;          // [64][kLd]
-  float* Ps = Ws + kC * kLd;          // [64][68]
-  float* dOs = Ps + kC * (kC + 4);    // [64][32]
-  float* Gs = dOs + kC * kSl;         // [128][32]
-  float* dV = Gs + kDh * kSl;         // [64][32]
-  float* eD = dV + kC * kSl;          // [64][32]  scale e_i dO_i
+  float* Ws = Ks + kC * kLd;          // [64][kLd]
+  float* Xs = Ws + kC * kLd;          // [64][16]
+  float* Hs = Xs + kC * kSl;          // [128][16]
+  float* Gs = Hs + kDh * kSl;         // [128][16]
+  float* dV = Gs + kDh * kSl;         // [64][16]
   const int64_t chain = blockIdx.x;
   const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
   for (int u = tid; u < kDh * kSl; u += 256) {
@@ -389,19 +378,15 @@ __global__ void __launch_bounds__(256) bwdc_rev(const Lay L, const float* dht, f
   }
   for (int c = NC - 1; c >= 0; --c) {
     const int64_t b = chain * NC + c;
-    const float* ev = vecp(L, b, kE);
     const float* Dv = vecp(L, b, kD);
     stage_rows(Ks, kLd, L.K + b * kC * kDh, kDh, kC, kDh, tid, 256);
-    stage_rows(Qs, kLd, L.Q + b * kC * kDh, kDh, kC, kDh, tid, 256);
     stage_rows(Ws, kLd, L.W + b * kC * kDh, kDh, kC, kDh, tid, 256);
-    stage_rows(Ps, kC + 4, L.P + b * kC * kC, kC, kC, kC, tid, 256);
-    stage_rows(dOs, kSl, L.dO + b * kC * kDh + e0, kDh, kC, kSl, tid, 256);
+    stage_rows(Xs, kSl, L.dVp + b * kC * kDh + e0, kDh, kC, kSl, tid, 256);
+    stage_rows(Hs, kSl, L.H + b * kDh * kDh + e0, kDh, kDh, kSl, tid, 256);
     cp_async_commit();
     if (c > 0) {
       prefetch_rows(L.K + (b - 1) * kC * kDh, kDh, kC, kDh, tid, 256);
-      prefetch_rows(L.Q + (b - 1) * kC * kDh, kDh, kC, kDh, tid, 256);
       prefetch_rows(L.W + (b - 1) * kC * kDh, kDh, kC, kDh, tid, 256);
-      prefetch_rows(L.P + (b - 1) * kC * kC, kC, kC, kC, tid, 256);
     }
     __syncthreads();   // G of the previous step complete
     for (int u = tid; u < kDh * kSl; u += 256) {
@@ -410,65 +395,45 @@ __global__ void __launch_bounds__(256) bwdc_rev(const Lay L, const float* dht, f
     }
     cp_async_wait_all();
     __syncthreads();
-    for (int u = tid; u < kC * kSl; u += 256) {
-      const int i = u / kSl;
-      eD[u] = scale * ev[i] * dOs[u];
-    }
-    // dV' (64 x 32): D_i sum_d K_id G_de + scale sum_j P_ji dO_je
+    // dV' (64 x 16) = D_i sum_d K_id G_de + X_ie: thread -> row i, 4 columns
     {
-      const int i = tid >> 2, c0 = 8 * (tid & 3);
-      float acc[8] = {}, acc2[8] = {};
-#pragma unroll 4
+      const int i = tid >> 2, c0 = 4 * (tid & 3);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
       for (int d = 0; d < kDh; ++d) {
         const float kd = Ks[i * kLd + d];
-        const float4 x0 = *reinterpret_cast<const float4*>(Gs + d * kSl + c0);
-        const float4 x1 = *reinterpret_cast<const float4*>(Gs + d * kSl + c0 + 4);
-        acc[0] = fmaf(kd, x0.x, acc[0]); acc[1] = fmaf(kd, x0.y, acc[1]);
-        acc[2] = fmaf(kd, x0.z, acc[2]); acc[3] = fmaf(kd, x0.w, acc[3]);
-        acc[4] = fmaf(kd, x1.x, acc[4]); acc[5] = fmaf(kd, x1.y, acc[5]);
-        acc[6] = fmaf(kd, x1.z, acc[6]); acc[7] = fmaf(kd, x1.w, acc[7]);
+        const float4 x = *reinterpret_cast<const float4*>(Gs + d * kSl + c0);
+        acc.x = fmaf(kd, x.x, acc.x); acc.y = fmaf(kd, x.y, acc.y);
+        acc.z = fmaf(kd, x.z, acc.z); acc.w = fmaf(kd, x.w, acc.w);
       }
-#pragma unroll 4
-      for (int j = 0; j < kC; ++j) {
-        const float pj = Ps[j * (kC + 4) + i];   // P^T(i, j) = P(j, i)
-        const float4 x0 = *reinterpret_cast<const float4*>(dOs + j * kSl + c0);
-        const float4 x1 = *reinterpret_cast<const float4*>(dOs + j * kSl + c0 + 4);
-        acc2[0] = fmaf(pj, x0.x, acc2[0]); acc2[1] = fmaf(pj, x0.y, acc2[1]);
-        acc2[2] = fmaf(pj, x0.z, acc2[2]); acc2[3] = fmaf(pj, x0.w, acc2[3]);
-        acc2[4] = fmaf(pj, x1.x, acc2[4]); acc2[5] = fmaf(pj, x1.y, acc2[5]);
-        acc2[6] = fmaf(pj, x1.z, acc2[6]); acc2[7] = fmaf(pj, x1.w, acc2[7]);
-      }
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const float x = Dv[i] * acc[s] + scale * acc2[s];
-        dV[i * kSl + c0 + s] = x;
-        L.dVp[(b * kC + i) * kDh + e0 + c0 + s] = x;
-      }
+      const float4 xs = *reinterpret_cast<const float4*>(Xs + i * kSl + c0);
+      const float di = Dv[i];
+      const float4 r = make_float4(fmaf(di, acc.x, xs.x), fmaf(di, acc.y, xs.y), fmaf(di, acc.z, xs.z),
+                                   fmaf(di, acc.w, xs.w));
+      *reinterpret_cast<float4*>(dV + i * kSl + c0) = r;
+      *reinterpret_cast<float4*>(L.dVp + (b * kC + i) * kDh + e0 + c0) = r;
     }
     __syncthreads();
-    // G <- e_l G + Q^T (scale e dO) - W^T dV'   (128 x 32: row d, 16 columns per thread)
+    // G <- e_l G + H - W^T dV'   (128 x 16: row d, 8 columns per thread)
     {
-      const float el = ev[kC - 1];
-      const int d = tid >> 1, c0 = 16 * (tid & 1);
-      float acc[16];
+      const float el = vecp(L, b, kE)[kC - 1];
+      const int d = tid >> 1, c0 = 8 * (tid & 1);
+      float acc[8];
 #pragma unroll
-      for (int s = 0; s < 16; ++s) acc[s] = el * Gs[d * kSl + c0 + s];
-#pragma unroll 2
+      for (int s = 0; s < 8; ++s) acc[s] = fmaf(el, Gs[d * kSl + c0 + s], Hs[d * kSl + c0 + s]);
+#pragma unroll 4
       for (int i = 0; i < kC; ++i) {
-        const float qd = Qs[i * kLd + d], wd = Ws[i * kLd + d];
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const float4 x = *reinterpret_cast<const float4*>(eD + i * kSl + c0 + 4 * s4);
-          const float4 y = *reinterpret_cast<const float4*>(dV + i * kSl + c0 + 4 * s4);
-          acc[4 * s4] = fmaf(qd, x.x, fmaf(-wd, y.x, acc[4 * s4]));
-          acc[4 * s4 + 1] = fmaf(qd, x.y, fmaf(-wd, y.y, acc[4 * s4 + 1]));
-          acc[4 * s4 + 2] = fmaf(qd, x.z, fmaf(-wd, y.z, acc[4 * s4 + 2]));
-          acc[4 * s4 + 3] = fmaf(qd, x.w, fmaf(-wd, y.w, acc[4 * s4 + 3]));
-        }
+        const float wd = Ws[i * kLd + d];
+        const float4 y0 = *reinterpret_cast<const float4*>(dV + i * kSl + c0);
+        const float4 y1 = *reinterpret_cast<const float4*>(dV + i * kSl + c0 + 4);
+        acc[0] = fmaf(-wd, y0.x, acc[0]); acc[1] = fmaf(-wd, y0.y, acc[1]);
+        acc[2] = fmaf(-wd, y0.z, acc[2]); acc[3] = fmaf(-wd, y0.w, acc[3]);
+        acc[4] = fmaf(-wd, y1.x, acc[4]); acc[5] = fmaf(-wd, y1.y, acc[5]);
+        acc[6] = fmaf(-wd, y1.z, acc[6]); acc[7] = fmaf(-wd, y1.w, acc[7]);
       }
       __syncthreads();   // every thread done with this step's tiles and G
 #pragma unroll
-      for (int s = 0; s < 16; ++s) Gs[d * kSl + c0 + s] = acc[s];
+      for (int s = 0; s < 8; ++s) Gs[d * kSl + c0 + s] = acc[s];
     }
   }
   __syncthreads();
@@ -477,6 +442,18 @@ __global__ void __launch_bounds__(256) bwdc_rev(const Lay L, const float* dht, f
       const int d = u / kSl, e = u % kSl;
       dh0[(chain * kDh + d) * kDh + e0 + e] = Gs[d * kSl + e];
     }
+}
+
+// dst[i][:] = vec[i] src[i][:] for a pair's [64][128] rows.  Grid nb, 256 threads.
+__global__ void __launch_bounds__(256) bwdc_scale_rows(float* dst, const float* src, const Lay L, int which) {
+  const int64_t b = blockIdx.x;
+  const float* v = vecp(L, b, which);
+  for (int u = threadIdx.x; u < kC * kDh / 4; u += 256) {
+    const int i = (4 * u) / kDh;
+    const float4 x = reinterpret_cast<const float4*>(src + b * kC * kDh)[u];
+    const float f = v[i];
+    reinterpret_cast<float4*>(dst + b * kC * kDh)[u] = make_float4(f * x.x, f * x.y, f * x.z, f * x.w);
+  }
 }
 
 // Row sums over the 128 columns of products of two [64][128] matrices (four
@@ -719,7 +696,11 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
       cudaFuncSetAttribute(bwdc_rev, cudaFuncAttributeMaxDynamicSharedMemorySize, kRevSmem) != cudaSuccess)
     return GDN_ERR_CUDA;
   bwdc_fwd_states<<<dim3((unsigned)chains, kDh / kSl), 256, kFwdSmem, s>>>(L, h0, NC);
-  bwdc_rev<<<dim3((unsigned)chains, kDh / kSl), 256, kRevSmem, s>>>(L, dht, dh0, NC, scale);
+  // the reverse pass's G-independent terms: X = scale P^T dO (in dVp), H = scale Q^T diag(e) dO
+  ok = ok && gemm(s, nb, kC, kDh, kC, scale, L.P, Q2, kC, true, L.dO, B2, kDh, false, 0.f, L.dVp, B2, kDh);
+  bwdc_scale_rows<<<nbu, 256, 0, s>>>(L.X3, L.dO, L, kE);
+  ok = ok && gemm(s, nb, kDh, kDh, kC, scale, L.Q, B2, kDh, true, L.X3, B2, kDh, false, 0.f, L.H, S2, kDh);
+  bwdc_rev<<<dim3((unsigned)chains, kDh / kSl), 256, kRevSmem, s>>>(L, dht, dh0, NC);
   // dQ = scale diag(e) dO S0^T ;  dK = diag(D) V' G^T
   ok = ok && gemm(s, nb, kC, kDh, kDh, scale, L.dO, B2, kDh, false, L.S0, S2, kDh, true, 0.f, L.dQ, B2, kDh,
                   L.vec + kE * kC, V8);
