@@ -273,8 +273,13 @@ gdn_status gdn_recurrent_fwd(const gdn_problem* p, const void* q, const void* k,
  *     dg_t = e^{g_t} (<G, S_{t-1}> - beta_t w.u);  dbeta_t = -e^{g_t} w.u + w.v_t
  *     dk_t = -e^{g_t} beta_t (G u + S_{t-1} w) + beta_t G v_t
  *     G <- e^{g_t} (G - beta_t k_t w^T)
- * from G = dht down to dh0 = G (S_t the state after token t, S_0 = h0).  The
- * states are recomputed in fp32 from checkpoints at every 64th token.
+ * from G = dht down to dh0 = G (S_t the state after token t, S_0 = h0).
+ * Equal-length batches with K = V = 128 run the chunked form of the same
+ * reverse mode (64-token chunks: batched fp32 products for everything but
+ * the chunk-to-chunk state and adjoint recurrences; about 0.8 MB of workspace
+ * per (chunk, value head), the batch taken in sequence groups within 16 GiB);
+ * other problems recompute the states in fp32 from checkpoints at every 64th
+ * token.  Both compute in fp32.
  *   p, q, k, v, g, beta, scale, h0, cu_seqlens : as for gdn_chunk_fwd (K in
  *                 {64, 128}, V a multiple of 16; any C)
  *   dout        : [B, T, Hv, V], dtype p->dt;  dht : [N, Hv, K, V] fp32 or NULL (= 0)
@@ -282,9 +287,10 @@ gdn_status gdn_recurrent_fwd(const gdn_problem* p, const void* q, const void* k,
  *                 q/k head);  dv : out [B, T, Hv, V] fp32
  *   dg, dbeta   : out [B, T, Hv] fp32;  dh0 : out [N, Hv, K, V] fp32 or NULL
  *   workspace   : gdn_chunk_bwd_workspace_size(p) bytes, 256-byte aligned
- *                 (state checkpoints and the device status word)
- * dq, dk, dg and dbeta are sums of fp32 atomic additions (their rounding may
- * differ between runs).  Malformed cu_seqlens set the status word (read it
+ *                 (the device status word and the per-chunk intermediates)
+ * dq and dk (and, for packed sequences or K = 64, dg and dbeta) are sums of
+ * fp32 atomic additions across value heads or column slices (their rounding
+ * may differ between runs).  Malformed cu_seqlens set the status word (read it
  * with gdn_chunk_bwd_get_device_status) and leave the gradients incomplete.
  * Asynchronous on `stream`.
  */
