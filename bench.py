@@ -377,11 +377,16 @@ def run_decode(args, rank, world, dev):
 FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
+BWDC_LAUNCHES = 36          # kernels of one sequence group of the chunked backward (gdn_bwdc.cu)
+BWDC_GROUP_BYTES = 16 << 30  # the chunked backward's per-group workspace budget
+
+
 def run_bwd(args, rank, world, dev):
     """Backward pass on the 16 x 8192, 32-head batch (bf16 inputs, fp32
-    gradients).  One step = one gdn_chunk_bwd call (checkpoint pass +
-    backward).  Algorithmic FLOPs per (token, value head): one forward step of
-    the recurrence (4 K V) and one reverse step (16 K V)."""
+    gradients).  One step = one gdn_chunk_bwd call (the chunked backward for
+    this equal-length K = V = 128 batch, in sequence groups).  Algorithmic
+    FLOPs per (token, value head): one forward step of the recurrence (4 K V)
+    and one reverse step (16 K V)."""
     import torch
     from gated_deltanet_chunked_gdn_gb300 import binding
     from gated_deltanet_chunked_gdn_gb300 import inputs as I
@@ -392,6 +397,12 @@ def run_bwd(args, rank, world, dev):
     dht = torch.randn((w.B, w.Hv, w.K, w.V), generator=gen, device=dev)
     p = binding.problem_of(x["q"], x["v"], 64)
     ws = torch.empty(binding.gdn_chunk_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
+    # sequence groups of the chunked backward: as many whole sequences as fit
+    # its budget, from the workspace of one sequence
+    p1 = binding.problem_of(x["q"][:1], x["v"][:1], 64)
+    per_seq = binding.gdn_chunk_bwd_workspace_size(p1)
+    group = max(1, min(w.B, BWDC_GROUP_BYTES // max(per_seq, 1)))
+    groups = -(-w.B // group)
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -417,8 +428,8 @@ def run_bwd(args, rank, world, dev):
                    "l2": "inputs larger than L2 (4.4 GB of inputs and upstream gradients per step)"},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_SIMT_TFLOPS, "unit": "TFLOP/s",
                      "frac": achieved / FP32_SIMT_TFLOPS, "traffic": None, "peak_source": "derived (unit counts x clock)",
-                     "kernel": "gdn_bwd_ckpt_kernel + gdn_bwd_kernel (one step)", "alg_flops": flops},
-        "gpu_launches": 2 * args.steps,
+                     "kernel": "chunked backward, all launches of one step", "alg_flops": flops},
+        "gpu_launches": BWDC_LAUNCHES * groups * args.steps,
         "clocks": clocks,
     }
     if rank == 0:
