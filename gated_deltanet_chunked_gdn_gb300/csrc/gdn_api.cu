@@ -213,7 +213,9 @@ gdn_status gdn_chunk_bwd(const gdn_problem* pp, const void* q, const void* k, co
   if (any_tokens && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
     return GDN_ERR_INVALID_ARG;
   if (p.varlen != (cu_seqlens != nullptr)) return GDN_ERR_INVALID_ARG;
-  const bool chunked = bwdc_supported(p) && (int64_t)p.N * p.Hv > 0;
+  // the chunked backward reads q, k, v and dout in 16-byte vectors
+  const bool chunked = bwdc_supported(p) && (int64_t)p.N * p.Hv > 0 && aligned(q, 16) && aligned(k, 16) &&
+                       aligned(v, 16) && aligned(dout, 16);
   const size_t need = chunked ? bwdc_workspace_bytes(p) : bwd_workspace_bytes(p);
   if (!workspace || workspace_bytes < need || !aligned(workspace, kAlign)) return GDN_ERR_INVALID_ARG;
   const void* a16[] = {dh0, dht, h0};

@@ -159,8 +159,14 @@ Lay layout(const gdn_problem& p, uint8_t* base) {
 enum { kGam = 0, kE = 1, kBeta = 2, kD = 3, kBe = 4, kDgam = 5, kDbeta = 6 };
 __device__ __forceinline__ float* vecp(const Lay& L, int64_t b, int which) { return L.vec + (b * 8 + which) * kC; }
 
-template <typename Tin>
-__device__ __forceinline__ float ldf(const Tin* p, int64_t i) { return to_f(p[i]); }
+// Four consecutive elements (16-byte aligned for fp32, 8-byte for bf16) as fp32.
+__device__ __forceinline__ float4 ld4f(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4f(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
 
 // Gather one pair's rows (fp32, zero-padded) and its per-row scalars.
 // Grid nb, 256 threads.  Pair b = ((n Hv + h) NC + c).
@@ -174,14 +180,15 @@ __global__ void __launch_bounds__(256) bwdc_gather(const Lay L, const Tin* q, co
   const int64_t t0 = (int64_t)n * T + (int64_t)c * kC;
   const int Lc = T - c * kC < kC ? T - c * kC : kC;
   const int tid = threadIdx.x;
-  for (int u = tid; u < kC * kDh; u += 256) {
-    const int i = u / kDh, d = u % kDh;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = tid; u < kC * kDh / 4; u += 256) {
+    const int i = (4 * u) / kDh, d = (4 * u) % kDh;
     const bool in = i < Lc;
     const int64_t qk = ((t0 + i) * Hqk + hq) * (int64_t)kDh + d, vo = ((t0 + i) * Hv + h) * (int64_t)kDh + d;
-    L.K[b * kC * kDh + u] = in ? ldf(k, qk) : 0.f;
-    L.Q[b * kC * kDh + u] = in ? ldf(q, qk) : 0.f;
-    L.V[b * kC * kDh + u] = in ? ldf(v, vo) : 0.f;
-    L.dO[b * kC * kDh + u] = in ? ldf(dout, vo) : 0.f;
+    reinterpret_cast<float4*>(L.K + b * kC * kDh)[u] = in ? ld4f(k + qk) : z;
+    reinterpret_cast<float4*>(L.Q + b * kC * kDh)[u] = in ? ld4f(q + qk) : z;
+    reinterpret_cast<float4*>(L.V + b * kC * kDh)[u] = in ? ld4f(v + vo) : z;
+    reinterpret_cast<float4*>(L.dO + b * kC * kDh)[u] = in ? ld4f(dout + vo) : z;
   }
   if (tid < 32) {
     // gamma by a warp scan over two rows per lane
@@ -248,11 +255,13 @@ __global__ void __launch_bounds__(256) bwdc_scale_kv(const Lay L) {
   const int64_t b = blockIdx.x;
   const float* be = vecp(L, b, kBe);
   const float* bet = vecp(L, b, kBeta);
-  for (int u = threadIdx.x; u < kC * kDh; u += 256) {
-    const int i = u / kDh;
-    const int64_t x = b * kC * kDh + u;
-    L.X1[x] = be[i] * L.K[x];
-    L.X2[x] = bet[i] * L.V[x];
+  for (int u = threadIdx.x; u < kC * kDh / 4; u += 256) {
+    const int i = (4 * u) / kDh;
+    const float4 k4 = reinterpret_cast<const float4*>(L.K + b * kC * kDh)[u];
+    const float4 v4 = reinterpret_cast<const float4*>(L.V + b * kC * kDh)[u];
+    const float fb = be[i], fv = bet[i];
+    reinterpret_cast<float4*>(L.X1 + b * kC * kDh)[u] = make_float4(fb * k4.x, fb * k4.y, fb * k4.z, fb * k4.w);
+    reinterpret_cast<float4*>(L.X2 + b * kC * kDh)[u] = make_float4(fv * v4.x, fv * v4.y, fv * v4.z, fv * v4.w);
   }
 }
 
