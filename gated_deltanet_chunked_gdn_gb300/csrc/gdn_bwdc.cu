@@ -265,18 +265,6 @@ __global__ void __launch_bounds__(256) bwdc_scale_kv(const Lay L) {
   }
 }
 
-// Rows [0, rows) x [0, cols) floats of a row-major matrix (leading dimension
-// ld) into shared memory (leading dimension sld) by 16-byte cp.async copies;
-// cols, ld, sld and the column offset are multiples of 4.
-__device__ __forceinline__ void stage_rows(float* dst, int sld, const float* src, int64_t ld, int rows, int cols,
-                                           int tid, int nthreads) {
-  const int q = cols / 4;
-  for (int u = tid; u < rows * q; u += nthreads) {
-    const int r = u / q, c = 4 * (u % q);
-    cp_async16(dst + r * sld + c, src + r * ld + c);
-  }
-}
-
 // L2 prefetch of rows x (cols floats) of a row-major matrix.
 __device__ __forceinline__ void prefetch_rows(const float* src, int64_t ld, int rows, int cols, int tid, int nthreads) {
   const int lines = (cols * 4 + 127) / 128;
@@ -286,171 +274,313 @@ __device__ __forceinline__ void prefetch_rows(const float* src, int64_t ld, int 
   }
 }
 
-constexpr int kLd = kDh + 4;   // padded row of the staged [64][128] tiles (no bank conflicts across rows)
+// The serial passes run their two products per chunk on the tensor cores
+// (mma.sync m16n8k8, tf32) in three terms, hi hi + hi lo + lo hi, where
+// x = hi + lo with hi = x cut to its top 10 mantissa bits and lo = x - hi
+// (exact in fp32): the dropped lo lo term and the unit's truncation of lo
+// leave about 2^-19 of each product, near fp32.  Operands that sit in shared
+// memory are stored as separate hi and lo arrays in the order of the MMA
+// fragments, so that a lane reads its four values of a k-step with one
+// 16-byte load.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
 
-// Serial forward over a chain's chunks for 16 state columns: S0 of every
-// chunk and V' = U - W S0.  Each chunk's W, K and U slice are staged in
-// shared memory (the next chunk's prefetched to L2 meanwhile).  Grid
-// (N Hv, 8), 256 threads, dynamic shared memory kFwdSmem (two CTAs an SM).
-constexpr int kFwdSmem = (2 * kC * kLd + kC * kSl + kDh * kSl + kC * kSl) * 4;
-__global__ void __launch_bounds__(256) bwdc_fwd_states(const Lay L, const float* h0, int NC) {
-  extern __shared__ __align__(16) float smf[];
-  float* Ws = smf;                    // [64][kLd]
-  float* Ks = Ws + kC * kLd;          // [64][kLd]
-  float* Us = Ks + kC * kLd;          // [64][16]
-  float* S = Us + kC * kSl;           // [128][16]
-  float* Vp = S + kDh * kSl;          // [64][16]
-  const int64_t chain = blockIdx.x;
-  const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
-  for (int u = tid; u < kDh * kSl; u += 256) {
-    const int d = u / kSl, e = u % kSl;
-    S[d * kSl + e] = h0 ? h0[(chain * kDh + d) * kDh + e0 + e] : 0.f;
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// A [128][16] slice X (the state, or G) as the A operand of X^T R^T: k-step
+// ks = 2 kk + p covers rows d = 16 kk + 4 t + 2 p (fragment column t) and
+// d + 1 (column t + 4), fragment row g = column c % 8, c / 8 = the lower or
+// upper 8 rows; lane 4 g + t holds {(d, g), (d, g + 8), (d + 1, g), (d + 1, g + 8)}.
+__device__ __forceinline__ int xf_index(int d, int c) {
+  const int ks = 2 * (d >> 4) + ((d >> 1) & 1), t = (d >> 2) & 3;
+  return ((ks * 32 + 4 * (c & 7) + t) << 2) + 2 * (d & 1) + (c >> 3);
+}
+// A [64][16] slice V as the B operand of Col^T V: k-step ks covers rows
+// 8 ks + t (fragment row t) and 8 ks + t + 4 (row t + 4), fragment column g
+// = c % 8 of n-tile c / 8; lane 4 g + t holds {b0, b1} of n-tile 0, then of 1.
+__device__ __forceinline__ int vf_index(int i, int c) {
+  return (((i >> 3) * 32 + 4 * (c & 7) + (i & 3)) << 2) + 2 * (c >> 3) + ((i >> 2) & 1);
+}
+constexpr int kXF = kDh * kSl;   // floats of one XF array
+constexpr int kVF = kC * kSl;    // floats of one VF array
+
+__device__ __forceinline__ void put_split(float* hi, float* lo, int at, float x) {
+  uint32_t h, l;
+  split_tf32(x, h, l);
+  hi[at] = __uint_as_float(h);
+  lo[at] = __uint_as_float(l);
+}
+
+// out = (R X)[i][c] at i = 8 w + 2 t (+1), c = g (+8): out[0] = (i, c),
+// out[1] = (i + 1, c), out[2] = (i, c + 8), out[3] = (i + 1, c + 8).  The warp
+// computes n-tile w of X^T R^T over 16 k-steps; r[kk] holds R[8 w + g][16 kk + 4 t .. + 3].
+__device__ __forceinline__ void row_product(const float4 (&r)[8], const float* xh, const float* xl, int lane,
+                                            float (&out)[4]) {
+  out[0] = out[1] = out[2] = out[3] = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const float rv[4] = {r[kk].x, r[kk].y, r[kk].z, r[kk].w};
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const int ks = 2 * kk + p;
+      uint32_t bh0, bl0, bh1, bl1;
+      split_tf32(rv[2 * p], bh0, bl0);
+      split_tf32(rv[2 * p + 1], bh1, bl1);
+      const uint4 ah = *reinterpret_cast<const uint4*>(xh + ((ks * 32 + lane) << 2));
+      const uint4 al = *reinterpret_cast<const uint4*>(xl + ((ks * 32 + lane) << 2));
+      mma_tf32(out, al.x, al.y, al.z, al.w, bh0, bh1);
+      mma_tf32(out, ah.x, ah.y, ah.z, ah.w, bl0, bl1);
+      mma_tf32(out, ah.x, ah.y, ah.z, ah.w, bh0, bh1);
+    }
   }
+}
+
+// st[nt] += sign Col^T V for the rows d = 16 w + g (+8) and columns 8 nt + 2 t
+// (+1) (the C fragments of m-tile w); col[4 ks + r] holds Col[8 ks + t (+4 for
+// r >= 2)][16 w + g (+8 for odd r)].
+__device__ __forceinline__ void col_product(float (&st)[2][4], const float (&col)[32], const float* vh,
+                                            const float* vl, int lane, float sign) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    uint32_t ah[4], al[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) split_tf32(sign * col[4 * ks + r], ah[r], al[r]);
+    const uint4 bh = *reinterpret_cast<const uint4*>(vh + ((ks * 32 + lane) << 2));
+    const uint4 bl = *reinterpret_cast<const uint4*>(vl + ((ks * 32 + lane) << 2));
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint32_t h0 = nt ? bh.z : bh.x, h1 = nt ? bh.w : bh.y;
+      const uint32_t l0 = nt ? bl.z : bl.x, l1 = nt ? bl.w : bl.y;
+      mma_tf32(st[nt], al[0], al[1], al[2], al[3], h0, h1);
+      mma_tf32(st[nt], ah[0], ah[1], ah[2], ah[3], l0, l1);
+      mma_tf32(st[nt], ah[0], ah[1], ah[2], ah[3], h0, h1);
+    }
+  }
+}
+
+// Row d and column c of state element r of the C fragment st[nt][r].
+__device__ __forceinline__ int st_row(int w, int g, int r) { return 16 * w + g + 8 * (r >> 1); }
+__device__ __forceinline__ int st_col(int t, int nt, int r) { return 8 * nt + 2 * t + (r & 1); }
+
+__device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpret_cast<const float4*>(p)); }
+
+// Serial forward over a chain's chunks for the 16 state columns e0 .. e0 + 15:
+// S0 of every chunk, V' = U - W S0 and S <- e_l S + K^T diag(D) V'.  The
+// state slice lives in the MMA accumulators of the state update (warp w: rows
+// 16 w .. 16 w + 15) and, split for the next V' product, in shared memory;
+// each lane holds its fragments of the chunk's W rows and K columns in
+// registers, loaded one chunk ahead so that their latency hides behind the
+// arithmetic of the chunk before.  Grid (N Hv, 8), 256 threads.
+__global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const float* h0, int NC) {
+  __shared__ __align__(16) float xh[kXF], xl[kXF], vh[kVF], vl[kVF];
+  const int64_t chain = blockIdx.x, b0 = chain * NC;
+  const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
+  const int w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int i0 = 8 * w + 2 * t;   // rows i0, i0 + 1 of the V' product's output
+  float st[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int d = st_row(w, g, r), c = st_col(t, nt, r);
+      st[nt][r] = h0 ? h0[(chain * kDh + d) * kDh + e0 + c] : 0.f;   // h0 may be 4-byte aligned only
+      put_split(xh, xl, xf_index(d, c), st[nt][r]);
+    }
+  auto put_s0 = [&](int64_t b) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        *reinterpret_cast<float2*>(L.S0 + (b * kDh + st_row(w, g, 2 * h)) * kDh + e0 + st_col(t, nt, 0)) =
+            make_float2(st[nt][2 * h], st[nt][2 * h + 1]);
+  };
+  put_s0(b0);
+  float4 wr[8];
+  float ur[4], dr[2], kc[32], el;
+  auto load_r = [&](int64_t b) {   // W rows 8 w + g; U and D at the V' product's output
+    const float* wp = L.W + (b * kC + 8 * w + g) * kDh + 4 * t;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) wr[kk] = ldg4(wp + 16 * kk);
+    const float* up = L.U + (b * kC + i0) * kDh + e0 + g;
+    ur[0] = __ldg(up), ur[1] = __ldg(up + kDh), ur[2] = __ldg(up + 8), ur[3] = __ldg(up + kDh + 8);
+    const float* dp = vecp(L, b, kD) + i0;
+    dr[0] = __ldg(dp), dr[1] = __ldg(dp + 1);
+  };
+  auto load_c = [&](int64_t b) {   // K columns 16 w + g (+8) at rows 8 ks + t (+4)
+    const float* kp = L.K + (b * kC + t) * kDh + 16 * w + g;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      kc[4 * ks] = __ldg(kp + 8 * ks * kDh);
+      kc[4 * ks + 1] = __ldg(kp + 8 * ks * kDh + 8);
+      kc[4 * ks + 2] = __ldg(kp + (8 * ks + 4) * kDh);
+      kc[4 * ks + 3] = __ldg(kp + (8 * ks + 4) * kDh + 8);
+    }
+    el = __ldg(vecp(L, b, kE) + kC - 1);
+  };
+  load_r(b0);
+  load_c(b0);
+  __syncthreads();
+#pragma unroll 1
   for (int c = 0; c < NC; ++c) {
-    const int64_t b = chain * NC + c;
-    stage_rows(Ws, kLd, L.W + b * kC * kDh, kDh, kC, kDh, tid, 256);
-    stage_rows(Ks, kLd, L.K + b * kC * kDh, kDh, kC, kDh, tid, 256);
-    stage_rows(Us, kSl, L.U + b * kC * kDh + e0, kDh, kC, kSl, tid, 256);
-    cp_async_commit();
-    if (c + 1 < NC) {
-      prefetch_rows(L.W + (b + 1) * kC * kDh, kDh, kC, kDh, tid, 256);
-      prefetch_rows(L.K + (b + 1) * kC * kDh, kDh, kC, kDh, tid, 256);
+    const int64_t b = b0 + c;
+    if (c + 2 < NC) {
+      prefetch_rows(L.W + (b + 2) * kC * kDh, kDh, kC, kDh, tid, 256);
+      prefetch_rows(L.K + (b + 2) * kC * kDh, kDh, kC, kDh, tid, 256);
     }
-    __syncthreads();   // S of the previous step complete
-    for (int u = tid; u < kDh * kSl; u += 256) {
-      const int d = u / kSl, e = u % kSl;
-      L.S0[(b * kDh + d) * kDh + e0 + e] = S[d * kSl + e];
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    // V' = U - W S0 (64 x 16): thread -> row i, 4 columns
     {
-      const int i = tid >> 2, c0 = 4 * (tid & 3);
-      float4 acc = *reinterpret_cast<const float4*>(Us + i * kSl + c0);
-#pragma unroll 8
-      for (int d = 0; d < kDh; ++d) {
-        const float w = Ws[i * kLd + d];
-        const float4 x = *reinterpret_cast<const float4*>(S + d * kSl + c0);
-        acc.x = fmaf(-w, x.x, acc.x); acc.y = fmaf(-w, x.y, acc.y);
-        acc.z = fmaf(-w, x.z, acc.z); acc.w = fmaf(-w, x.w, acc.w);
-      }
-      *reinterpret_cast<float4*>(Vp + i * kSl + c0) = acc;
-      *reinterpret_cast<float4*>(L.Vp + (b * kC + i) * kDh + e0 + c0) = acc;
+      // V' = U - W S0 at rows i0, i0 + 1 and columns g, g + 8
+      float o[4];
+      row_product(wr, xh, xl, lane, o);
+      const float v[4] = {ur[0] - o[0], ur[1] - o[1], ur[2] - o[2], ur[3] - o[3]};
+      const float d0 = dr[0], d1 = dr[1];
+      if (c + 1 < NC) load_r(b + 1);
+      float* vp = L.Vp + (b * kC + i0) * kDh + e0 + g;
+      vp[0] = v[0], vp[kDh] = v[1], vp[8] = v[2], vp[kDh + 8] = v[3];
+      put_split(vh, vl, vf_index(i0, g), d0 * v[0]);
+      put_split(vh, vl, vf_index(i0 + 1, g), d1 * v[1]);
+      put_split(vh, vl, vf_index(i0, g + 8), d0 * v[2]);
+      put_split(vh, vl, vf_index(i0 + 1, g + 8), d1 * v[3]);
     }
     __syncthreads();
-    // S <- e_l S + K^T diag(D) V'  (128 x 16: row d, 8 columns per thread)
     {
-      const float* Dv = vecp(L, b, kD);
-      const float el = vecp(L, b, kE)[kC - 1];
-      const int d = tid >> 1, c0 = 8 * (tid & 1);
-      float acc[8];
+      // S <- e_l S + K^T (D V')
 #pragma unroll
-      for (int s = 0; s < 8; ++s) acc[s] = el * S[d * kSl + c0 + s];
-#pragma unroll 4
-      for (int i = 0; i < kC; ++i) {
-        const float kd = Ks[i * kLd + d] * Dv[i];
-        const float4 x0 = *reinterpret_cast<const float4*>(Vp + i * kSl + c0);
-        const float4 x1 = *reinterpret_cast<const float4*>(Vp + i * kSl + c0 + 4);
-        acc[0] = fmaf(kd, x0.x, acc[0]); acc[1] = fmaf(kd, x0.y, acc[1]);
-        acc[2] = fmaf(kd, x0.z, acc[2]); acc[3] = fmaf(kd, x0.w, acc[3]);
-        acc[4] = fmaf(kd, x1.x, acc[4]); acc[5] = fmaf(kd, x1.y, acc[5]);
-        acc[6] = fmaf(kd, x1.z, acc[6]); acc[7] = fmaf(kd, x1.w, acc[7]);
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) st[nt][r] *= el;
+      col_product(st, kc, vh, vl, lane, 1.f);
+      if (c + 1 < NC) {
+        load_c(b + 1);
+        put_s0(b + 1);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) put_split(xh, xl, xf_index(st_row(w, g, r), st_col(t, nt, r)), st[nt][r]);
       }
-      __syncthreads();   // every thread done with this step's tiles and S
-#pragma unroll
-      for (int s = 0; s < 8; ++s) S[d * kSl + c0 + s] = acc[s];
     }
+    __syncthreads();
   }
 }
 
 // Serial reverse over a chain's chunks for 16 columns of G = dL/dS1, with the
 // G-independent terms computed beforehand by batched GEMMs (X = scale P^T dO
 // in dVp, H = scale Q^T diag(e) dO): G of every chunk (before its update),
-// dV' = D (K G) + X (over X in dVp), G <- e_l G + H - W^T dV'.  dh0 = the last
-// G.  Each chunk's K, W and the X, H slices are staged in shared memory (the
-// previous chunk's K and W prefetched to L2 meanwhile).  Grid (N Hv, 8), 256
-// threads, dynamic shared memory kRevSmem (two CTAs an SM).
-constexpr int kRevSmem = (2 * kC * kLd + kC * kSl + 2 * kDh * kSl + kC * kSl) * 4;
-__global__ void __launch_bounds__(256) bwdc_rev(const Lay L, const float* dht, float* dh0, int NC) {
-  extern __shared__ __align__(16) float smr[];
-  float* Ks = smr;                    // [64][kLd]
-  float* Ws = Ks + kC * kLd;          // [64][kLd]
-  float* Xs = Ws + kC * kLd;          // [64][16]
-  float* Hs = Xs + kC * kSl;          // [128][16]
-  float* Gs = Hs + kDh * kSl;         // [128][16]
-  float* dV = Gs + kDh * kSl;         // [64][16]
-  const int64_t chain = blockIdx.x;
+// dV' = D (K G) + X (over X in dVp), G <- e_l G + H - W^T dV'; dh0 = the last
+// G.  Same arrangement as the forward pass, with K rows and W columns.  Grid
+// (N Hv, 8), 256 threads.
+__global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht, float* dh0, int NC) {
+  __shared__ __align__(16) float xh[kXF], xl[kXF], vh[kVF], vl[kVF];
+  const int64_t chain = blockIdx.x, b0 = chain * NC;
   const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
-  for (int u = tid; u < kDh * kSl; u += 256) {
-    const int d = u / kSl, e = u % kSl;
-    Gs[d * kSl + e] = dht ? dht[(chain * kDh + d) * kDh + e0 + e] : 0.f;
-  }
-  for (int c = NC - 1; c >= 0; --c) {
-    const int64_t b = chain * NC + c;
-    const float* Dv = vecp(L, b, kD);
-    stage_rows(Ks, kLd, L.K + b * kC * kDh, kDh, kC, kDh, tid, 256);
-    stage_rows(Ws, kLd, L.W + b * kC * kDh, kDh, kC, kDh, tid, 256);
-    stage_rows(Xs, kSl, L.dVp + b * kC * kDh + e0, kDh, kC, kSl, tid, 256);
-    stage_rows(Hs, kSl, L.H + b * kDh * kDh + e0, kDh, kDh, kSl, tid, 256);
-    cp_async_commit();
-    if (c > 0) {
-      prefetch_rows(L.K + (b - 1) * kC * kDh, kDh, kC, kDh, tid, 256);
-      prefetch_rows(L.W + (b - 1) * kC * kDh, kDh, kC, kDh, tid, 256);
-    }
-    __syncthreads();   // G of the previous step complete
-    for (int u = tid; u < kDh * kSl; u += 256) {
-      const int d = u / kSl, e = u % kSl;
-      L.G[(b * kDh + d) * kDh + e0 + e] = Gs[d * kSl + e];
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    // dV' (64 x 16) = D_i sum_d K_id G_de + X_ie: thread -> row i, 4 columns
-    {
-      const int i = tid >> 2, c0 = 4 * (tid & 3);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int d = 0; d < kDh; ++d) {
-        const float kd = Ks[i * kLd + d];
-        const float4 x = *reinterpret_cast<const float4*>(Gs + d * kSl + c0);
-        acc.x = fmaf(kd, x.x, acc.x); acc.y = fmaf(kd, x.y, acc.y);
-        acc.z = fmaf(kd, x.z, acc.z); acc.w = fmaf(kd, x.w, acc.w);
-      }
-      const float4 xs = *reinterpret_cast<const float4*>(Xs + i * kSl + c0);
-      const float di = Dv[i];
-      const float4 r = make_float4(fmaf(di, acc.x, xs.x), fmaf(di, acc.y, xs.y), fmaf(di, acc.z, xs.z),
-                                   fmaf(di, acc.w, xs.w));
-      *reinterpret_cast<float4*>(dV + i * kSl + c0) = r;
-      *reinterpret_cast<float4*>(L.dVp + (b * kC + i) * kDh + e0 + c0) = r;
-    }
-    __syncthreads();
-    // G <- e_l G + H - W^T dV'   (128 x 16: row d, 8 columns per thread)
-    {
-      const float el = vecp(L, b, kE)[kC - 1];
-      const int d = tid >> 1, c0 = 8 * (tid & 1);
-      float acc[8];
+  const int w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  const int i0 = 8 * w + 2 * t;
+  float st[2][4];
 #pragma unroll
-      for (int s = 0; s < 8; ++s) acc[s] = fmaf(el, Gs[d * kSl + c0 + s], Hs[d * kSl + c0 + s]);
-#pragma unroll 4
-      for (int i = 0; i < kC; ++i) {
-        const float wd = Ws[i * kLd + d];
-        const float4 y0 = *reinterpret_cast<const float4*>(dV + i * kSl + c0);
-        const float4 y1 = *reinterpret_cast<const float4*>(dV + i * kSl + c0 + 4);
-        acc[0] = fmaf(-wd, y0.x, acc[0]); acc[1] = fmaf(-wd, y0.y, acc[1]);
-        acc[2] = fmaf(-wd, y0.z, acc[2]); acc[3] = fmaf(-wd, y0.w, acc[3]);
-        acc[4] = fmaf(-wd, y1.x, acc[4]); acc[5] = fmaf(-wd, y1.y, acc[5]);
-        acc[6] = fmaf(-wd, y1.z, acc[6]); acc[7] = fmaf(-wd, y1.w, acc[7]);
-      }
-      __syncthreads();   // every thread done with this step's tiles and G
+  for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int s = 0; s < 8; ++s) Gs[d * kSl + c0 + s] = acc[s];
+    for (int r = 0; r < 4; ++r) {
+      const int d = st_row(w, g, r), cc = st_col(t, nt, r);
+      st[nt][r] = dht ? dht[(chain * kDh + d) * kDh + e0 + cc] : 0.f;   // dht may be 4-byte aligned only
+      put_split(xh, xl, xf_index(d, cc), st[nt][r]);
     }
-  }
+  auto put_g = [&](int64_t b) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        *reinterpret_cast<float2*>(L.G + (b * kDh + st_row(w, g, 2 * h)) * kDh + e0 + st_col(t, nt, 0)) =
+            make_float2(st[nt][2 * h], st[nt][2 * h + 1]);
+  };
+  put_g(b0 + NC - 1);
+  float4 kr[8];
+  float xr[4], dr[2], wc[32], hr[2][4], el;
+  auto load_r = [&](int64_t b) {   // K rows 8 w + g; X and D at the dV' product's output
+    const float* kp = L.K + (b * kC + 8 * w + g) * kDh + 4 * t;
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) kr[kk] = ldg4(kp + 16 * kk);
+    const float* xp = L.dVp + (b * kC + i0) * kDh + e0 + g;
+    xr[0] = xp[0], xr[1] = xp[kDh], xr[2] = xp[8], xr[3] = xp[kDh + 8];   // plain loads: this kernel writes dVp
+    const float* dp = vecp(L, b, kD) + i0;
+    dr[0] = __ldg(dp), dr[1] = __ldg(dp + 1);
+  };
+  auto load_c = [&](int64_t b) {   // W columns 16 w + g (+8) at rows 8 ks + t (+4); H at the state's places
+    const float* wp = L.W + (b * kC + t) * kDh + 16 * w + g;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      wc[4 * ks] = __ldg(wp + 8 * ks * kDh);
+      wc[4 * ks + 1] = __ldg(wp + 8 * ks * kDh + 8);
+      wc[4 * ks + 2] = __ldg(wp + (8 * ks + 4) * kDh);
+      wc[4 * ks + 3] = __ldg(wp + (8 * ks + 4) * kDh + 8);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float2 x = __ldg(reinterpret_cast<const float2*>(L.H + (b * kDh + st_row(w, g, 2 * h)) * kDh + e0 +
+                                                               st_col(t, nt, 0)));
+        hr[nt][2 * h] = x.x, hr[nt][2 * h + 1] = x.y;
+      }
+    el = __ldg(vecp(L, b, kE) + kC - 1);
+  };
+  load_r(b0 + NC - 1);
+  load_c(b0 + NC - 1);
   __syncthreads();
-  if (dh0)
-    for (int u = tid; u < kDh * kSl; u += 256) {
-      const int d = u / kSl, e = u % kSl;
-      dh0[(chain * kDh + d) * kDh + e0 + e] = Gs[d * kSl + e];
+#pragma unroll 1
+  for (int c = NC - 1; c >= 0; --c) {
+    const int64_t b = b0 + c;
+    if (c >= 2) {
+      prefetch_rows(L.K + (b - 2) * kC * kDh, kDh, kC, kDh, tid, 256);
+      prefetch_rows(L.W + (b - 2) * kC * kDh, kDh, kC, kDh, tid, 256);
     }
+    {
+      // dV' = D (K G) + X at rows i0, i0 + 1 and columns g, g + 8 (X was read
+      // by this lane from the places dV' now overwrites)
+      float o[4];
+      row_product(kr, xh, xl, lane, o);
+      const float v[4] = {fmaf(dr[0], o[0], xr[0]), fmaf(dr[1], o[1], xr[1]), fmaf(dr[0], o[2], xr[2]),
+                          fmaf(dr[1], o[3], xr[3])};
+      if (c > 0) load_r(b - 1);
+      float* vp = L.dVp + (b * kC + i0) * kDh + e0 + g;
+      vp[0] = v[0], vp[kDh] = v[1], vp[8] = v[2], vp[kDh + 8] = v[3];
+      put_split(vh, vl, vf_index(i0, g), v[0]);
+      put_split(vh, vl, vf_index(i0 + 1, g), v[1]);
+      put_split(vh, vl, vf_index(i0, g + 8), v[2]);
+      put_split(vh, vl, vf_index(i0 + 1, g + 8), v[3]);
+    }
+    __syncthreads();
+    {
+      // G <- e_l G + H - W^T dV'
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) st[nt][r] = fmaf(el, st[nt][r], hr[nt][r]);
+      col_product(st, wc, vh, vl, lane, -1.f);
+      if (c > 0) {
+        load_c(b - 1);
+        put_g(b - 1);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) put_split(xh, xl, xf_index(st_row(w, g, r), st_col(t, nt, r)), st[nt][r]);
+      } else if (dh0) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            dh0[(chain * kDh + st_row(w, g, r)) * kDh + e0 + st_col(t, nt, r)] = st[nt][r];
+      }
+    }
+    __syncthreads();
+  }
 }
 
 // dst[i][:] = vec[i] src[i][:] for a pair's [64][128] rows.  Grid nb, 256 threads.
@@ -701,15 +831,12 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, false, L.X1, B2, kDh, false, 0.f, L.W, B2, kDh);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, false, L.X2, B2, kDh, false, 0.f, L.U, B2, kDh);
   // the serial passes
-  if (cudaFuncSetAttribute(bwdc_fwd_states, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem) != cudaSuccess ||
-      cudaFuncSetAttribute(bwdc_rev, cudaFuncAttributeMaxDynamicSharedMemorySize, kRevSmem) != cudaSuccess)
-    return GDN_ERR_CUDA;
-  bwdc_fwd_states<<<dim3((unsigned)chains, kDh / kSl), 256, kFwdSmem, s>>>(L, h0, NC);
+  bwdc_fwd_states<<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, h0, NC);
   // the reverse pass's G-independent terms: X = scale P^T dO (in dVp), H = scale Q^T diag(e) dO
   ok = ok && gemm(s, nb, kC, kDh, kC, scale, L.P, Q2, kC, true, L.dO, B2, kDh, false, 0.f, L.dVp, B2, kDh);
   bwdc_scale_rows<<<nbu, 256, 0, s>>>(L.X3, L.dO, L, kE);
   ok = ok && gemm(s, nb, kDh, kDh, kC, scale, L.Q, B2, kDh, true, L.X3, B2, kDh, false, 0.f, L.H, S2, kDh);
-  bwdc_rev<<<dim3((unsigned)chains, kDh / kSl), 256, kRevSmem, s>>>(L, dht, dh0, NC);
+  bwdc_rev<<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, dht, dh0, NC);
   // dQ = scale diag(e) dO S0^T ;  dK = diag(D) V' G^T
   ok = ok && gemm(s, nb, kC, kDh, kDh, scale, L.dO, B2, kDh, false, L.S0, S2, kDh, true, 0.f, L.dQ, B2, kDh,
                   L.vec + kE * kC, V8);
