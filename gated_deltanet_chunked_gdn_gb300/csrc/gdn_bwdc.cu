@@ -49,16 +49,40 @@ struct GemmArgs {
   float alpha, beta;
 };
 
+// x = hi + lo, hi = x cut to its top 10 mantissa bits (exact tf32), lo = x - hi
+// (exact in fp32); the three-term products hi hi + hi lo + lo hi leave about
+// 2^-19 of each product (the lo lo term and the unit's truncation of lo).
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One 64 x 64 tile of C per CTA on the tensor cores (mma.sync m16n8k8, tf32
+// in three terms): warp w computes rows 16 (w % 4) .. + 15 and columns
+// 32 (w / 4) .. + 31 as four 16 x 8 accumulators.
 __global__ void __launch_bounds__(256) bgemm_kernel(const GemmArgs g) {
-  // k-tiles of 16 staged in two shared buffers; each thread fetches one float4
-  // of A and one of B per tile into registers one tile ahead
-  __shared__ __align__(16) float As[2][16][64 + 4];
-  __shared__ __align__(16) float Bs[2][16][64 + 4];
+  // k-tiles of 16 staged as [k][m] and [k][n] in two shared buffers (row
+  // stride 72: the fragment loads of a warp hit 32 different banks); each
+  // thread fetches one float4 of A and one of B per tile into registers one
+  // tile ahead
+  constexpr int kS = 72;
+  __shared__ __align__(16) float As[2][16][kS];
+  __shared__ __align__(16) float Bs[2][16][kS];
   const int64_t b = blockIdx.z;
   const int i0 = 64 * blockIdx.y, j0 = 64 * blockIdx.x;
   const float* A = g.A + b * g.sA;
   const float* B = g.B + b * g.sB;
-  const int tid = threadIdx.x, ti = 4 * (tid >> 4), tj = 4 * (tid & 15);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, gq = lane >> 2, tq = lane & 3;
+  const int mt = w & 3, nh = w >> 2;
   // this thread's float4 of each tile: A (!tA) row ar, k 4 aq..; (tA) k ar, row 4 aq..
   const int ar = g.tA ? tid >> 4 : tid >> 2, aq = g.tA ? 4 * (tid & 15) : 4 * (tid & 3);
   const int br = g.tB ? tid >> 2 : tid >> 4, bq = g.tB ? 4 * (tid & 3) : 4 * (tid & 15);
@@ -90,31 +114,47 @@ __global__ void __launch_bounds__(256) bgemm_kernel(const GemmArgs g) {
     const bool more = k0 + 16 < g.Kd;
     if (more) fetch(k0 + 16, ra, rb);
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      const float4 a = *reinterpret_cast<const float4*>(&As[buf][kk][ti]);
-      const float4 c = *reinterpret_cast<const float4*>(&Bs[buf][kk][tj]);
-      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {c.x, c.y, c.z, c.w};
+    for (int ks = 0; ks < 16; ks += 8) {
+      // A fragment: (row g, k t), (g + 8, t), (g, t + 4), (g + 8, t + 4) of m-tile mt
+      uint32_t ah[4], al[4];
+      const float* ap = &As[buf][ks + tq][16 * mt + gq];
+      split_tf32(ap[0], ah[0], al[0]);
+      split_tf32(ap[8], ah[1], al[1]);
+      split_tf32(ap[4 * kS], ah[2], al[2]);
+      split_tf32(ap[4 * kS + 8], ah[3], al[3]);
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(av[r], bv[s], acc[r][s]);
+      for (int nt = 0; nt < 4; ++nt) {
+        // B fragment: (k t, col g), (k t + 4, col g) of n-tile nt
+        const float* bp = &Bs[buf][ks + tq][32 * nh + 8 * nt + gq];
+        uint32_t bh0, bl0, bh1, bl1;
+        split_tf32(bp[0], bh0, bl0);
+        split_tf32(bp[4 * kS], bh1, bl1);
+        mma_tf32(acc[nt], al[0], al[1], al[2], al[3], bh0, bh1);
+        mma_tf32(acc[nt], ah[0], ah[1], ah[2], ah[3], bl0, bl1);
+        mma_tf32(acc[nt], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
+      }
     }
     if (more) put(buf ^ 1, ra, rb);
     __syncthreads();
     buf ^= 1;
   }
+  // accumulator nt: (row g, cols 2t, 2t + 1) and (row g + 8, same cols)
   float* C = g.C + b * g.sC;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = i0 + ti + r;
+  for (int h = 0; h < 2; ++h) {
+    const int i = i0 + 16 * mt + gq + 8 * h;
     const float f = g.alpha * (g.rs ? g.rs[b * g.sR + i] : 1.f);
-    float4* c = reinterpret_cast<float4*>(C + (int64_t)i * g.ldc + j0 + tj);
-    float4 o = make_float4(f * acc[r][0], f * acc[r][1], f * acc[r][2], f * acc[r][3]);
-    if (g.beta != 0.f) {
-      const float4 x = *c;
-      o.x += g.beta * x.x; o.y += g.beta * x.y; o.z += g.beta * x.z; o.w += g.beta * x.w;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      float2* c = reinterpret_cast<float2*>(C + (int64_t)i * g.ldc + j0 + 32 * nh + 8 * nt + 2 * tq);
+      float2 o = make_float2(f * acc[nt][2 * h], f * acc[nt][2 * h + 1]);
+      if (g.beta != 0.f) {
+        const float2 x = *c;
+        o.x += g.beta * x.x;
+        o.y += g.beta * x.y;
+      }
+      *c = o;
     }
-    *c = o;
   }
 }
 
@@ -274,28 +314,10 @@ __device__ __forceinline__ void prefetch_rows(const float* src, int64_t ld, int 
   }
 }
 
-// The serial passes run their two products per chunk on the tensor cores
-// (mma.sync m16n8k8, tf32) in three terms, hi hi + hi lo + lo hi, where
-// x = hi + lo with hi = x cut to its top 10 mantissa bits and lo = x - hi
-// (exact in fp32): the dropped lo lo term and the unit's truncation of lo
-// leave about 2^-19 of each product, near fp32.  Operands that sit in shared
-// memory are stored as separate hi and lo arrays in the order of the MMA
-// fragments, so that a lane reads its four values of a k-step with one
-// 16-byte load.
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = __float_as_uint(x) & 0xffffe000u;
-  lo = __float_as_uint(x - __uint_as_float(hi));
-}
-
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-      "{%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
+// The serial passes run their two products per chunk on the same three-term
+// tf32 MMAs.  Operands that sit in shared memory are stored as separate hi and
+// lo arrays in the order of the MMA fragments, so that a lane reads its four
+// values of a k-step with one 16-byte load.
 // A [128][16] slice X (the state, or G) as the A operand of X^T R^T: k-step
 // ks = 2 kk + p covers rows d = 16 kk + 4 t + 2 p (fragment column t) and
 // d + 1 (column t + 4), fragment row g = column c % 8, c / 8 = the lower or
@@ -325,7 +347,9 @@ __device__ __forceinline__ void put_split(float* hi, float* lo, int at, float x)
 // computes n-tile w of X^T R^T over 16 k-steps; r[kk] holds R[8 w + g][16 kk + 4 t .. + 3].
 __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* xh, const float* xl, int lane,
                                             float (&out)[4]) {
-  out[0] = out[1] = out[2] = out[3] = 0.f;
+  // four independent accumulators (even / odd k-steps x main / correction
+  // terms) keep the MMA dependency chains short
+  float acc[4][4] = {};
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const float rv[4] = {r[kk].x, r[kk].y, r[kk].z, r[kk].w};
@@ -337,11 +361,13 @@ __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* x
       split_tf32(rv[2 * p + 1], bh1, bl1);
       const uint4 ah = *reinterpret_cast<const uint4*>(xh + ((ks * 32 + lane) << 2));
       const uint4 al = *reinterpret_cast<const uint4*>(xl + ((ks * 32 + lane) << 2));
-      mma_tf32(out, al.x, al.y, al.z, al.w, bh0, bh1);
-      mma_tf32(out, ah.x, ah.y, ah.z, ah.w, bl0, bl1);
-      mma_tf32(out, ah.x, ah.y, ah.z, ah.w, bh0, bh1);
+      mma_tf32(acc[2 * p + 1], al.x, al.y, al.z, al.w, bh0, bh1);
+      mma_tf32(acc[2 * p + 1], ah.x, ah.y, ah.z, ah.w, bl0, bl1);
+      mma_tf32(acc[2 * p], ah.x, ah.y, ah.z, ah.w, bh0, bh1);
     }
   }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) out[q] = (acc[1][q] + acc[3][q]) + (acc[0][q] + acc[2][q]);
 }
 
 // st[nt] += sign Col^T V for the rows d = 16 w + g (+8) and columns 8 nt + 2 t
@@ -349,6 +375,7 @@ __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* x
 // r >= 2)][16 w + g (+8 for odd r)].
 __device__ __forceinline__ void col_product(float (&st)[2][4], const float (&col)[32], const float* vh,
                                             const float* vl, int lane, float sign) {
+  float cor[2][4] = {};   // the correction terms, in their own accumulators
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     uint32_t ah[4], al[4];
@@ -360,11 +387,15 @@ __device__ __forceinline__ void col_product(float (&st)[2][4], const float (&col
     for (int nt = 0; nt < 2; ++nt) {
       const uint32_t h0 = nt ? bh.z : bh.x, h1 = nt ? bh.w : bh.y;
       const uint32_t l0 = nt ? bl.z : bl.x, l1 = nt ? bl.w : bl.y;
-      mma_tf32(st[nt], al[0], al[1], al[2], al[3], h0, h1);
-      mma_tf32(st[nt], ah[0], ah[1], ah[2], ah[3], l0, l1);
+      mma_tf32(cor[nt], al[0], al[1], al[2], al[3], h0, h1);
+      mma_tf32(cor[nt], ah[0], ah[1], ah[2], ah[3], l0, l1);
       mma_tf32(st[nt], ah[0], ah[1], ah[2], ah[3], h0, h1);
     }
   }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) st[nt][q] += cor[nt][q];
 }
 
 // Row d and column c of state element r of the C fragment st[nt][r].
