@@ -22,6 +22,8 @@
 // The chunk-start states S0 come from a serial forward over the chunks and G
 // from a serial reverse (one CTA per chain and 32-column slice of V); every
 // other product is a batched fp32 GEMM over all (chunk, head) pairs at once.
+#include <type_traits>
+
 #include "gdn_internal.h"
 #include "gdn_sm100.cuh"
 
@@ -47,6 +49,7 @@ struct GemmArgs {
   int lda, ldb, ldc, M, N, Kd;
   bool tA, tB;
   float alpha, beta;
+  int exact;   // bit 0: op(A) is exact in tf32 (its lo part is zero), bit 1: op(B) is
 };
 
 // x = hi + lo, hi = x cut to its top 10 mantissa bits (exact tf32), lo = x - hi
@@ -129,8 +132,8 @@ __global__ void __launch_bounds__(256) bgemm_kernel(const GemmArgs g) {
         uint32_t bh0, bl0, bh1, bl1;
         split_tf32(bp[0], bh0, bl0);
         split_tf32(bp[4 * kS], bh1, bl1);
-        mma_tf32(acc[nt], al[0], al[1], al[2], al[3], bh0, bh1);
-        mma_tf32(acc[nt], ah[0], ah[1], ah[2], ah[3], bl0, bl1);
+        if (!(g.exact & 1)) mma_tf32(acc[nt], al[0], al[1], al[2], al[3], bh0, bh1);
+        if (!(g.exact & 2)) mma_tf32(acc[nt], ah[0], ah[1], ah[2], ah[3], bl0, bl1);
         mma_tf32(acc[nt], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
       }
     }
@@ -345,6 +348,7 @@ __device__ __forceinline__ void put_split(float* hi, float* lo, int at, float x)
 // out = (R X)[i][c] at i = 8 w + 2 t (+1), c = g (+8): out[0] = (i, c),
 // out[1] = (i + 1, c), out[2] = (i, c + 8), out[3] = (i + 1, c + 8).  The warp
 // computes n-tile w of X^T R^T over 16 k-steps; r[kk] holds R[8 w + g][16 kk + 4 t .. + 3].
+template <bool REXACT>   // R exact in tf32: its lo term is dropped
 __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* xh, const float* xl, int lane,
                                             float (&out)[4]) {
   // four independent accumulators (even / odd k-steps x main / correction
@@ -362,7 +366,7 @@ __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* x
       const uint4 ah = *reinterpret_cast<const uint4*>(xh + ((ks * 32 + lane) << 2));
       const uint4 al = *reinterpret_cast<const uint4*>(xl + ((ks * 32 + lane) << 2));
       mma_tf32(acc[2 * p + 1], al.x, al.y, al.z, al.w, bh0, bh1);
-      mma_tf32(acc[2 * p + 1], ah.x, ah.y, ah.z, ah.w, bl0, bl1);
+      if (!REXACT) mma_tf32(acc[2 * p + 1], ah.x, ah.y, ah.z, ah.w, bl0, bl1);
       mma_tf32(acc[2 * p], ah.x, ah.y, ah.z, ah.w, bh0, bh1);
     }
   }
@@ -373,6 +377,7 @@ __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* x
 // st[nt] += sign Col^T V for the rows d = 16 w + g (+8) and columns 8 nt + 2 t
 // (+1) (the C fragments of m-tile w); col[4 ks + r] holds Col[8 ks + t (+4 for
 // r >= 2)][16 w + g (+8 for odd r)].
+template <bool CEXACT>   // Col exact in tf32: its lo term is dropped
 __device__ __forceinline__ void col_product(float (&st)[2][4], const float (&col)[32], const float* vh,
                                             const float* vl, int lane, float sign) {
   float cor[2][4] = {};   // the correction terms, in their own accumulators
@@ -387,7 +392,7 @@ __device__ __forceinline__ void col_product(float (&st)[2][4], const float (&col
     for (int nt = 0; nt < 2; ++nt) {
       const uint32_t h0 = nt ? bh.z : bh.x, h1 = nt ? bh.w : bh.y;
       const uint32_t l0 = nt ? bl.z : bl.x, l1 = nt ? bl.w : bl.y;
-      mma_tf32(cor[nt], al[0], al[1], al[2], al[3], h0, h1);
+      if (!CEXACT) mma_tf32(cor[nt], al[0], al[1], al[2], al[3], h0, h1);
       mma_tf32(cor[nt], ah[0], ah[1], ah[2], ah[3], l0, l1);
       mma_tf32(st[nt], ah[0], ah[1], ah[2], ah[3], h0, h1);
     }
@@ -410,7 +415,9 @@ __device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpre
 // 16 w .. 16 w + 15) and, split for the next V' product, in shared memory;
 // each lane holds its fragments of the chunk's W rows and K columns in
 // registers, loaded one chunk ahead so that their latency hides behind the
-// arithmetic of the chunk before.  Grid (N Hv, 8), 256 threads.
+// arithmetic of the chunk before.  KEXACT: K holds bf16 values (exact in
+// tf32).  Grid (N Hv, 8), 256 threads.
+template <bool KEXACT>
 __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const float* h0, int NC) {
   __shared__ __align__(16) float xh[kXF], xl[kXF], vh[kVF], vl[kVF];
   const int64_t chain = blockIdx.x, b0 = chain * NC;
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
     {
       // V' = U - W S0 at rows i0, i0 + 1 and columns g, g + 8
       float o[4];
-      row_product(wr, xh, xl, lane, o);
+      row_product<false>(wr, xh, xl, lane, o);
       const float v[4] = {ur[0] - o[0], ur[1] - o[1], ur[2] - o[2], ur[3] - o[3]};
       const float d0 = dr[0], d1 = dr[1];
       if (c + 1 < NC) load_r(b + 1);
@@ -488,7 +495,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) st[nt][r] *= el;
-      col_product(st, kc, vh, vl, lane, 1.f);
+      col_product<KEXACT>(st, kc, vh, vl, lane, 1.f);
       if (c + 1 < NC) {
         load_c(b + 1);
         put_s0(b + 1);
@@ -508,6 +515,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
 // dV' = D (K G) + X (over X in dVp), G <- e_l G + H - W^T dV'; dh0 = the last
 // G.  Same arrangement as the forward pass, with K rows and W columns.  Grid
 // (N Hv, 8), 256 threads.
+template <bool KEXACT>
 __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht, float* dh0, int NC) {
   __shared__ __align__(16) float xh[kXF], xl[kXF], vh[kVF], vl[kVF];
   const int64_t chain = blockIdx.x, b0 = chain * NC;
@@ -576,7 +584,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht
       // dV' = D (K G) + X at rows i0, i0 + 1 and columns g, g + 8 (X was read
       // by this lane from the places dV' now overwrites)
       float o[4];
-      row_product(kr, xh, xl, lane, o);
+      row_product<KEXACT>(kr, xh, xl, lane, o);
       const float v[4] = {fmaf(dr[0], o[0], xr[0]), fmaf(dr[1], o[1], xr[1]), fmaf(dr[0], o[2], xr[2]),
                           fmaf(dr[1], o[3], xr[3])};
       if (c > 0) load_r(b - 1);
@@ -594,7 +602,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) st[nt][r] = fmaf(el, st[nt][r], hr[nt][r]);
-      col_product(st, wc, vh, vl, lane, -1.f);
+      col_product<false>(st, wc, vh, vl, lane, -1.f);
       if (c > 0) {
         load_c(b - 1);
         put_g(b - 1);
@@ -834,8 +842,8 @@ __global__ void __launch_bounds__(256) bwdc_scatter(const Lay L, float* dq, floa
 // ------------------------------------------------------------------- host side
 bool gemm(cudaStream_t s, int64_t nb, int M, int N, int Kd, float alpha, const float* A, int64_t sA, int lda,
           bool tA, const float* B, int64_t sB, int ldb, bool tB, float beta, float* C, int64_t sC, int ldc,
-          const float* rs = nullptr, int64_t sR = 0) {
-  GemmArgs g{A, B, C, rs, sA, sB, sC, sR, lda, ldb, ldc, M, N, Kd, tA, tB, alpha, beta};
+          int exact = 0, const float* rs = nullptr, int64_t sR = 0) {
+  GemmArgs g{A, B, C, rs, sA, sB, sC, sR, lda, ldb, ldc, M, N, Kd, tA, tB, alpha, beta, exact};
   bgemm_kernel<<<dim3(N / 64, M / 64, (unsigned)nb), 256, 0, s>>>(g);
   return cudaGetLastError() == cudaSuccess;
 }
@@ -849,40 +857,44 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   const int64_t nb = L.nb, B2 = (int64_t)kC * kDh, Q2 = (int64_t)kC * kC, S2 = (int64_t)kDh * kDh, V8 = 8 * kC;
   const unsigned nbu = (unsigned)nb;
   const int64_t chains = (int64_t)p.N * p.Hv;
+  // with bf16 inputs K, Q, V and dO hold bf16 values, exact in tf32: products
+  // with them drop the lo terms of those operands (xA, xB: op(A), op(B) exact)
+  constexpr bool kBf = std::is_same<Tin, __nv_bfloat16>::value;
+  const int xA = kBf ? 1 : 0, xB = kBf ? 2 : 0;
   bool ok = true;
   bwdc_gather<Tin><<<nbu, 256, 0, s>>>(L, static_cast<const Tin*>(q), static_cast<const Tin*>(k),
                                         static_cast<const Tin*>(v), static_cast<const Tin*>(dout), g, beta, p.T, NC,
                                         p.Hqk, p.Hv);
   // KK = K K^T, P <- Q K^T, then the masks, T, W and U
-  ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.K, B2, kDh, false, L.K, B2, kDh, true, 0.f, L.KK, Q2, kC);
-  ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.Q, B2, kDh, false, L.K, B2, kDh, true, 0.f, L.P, Q2, kC);
+  ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.K, B2, kDh, false, L.K, B2, kDh, true, 0.f, L.KK, Q2, kC, xA | xB);
+  ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.Q, B2, kDh, false, L.K, B2, kDh, true, 0.f, L.P, Q2, kC, xA | xB);
   bwdc_masks<<<nbu, 256, 0, s>>>(L);
   bwdc_solve<<<nbu, 64, 0, s>>>(L);
   bwdc_scale_kv<<<nbu, 256, 0, s>>>(L);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, false, L.X1, B2, kDh, false, 0.f, L.W, B2, kDh);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, false, L.X2, B2, kDh, false, 0.f, L.U, B2, kDh);
   // the serial passes
-  bwdc_fwd_states<<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, h0, NC);
+  bwdc_fwd_states<kBf><<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, h0, NC);
   // the reverse pass's G-independent terms: X = scale P^T dO (in dVp), H = scale Q^T diag(e) dO
-  ok = ok && gemm(s, nb, kC, kDh, kC, scale, L.P, Q2, kC, true, L.dO, B2, kDh, false, 0.f, L.dVp, B2, kDh);
+  ok = ok && gemm(s, nb, kC, kDh, kC, scale, L.P, Q2, kC, true, L.dO, B2, kDh, false, 0.f, L.dVp, B2, kDh, xB);
   bwdc_scale_rows<<<nbu, 256, 0, s>>>(L.X3, L.dO, L, kE);
-  ok = ok && gemm(s, nb, kDh, kDh, kC, scale, L.Q, B2, kDh, true, L.X3, B2, kDh, false, 0.f, L.H, S2, kDh);
-  bwdc_rev<<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, dht, dh0, NC);
+  ok = ok && gemm(s, nb, kDh, kDh, kC, scale, L.Q, B2, kDh, true, L.X3, B2, kDh, false, 0.f, L.H, S2, kDh, xA);
+  bwdc_rev<kBf><<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, dht, dh0, NC);
   // dQ = scale diag(e) dO S0^T ;  dK = diag(D) V' G^T
-  ok = ok && gemm(s, nb, kC, kDh, kDh, scale, L.dO, B2, kDh, false, L.S0, S2, kDh, true, 0.f, L.dQ, B2, kDh,
+  ok = ok && gemm(s, nb, kC, kDh, kDh, scale, L.dO, B2, kDh, false, L.S0, S2, kDh, true, 0.f, L.dQ, B2, kDh, xA,
                   L.vec + kE * kC, V8);
-  ok = ok && gemm(s, nb, kC, kDh, kDh, 1.f, L.Vp, B2, kDh, false, L.G, S2, kDh, true, 0.f, L.dK, B2, kDh,
+  ok = ok && gemm(s, nb, kC, kDh, kDh, 1.f, L.Vp, B2, kDh, false, L.G, S2, kDh, true, 0.f, L.dK, B2, kDh, 0,
                   L.vec + kD * kC, V8);
   // X1 = K G (the D (K G) . V' terms), X2 = Q S0 (the e (Q S0) . dO terms)
-  ok = ok && gemm(s, nb, kC, kDh, kDh, 1.f, L.K, B2, kDh, false, L.G, S2, kDh, false, 0.f, L.X1, B2, kDh);
-  ok = ok && gemm(s, nb, kC, kDh, kDh, 1.f, L.Q, B2, kDh, false, L.S0, S2, kDh, false, 0.f, L.X2, B2, kDh);
+  ok = ok && gemm(s, nb, kC, kDh, kDh, 1.f, L.K, B2, kDh, false, L.G, S2, kDh, false, 0.f, L.X1, B2, kDh, xA);
+  ok = ok && gemm(s, nb, kC, kDh, kDh, 1.f, L.Q, B2, kDh, false, L.S0, S2, kDh, false, 0.f, L.X2, B2, kDh, xA);
   bwdc_rowdots<<<nbu, 256, 0, s>>>(L, 0, scale);
   bwdc_rowdots<<<nbu, 256, 0, s>>>(L, 1, scale);
   // dP = lower(scale dO V'^T) -> (dP o E): dQ += . K, dK += .^T Q
-  ok = ok && gemm(s, nb, kC, kC, kDh, scale, L.dO, B2, kDh, false, L.Vp, B2, kDh, true, 0.f, L.M1, Q2, kC);
+  ok = ok && gemm(s, nb, kC, kC, kDh, scale, L.dO, B2, kDh, false, L.Vp, B2, kDh, true, 0.f, L.M1, Q2, kC, xA);
   bwdc_dp<<<nbu, 256, 0, s>>>(L);
-  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, false, L.K, B2, kDh, false, 1.f, L.dQ, B2, kDh);
-  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, true, L.Q, B2, kDh, false, 1.f, L.dK, B2, kDh);
+  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, false, L.K, B2, kDh, false, 1.f, L.dQ, B2, kDh, xB);
+  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, true, L.Q, B2, kDh, false, 1.f, L.dK, B2, kDh, xB);
   // dW = -dV' S0^T (X1); dT = dW (beta e K)^T + dV' (beta V)^T (M2)
   bwdc_scale_kv<<<nbu, 256, 0, s>>>(L);   // X1 = beta e K, X2 = beta V again (X1, X2 were reused)
   ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.dVp, B2, kDh, false, L.X2, B2, kDh, true, 0.f, L.M2, Q2, kC);
@@ -897,8 +909,8 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   ok = ok && gemm(s, nb, kC, kC, kC, -1.f, L.M1, Q2, kC, false, L.T, Q2, kC, true, 0.f, L.M3, Q2, kC);
   bwdc_da<<<nbu, 256, 0, s>>>(L);
   // dK += dKK K + dKK^T K
-  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M3, Q2, kC, false, L.K, B2, kDh, false, 1.f, L.dK, B2, kDh);
-  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M3, Q2, kC, true, L.K, B2, kDh, false, 1.f, L.dK, B2, kDh);
+  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M3, Q2, kC, false, L.K, B2, kDh, false, 1.f, L.dK, B2, kDh, xB);
+  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M3, Q2, kC, true, L.K, B2, kDh, false, 1.f, L.dK, B2, kDh, xB);
   if (p.Hv != p.Hqk) {
     const size_t tq = sizeof(float) * (size_t)p.B * p.T * p.Hqk * p.K;
     if (cudaMemsetAsync(dq, 0, tq, s) != cudaSuccess || cudaMemsetAsync(dk, 0, tq, s) != cudaSuccess) return GDN_ERR_CUDA;
