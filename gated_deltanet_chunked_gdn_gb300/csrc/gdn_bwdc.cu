@@ -38,7 +38,7 @@ constexpr int kSl = 16;     // V columns per CTA of the serial kernels
 
 // ---------------------------------------------------------------- batched GEMM
 // C[b] = alpha diag(rs[b]) op(A[b]) op(B[b]) + beta C[b] for M, N multiples of
-// 64 and Kd a multiple of 16; op(A)(i, k) = tA ? A[k lda + i] : A[i lda + k],
+// 64 and Kd a multiple of 32; op(A)(i, k) = tA ? A[k lda + i] : A[i lda + k],
 // op(B)(k, j) = tB ? B[j ldb + k] : B[k ldb + j]; rs may be null (all ones).
 struct GemmArgs {
   const float* A;
@@ -71,67 +71,70 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
 
 // One 64 x 64 tile of C per CTA on the tensor cores (mma.sync m16n8k8, tf32
 // in three terms): warp w computes rows 16 (w % 4) .. + 15 and columns
-// 32 (w / 4) .. + 31 as four 16 x 8 accumulators.
-__global__ void __launch_bounds__(256) bgemm_kernel(const GemmArgs g) {
-  // k-tiles of 16 staged as [k][m] and [k][n] in two shared buffers (row
-  // stride 72: the fragment loads of a warp hit 32 different banks); each
-  // thread fetches one float4 of A and one of B per tile into registers one
-  // tile ahead
-  constexpr int kS = 72;
-  __shared__ __align__(16) float As[2][16][kS];
-  __shared__ __align__(16) float Bs[2][16][kS];
+// 32 (w / 4) .. + 31 as four 16 x 8 accumulators.  k-tiles of 32 are staged in
+// two shared buffers in the operands' own orientation (A as [m][k] with row
+// stride 36 or [k][m] with 72, B as [k][n] with 72 or [n][k] with 36: the
+// fragment loads of a warp then hit 32 different banks and every store is a
+// 16-byte row piece); each thread fetches two float4 of A and two of B per
+// tile into registers one tile ahead.
+template <bool TA, bool TB>
+__global__ void __launch_bounds__(256, 4) bgemm_kernel(const GemmArgs g) {
+  constexpr int kT = 32, kBuf = 64 * 36;
+  constexpr int sAm = TA ? 1 : 36, sAk = TA ? 72 : 1;   // A(m, k) at As[m sAm + k sAk]
+  constexpr int sBk = TB ? 1 : 36 * 2, sBn = TB ? 36 : 1;
+  __shared__ __align__(16) float As[2][kBuf];
+  __shared__ __align__(16) float Bs[2][kBuf];
   const int64_t b = blockIdx.z;
   const int i0 = 64 * blockIdx.y, j0 = 64 * blockIdx.x;
   const float* A = g.A + b * g.sA;
   const float* B = g.B + b * g.sB;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, gq = lane >> 2, tq = lane & 3;
   const int mt = w & 3, nh = w >> 2;
-  // this thread's float4 of each tile: A (!tA) row ar, k 4 aq..; (tA) k ar, row 4 aq..
-  const int ar = g.tA ? tid >> 4 : tid >> 2, aq = g.tA ? 4 * (tid & 15) : 4 * (tid & 3);
-  const int br = g.tB ? tid >> 2 : tid >> 4, bq = g.tB ? 4 * (tid & 3) : 4 * (tid & 15);
-  auto fetch = [&](int k0, float4& ra, float4& rb) {
-    ra = g.tA ? *reinterpret_cast<const float4*>(A + (int64_t)(k0 + ar) * g.lda + i0 + aq)
-              : *reinterpret_cast<const float4*>(A + (int64_t)(i0 + ar) * g.lda + k0 + aq);
-    rb = g.tB ? *reinterpret_cast<const float4*>(B + (int64_t)(j0 + br) * g.ldb + k0 + bq)
-              : *reinterpret_cast<const float4*>(B + (int64_t)(k0 + br) * g.ldb + j0 + bq);
-  };
-  auto put = [&](int buf, const float4& ra, const float4& rb) {
-    if (g.tA) {
-      *reinterpret_cast<float4*>(&As[buf][ar][aq]) = ra;
-    } else {
-      As[buf][aq][ar] = ra.x; As[buf][aq + 1][ar] = ra.y; As[buf][aq + 2][ar] = ra.z; As[buf][aq + 3][ar] = ra.w;
+  // this thread's float4 pieces: row (TA: k, else m) ar + {0, half}, column aq
+  const int ar = TA ? tid >> 4 : tid >> 3, aq = TA ? 4 * (tid & 15) : 4 * (tid & 7), ah_ = TA ? 16 : 32;
+  const int br = TB ? tid >> 3 : tid >> 4, bq = TB ? 4 * (tid & 7) : 4 * (tid & 15), bh_ = TB ? 32 : 16;
+  const int sa = TA ? 72 : 36, sb = TB ? 36 : 72;   // shared row strides
+  auto fetch = [&](int k0, float4 (&ra)[2], float4 (&rb)[2]) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      ra[r] = TA ? *reinterpret_cast<const float4*>(A + (int64_t)(k0 + ar + r * ah_) * g.lda + i0 + aq)
+                 : *reinterpret_cast<const float4*>(A + (int64_t)(i0 + ar + r * ah_) * g.lda + k0 + aq);
+      rb[r] = TB ? *reinterpret_cast<const float4*>(B + (int64_t)(j0 + br + r * bh_) * g.ldb + k0 + bq)
+                 : *reinterpret_cast<const float4*>(B + (int64_t)(k0 + br + r * bh_) * g.ldb + j0 + bq);
     }
-    if (g.tB) {
-      Bs[buf][bq][br] = rb.x; Bs[buf][bq + 1][br] = rb.y; Bs[buf][bq + 2][br] = rb.z; Bs[buf][bq + 3][br] = rb.w;
-    } else {
-      *reinterpret_cast<float4*>(&Bs[buf][br][bq]) = rb;
+  };
+  auto put = [&](int buf, const float4 (&ra)[2], const float4 (&rb)[2]) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      *reinterpret_cast<float4*>(&As[buf][(ar + r * ah_) * sa + aq]) = ra[r];
+      *reinterpret_cast<float4*>(&Bs[buf][(br + r * bh_) * sb + bq]) = rb[r];
     }
   };
   float acc[4][4] = {};
-  float4 ra, rb;
+  float4 ra[2], rb[2];
   fetch(0, ra, rb);
   put(0, ra, rb);
   __syncthreads();
   int buf = 0;
-  for (int k0 = 0; k0 < g.Kd; k0 += 16) {
-    const bool more = k0 + 16 < g.Kd;
-    if (more) fetch(k0 + 16, ra, rb);
+  for (int k0 = 0; k0 < g.Kd; k0 += kT) {
+    const bool more = k0 + kT < g.Kd;
+    if (more) fetch(k0 + kT, ra, rb);
+    const float* as = As[buf] + (16 * mt + gq) * sAm + tq * sAk;
+    const float* bs = Bs[buf] + (32 * nh + gq) * sBn + tq * sBk;
 #pragma unroll
-    for (int ks = 0; ks < 16; ks += 8) {
+    for (int ks = 0; ks < kT; ks += 8) {
       // A fragment: (row g, k t), (g + 8, t), (g, t + 4), (g + 8, t + 4) of m-tile mt
       uint32_t ah[4], al[4];
-      const float* ap = &As[buf][ks + tq][16 * mt + gq];
-      split_tf32(ap[0], ah[0], al[0]);
-      split_tf32(ap[8], ah[1], al[1]);
-      split_tf32(ap[4 * kS], ah[2], al[2]);
-      split_tf32(ap[4 * kS + 8], ah[3], al[3]);
+      split_tf32(as[ks * sAk], ah[0], al[0]);
+      split_tf32(as[ks * sAk + 8 * sAm], ah[1], al[1]);
+      split_tf32(as[(ks + 4) * sAk], ah[2], al[2]);
+      split_tf32(as[(ks + 4) * sAk + 8 * sAm], ah[3], al[3]);
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         // B fragment: (k t, col g), (k t + 4, col g) of n-tile nt
-        const float* bp = &Bs[buf][ks + tq][32 * nh + 8 * nt + gq];
         uint32_t bh0, bl0, bh1, bl1;
-        split_tf32(bp[0], bh0, bl0);
-        split_tf32(bp[4 * kS], bh1, bl1);
+        split_tf32(bs[ks * sBk + 8 * nt * sBn], bh0, bl0);
+        split_tf32(bs[(ks + 4) * sBk + 8 * nt * sBn], bh1, bl1);
         if (!(g.exact & 1)) mma_tf32(acc[nt], al[0], al[1], al[2], al[3], bh0, bh1);
         if (!(g.exact & 2)) mma_tf32(acc[nt], ah[0], ah[1], ah[2], ah[3], bl0, bl1);
         mma_tf32(acc[nt], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
@@ -844,7 +847,11 @@ bool gemm(cudaStream_t s, int64_t nb, int M, int N, int Kd, float alpha, const f
           bool tA, const float* B, int64_t sB, int ldb, bool tB, float beta, float* C, int64_t sC, int ldc,
           int exact = 0, const float* rs = nullptr, int64_t sR = 0) {
   GemmArgs g{A, B, C, rs, sA, sB, sC, sR, lda, ldb, ldc, M, N, Kd, tA, tB, alpha, beta, exact};
-  bgemm_kernel<<<dim3(N / 64, M / 64, (unsigned)nb), 256, 0, s>>>(g);
+  const dim3 grid(N / 64, M / 64, (unsigned)nb);
+  if (tA)
+    tB ? bgemm_kernel<true, true><<<grid, 256, 0, s>>>(g) : bgemm_kernel<true, false><<<grid, 256, 0, s>>>(g);
+  else
+    tB ? bgemm_kernel<false, true><<<grid, 256, 0, s>>>(g) : bgemm_kernel<false, false><<<grid, 256, 0, s>>>(g);
   return cudaGetLastError() == cudaSuccess;
 }
 
