@@ -62,7 +62,9 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) 
 
 __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  // no side effects: not volatile, so that the compiler may schedule the
+  // operand loads of later k-steps ahead of it
+  asm(
       "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -637,29 +639,34 @@ __global__ void __launch_bounds__(256) bwdc_scale_rows(float* dst, const float* 
   }
 }
 
-// Row sums over the 128 columns of products of two [64][128] matrices (four
-// threads a row, 32 columns each).  mode 0: dgamma -= D_i (KG)_i . V'_i and
-// dgamma[last] += e_l <S0, G> + sum_i D_i (KG)_i . V'_i (the <S1, G> term);
-// mode 1: dgamma += scale e_i (Q S0)_i . dO_i.  Grid nb, 256 threads.
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
+}
+
+// Row sums over the 128 columns of products of two [64][128] matrices (warp
+// w takes rows w, w + 8, ..; lane l the float4 column l).  mode 0: dgamma -=
+// D_i (KG)_i . V'_i and dgamma[last] += e_l <S0, G> + sum_i D_i (KG)_i . V'_i
+// (the <S1, G> term); mode 1: dgamma += scale e_i (Q S0)_i . dO_i.  Grid nb,
+// 256 threads.
 __global__ void __launch_bounds__(256) bwdc_rowdots(const Lay L, int mode, float scale) {
   const int64_t b = blockIdx.x;
-  const int tid = threadIdx.x, i = tid >> 2, d0 = 32 * (tid & 3);
-  const float* X = (mode == 0 ? L.X1 : L.X2) + (b * kC + i) * kDh + d0;
-  const float* Y = (mode == 0 ? L.Vp : L.dO) + (b * kC + i) * kDh + d0;
-  float s = 0.f;
-#pragma unroll
-  for (int d = 0; d < 32; d += 4) {
-    const float4 x = *reinterpret_cast<const float4*>(X + d), y = *reinterpret_cast<const float4*>(Y + d);
-    s = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, s))));
-  }
-  s += __shfl_xor_sync(0xffffffffu, s, 1);
-  s += __shfl_xor_sync(0xffffffffu, s, 2);
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31;
+  const float4* X = reinterpret_cast<const float4*>((mode == 0 ? L.X1 : L.X2) + b * kC * kDh) + lane;
+  const float4* Y = reinterpret_cast<const float4*>((mode == 0 ? L.Vp : L.dO) + b * kC * kDh) + lane;
   float* dg = vecp(L, b, kDgam);
-  if (mode == 1) {
-    if ((tid & 3) == 0) dg[i] += scale * vecp(L, b, kE)[i] * s;
-    return;
+  const float* f = vecp(L, b, mode == 0 ? kD : kE);
+  float tt = 0.f;   // mode 0: sum over this warp's rows of D_i (KG)_i . V'_i
+#pragma unroll 2
+  for (int i = w; i < kC; i += 8) {
+    const float4 x = X[i * (kDh / 4)], y = Y[i * (kDh / 4)];
+    const float s = warp_sum(fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, x.w * y.w))));
+    const float t = (mode == 0 ? 1.f : scale) * f[i] * s;
+    if (lane == 0) dg[i] += mode == 0 ? -t : t;
+    tt += t;
   }
-  const float t = vecp(L, b, kD)[i] * s;
+  if (mode == 1) return;
   // <S1, G> = e_l <S0, G> + sum_i t_i
   const float4* S0 = reinterpret_cast<const float4*>(L.S0 + b * kDh * kDh);
   const float4* G = reinterpret_cast<const float4*>(L.G + b * kDh * kDh);
@@ -668,129 +675,127 @@ __global__ void __launch_bounds__(256) bwdc_rowdots(const Lay L, int mode, float
     const float4 u = S0[x], v = G[x];
     sg = fmaf(u.x, v.x, fmaf(u.y, v.y, fmaf(u.z, v.z, fmaf(u.w, v.w, sg))));
   }
-  float tt = (tid & 3) == 0 ? t : 0.f;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    sg += __shfl_xor_sync(0xffffffffu, sg, off);
-    tt += __shfl_xor_sync(0xffffffffu, tt, off);
-  }
+  sg = warp_sum(sg);
   __shared__ float red[8], red2[8];
-  if ((tid & 31) == 0) {
-    red[tid >> 5] = tt;
-    red2[tid >> 5] = sg;
+  if (lane == 0) {
+    red[w] = tt;
+    red2[w] = sg;
   }
-  if ((tid & 3) == 0) dg[i] -= t;
   __syncthreads();
   if (tid == 0) {
     float tot = 0.f, sgt = 0.f;
-    for (int w = 0; w < 8; ++w) {
-      tot += red[w];
-      sgt += red2[w];
+    for (int v = 0; v < 8; ++v) {
+      tot += red[v];
+      sgt += red2[v];
     }
     dg[kC - 1] += vecp(L, b, kE)[kC - 1] * sgt + tot;
   }
 }
 
 // dP = lower(M1) (M1 = scale dO V'^T): dgamma += rowsum(dP o P) - colsum(dP o P);
-// M1 <- dP o E (for dQ += M1 K, dK += M1^T Q).  Four threads a row, 16
-// columns each.  Grid nb, 256 threads.
+// M1 <- dP o E (for dQ += M1 K, dK += M1^T Q).  Warp w takes rows w, w + 8, ..;
+// lane l columns 2 l, 2 l + 1.  Grid nb, 256 threads.
 __global__ void __launch_bounds__(256) bwdc_dp(const Lay L) {
   const int64_t b = blockIdx.x;
-  const int tid = threadIdx.x, r = tid >> 2, j0 = 16 * (tid & 3);
-  __shared__ float col[64][65];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, j = 2 * lane;
+  __shared__ float csum[8][kC], rsum[kC];
   const float* gam = vecp(L, b, kGam);
-  const float gr = gam[r];
-  float rs = 0.f;
-#pragma unroll 4
-  for (int jj = 0; jj < 16; ++jj) {
-    const int j = j0 + jj;
-    const int64_t x = b * kC * kC + r * kC + j;
-    const float dp = r >= j ? L.M1[x] : 0.f;
-    const float pp = dp * L.P[x];
-    rs += pp;
-    col[r][j] = pp;
-    L.M1[x] = r >= j ? dp * expf(gr - gam[j]) : 0.f;
+  const float gj0 = gam[j], gj1 = gam[j + 1];
+  float c0 = 0.f, c1 = 0.f;
+#pragma unroll 2
+  for (int r = w; r < kC; r += 8) {
+    float2* mp = reinterpret_cast<float2*>(L.M1 + b * kC * kC + r * kC + j);
+    const float2 m = *mp, pv = *reinterpret_cast<const float2*>(L.P + b * kC * kC + r * kC + j);
+    const float gr = gam[r];
+    const float d0 = r >= j ? m.x : 0.f, d1 = r >= j + 1 ? m.y : 0.f;
+    const float p0 = d0 * pv.x, p1 = d1 * pv.y;
+    c0 += p0;
+    c1 += p1;
+    const float rs = warp_sum(p0 + p1);
+    if (lane == 0) rsum[r] = rs;
+    *mp = make_float2(r >= j ? d0 * expf(gr - gj0) : 0.f, r >= j + 1 ? d1 * expf(gr - gj1) : 0.f);
   }
-  rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-  rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+  csum[w][j] = c0;
+  csum[w][j + 1] = c1;
   __syncthreads();
   if (tid < kC) {
     float cs = 0.f;
-    for (int i = 0; i < kC; ++i) cs += col[i][tid];
-    col[0][tid] = cs;   // column sums, read back below (row 0 of col is no longer needed)
+#pragma unroll
+    for (int v = 0; v < 8; ++v) cs += csum[v][tid];
+    vecp(L, b, kDgam)[tid] += rsum[tid] - cs;
   }
-  __syncthreads();
-  if ((tid & 3) == 0) vecp(L, b, kDgam)[r] += rs - col[0][r];
 }
 
 // From TdW = T^T dW and TdV = T^T dV': dK += diag(beta e) TdW, dbeta += e rowsum(K o TdW)
 // + rowsum(V o TdV), dgamma += beta e rowsum(K o TdW), TdV <- diag(beta) TdV (= dV).
-// Four threads a row, 32 columns each.  Grid nb, 256 threads.
+// Warp w takes rows w, w + 8, ..; lane l the float4 column l.  Grid nb, 256 threads.
 __global__ void __launch_bounds__(256) bwdc_wy(const Lay L, const float* TdW, float* TdV) {
   const int64_t b = blockIdx.x;
-  const int tid = threadIdx.x, i = tid >> 2, d0 = 32 * (tid & 3);
-  const float be = vecp(L, b, kBe)[i], bt = vecp(L, b, kBeta)[i], e = vecp(L, b, kE)[i];
-  const int64_t r = (b * kC + i) * kDh + d0;
-  float kx = 0.f, vx = 0.f;
-#pragma unroll
-  for (int d = 0; d < 32; d += 4) {
-    const float4 x3 = *reinterpret_cast<const float4*>(TdW + r + d);
-    const float4 x4 = *reinterpret_cast<const float4*>(TdV + r + d);
-    const float4 k4 = *reinterpret_cast<const float4*>(L.K + r + d);
-    const float4 v4 = *reinterpret_cast<const float4*>(L.V + r + d);
-    float4 dk = *reinterpret_cast<const float4*>(L.dK + r + d);
-    kx = fmaf(k4.x, x3.x, fmaf(k4.y, x3.y, fmaf(k4.z, x3.z, fmaf(k4.w, x3.w, kx))));
-    vx = fmaf(v4.x, x4.x, fmaf(v4.y, x4.y, fmaf(v4.z, x4.z, fmaf(v4.w, x4.w, vx))));
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* vbe = vecp(L, b, kBe);
+  const float* vbt = vecp(L, b, kBeta);
+  const float* ve = vecp(L, b, kE);
+#pragma unroll 2
+  for (int i = w; i < kC; i += 8) {
+    const int64_t r = (b * kC + i) * kDh + 4 * lane;
+    const float be = vbe[i], bt = vbt[i];
+    const float4 x3 = *reinterpret_cast<const float4*>(TdW + r);
+    const float4 x4 = *reinterpret_cast<const float4*>(TdV + r);
+    const float4 k4 = *reinterpret_cast<const float4*>(L.K + r);
+    const float4 v4 = *reinterpret_cast<const float4*>(L.V + r);
+    float4 dk = *reinterpret_cast<const float4*>(L.dK + r);
+    const float kx = warp_sum(fmaf(k4.x, x3.x, fmaf(k4.y, x3.y, fmaf(k4.z, x3.z, k4.w * x3.w))));
+    const float vx = warp_sum(fmaf(v4.x, x4.x, fmaf(v4.y, x4.y, fmaf(v4.z, x4.z, v4.w * x4.w))));
     dk.x = fmaf(be, x3.x, dk.x); dk.y = fmaf(be, x3.y, dk.y); dk.z = fmaf(be, x3.z, dk.z); dk.w = fmaf(be, x3.w, dk.w);
-    *reinterpret_cast<float4*>(L.dK + r + d) = dk;
-    *reinterpret_cast<float4*>(TdV + r + d) = make_float4(bt * x4.x, bt * x4.y, bt * x4.z, bt * x4.w);
-  }
-  kx += __shfl_xor_sync(0xffffffffu, kx, 1);
-  kx += __shfl_xor_sync(0xffffffffu, kx, 2);
-  vx += __shfl_xor_sync(0xffffffffu, vx, 1);
-  vx += __shfl_xor_sync(0xffffffffu, vx, 2);
-  if ((tid & 3) == 0) {
-    vecp(L, b, kDbeta)[i] += e * kx + vx;
-    vecp(L, b, kDgam)[i] += be * kx;
+    *reinterpret_cast<float4*>(L.dK + r) = dk;
+    *reinterpret_cast<float4*>(TdV + r) = make_float4(bt * x4.x, bt * x4.y, bt * x4.z, bt * x4.w);
+    if (lane == 0) {
+      vecp(L, b, kDbeta)[i] += ve[i] * kx + vx;
+      vecp(L, b, kDgam)[i] += be * kx;
+    }
   }
 }
 
 // dA = strict-lower(M3) (M3 = -T^T dT T^T): dbeta += rowsum(dA o E o KK),
-// dgamma += rowsum(dA o A) - colsum(dA o A), M3 <- dKK = dA o beta_i E.  Four
-// threads a row, 16 columns each.  Grid nb, 256 threads.
+// dgamma += rowsum(dA o A) - colsum(dA o A), M3 <- dKK = dA o beta_i E.  Warp
+// w takes rows w, w + 8, ..; lane l columns 2 l, 2 l + 1.  Grid nb, 256 threads.
 __global__ void __launch_bounds__(256) bwdc_da(const Lay L) {
   const int64_t b = blockIdx.x;
-  const int tid = threadIdx.x, r = tid >> 2, j0 = 16 * (tid & 3);
-  __shared__ float col[64][65];
+  const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, j = 2 * lane;
+  __shared__ float csum[8][kC], rsum[kC], dbs[kC];
   const float* gam = vecp(L, b, kGam);
-  const float bt = vecp(L, b, kBeta)[r], gr = gam[r];
-  float db = 0.f, rs = 0.f;
-#pragma unroll 4
-  for (int jj = 0; jj < 16; ++jj) {
-    const int j = j0 + jj;
+  const float* bet = vecp(L, b, kBeta);
+  const float gj0 = gam[j], gj1 = gam[j + 1];
+  float c0 = 0.f, c1 = 0.f;
+#pragma unroll 2
+  for (int r = w; r < kC; r += 8) {
     const int64_t x = b * kC * kC + r * kC + j;
-    const float da = r > j ? L.M3[x] : 0.f;
-    const float E = r > j ? expf(gr - gam[j]) : 0.f;
-    db = fmaf(da, E * L.KK[x], db);
-    const float aa = da * L.A[x];
-    rs += aa;
-    col[r][j] = aa;
-    L.M3[x] = da * bt * E;
+    float2* mp = reinterpret_cast<float2*>(L.M3 + x);
+    const float2 m = *mp, kk = *reinterpret_cast<const float2*>(L.KK + x),
+                 av = *reinterpret_cast<const float2*>(L.A + x);
+    const float gr = gam[r], bt = bet[r];
+    const float d0 = r > j ? m.x : 0.f, d1 = r > j + 1 ? m.y : 0.f;
+    const float E0 = r > j ? expf(gr - gj0) : 0.f, E1 = r > j + 1 ? expf(gr - gj1) : 0.f;
+    const float a0 = d0 * av.x, a1 = d1 * av.y;
+    c0 += a0;
+    c1 += a1;
+    const float db = warp_sum(fmaf(d0, E0 * kk.x, d1 * (E1 * kk.y)));
+    const float rs = warp_sum(a0 + a1);
+    if (lane == 0) {
+      rsum[r] = rs;
+      dbs[r] = db;
+    }
+    *mp = make_float2(d0 * bt * E0, d1 * bt * E1);
   }
-  db += __shfl_xor_sync(0xffffffffu, db, 1);
-  db += __shfl_xor_sync(0xffffffffu, db, 2);
-  rs += __shfl_xor_sync(0xffffffffu, rs, 1);
-  rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+  csum[w][j] = c0;
+  csum[w][j + 1] = c1;
   __syncthreads();
   if (tid < kC) {
     float cs = 0.f;
-    for (int i = 0; i < kC; ++i) cs += col[i][tid];
-    col[0][tid] = cs;
-  }
-  __syncthreads();
-  if ((tid & 3) == 0) {
-    vecp(L, b, kDgam)[r] += rs - col[0][r];
-    vecp(L, b, kDbeta)[r] += db;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) cs += csum[v][tid];
+    vecp(L, b, kDgam)[tid] += rsum[tid] - cs;
+    vecp(L, b, kDbeta)[tid] += dbs[tid];
   }
 }
 
