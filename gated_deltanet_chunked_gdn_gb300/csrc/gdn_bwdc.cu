@@ -37,8 +37,8 @@ constexpr int kDh = 128;    // K = V
 constexpr int kSl = 16;     // V columns per CTA of the serial kernels
 
 // ---------------------------------------------------------------- batched GEMM
-// C[b] = alpha diag(rs[b]) op(A[b]) op(B[b]) + beta C[b] for M, N multiples of
-// 64 and Kd a multiple of 32; op(A)(i, k) = tA ? A[k lda + i] : A[i lda + k],
+// C[b] = alpha diag(rs[b]) op(A[b]) op(B[b]) diag(cs[b]) + beta C[b] for M, N multiples of
+// 64 and Kd a multiple of 32 (rs, cs may be null: all ones); op(A)(i, k) = tA ? A[k lda + i] : A[i lda + k],
 // op(B)(k, j) = tB ? B[j ldb + k] : B[k ldb + j]; rs may be null (all ones).
 struct GemmArgs {
   const float* A;
@@ -50,6 +50,8 @@ struct GemmArgs {
   bool tA, tB;
   float alpha, beta;
   int exact;   // bit 0: op(A) is exact in tf32 (its lo part is zero), bit 1: op(B) is
+  const float* cs;
+  int64_t sCs;
 };
 
 // x = hi + lo, hi = x cut to its top 10 mantissa bits (exact tf32), lo = x - hi
@@ -80,7 +82,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
 // 16-byte row piece); each thread fetches two float4 of A and two of B per
 // tile into registers one tile ahead.
 template <bool TA, bool TB>
-__global__ void __launch_bounds__(256, 4) bgemm_kernel(const GemmArgs g) {
+__global__ void __launch_bounds__(256, 3) bgemm_kernel(const GemmArgs g) {
   constexpr int kT = 32, kBuf = 64 * 36;
   constexpr int sAm = TA ? 1 : 36, sAk = TA ? 72 : 1;   // A(m, k) at As[m sAm + k sAk]
   constexpr int sBk = TB ? 1 : 36 * 2, sBn = TB ? 36 : 1;
@@ -146,22 +148,33 @@ __global__ void __launch_bounds__(256, 4) bgemm_kernel(const GemmArgs g) {
     __syncthreads();
     buf ^= 1;
   }
-  // accumulator nt: (row g, cols 2t, 2t + 1) and (row g + 8, same cols)
+  // accumulator nt: (row g, cols 2t, 2t + 1) and (row g + 8, same cols).  All
+  // loads of the epilogue (row and column scales, C for beta) are issued before
+  // its first store: the compiler cannot reorder them past stores to C.
   float* C = g.C + b * g.sC;
+  const int jc = j0 + 32 * nh + 2 * tq;
+  float2 cv[4], cx[2][4];
+  float f[2];
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+    cv[nt] = g.cs ? *reinterpret_cast<const float2*>(g.cs + b * g.sCs + jc + 8 * nt) : make_float2(1.f, 1.f);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const int i = i0 + 16 * mt + gq + 8 * h;
-    const float f = g.alpha * (g.rs ? g.rs[b * g.sR + i] : 1.f);
+    f[h] = g.alpha * (g.rs ? g.rs[b * g.sR + i] : 1.f);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+      cx[h][nt] = g.beta != 0.f ? *reinterpret_cast<const float2*>(C + (int64_t)i * g.ldc + jc + 8 * nt)
+                                : make_float2(0.f, 0.f);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int i = i0 + 16 * mt + gq + 8 * h;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      float2* c = reinterpret_cast<float2*>(C + (int64_t)i * g.ldc + j0 + 32 * nh + 8 * nt + 2 * tq);
-      float2 o = make_float2(f * acc[nt][2 * h], f * acc[nt][2 * h + 1]);
-      if (g.beta != 0.f) {
-        const float2 x = *c;
-        o.x += g.beta * x.x;
-        o.y += g.beta * x.y;
-      }
-      *c = o;
+      const float2 o = make_float2(fmaf(f[h] * acc[nt][2 * h], cv[nt].x, g.beta * cx[h][nt].x),
+                                   fmaf(f[h] * acc[nt][2 * h + 1], cv[nt].y, g.beta * cx[h][nt].y));
+      *reinterpret_cast<float2*>(C + (int64_t)i * g.ldc + jc + 8 * nt) = o;
     }
   }
 }
@@ -279,7 +292,9 @@ __global__ void __launch_bounds__(256) bwdc_masks(const Lay L) {
   }
 }
 
-// T = (I + A)^-1 by forward substitution: thread l owns column l.  Grid nb, 64 threads.
+// T = (I + A)^-1 by forward substitution: thread l owns column l; also
+// T diag(beta e) (in M1) and T diag(beta) (in M2), the left factors of W and
+// U.  Grid nb, 64 threads.
 __global__ void __launch_bounds__(64) bwdc_solve(const Lay L) {
   const int64_t b = blockIdx.x;
   __shared__ float As[kC][kC + 1];
@@ -287,6 +302,9 @@ __global__ void __launch_bounds__(64) bwdc_solve(const Lay L) {
   for (int u = l; u < kC * kC; u += 64) As[u / kC][u % kC] = L.A[b * kC * kC + u];
   __syncthreads();
   float* T = L.T + b * kC * kC;
+  float* Tbe = L.M1 + b * kC * kC;
+  float* Tb = L.M2 + b * kC * kC;
+  const float fbe = vecp(L, b, kBe)[l], fb = vecp(L, b, kBeta)[l];
   float t[kC];
 #pragma unroll
   for (int i = 0; i < kC; ++i) {
@@ -295,21 +313,8 @@ __global__ void __launch_bounds__(64) bwdc_solve(const Lay L) {
     for (int j = 0; j < i; ++j) x = fmaf(-As[i][j], t[j], x);
     t[i] = x;
     T[i * kC + l] = x;
-  }
-}
-
-// X1 = diag(beta e) K, X2 = diag(beta) V.  Grid nb, 256 threads.
-__global__ void __launch_bounds__(256) bwdc_scale_kv(const Lay L) {
-  const int64_t b = blockIdx.x;
-  const float* be = vecp(L, b, kBe);
-  const float* bet = vecp(L, b, kBeta);
-  for (int u = threadIdx.x; u < kC * kDh / 4; u += 256) {
-    const int i = (4 * u) / kDh;
-    const float4 k4 = reinterpret_cast<const float4*>(L.K + b * kC * kDh)[u];
-    const float4 v4 = reinterpret_cast<const float4*>(L.V + b * kC * kDh)[u];
-    const float fb = be[i], fv = bet[i];
-    reinterpret_cast<float4*>(L.X1 + b * kC * kDh)[u] = make_float4(fb * k4.x, fb * k4.y, fb * k4.z, fb * k4.w);
-    reinterpret_cast<float4*>(L.X2 + b * kC * kDh)[u] = make_float4(fv * v4.x, fv * v4.y, fv * v4.z, fv * v4.w);
+    Tbe[i * kC + l] = x * fbe;
+    Tb[i * kC + l] = x * fb;
   }
 }
 
@@ -800,27 +805,45 @@ __global__ void __launch_bounds__(256) bwdc_da(const Lay L) {
 }
 
 // Scatter a pair's gradients: dq, dk (atomics across the value heads of a
-// qk group), dv, dg (reverse cumsum of dgamma), dbeta.  Grid nb, 256 threads.
+// qk group), dv, dg (reverse cumsum of dgamma), dbeta.  vec: dq, dk and dv are
+// 16-byte aligned (float4 copies).  Grid nb, 256 threads.
 __global__ void __launch_bounds__(256) bwdc_scatter(const Lay L, float* dq, float* dk, float* dv, float* dg,
-                                                    float* dbeta, int T, int NC, int Hqk, int Hv) {
+                                                    float* dbeta, int T, int NC, int Hqk, int Hv, bool vec) {
   const int64_t b = blockIdx.x;
   const int c = (int)(b % NC), h = (int)((b / NC) % Hv), n = (int)(b / ((int64_t)NC * Hv));
   const int hq = h / (Hv / Hqk);
   const int64_t t0 = (int64_t)n * T + (int64_t)c * kC;
   const int Lc = T - c * kC < kC ? T - c * kC : kC;
   const bool share = Hv != Hqk;
-  for (int u = threadIdx.x; u < Lc * kDh; u += 256) {
-    const int i = u / kDh, d = u % kDh;
-    const int64_t qk = ((t0 + i) * Hqk + hq) * (int64_t)kDh + d, vo = ((t0 + i) * Hv + h) * (int64_t)kDh + d;
-    const int64_t x = b * kC * kDh + u;
-    if (share) {
-      atomicAdd(dq + qk, L.dQ[x]);
-      atomicAdd(dk + qk, L.dK[x]);
-    } else {
-      dq[qk] = L.dQ[x];
-      dk[qk] = L.dK[x];
+  if (vec) {
+    for (int u = threadIdx.x; u < Lc * kDh / 4; u += 256) {
+      const int i = (4 * u) / kDh, d = (4 * u) % kDh;
+      const int64_t qk = ((t0 + i) * Hqk + hq) * (int64_t)kDh + d, vo = ((t0 + i) * Hv + h) * (int64_t)kDh + d;
+      const int64_t x = b * kC * kDh + 4 * u;
+      const float4 a = *reinterpret_cast<const float4*>(L.dQ + x), k4 = *reinterpret_cast<const float4*>(L.dK + x);
+      if (share) {
+        atomicAdd(dq + qk, a.x); atomicAdd(dq + qk + 1, a.y); atomicAdd(dq + qk + 2, a.z); atomicAdd(dq + qk + 3, a.w);
+        atomicAdd(dk + qk, k4.x); atomicAdd(dk + qk + 1, k4.y); atomicAdd(dk + qk + 2, k4.z); atomicAdd(dk + qk + 3, k4.w);
+      } else {
+        *reinterpret_cast<float4*>(dq + qk) = a;
+        *reinterpret_cast<float4*>(dk + qk) = k4;
+      }
+      *reinterpret_cast<float4*>(dv + vo) = *reinterpret_cast<const float4*>(L.X4 + x);
     }
-    dv[vo] = L.X4[x];
+  } else {
+    for (int u = threadIdx.x; u < Lc * kDh; u += 256) {
+      const int i = u / kDh, d = u % kDh;
+      const int64_t qk = ((t0 + i) * Hqk + hq) * (int64_t)kDh + d, vo = ((t0 + i) * Hv + h) * (int64_t)kDh + d;
+      const int64_t x = b * kC * kDh + u;
+      if (share) {
+        atomicAdd(dq + qk, L.dQ[x]);
+        atomicAdd(dk + qk, L.dK[x]);
+      } else {
+        dq[qk] = L.dQ[x];
+        dk[qk] = L.dK[x];
+      }
+      dv[vo] = L.X4[x];
+    }
   }
   if (threadIdx.x < 32) {
     // dg_s = sum_{i >= s} dgamma_i over all 64 rows (padding rows included:
@@ -850,8 +873,8 @@ __global__ void __launch_bounds__(256) bwdc_scatter(const Lay L, float* dq, floa
 // ------------------------------------------------------------------- host side
 bool gemm(cudaStream_t s, int64_t nb, int M, int N, int Kd, float alpha, const float* A, int64_t sA, int lda,
           bool tA, const float* B, int64_t sB, int ldb, bool tB, float beta, float* C, int64_t sC, int ldc,
-          int exact = 0, const float* rs = nullptr, int64_t sR = 0) {
-  GemmArgs g{A, B, C, rs, sA, sB, sC, sR, lda, ldb, ldc, M, N, Kd, tA, tB, alpha, beta, exact};
+          int exact = 0, const float* rs = nullptr, int64_t sR = 0, const float* cs = nullptr, int64_t sCs = 0) {
+  GemmArgs g{A, B, C, rs, sA, sB, sC, sR, lda, ldb, ldc, M, N, Kd, tA, tB, alpha, beta, exact, cs, sCs};
   const dim3 grid(N / 64, M / 64, (unsigned)nb);
   if (tA)
     tB ? bgemm_kernel<true, true><<<grid, 256, 0, s>>>(g) : bgemm_kernel<true, false><<<grid, 256, 0, s>>>(g);
@@ -882,9 +905,9 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.Q, B2, kDh, false, L.K, B2, kDh, true, 0.f, L.P, Q2, kC, xA | xB);
   bwdc_masks<<<nbu, 256, 0, s>>>(L);
   bwdc_solve<<<nbu, 64, 0, s>>>(L);
-  bwdc_scale_kv<<<nbu, 256, 0, s>>>(L);
-  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, false, L.X1, B2, kDh, false, 0.f, L.W, B2, kDh);
-  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, false, L.X2, B2, kDh, false, 0.f, L.U, B2, kDh);
+  // W = (T diag(beta e)) K, U = (T diag(beta)) V
+  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, false, L.K, B2, kDh, false, 0.f, L.W, B2, kDh, xB);
+  ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M2, Q2, kC, false, L.V, B2, kDh, false, 0.f, L.U, B2, kDh, xB);
   // the serial passes
   bwdc_fwd_states<kBf><<<dim3((unsigned)chains, kDh / kSl), 256, 0, s>>>(L, h0, NC);
   // the reverse pass's G-independent terms: X = scale P^T dO (in dVp), H = scale Q^T diag(e) dO
@@ -907,11 +930,12 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   bwdc_dp<<<nbu, 256, 0, s>>>(L);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, false, L.K, B2, kDh, false, 1.f, L.dQ, B2, kDh, xB);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.M1, Q2, kC, true, L.Q, B2, kDh, false, 1.f, L.dK, B2, kDh, xB);
-  // dW = -dV' S0^T (X1); dT = dW (beta e K)^T + dV' (beta V)^T (M2)
-  bwdc_scale_kv<<<nbu, 256, 0, s>>>(L);   // X1 = beta e K, X2 = beta V again (X1, X2 were reused)
-  ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.dVp, B2, kDh, false, L.X2, B2, kDh, true, 0.f, L.M2, Q2, kC);
+  // dW = -dV' S0^T (X3); dT = (dW K^T) diag(beta e) + (dV' V^T) diag(beta) (M2)
   ok = ok && gemm(s, nb, kC, kDh, kDh, -1.f, L.dVp, B2, kDh, false, L.S0, S2, kDh, true, 0.f, L.X3, B2, kDh);
-  ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.X3, B2, kDh, false, L.X1, B2, kDh, true, 1.f, L.M2, Q2, kC);
+  ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.X3, B2, kDh, false, L.K, B2, kDh, true, 0.f, L.M2, Q2, kC, xB,
+                  nullptr, 0, L.vec + kBe * kC, V8);
+  ok = ok && gemm(s, nb, kC, kC, kDh, 1.f, L.dVp, B2, kDh, false, L.V, B2, kDh, true, 1.f, L.M2, Q2, kC, xB,
+                  nullptr, 0, L.vec + kBeta * kC, V8);
   // X1 <- T^T dW, X4 = T^T dV'
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, true, L.X3, B2, kDh, false, 0.f, L.X1, B2, kDh);
   ok = ok && gemm(s, nb, kC, kDh, kC, 1.f, L.T, Q2, kC, true, L.dVp, B2, kDh, false, 0.f, L.X4, B2, kDh);
@@ -927,7 +951,9 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
     const size_t tq = sizeof(float) * (size_t)p.B * p.T * p.Hqk * p.K;
     if (cudaMemsetAsync(dq, 0, tq, s) != cudaSuccess || cudaMemsetAsync(dk, 0, tq, s) != cudaSuccess) return GDN_ERR_CUDA;
   }
-  bwdc_scatter<<<nbu, 256, 0, s>>>(L, dq, dk, dv, dg, dbeta, p.T, NC, p.Hqk, p.Hv);
+  const bool vec = ((reinterpret_cast<uintptr_t>(dq) | reinterpret_cast<uintptr_t>(dk) |
+                     reinterpret_cast<uintptr_t>(dv)) & 15) == 0;
+  bwdc_scatter<<<nbu, 256, 0, s>>>(L, dq, dk, dv, dg, dbeta, p.T, NC, p.Hqk, p.Hv, vec);
   ok = ok && cudaGetLastError() == cudaSuccess;
   return ok ? GDN_OK : GDN_ERR_CUDA;
 }
