@@ -372,12 +372,9 @@ def run_decode(args, rank, world, dev):
         print(json.dumps(line), flush=True)
 
 
-# fp32 SIMT peak of this GB300 from its unit counts: 152 SMs x 128 FP32 lanes
-# x 2 FLOP (FMA) x 2.07 GHz boost clock
-FP32_SIMT_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
-BWDC_LAUNCHES = 36          # kernels of one sequence group of the chunked backward (gdn_bwdc.cu)
+BWDC_LAUNCHES = 34          # kernels of one sequence group of the chunked backward (gdn_bwdc.cu)
 BWDC_GROUP_BYTES = 16 << 30  # the chunked backward's per-group workspace budget
 
 
@@ -418,6 +415,10 @@ def run_bwd(args, rank, world, dev):
     sec_step = sec_total / args.steps
     flops = 20.0 * w.K * w.V * tokens * w.Hv
     achieved = flops / sec_step / 1e12
+    # the products run on the tensor cores as tf32 (nominal dense tf32 : bf16 = 1.1 : 2.25 PFLOP/s);
+    # a long step, so the sustained bf16 figure
+    pk = peaks()
+    tf32_peak = pk["bf16_tflops_sustained"] * 1.1 / 2.25
     line = {
         "metric": "GDN backward tokens/s (16x8192, H=32, K=V=128, bf16 inputs, fp32 gradients)", "value": value,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -426,9 +427,11 @@ def run_bwd(args, rank, world, dev):
         "config": {"workload": f"bwd_{w.B}x{w.T}_H{w.Hv}", "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv, "K": w.K,
                    "V": w.V, "parallelism": f"dp{world} (independent batches)",
                    "l2": "inputs larger than L2 (4.4 GB of inputs and upstream gradients per step)"},
-        "roofline": {"bound": "alu", "achieved": achieved, "peak": FP32_SIMT_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / FP32_SIMT_TFLOPS, "traffic": None, "peak_source": "derived (unit counts x clock)",
-                     "kernel": "chunked backward, all launches of one step", "alg_flops": flops},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
+                     "frac": achieved / tf32_peak, "traffic": None,
+                     "peak_source": f"measured bf16 sustained x nominal tf32/bf16 ratio ({pk['source']})",
+                     "kernel": "chunked backward, all launches of one step (mma.sync tf32, three terms)",
+                     "alg_flops": flops},
         "gpu_launches": BWDC_LAUNCHES * groups * args.steps,
         "clocks": clocks,
     }
