@@ -372,8 +372,6 @@ def run_decode(args, rank, world, dev):
         print(json.dumps(line), flush=True)
 
 
-
-
 BWDC_LAUNCHES = 34          # kernels of one sequence group of the chunked backward (gdn_bwdc.cu)
 BWDC_GROUP_BYTES = 16 << 30  # the chunked backward's per-group workspace budget
 
@@ -387,52 +385,67 @@ def run_bwd(args, rank, world, dev):
     import torch
     from gated_deltanet_chunked_gdn_gb300 import binding
     from gated_deltanet_chunked_gdn_gb300 import inputs as I
-    w = I.WORKLOADS[2].with_(B=args.B, Hqk=args.H, Hv=args.H, seed=2 + rank)
+    packed = args.workload == "varlen_64"
+    if packed:
+        w = I.WORKLOADS[3].with_(seed=3 + rank)
+    else:
+        w = I.WORKLOADS[2].with_(B=args.B, Hqk=args.H, Hv=args.H, seed=2 + rank)
     x = I.make_inputs(w, dev)
+    N = x["N"]
     gen = torch.Generator(device=dev).manual_seed(7 + rank)
     do = torch.randn(x["v"].shape, generator=gen, device=dev).to(x["v"].dtype)
-    dht = torch.randn((w.B, w.Hv, w.K, w.V), generator=gen, device=dev)
-    p = binding.problem_of(x["q"], x["v"], 64)
+    dht = torch.randn((N, w.Hv, w.K, w.V), generator=gen, device=dev)
+    p = binding.problem_of(x["q"], x["v"], 64, x["cu_seqlens"])
     ws = torch.empty(binding.gdn_chunk_bwd_workspace_size(p), dtype=torch.uint8, device=dev)
-    # sequence groups of the chunked backward: as many whole sequences as fit
-    # its budget, from the workspace of one sequence
-    p1 = binding.problem_of(x["q"][:1], x["v"][:1], 64)
-    per_seq = binding.gdn_chunk_bwd_workspace_size(p1)
-    group = max(1, min(w.B, BWDC_GROUP_BYTES // max(per_seq, 1)))
-    groups = -(-w.B // group)
+    if packed:
+        # one group with the chunk tables built on the device (the bound of this
+        # batch, about 28 K (chunk, head) pairs, is within the packed budget)
+        groups, launches = 1, BWDC_LAUNCHES + 1
+    else:
+        # sequence groups of the chunked backward: as many whole sequences as fit
+        # its budget, from the workspace of one sequence
+        p1 = binding.problem_of(x["q"][:1], x["v"][:1], 64)
+        per_seq = binding.gdn_chunk_bwd_workspace_size(p1)
+        group = max(1, min(w.B, BWDC_GROUP_BYTES // max(per_seq, 1)))
+        groups, launches = -(-w.B // group), BWDC_LAUNCHES
     stream = torch.cuda.current_stream(dev)
 
     def step():
         binding.gdn_chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], do, scale=x["scale"], h0=x["h0"], dht=dht,
-                              workspace=ws, stream=stream.cuda_stream)
+                              cu_seqlens=x["cu_seqlens"], workspace=ws, stream=stream.cuda_stream)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
     sec, clocks = timed(step, args.steps, world, dev, stream)
-    tokens = w.B * w.T
+    tokens = x["q"].shape[0] * x["q"].shape[1]
     value, sec_total = aggregate(sec, tokens, args.steps, world, dev)
     sec_step = sec_total / args.steps
     flops = 20.0 * w.K * w.V * tokens * w.Hv
+    in_bytes = sum(t.numel() * t.element_size() for t in (x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], do, dht)
+                   if t is not None)
     achieved = flops / sec_step / 1e12
     # the products run on the tensor cores as tf32 (nominal dense tf32 : bf16 = 1.1 : 2.25 PFLOP/s);
     # a long step, so the sustained bf16 figure
     pk = peaks()
     tf32_peak = pk["bf16_tflops_sustained"] * 1.1 / 2.25
     line = {
-        "metric": "GDN backward tokens/s (16x8192, H=32, K=V=128, bf16 inputs, fp32 gradients)", "value": value,
+        "metric": ("GDN backward tokens/s (varlen_64, Hqk=16, Hv=32, K=V=128, bf16 inputs, fp32 gradients)" if packed
+                   else "GDN backward tokens/s (16x8192, H=32, K=V=128, bf16 inputs, fp32 gradients)"), "value": value,
         "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * sec_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"bwd_{w.B}x{w.T}_H{w.Hv}", "B": w.B, "T": w.T, "Hqk": w.Hqk, "Hv": w.Hv, "K": w.K,
+        "config": {"workload": (f"bwd_varlen_{N}seqs_{tokens}tok_Hqk{w.Hqk}_Hv{w.Hv}" if packed
+                                else f"bwd_{w.B}x{w.T}_H{w.Hv}"), "B": x["q"].shape[0], "T": x["q"].shape[1], "N": N,
+                   "Hqk": w.Hqk, "Hv": w.Hv, "K": w.K,
                    "V": w.V, "parallelism": f"dp{world} (independent batches)",
-                   "l2": "inputs larger than L2 (4.4 GB of inputs and upstream gradients per step)"},
+                   "l2": f"inputs larger than L2 ({in_bytes / 1e9:.2f} GB of inputs and upstream gradients per step)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
                      "frac": achieved / tf32_peak, "traffic": None,
                      "peak_source": f"measured bf16 sustained x nominal tf32/bf16 ratio ({pk['source']})",
                      "kernel": "chunked backward, all launches of one step (mma.sync tf32, three terms)",
                      "alg_flops": flops},
-        "gpu_launches": BWDC_LAUNCHES * groups * args.steps,
+        "gpu_launches": launches * groups * args.steps,
         "clocks": clocks,
     }
     if rank == 0:

@@ -225,7 +225,7 @@ gdn_status gdn_chunk_bwd(const gdn_problem* pp, const void* q, const void* k, co
   for (const void* x : a4)
     if (x && !aligned(x, 4)) return GDN_ERR_INVALID_ARG;
   if (chunked)
-    return run_bwdc(p, q, k, v, g, beta, scale, h0, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
+    return run_bwdc(p, q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
                     static_cast<cudaStream_t>(stream));
   return run_bwd(p, q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, workspace,
                  static_cast<cudaStream_t>(stream));

@@ -191,13 +191,22 @@ struct Lay {
   float *M1, *M2, *M3;        // [nb][64][64] scratch
   float *S0, *G, *H;          // [nb][128][128]
   float *vec;                 // [nb][8][64]: gamma, e, beta, D, beta e, dgamma, dbeta, spare
+  int4* pinfo;                // packed sequences: [nb] {first token, rows, value head, chain} of pair b
+                              // (rows = 0: a padding pair); null for equal lengths
+  int2* cinfo;                // packed sequences: [N Hv] {first pair, chunks} of chain n Hv + h
   size_t bytes;
 };
+
+// Pairs of a packed batch: at most ceil(T / 64) + N chunks a value head.
+int64_t varlen_pairs(const gdn_problem& p) {
+  const int64_t Ttot = (int64_t)p.B * p.T;
+  return (int64_t)p.Hv * ((Ttot + kC - 1) / kC + p.N);
+}
 
 Lay layout(const gdn_problem& p, uint8_t* base) {
   Lay L;
   const int64_t NC = ((int64_t)p.T + kC - 1) / kC;
-  L.nb = (int64_t)p.N * p.Hv * NC;
+  L.nb = p.varlen ? varlen_pairs(p) : (int64_t)p.N * p.Hv * NC;
   size_t off = 0;
   auto take = [&](size_t floats) {
     float* r = reinterpret_cast<float*>(base ? base + off : nullptr);
@@ -212,6 +221,8 @@ Lay layout(const gdn_problem& p, uint8_t* base) {
   L.KK = take(sq); L.P = take(sq); L.A = take(sq); L.T = take(sq);
   L.M1 = take(sq); L.M2 = take(sq); L.M3 = take(sq);
   L.S0 = take(st); L.G = take(st); L.H = take(st);
+  L.pinfo = p.varlen ? reinterpret_cast<int4*>(take((size_t)L.nb * 4)) : nullptr;
+  L.cinfo = p.varlen ? reinterpret_cast<int2*>(take((size_t)p.N * p.Hv * 2)) : nullptr;
   L.vec = take((size_t)L.nb * 8 * kC);
   L.bytes = off;
   return L;
@@ -219,6 +230,88 @@ Lay layout(const gdn_problem& p, uint8_t* base) {
 
 enum { kGam = 0, kE = 1, kBeta = 2, kD = 3, kBe = 4, kDgam = 5, kDbeta = 6 };
 __device__ __forceinline__ float* vecp(const Lay& L, int64_t b, int which) { return L.vec + (b * 8 + which) * kC; }
+
+// Packed sequences: validates cu_seqlens (0 <= cu[n] <= cu[n + 1] <= Ttot,
+// cu[0] = 0, cu[N] = Ttot) and writes the chain and pair tables.  Chain
+// n Hv + h owns pairs Hv P_n + h C_n .. + C_n - 1 (C_n = ceil(L_n / 64) chunks,
+// P_n their exclusive prefix over the sequences); its pair c holds tokens
+// cu[n] + 64 c .. + min(64, L_n - 64 c) - 1.  The pairs past the last chain's
+// are padding (no rows: they compute zeros and scatter nothing).  A malformed
+// cu_seqlens sets the status word and leaves every chain and pair empty.  One
+// CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) bwdc_prepare(const Lay L, const int32_t* cu, int N, int64_t Ttot, int Hv,
+                                                     int32_t* status) {
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int ok = 1;
+  for (int n = tid; n < N; n += 1024) {
+    const int64_t a = cu[n], e = cu[n + 1];
+    if (!(0 <= a && a <= e && e <= Ttot)) ok = 0;
+  }
+  if (tid == 0 && (cu[0] != 0 || cu[N] != Ttot)) ok = 0;
+  ok = __syncthreads_and(ok);
+  for (int64_t b = tid; b < L.nb; b += 1024) L.pinfo[b] = make_int4(0, 0, 0, 0);
+  if (!ok) {
+    if (tid == 0) atomicExch(status, GDN_DEV_BAD_CU_SEQLENS);
+    for (int64_t c = tid; c < (int64_t)N * Hv; c += 1024) L.cinfo[c] = make_int2(0, 0);
+    return;
+  }
+  __syncthreads();   // the padding entries are written before the real ones
+  int carry = 0;     // chunks of the sequences before this tile
+  for (int n0 = 0; n0 < N; n0 += 1024) {
+    const int n = n0 + tid;
+    const int64_t t0 = n < N ? cu[n] : 0, len = n < N ? cu[n + 1] - t0 : 0;
+    const int nc = (int)((len + kC - 1) / kC);
+    int x = nc;   // inclusive scan within the warp, then over the warp sums
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int v = wsum[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += y;
+      }
+      wsum[lane] = v;   // inclusive over warps
+    }
+    __syncthreads();
+    const int pre = carry + (warp > 0 ? wsum[warp - 1] : 0) + x - nc;
+    if (n < N) {
+      for (int h = 0; h < Hv; ++h) {
+        const int base = Hv * pre + h * nc;
+        L.cinfo[(int64_t)n * Hv + h] = make_int2(base, nc);
+        for (int c = 0; c < nc; ++c) {
+          const int64_t rest = len - (int64_t)kC * c;
+          L.pinfo[base + c] = make_int4((int)(t0 + (int64_t)kC * c), rest < kC ? (int)rest : kC, h, n * Hv + h);
+        }
+      }
+    }
+    carry += wsum[31];
+    __syncthreads();   // wsum is rewritten by the next tile
+  }
+}
+
+// First token, valid rows and value head of pair b: from the pair table for
+// packed sequences, else b = (n Hv + h) NC + c over sequences of T tokens.
+__device__ __forceinline__ void pair_rows(const Lay& L, int64_t b, int T, int NC, int Hv, int64_t& t0, int& Lc,
+                                          int& h) {
+  if (L.pinfo) {
+    const int4 pi = L.pinfo[b];
+    t0 = pi.x;
+    Lc = pi.y;
+    h = pi.z;
+  } else {
+    const int c = (int)(b % NC), n = (int)(b / ((int64_t)NC * Hv));
+    h = (int)((b / NC) % Hv);
+    t0 = (int64_t)n * T + (int64_t)c * kC;
+    Lc = T - c * kC < kC ? T - c * kC : kC;
+  }
+}
 
 // Four consecutive elements (16-byte aligned for fp32, 8-byte for bf16) as fp32.
 __device__ __forceinline__ float4 ld4f(const float* p) { return *reinterpret_cast<const float4*>(p); }
@@ -236,10 +329,10 @@ __global__ void __launch_bounds__(256) bwdc_gather(const Lay L, const Tin* q, co
                                                    const Tin* dout, const float* g, const float* beta, int T, int NC,
                                                    int Hqk, int Hv) {
   const int64_t b = blockIdx.x;
-  const int c = (int)(b % NC), h = (int)((b / NC) % Hv), n = (int)(b / ((int64_t)NC * Hv));
+  int64_t t0;
+  int Lc, h;
+  pair_rows(L, b, T, NC, Hv, t0, Lc, h);
   const int hq = h / (Hv / Hqk);
-  const int64_t t0 = (int64_t)n * T + (int64_t)c * kC;
-  const int Lc = T - c * kC < kC ? T - c * kC : kC;
   const int tid = threadIdx.x;
   const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int u = tid; u < kC * kDh / 4; u += 256) {
@@ -430,7 +523,15 @@ __device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpre
 template <bool KEXACT>
 __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const float* h0, int NC) {
   __shared__ __align__(16) float xh[kXF], xl[kXF], vh[kVF], vl[kVF];
-  const int64_t chain = blockIdx.x, b0 = chain * NC;
+  const int64_t chain = blockIdx.x;
+  int64_t b0 = chain * NC;
+  int nc = NC;
+  if (L.cinfo) {
+    const int2 ci = L.cinfo[chain];
+    b0 = ci.x;
+    nc = ci.y;
+  }
+  if (nc == 0) return;   // an empty sequence has no chunk states
   const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int i0 = 8 * w + 2 * t;   // rows i0, i0 + 1 of the V' product's output
@@ -478,9 +579,9 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
   load_c(b0);
   __syncthreads();
 #pragma unroll 1
-  for (int c = 0; c < NC; ++c) {
+  for (int c = 0; c < nc; ++c) {
     const int64_t b = b0 + c;
-    if (c + 2 < NC) {
+    if (c + 2 < nc) {
       prefetch_rows(L.W + (b + 2) * kC * kDh, kDh, kC, kDh, tid, 256);
       prefetch_rows(L.K + (b + 2) * kC * kDh, kDh, kC, kDh, tid, 256);
     }
@@ -490,7 +591,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
       row_product<false>(wr, xh, xl, lane, o);
       const float v[4] = {ur[0] - o[0], ur[1] - o[1], ur[2] - o[2], ur[3] - o[3]};
       const float d0 = dr[0], d1 = dr[1];
-      if (c + 1 < NC) load_r(b + 1);
+      if (c + 1 < nc) load_r(b + 1);
       float* vp = L.Vp + (b * kC + i0) * kDh + e0 + g;
       vp[0] = v[0], vp[kDh] = v[1], vp[8] = v[2], vp[kDh + 8] = v[3];
       put_split(vh, vl, vf_index(i0, g), d0 * v[0]);
@@ -506,7 +607,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
 #pragma unroll
         for (int r = 0; r < 4; ++r) st[nt][r] *= el;
       col_product<KEXACT>(st, kc, vh, vl, lane, 1.f);
-      if (c + 1 < NC) {
+      if (c + 1 < nc) {
         load_c(b + 1);
         put_s0(b + 1);
 #pragma unroll
@@ -528,10 +629,26 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
 template <bool KEXACT>
 __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht, float* dh0, int NC) {
   __shared__ __align__(16) float xh[kXF], xl[kXF], vh[kVF], vl[kVF];
-  const int64_t chain = blockIdx.x, b0 = chain * NC;
+  const int64_t chain = blockIdx.x;
+  int64_t b0 = chain * NC;
+  int nc = NC;
+  if (L.cinfo) {
+    const int2 ci = L.cinfo[chain];
+    b0 = ci.x;
+    nc = ci.y;
+  }
   const int e0 = kSl * blockIdx.y, tid = threadIdx.x;
   const int w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
   const int i0 = 8 * w + 2 * t;
+  if (nc == 0) {
+    // an empty sequence passes dht through: dh0 = dht
+    if (dh0)
+      for (int u = tid; u < kDh * kSl; u += 256) {
+        const int64_t at = (chain * kDh + u / kSl) * kDh + e0 + u % kSl;
+        dh0[at] = dht ? dht[at] : 0.f;
+      }
+    return;
+  }
   float st[2][4];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
@@ -549,7 +666,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht
         *reinterpret_cast<float2*>(L.G + (b * kDh + st_row(w, g, 2 * h)) * kDh + e0 + st_col(t, nt, 0)) =
             make_float2(st[nt][2 * h], st[nt][2 * h + 1]);
   };
-  put_g(b0 + NC - 1);
+  put_g(b0 + nc - 1);
   float4 kr[8];
   float xr[4], dr[2], wc[32], hr[2][4], el;
   auto load_r = [&](int64_t b) {   // K rows 8 w + g; X and D at the dV' product's output
@@ -580,11 +697,11 @@ __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht
       }
     el = __ldg(vecp(L, b, kE) + kC - 1);
   };
-  load_r(b0 + NC - 1);
-  load_c(b0 + NC - 1);
+  load_r(b0 + nc - 1);
+  load_c(b0 + nc - 1);
   __syncthreads();
 #pragma unroll 1
-  for (int c = NC - 1; c >= 0; --c) {
+  for (int c = nc - 1; c >= 0; --c) {
     const int64_t b = b0 + c;
     if (c >= 2) {
       prefetch_rows(L.K + (b - 2) * kC * kDh, kDh, kC, kDh, tid, 256);
@@ -810,10 +927,10 @@ __global__ void __launch_bounds__(256) bwdc_da(const Lay L) {
 __global__ void __launch_bounds__(256) bwdc_scatter(const Lay L, float* dq, float* dk, float* dv, float* dg,
                                                     float* dbeta, int T, int NC, int Hqk, int Hv, bool vec) {
   const int64_t b = blockIdx.x;
-  const int c = (int)(b % NC), h = (int)((b / NC) % Hv), n = (int)(b / ((int64_t)NC * Hv));
+  int64_t t0;
+  int Lc, h;
+  pair_rows(L, b, T, NC, Hv, t0, Lc, h);
   const int hq = h / (Hv / Hqk);
-  const int64_t t0 = (int64_t)n * T + (int64_t)c * kC;
-  const int Lc = T - c * kC < kC ? T - c * kC : kC;
   const bool share = Hv != Hqk;
   if (vec) {
     for (int u = threadIdx.x; u < Lc * kDh / 4; u += 256) {
@@ -885,9 +1002,9 @@ bool gemm(cudaStream_t s, int64_t nb, int M, int N, int Kd, float alpha, const f
 
 template <typename Tin>
 gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g, const float* beta,
-               float scale, const float* h0, const void* dout, const float* dht, float* dq, float* dk, float* dv,
-               float* dg, float* dbeta, float* dh0, void* ws, cudaStream_t s) {
-  const int NC = (p.T + kC - 1) / kC;
+               float scale, const float* h0, const int32_t* cu, const void* dout, const float* dht, float* dq,
+               float* dk, float* dv, float* dg, float* dbeta, float* dh0, int32_t* status, void* ws, cudaStream_t s) {
+  const int NC = (p.T + kC - 1) / kC;   // equal lengths (packed sequences: the tables)
   const Lay L = layout(p, static_cast<uint8_t*>(ws));
   const int64_t nb = L.nb, B2 = (int64_t)kC * kDh, Q2 = (int64_t)kC * kC, S2 = (int64_t)kDh * kDh, V8 = 8 * kC;
   const unsigned nbu = (unsigned)nb;
@@ -897,6 +1014,7 @@ gdn_status run(const gdn_problem& p, const void* q, const void* k, const void* v
   constexpr bool kBf = std::is_same<Tin, __nv_bfloat16>::value;
   const int xA = kBf ? 1 : 0, xB = kBf ? 2 : 0;
   bool ok = true;
+  if (p.varlen) bwdc_prepare<<<1, 1024, 0, s>>>(L, cu, p.N, (int64_t)p.B * p.T, p.Hv, status);
   bwdc_gather<Tin><<<nbu, 256, 0, s>>>(L, static_cast<const Tin*>(q), static_cast<const Tin*>(k),
                                         static_cast<const Tin*>(v), static_cast<const Tin*>(dout), g, beta, p.T, NC,
                                         p.Hqk, p.Hv);
@@ -979,18 +1097,34 @@ gdn_problem group_problem(const gdn_problem& p, int n) {
 
 }  // namespace
 
-bool bwdc_supported(const gdn_problem& p) { return !p.varlen && p.K == kDh && p.V == kDh && p.T > 0; }
+// Packed sequences run as one group, sized for the bound of ceil(T / 64) + N
+// chunks a value head; larger packed batches take the token recurrence.
+constexpr size_t kVarlenBytes = size_t(32) << 30;
+
+bool bwdc_supported(const gdn_problem& p) {
+  if (p.K != kDh || p.V != kDh || p.T <= 0) return false;
+  return !p.varlen || layout(p, nullptr).bytes <= kVarlenBytes;
+}
 
 size_t bwdc_workspace_bytes(const gdn_problem& p) {
+  if (p.varlen) return kAlign + layout(p, nullptr).bytes;
   return kAlign + layout(group_problem(p, group_seqs(p)), nullptr).bytes;
 }
 
 gdn_status run_bwdc(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
-                    const float* beta, float scale, const float* h0, const void* dout, const float* dht, float* dq,
-                    float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws, cudaStream_t s) {
+                    const float* beta, float scale, const float* h0, const int32_t* cu_seqlens, const void* dout,
+                    const float* dht, float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws,
+                    cudaStream_t s) {
   int32_t* status = static_cast<int32_t*>(ws);
   if (cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return GDN_ERR_CUDA;
   void* w = static_cast<uint8_t*>(ws) + kAlign;
+  if (p.varlen) {
+    if (p.dt == GDN_F32)
+      return run<float>(p, q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0, status, w,
+                        s);
+    return run<__nv_bfloat16>(p, q, k, v, g, beta, scale, h0, cu_seqlens, dout, dht, dq, dk, dv, dg, dbeta, dh0,
+                              status, w, s);
+  }
   const int G = group_seqs(p);
   const size_t e = p.dt == GDN_F32 ? 4 : 2;
   const int64_t kv = (int64_t)p.K * p.V;
@@ -1006,12 +1140,13 @@ gdn_status run_bwdc(const gdn_problem& p, const void* q, const void* k, const vo
     const int64_t tq = t0 * p.Hqk * p.K, tv = t0 * p.Hv * p.V, tg = t0 * p.Hv, ts = (int64_t)n0 * p.Hv * kv;
     gdn_status st;
     if (p.dt == GDN_F32)
-      st = run<float>(gp, off(q, tq), off(k, tq), off(v, tv), g + tg, beta + tg, scale, offf(h0, ts), off(dout, tv),
-                      offf(dht, ts), dq + tq, dk + tq, dv + tv, dg + tg, dbeta + tg, offw(dh0, ts), w, s);
+      st = run<float>(gp, off(q, tq), off(k, tq), off(v, tv), g + tg, beta + tg, scale, offf(h0, ts), nullptr,
+                      off(dout, tv), offf(dht, ts), dq + tq, dk + tq, dv + tv, dg + tg, dbeta + tg, offw(dh0, ts),
+                      status, w, s);
     else
       st = run<__nv_bfloat16>(gp, off(q, tq), off(k, tq), off(v, tv), g + tg, beta + tg, scale, offf(h0, ts),
-                              off(dout, tv), offf(dht, ts), dq + tq, dk + tq, dv + tv, dg + tg, dbeta + tg,
-                              offw(dh0, ts), w, s);
+                              nullptr, off(dout, tv), offf(dht, ts), dq + tq, dk + tq, dv + tv, dg + tg, dbeta + tg,
+                              offw(dh0, ts), status, w, s);
     if (st != GDN_OK) return st;
   }
   return GDN_OK;

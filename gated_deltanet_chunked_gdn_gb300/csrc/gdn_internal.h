@@ -99,13 +99,16 @@ gdn_status run_bwd(const gdn_problem& p, const void* q, const void* k, const voi
                    const float* dht, float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws,
                    cudaStream_t s);
 
-// Chunked backward (gdn_bwdc.cu): equal-length sequences, K = V = 128; the
-// token-recurrence backward above covers the rest.
+// Chunked backward (gdn_bwdc.cu): K = V = 128; equal-length batches in
+// sequence groups, packed sequences in one group (bounded workspace, tables
+// built on the device from cu_seqlens); the token-recurrence backward above
+// covers the rest.
 bool bwdc_supported(const gdn_problem& p);
 size_t bwdc_workspace_bytes(const gdn_problem& p);
 gdn_status run_bwdc(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
-                    const float* beta, float scale, const float* h0, const void* dout, const float* dht, float* dq,
-                    float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws, cudaStream_t s);
+                    const float* beta, float scale, const float* h0, const int32_t* cu_seqlens, const void* dout,
+                    const float* dht, float* dq, float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws,
+                    cudaStream_t s);
 
 // Chunk-parallel path (gdn_cp.cu): sequences cut into segments run in parallel.
 size_t cp_workspace_bytes(const gdn_problem& p);

@@ -274,12 +274,16 @@ gdn_status gdn_recurrent_fwd(const gdn_problem* p, const void* q, const void* k,
  *     dk_t = -e^{g_t} beta_t (G u + S_{t-1} w) + beta_t G v_t
  *     G <- e^{g_t} (G - beta_t k_t w^T)
  * from G = dht down to dh0 = G (S_t the state after token t, S_0 = h0).
- * Equal-length batches with K = V = 128 run the chunked form of the same
- * reverse mode (64-token chunks: batched fp32 products for everything but
- * the chunk-to-chunk state and adjoint recurrences; about 0.8 MB of workspace
- * per (chunk, value head), the batch taken in sequence groups within 16 GiB);
- * other problems recompute the states in fp32 from checkpoints at every 64th
- * token.  Both compute in fp32.
+ * With K = V = 128 (and q, k, v, dout 16-byte aligned) the chunked form of
+ * the same reverse mode runs (64-token chunks: batched products for
+ * everything but the chunk-to-chunk state and adjoint recurrences, on the
+ * tensor cores as tf32 in three terms, about 2^-19 of each product; about
+ * 0.8 MB of workspace per (chunk, value head)): equal-length batches in
+ * sequence groups within 16 GiB; packed sequences in one group sized for
+ * ceil(T / 64) + N chunks a value head, with the chunk tables built on the
+ * device from cu_seqlens (packed batches whose bound exceeds 32 GiB take the
+ * token recurrence).  Other problems recompute the states in fp32 from
+ * checkpoints at every 64th token.  Both keep fp32 accuracy.
  *   p, q, k, v, g, beta, scale, h0, cu_seqlens : as for gdn_chunk_fwd (K in
  *                 {64, 128}, V a multiple of 16; any C)
  *   dout        : [B, T, Hv, V], dtype p->dt;  dht : [N, Hv, K, V] fp32 or NULL (= 0)

@@ -2,8 +2,9 @@
 the fp64 oracle's reverse-mode gradients on the same seeded inputs and
 upstream gradients.  The backward computes in fp32 from the stored inputs
 (bf16 or fp32), so the bar is a relative Frobenius error of at most 1e-4 on
-every gradient.  Equal-length batches with K = V = 128 take the chunked
-backward; packed sequences and K = 64 the token-recurrence one."""
+every gradient.  K = V = 128 takes the chunked backward (equal lengths in
+sequence groups, packed sequences in one group with device-built chunk
+tables); K = 64 the token-recurrence one."""
 import numpy as np
 import pytest
 import torch
@@ -63,6 +64,21 @@ def test_bwd_fp32_chunked_gqa_ragged(gdn, oracle_mod):
 
 def test_bwd_bf16_varlen_gqa(gdn, oracle_mod):
     check(gdn, oracle_mod, I.WORKLOADS[3].with_(Hqk=2, Hv=4), lens=[5, 64, 200, 1, 0, 129, 63, 65])
+
+
+def test_bwd_fp32_chunked_varlen(gdn, oracle_mod):
+    # packed sequences on the chunked form: several chunks with a ragged tail,
+    # a one-token and an empty sequence, exactly one chunk
+    check(gdn, oracle_mod, I.WORKLOADS[3].with_(Hqk=2, Hv=4, dtype="f32"), lens=[300, 1, 64, 0, 129])
+
+
+def test_bwd_bf16_chunked_varlen_without_h0_and_dht(gdn, oracle_mod):
+    check(gdn, oracle_mod, I.WORKLOADS[3].with_(Hqk=1, Hv=2), lens=[200, 65, 7], with_h0=False, with_dht=False)
+
+
+def test_bwd_fp32_varlen_token_path(gdn, oracle_mod):
+    # K = 64: packed sequences on the token recurrence
+    check(gdn, oracle_mod, I.WORKLOADS[0].with_(Hqk=1, Hv=2), lens=[5, 70, 0, 130])
 
 
 def test_bwd_without_h0_and_dht(gdn, oracle_mod):
