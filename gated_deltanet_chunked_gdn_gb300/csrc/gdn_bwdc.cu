@@ -1,5 +1,6 @@
 // gdn_bwdc.cu -- chunked backward pass of the Gated DeltaNet forward for
-// equal-length sequences (fp32 arithmetic on the stored inputs).
+// K = V = 128, equal-length or packed sequences (fp32 accuracy on the stored
+// inputs: every product on the tensor cores as tf32 in three terms).
 //
 // Per 64-token chunk (rows i, j; padding rows have g = beta = 0 and zero
 // k, q, v, dout) the forward is, with gamma the in-chunk cumsum of g,
@@ -20,8 +21,8 @@
 //           scale e_i (Q S0)_i . dO_i, rowsum - colsum of dP o P and dA o A,
 //           beta_i e_i k_i . (T^T dW)_i;   dg = reverse cumsum of dgamma.
 // The chunk-start states S0 come from a serial forward over the chunks and G
-// from a serial reverse (one CTA per chain and 32-column slice of V); every
-// other product is a batched fp32 GEMM over all (chunk, head) pairs at once.
+// from a serial reverse (one CTA per chain and 16-column slice of V); every
+// other product is a batched GEMM over all (chunk, head) pairs at once.
 #include <type_traits>
 
 #include "gdn_internal.h"
@@ -37,9 +38,10 @@ constexpr int kDh = 128;    // K = V
 constexpr int kSl = 16;     // V columns per CTA of the serial kernels
 
 // ---------------------------------------------------------------- batched GEMM
-// C[b] = alpha diag(rs[b]) op(A[b]) op(B[b]) diag(cs[b]) + beta C[b] for M, N multiples of
-// 64 and Kd a multiple of 32 (rs, cs may be null: all ones); op(A)(i, k) = tA ? A[k lda + i] : A[i lda + k],
-// op(B)(k, j) = tB ? B[j ldb + k] : B[k ldb + j]; rs may be null (all ones).
+// C[b] = alpha diag(rs[b]) op(A[b]) op(B[b]) diag(cs[b]) + beta C[b] for M, N
+// multiples of 64 and Kd a multiple of 32; op(A)(i, k) = tA ? A[k lda + i] :
+// A[i lda + k], op(B)(k, j) = tB ? B[j ldb + k] : B[k ldb + j]; rs and cs may
+// be null (all ones).
 struct GemmArgs {
   const float* A;
   const float* B;
