@@ -13,8 +13,9 @@
 // thread owns 8 consecutive channels (one 16-byte vector of bf16) over a run
 // of kTok tokens; a warp reads and writes 512 contiguous bytes per token.  The
 // W-1 previous inputs stay in registers as raw vectors (a sliding window), so
-// x is read once plus a W-1 token halo per run; loads run kUnroll tokens
-// ahead of the arithmetic.  The state pool is rewritten by a second launch,
+// x is read once plus a W-1 token halo per run; the loads of the next
+// kUnroll tokens are issued before the arithmetic of the current ones, so
+// that the memory stream overlaps the activation.  The state pool is rewritten by a second launch,
 // after the first has read every old state.
 #include "gdn_internal.h"
 #include "gdn_sm100.cuh"
@@ -24,7 +25,7 @@ namespace {
 
 constexpr int kConvThreads = 128;   // channel vectors per CTA
 constexpr int kTok = 64;            // tokens per thread run
-constexpr int kUnroll = 8;          // tokens loaded ahead
+constexpr int kUnroll = 4;          // tokens a batch (the next batch loaded ahead)
 
 template <typename T>
 struct Vec8;
@@ -120,7 +121,7 @@ __device__ __forceinline__ float rcp_approx(float y) {
 __device__ __forceinline__ float silu(float u) { return u * rcp_approx(1.f + sm100::exp_fast(-u)); }
 
 template <typename T, int W, bool SILU>
-__global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const ConvArgs a) {
+__global__ void __launch_bounds__(kConvThreads, sizeof(T) == 2 ? 4 : 2) conv1d_kernel(const ConvArgs a) {
   const int c0 = 8 * (blockIdx.y * kConvThreads + threadIdx.x);
   if (c0 >= a.D) return;
   const int64_t t0 = (int64_t)blockIdx.x * kTok;
@@ -197,12 +198,26 @@ __global__ void __launch_bounds__(kConvThreads) conv1d_kernel(const ConvArgs a) 
       o.from_float(acc);
       o.store(y + tt * D + c0);
     };
-    for (; t + kUnroll <= end; t += kUnroll) {
+    // batches of kUnroll tokens, the next batch's loads issued before this
+    // batch's arithmetic so that they overlap it
+    if (t + kUnroll <= end) {
       Vec8<T> v[kUnroll];
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) v[u].load(x + (t + u) * D + c0);
+      for (;;) {
+        const bool more = t + 2 * kUnroll <= end;
+        Vec8<T> nv[kUnroll];
+        if (more) {
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) emit(v[u], t + u);
+          for (int u = 0; u < kUnroll; ++u) nv[u].load(x + (t + kUnroll + u) * D + c0);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) emit(v[u], t + u);
+        t += kUnroll;
+        if (!more) break;
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) v[u] = nv[u];
+      }
     }
     for (; t < end; ++t) {
       Vec8<T> v;
