@@ -199,7 +199,12 @@ gdn_status gdn_causal_conv1d_fwd(const void* x, const float* weight, const float
 size_t gdn_chunk_bwd_workspace_size(const gdn_problem* pp) {
   gdn_problem p;
   if (!problem_ok(pp, &p) || !bwd_supported(p)) return 0;
-  return bwdc_supported(p) ? bwdc_workspace_bytes(p) : bwd_workspace_bytes(p);
+  // the chunked form also needs 16-byte aligned q, k, v and dout, which the
+  // query cannot see: size for whichever form the call takes
+  const size_t token = bwd_workspace_bytes(p);
+  if (!bwdc_supported(p)) return token;
+  const size_t chunked = bwdc_workspace_bytes(p);
+  return chunked > token ? chunked : token;
 }
 
 gdn_status gdn_chunk_bwd(const gdn_problem* pp, const void* q, const void* k, const void* v, const float* g,

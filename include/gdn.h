@@ -291,7 +291,9 @@ gdn_status gdn_recurrent_fwd(const gdn_problem* p, const void* q, const void* k,
  *                 q/k head);  dv : out [B, T, Hv, V] fp32
  *   dg, dbeta   : out [B, T, Hv] fp32;  dh0 : out [N, Hv, K, V] fp32 or NULL
  *   workspace   : gdn_chunk_bwd_workspace_size(p) bytes, 256-byte aligned
- *                 (the device status word and the per-chunk intermediates)
+ *                 (the device status word and the per-chunk intermediates;
+ *                 the size covers either form, since the choice also depends
+ *                 on the alignment of q, k, v and dout)
  * dq and dk (and, for packed sequences or K = 64, dg and dbeta) are sums of
  * fp32 atomic additions across value heads or column slices (their rounding
  * may differ between runs).  Malformed cu_seqlens set the status word (read it

@@ -134,3 +134,17 @@ def test_conv1d_rejects_bad_arguments():
     assert conv_call(N=3) == bad                     # fixed length: N == B
     assert conv_call(cu=6 << 12, B=2) == bad         # packed batches have B == 1
     assert conv_call(dt=7) == bad and conv_call(act=2) == bad
+
+
+def test_bwd_workspace_covers_both_forms():
+    # the backward picks its form at call time (the chunked one needs 16-byte
+    # aligned q, k, v and dout), so the queried size must cover the token
+    # recurrence's checkpoints too: 64 KB a value head for every 64 tokens
+    # (plus one a sequence) when K = V = 128
+    for p in (P(B=256, T=8192, N=256, Hqk=32, Hv=32), P(B=2, T=300, N=2), P(B=1, T=5000, N=7, varlen=1)):
+        slots = (p.B * p.T + 63) // 64 + p.N
+        assert b.gdn_chunk_bwd_workspace_size(p) >= slots * p.Hv * p.K * p.V * 4
+    # K = 64 only has the token recurrence
+    q = P(K=64, V=64)
+    slots = (q.B * q.T + 63) // 64 + q.N
+    assert b.gdn_chunk_bwd_workspace_size(q) >= slots * q.Hv * 64 * 64 * 4
