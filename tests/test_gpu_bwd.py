@@ -33,14 +33,27 @@ def upstream(x, N, Hv, K, V, seed, with_dht=True):
     return do, dht
 
 
-def check(gdn, oracle_mod, w, lens=None, with_h0=True, with_dht=True, seed=11):
+def shifted(t):
+    """A CUDA copy of t whose data starts 4 bytes past a 16-byte boundary."""
+    flat = torch.empty(t.numel() + 16, dtype=t.dtype, device="cuda")
+    off = (-(flat.data_ptr() % 16) + 4) % 16 // t.element_size()
+    v = flat[off:off + t.numel()].view(t.shape)
+    v.copy_(t.cuda())
+    assert v.data_ptr() % 16 == 4
+    return v
+
+
+def check(gdn, oracle_mod, w, lens=None, with_h0=True, with_dht=True, seed=11, unaligned=False):
     x = I.make_inputs(w, "cpu", lengths=lens)
     if not with_h0:
         x["h0"] = None
     N = x["N"]
     do, dht = upstream(x, N, w.Hv, w.K, w.V, seed, with_dht)
     d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
-    r = gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], do.cuda(), scale=d["scale"], h0=d["h0"],
+    do_d = do.cuda()
+    if unaligned:
+        d["q"], d["k"], d["v"], do_d = shifted(x["q"]), shifted(x["k"]), shifted(x["v"]), shifted(do)
+    r = gdn.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], do_d, scale=d["scale"], h0=d["h0"],
                           dht=dht.cuda() if dht is not None else None, cu_seqlens=d["cu_seqlens"])
     assert gdn.gdn_chunk_bwd_get_device_status(r["workspace"]) == gdn.DEV_OK
     ref = oracle_mod.recurrent_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], do, h0=x["h0"], dht=dht,
@@ -79,6 +92,12 @@ def test_bwd_bf16_chunked_varlen_without_h0_and_dht(gdn, oracle_mod):
 def test_bwd_fp32_varlen_token_path(gdn, oracle_mod):
     # K = 64: packed sequences on the token recurrence
     check(gdn, oracle_mod, I.WORKLOADS[0].with_(Hqk=1, Hv=2), lens=[5, 70, 0, 130])
+
+
+def test_bwd_unaligned_inputs_take_token_path(gdn, oracle_mod):
+    # q, k, v and dout 4-byte aligned only: the chunked form needs 16-byte
+    # alignment, so the token recurrence runs on a K = V = 128 problem
+    check(gdn, oracle_mod, I.WORKLOADS[2].with_(B=2, T=130, Hqk=1, Hv=2), unaligned=True)
 
 
 def test_bwd_without_h0_and_dht(gdn, oracle_mod):
