@@ -429,16 +429,32 @@ __device__ __forceinline__ void prefetch_rows(const float* src, int64_t ld, int 
 // A [128][16] slice X (the state, or G) as the A operand of X^T R^T: k-step
 // ks = 2 kk + p covers rows d = 16 kk + 4 t + 2 p (fragment column t) and
 // d + 1 (column t + 4), fragment row g = column c % 8, c / 8 = the lower or
-// upper 8 rows; lane 4 g + t holds {(d, g), (d, g + 8), (d + 1, g), (d + 1, g + 8)}.
+// upper 8 rows; lane 4 g + t holds {(d, g), (d, g + 8), (d + 1, g), (d + 1, g + 8)}
+// in 16-byte chunk ks * 32 + lane.  Within each 128-byte row of chunks (row =
+// chunk / 8) the chunk position is XORed with xf_swz(row): a lane's read stays
+// one 16-byte load, a quarter warp still reads one row (conflict-free), and the
+// scattered stores of the state meet at most two to a bank instead of eight.
+__device__ __forceinline__ int xf_swz(int row) { return 2 * (row & 3) + ((row >> 2) & 1); }
 __device__ __forceinline__ int xf_index(int d, int c) {
   const int ks = 2 * (d >> 4) + ((d >> 1) & 1), t = (d >> 2) & 3;
-  return ((ks * 32 + 4 * (c & 7) + t) << 2) + 2 * (d & 1) + (c >> 3);
+  const int ch = ks * 32 + 4 * (c & 7) + t;
+  return (((ch & ~7) | ((ch & 7) ^ xf_swz(ch >> 3))) << 2) + 2 * (d & 1) + (c >> 3);
+}
+// Chunk of lane `lane` in k-step ks of the X array (rows ks * 4 + lane / 8).
+__device__ __forceinline__ int xf_chunk(int ks, int lane) {
+  return ks * 32 + (lane & ~7) + ((lane & 7) ^ (2 * (lane >> 3) + (ks & 1)));
 }
 // A [64][16] slice V as the B operand of Col^T V: k-step ks covers rows
 // 8 ks + t (fragment row t) and 8 ks + t + 4 (row t + 4), fragment column g
-// = c % 8 of n-tile c / 8; lane 4 g + t holds {b0, b1} of n-tile 0, then of 1.
+// = c % 8 of n-tile c / 8; lane 4 g + t holds {b0, b1} of n-tile 0, then of 1,
+// in chunk ks * 32 + lane, XORed within its row by (row / 2) % 2 (the stores
+// of V' then meet at most two to a bank instead of four).
 __device__ __forceinline__ int vf_index(int i, int c) {
-  return (((i >> 3) * 32 + 4 * (c & 7) + (i & 3)) << 2) + 2 * (c >> 3) + ((i >> 2) & 1);
+  const int ch = (i >> 3) * 32 + 4 * (c & 7) + (i & 3);
+  return (((ch & ~7) | ((ch & 7) ^ ((ch >> 4) & 1))) << 2) + 2 * (c >> 3) + ((i >> 2) & 1);
+}
+__device__ __forceinline__ int vf_chunk(int ks, int lane) {
+  return ks * 32 + (lane & ~7) + ((lane & 7) ^ ((lane >> 4) & 1));
 }
 constexpr int kXF = kDh * kSl;   // floats of one XF array
 constexpr int kVF = kC * kSl;    // floats of one VF array
@@ -468,8 +484,8 @@ __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* x
       uint32_t bh0, bl0, bh1, bl1;
       split_tf32(rv[2 * p], bh0, bl0);
       split_tf32(rv[2 * p + 1], bh1, bl1);
-      const uint4 ah = *reinterpret_cast<const uint4*>(xh + ((ks * 32 + lane) << 2));
-      const uint4 al = *reinterpret_cast<const uint4*>(xl + ((ks * 32 + lane) << 2));
+      const uint4 ah = *reinterpret_cast<const uint4*>(xh + (xf_chunk(ks, lane) << 2));
+      const uint4 al = *reinterpret_cast<const uint4*>(xl + (xf_chunk(ks, lane) << 2));
       mma_tf32(acc[2 * p + 1], al.x, al.y, al.z, al.w, bh0, bh1);
       if (!REXACT) mma_tf32(acc[2 * p + 1], ah.x, ah.y, ah.z, ah.w, bl0, bl1);
       mma_tf32(acc[2 * p], ah.x, ah.y, ah.z, ah.w, bh0, bh1);
@@ -491,8 +507,8 @@ __device__ __forceinline__ void col_product(float (&st)[2][4], const float (&col
     uint32_t ah[4], al[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) split_tf32(sign * col[4 * ks + r], ah[r], al[r]);
-    const uint4 bh = *reinterpret_cast<const uint4*>(vh + ((ks * 32 + lane) << 2));
-    const uint4 bl = *reinterpret_cast<const uint4*>(vl + ((ks * 32 + lane) << 2));
+    const uint4 bh = *reinterpret_cast<const uint4*>(vh + (vf_chunk(ks, lane) << 2));
+    const uint4 bl = *reinterpret_cast<const uint4*>(vl + (vf_chunk(ks, lane) << 2));
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const uint32_t h0 = nt ? bh.z : bh.x, h1 = nt ? bh.w : bh.y;
