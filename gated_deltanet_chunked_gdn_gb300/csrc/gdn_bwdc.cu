@@ -77,19 +77,22 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
 
 // One 64 x 64 tile of C per CTA on the tensor cores (mma.sync m16n8k8, tf32
 // in three terms): warp w computes rows 16 (w % 4) .. + 15 and columns
-// 32 (w / 4) .. + 31 as four 16 x 8 accumulators.  k-tiles of 32 are staged in
-// two shared buffers in the operands' own orientation (A as [m][k] with row
-// stride 36 or [k][m] with 72, B as [k][n] with 72 or [n][k] with 36: the
-// fragment loads of a warp then hit 32 different banks and every store is a
-// 16-byte row piece); each thread fetches two float4 of A and two of B per
-// tile into registers one tile ahead.
+// 32 (w / 4) .. + 31 as four 16 x 8 accumulators.  k-tiles of 32 go from global
+// to shared memory by cp.async through a ring of three stages (two k-tiles in
+// flight while the tensor cores work on the third), in the operands' own
+// orientation (A as [m][k] with row stride 36 or [k][m] with 72, B as [k][n]
+// with 72 or [n][k] with 36: the fragment loads of a warp then hit 32
+// different banks).  Dynamic shared memory kGemmSmem.
+constexpr int kGemmStages = 3, kGemmBuf = 64 * 36;
+constexpr int kGemmSmem = 2 * kGemmStages * kGemmBuf * 4;
 template <bool TA, bool TB>
 __global__ void __launch_bounds__(256, 3) bgemm_kernel(const GemmArgs g) {
-  constexpr int kT = 32, kBuf = 64 * 36;
+  constexpr int kT = 32, kBuf = kGemmBuf;
   constexpr int sAm = TA ? 1 : 36, sAk = TA ? 72 : 1;   // A(m, k) at As[m sAm + k sAk]
   constexpr int sBk = TB ? 1 : 36 * 2, sBn = TB ? 36 : 1;
-  __shared__ __align__(16) float As[2][kBuf];
-  __shared__ __align__(16) float Bs[2][kBuf];
+  extern __shared__ __align__(16) float gsm[];
+  float* const As = gsm;
+  float* const Bs = gsm + kGemmStages * kBuf;
   const int64_t b = blockIdx.z;
   const int i0 = 64 * blockIdx.y, j0 = 64 * blockIdx.x;
   const float* A = g.A + b * g.sA;
@@ -100,33 +103,29 @@ __global__ void __launch_bounds__(256, 3) bgemm_kernel(const GemmArgs g) {
   const int ar = TA ? tid >> 4 : tid >> 3, aq = TA ? 4 * (tid & 15) : 4 * (tid & 7), ah_ = TA ? 16 : 32;
   const int br = TB ? tid >> 3 : tid >> 4, bq = TB ? 4 * (tid & 7) : 4 * (tid & 15), bh_ = TB ? 32 : 16;
   const int sa = TA ? 72 : 36, sb = TB ? 36 : 72;   // shared row strides
-  auto fetch = [&](int k0, float4 (&ra)[2], float4 (&rb)[2]) {
+  // this thread's 16-byte pieces of a k-tile, straight to shared memory
+  auto issue = [&](int stage, int k0) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      ra[r] = TA ? *reinterpret_cast<const float4*>(A + (int64_t)(k0 + ar + r * ah_) * g.lda + i0 + aq)
-                 : *reinterpret_cast<const float4*>(A + (int64_t)(i0 + ar + r * ah_) * g.lda + k0 + aq);
-      rb[r] = TB ? *reinterpret_cast<const float4*>(B + (int64_t)(j0 + br + r * bh_) * g.ldb + k0 + bq)
-                 : *reinterpret_cast<const float4*>(B + (int64_t)(k0 + br + r * bh_) * g.ldb + j0 + bq);
+      cp_async16(As + stage * kBuf + (ar + r * ah_) * sa + aq,
+                 TA ? A + (int64_t)(k0 + ar + r * ah_) * g.lda + i0 + aq : A + (int64_t)(i0 + ar + r * ah_) * g.lda + k0 + aq);
+      cp_async16(Bs + stage * kBuf + (br + r * bh_) * sb + bq,
+                 TB ? B + (int64_t)(j0 + br + r * bh_) * g.ldb + k0 + bq : B + (int64_t)(k0 + br + r * bh_) * g.ldb + j0 + bq);
     }
-  };
-  auto put = [&](int buf, const float4 (&ra)[2], const float4 (&rb)[2]) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      *reinterpret_cast<float4*>(&As[buf][(ar + r * ah_) * sa + aq]) = ra[r];
-      *reinterpret_cast<float4*>(&Bs[buf][(br + r * bh_) * sb + bq]) = rb[r];
-    }
+    cp_async_commit();
   };
   float acc[4][4] = {};
-  float4 ra[2], rb[2];
-  fetch(0, ra, rb);
-  put(0, ra, rb);
-  __syncthreads();
-  int buf = 0;
-  for (int k0 = 0; k0 < g.Kd; k0 += kT) {
-    const bool more = k0 + kT < g.Kd;
-    if (more) fetch(k0 + kT, ra, rb);
-    const float* as = As[buf] + (16 * mt + gq) * sAm + tq * sAk;
-    const float* bs = Bs[buf] + (32 * nh + gq) * sBn + tq * sBk;
+  const int nk = g.Kd / kT;
+  issue(0, 0);
+  if (nk > 1) issue(1, kT);
+  for (int kt = 0; kt < nk; ++kt) {
+    // k-tile kt has landed once at most one later group is still pending
+    if (kt + 1 < nk) cp_async_wait_prev(); else cp_async_wait_all();
+    __syncthreads();   // every thread's pieces are in; stage (kt + 2) % 3 is free
+    if (kt + 2 < nk) issue((kt + 2) % kGemmStages, (kt + 2) * kT);
+    const int buf = kt % kGemmStages;
+    const float* as = As + buf * kBuf + (16 * mt + gq) * sAm + tq * sAk;
+    const float* bs = Bs + buf * kBuf + (32 * nh + gq) * sBn + tq * sBk;
 #pragma unroll
     for (int ks = 0; ks < kT; ks += 8) {
       // A fragment: (row g, k t), (g + 8, t), (g, t + 4), (g + 8, t + 4) of m-tile mt
@@ -146,9 +145,6 @@ __global__ void __launch_bounds__(256, 3) bgemm_kernel(const GemmArgs g) {
         mma_tf32(acc[nt], ah[0], ah[1], ah[2], ah[3], bh0, bh1);
       }
     }
-    if (more) put(buf ^ 1, ra, rb);
-    __syncthreads();
-    buf ^= 1;
   }
   // accumulator nt: (row g, cols 2t, 2t + 1) and (row g + 8, same cols).  All
   // loads of the epilogue (row and column scales, C for beta) are issued before
@@ -1010,11 +1006,21 @@ bool gemm(cudaStream_t s, int64_t nb, int M, int N, int Kd, float alpha, const f
           bool tA, const float* B, int64_t sB, int ldb, bool tB, float beta, float* C, int64_t sC, int ldc,
           int exact = 0, const float* rs = nullptr, int64_t sR = 0, const float* cs = nullptr, int64_t sCs = 0) {
   GemmArgs g{A, B, C, rs, sA, sB, sC, sR, lda, ldb, ldc, M, N, Kd, tA, tB, alpha, beta, exact, cs, sCs};
+  // dynamic shared memory above 48 KB (set on every call: the attribute is
+  // cheap and the caller's device may change between calls)
+  const auto set = [](const void* f) {
+    return cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem) == cudaSuccess;
+  };
+  const void* kf = tA ? (tB ? reinterpret_cast<const void*>(bgemm_kernel<true, true>)
+                            : reinterpret_cast<const void*>(bgemm_kernel<true, false>))
+                      : (tB ? reinterpret_cast<const void*>(bgemm_kernel<false, true>)
+                            : reinterpret_cast<const void*>(bgemm_kernel<false, false>));
+  if (!set(kf)) return false;
   const dim3 grid(N / 64, M / 64, (unsigned)nb);
   if (tA)
-    tB ? bgemm_kernel<true, true><<<grid, 256, 0, s>>>(g) : bgemm_kernel<true, false><<<grid, 256, 0, s>>>(g);
+    tB ? bgemm_kernel<true, true><<<grid, 256, kGemmSmem, s>>>(g) : bgemm_kernel<true, false><<<grid, 256, kGemmSmem, s>>>(g);
   else
-    tB ? bgemm_kernel<false, true><<<grid, 256, 0, s>>>(g) : bgemm_kernel<false, false><<<grid, 256, 0, s>>>(g);
+    tB ? bgemm_kernel<false, true><<<grid, 256, kGemmSmem, s>>>(g) : bgemm_kernel<false, false><<<grid, 256, kGemmSmem, s>>>(g);
   return cudaGetLastError() == cudaSuccess;
 }
 
