@@ -86,7 +86,7 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
 constexpr int kGemmStages = 3, kGemmBuf = 64 * 36;
 constexpr int kGemmSmem = 2 * kGemmStages * kGemmBuf * 4;
 template <bool TA, bool TB>
-__global__ void __launch_bounds__(256, 3) bgemm_kernel(const GemmArgs g) {
+__global__ void __launch_bounds__(256, 4) bgemm_kernel(const GemmArgs g) {
   constexpr int kT = 32, kBuf = kGemmBuf;
   constexpr int sAm = TA ? 1 : 36, sAk = TA ? 72 : 1;   // A(m, k) at As[m sAm + k sAk]
   constexpr int sBk = TB ? 1 : 36 * 2, sBn = TB ? 36 : 1;
