@@ -121,3 +121,27 @@ def test_bwd_malformed_cu_seqlens(gdn):
     bad = torch.tensor([0, 10, 70, 60], dtype=torch.int32, device="cuda")
     r = gdn.gdn_chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], torch.zeros_like(x["v"]), cu_seqlens=bad)
     assert gdn.gdn_chunk_bwd_get_device_status(r["workspace"]) == gdn.DEV_BAD_CU_SEQLENS
+
+
+@pytest.mark.parametrize("B,chains", [(1, [(0, 0), (0, 31)]), (16, [(0, 5), (7, 12), (15, 31)])])
+def test_bwd_fullsize_sampled_chains(gdn, oracle_mod, B, chains):
+    # the bench's shape at full length (8192 tokens, 128 chunks a chain, H = 32;
+    # B = 16 runs in sequence groups, the last holding one sequence): sampled
+    # (sequence, head) chains against the oracle run on each chain alone (with
+    # Hqk = Hv every gradient of head h depends on chain (n, h) only)
+    w = I.WORKLOADS[2].with_(B=B)
+    x = I.make_inputs(w, "cuda")
+    gen = torch.Generator(device="cuda").manual_seed(13)
+    do = torch.randn(x["v"].shape, generator=gen, device="cuda").to(x["v"].dtype)
+    dht = torch.randn((B, w.Hv, w.K, w.V), generator=gen, device="cuda")
+    r = gdn.gdn_chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], do, scale=x["scale"], h0=x["h0"], dht=dht)
+    assert gdn.gdn_chunk_bwd_get_device_status(r["workspace"]) == gdn.DEV_OK
+    for n, h in chains:
+        sl = lambda t: t[n:n + 1, :, h:h + 1].cpu()
+        ref = oracle_mod.recurrent_bwd(sl(x["q"]), sl(x["k"]), sl(x["v"]), sl(x["g"]), sl(x["beta"]), x["scale"],
+                                       sl(do), h0=x["h0"][n:n + 1, h:h + 1].cpu(), dht=dht[n:n + 1, h:h + 1].cpu())
+        for key in ("dq", "dk", "dv", "dg", "dbeta"):
+            got = sl(r[key]).numpy()
+            assert rel_fro(got, ref[key]) <= TOL, (n, h, key, rel_fro(got, ref[key]))
+        got = r["dh0"][n:n + 1, h:h + 1].cpu().numpy()
+        assert rel_fro(got, ref["dh0"]) <= TOL, (n, h, "dh0", rel_fro(got, ref["dh0"]))
