@@ -145,3 +145,33 @@ def test_bwd_fullsize_sampled_chains(gdn, oracle_mod, B, chains):
             assert rel_fro(got, ref[key]) <= TOL, (n, h, key, rel_fro(got, ref[key]))
         got = r["dh0"][n:n + 1, h:h + 1].cpu().numpy()
         assert rel_fro(got, ref["dh0"]) <= TOL, (n, h, "dh0", rel_fro(got, ref["dh0"]))
+
+
+def test_bwd_fullsize_packed_sampled(gdn, oracle_mod):
+    # the 64-sequence packed batch (51 606 tokens, Hqk = 16, Hv = 32) on the
+    # chunked form with device-built tables: the longest sequence and one of
+    # the shortest against the oracle, each with the G value heads of one q/k
+    # head (dq and dk sum over them)
+    w = I.WORKLOADS[3]
+    x = I.make_inputs(w, "cuda")
+    N, G = x["N"], w.Hv // w.Hqk
+    cu = x["cu_seqlens"].cpu().tolist()
+    lens = [cu[i + 1] - cu[i] for i in range(N)]
+    gen = torch.Generator(device="cuda").manual_seed(17)
+    do = torch.randn(x["v"].shape, generator=gen, device="cuda").to(x["v"].dtype)
+    dht = torch.randn((N, w.Hv, w.K, w.V), generator=gen, device="cuda")
+    r = gdn.gdn_chunk_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], do, scale=x["scale"], h0=x["h0"], dht=dht,
+                          cu_seqlens=x["cu_seqlens"])
+    assert gdn.gdn_chunk_bwd_get_device_status(r["workspace"]) == gdn.DEV_OK
+    longest = max(range(N), key=lambda i: lens[i])
+    shortest = min((i for i in range(N) if lens[i] > 0), key=lambda i: lens[i])
+    for n, hq in ((longest, 3), (shortest, 15)):
+        a, e, hv = cu[n], cu[n + 1], slice(G * hq, G * hq + G)
+        sq = lambda t: t[:, a:e, hq:hq + 1].cpu()
+        sv = lambda t: t[:, a:e, hv].cpu()
+        ref = oracle_mod.recurrent_bwd(sq(x["q"]), sq(x["k"]), sv(x["v"]), sv(x["g"]), sv(x["beta"]), x["scale"],
+                                       sv(do), h0=x["h0"][n:n + 1, hv].cpu(), dht=dht[n:n + 1, hv].cpu())
+        got = {"dq": sq(r["dq"]), "dk": sq(r["dk"]), "dv": sv(r["dv"]), "dg": sv(r["dg"]), "dbeta": sv(r["dbeta"]),
+               "dh0": r["dh0"][n:n + 1, hv].cpu()}
+        for key, val in got.items():
+            assert rel_fro(val.numpy(), ref[key]) <= TOL, (n, lens[n], key, rel_fro(val.numpy(), ref[key]))
