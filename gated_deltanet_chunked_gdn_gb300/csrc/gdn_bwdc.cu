@@ -419,9 +419,11 @@ __device__ __forceinline__ void prefetch_rows(const float* src, int64_t ld, int 
 }
 
 // The serial passes run their two products per chunk on the same three-term
-// tf32 MMAs.  Operands that sit in shared memory are stored as separate hi and
-// lo arrays in the order of the MMA fragments, so that a lane reads its four
-// values of a k-step with one 16-byte load.
+// tf32 MMAs.  Operands that sit in shared memory are stored in fp32, in the
+// order of the MMA fragments, so that a lane reads its four values of a
+// k-step with one 16-byte load; every warp splits what it reads into hi and lo
+// (a few integer and FMA operations, where shared-memory reads are the scarce
+// resource: the V' product's warps all read the whole state slice).
 // A [128][16] slice X (the state, or G) as the A operand of X^T R^T: k-step
 // ks = 2 kk + p covers rows d = 16 kk + 4 t + 2 p (fragment column t) and
 // d + 1 (column t + 4), fragment row g = column c % 8, c / 8 = the lower or
@@ -455,19 +457,19 @@ __device__ __forceinline__ int vf_chunk(int ks, int lane) {
 constexpr int kXF = kDh * kSl;   // floats of one XF array
 constexpr int kVF = kC * kSl;    // floats of one VF array
 
-__device__ __forceinline__ void put_split(float* hi, float* lo, int at, float x) {
-  uint32_t h, l;
-  split_tf32(x, h, l);
-  hi[at] = __uint_as_float(h);
-  lo[at] = __uint_as_float(l);
+// hi and lo parts of a 16-byte fragment load
+__device__ __forceinline__ void split4(const float4& x, uint4& hi, uint4& lo) {
+  split_tf32(x.x, hi.x, lo.x);
+  split_tf32(x.y, hi.y, lo.y);
+  split_tf32(x.z, hi.z, lo.z);
+  split_tf32(x.w, hi.w, lo.w);
 }
 
 // out = (R X)[i][c] at i = 8 w + 2 t (+1), c = g (+8): out[0] = (i, c),
 // out[1] = (i + 1, c), out[2] = (i, c + 8), out[3] = (i + 1, c + 8).  The warp
 // computes n-tile w of X^T R^T over 16 k-steps; r[kk] holds R[8 w + g][16 kk + 4 t .. + 3].
 template <bool REXACT>   // R exact in tf32: its lo term is dropped
-__device__ __forceinline__ void row_product(const float4 (&r)[8], const float* xh, const float* xl, int lane,
-                                            float (&out)[4]) {
+__device__ __forceinline__ void row_product(const float4 (&r)[8], const float* xs, int lane, float (&out)[4]) {
   // four independent accumulators (even / odd k-steps x main / correction
   // terms) keep the MMA dependency chains short
   float acc[4][4] = {};
@@ -480,8 +482,8 @@ __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* x
       uint32_t bh0, bl0, bh1, bl1;
       split_tf32(rv[2 * p], bh0, bl0);
       split_tf32(rv[2 * p + 1], bh1, bl1);
-      const uint4 ah = *reinterpret_cast<const uint4*>(xh + (xf_chunk(ks, lane) << 2));
-      const uint4 al = *reinterpret_cast<const uint4*>(xl + (xf_chunk(ks, lane) << 2));
+      uint4 ah, al;
+      split4(*reinterpret_cast<const float4*>(xs + (xf_chunk(ks, lane) << 2)), ah, al);
       mma_tf32(acc[2 * p + 1], al.x, al.y, al.z, al.w, bh0, bh1);
       if (!REXACT) mma_tf32(acc[2 * p + 1], ah.x, ah.y, ah.z, ah.w, bl0, bl1);
       mma_tf32(acc[2 * p], ah.x, ah.y, ah.z, ah.w, bh0, bh1);
@@ -495,16 +497,16 @@ __device__ __forceinline__ void row_product(const float4 (&r)[8], const float* x
 // (+1) (the C fragments of m-tile w); col[4 ks + r] holds Col[8 ks + t (+4 for
 // r >= 2)][16 w + g (+8 for odd r)].
 template <bool CEXACT>   // Col exact in tf32: its lo term is dropped
-__device__ __forceinline__ void col_product(float (&st)[2][4], const float (&col)[32], const float* vh,
-                                            const float* vl, int lane, float sign) {
+__device__ __forceinline__ void col_product(float (&st)[2][4], const float (&col)[32], const float* vs, int lane,
+                                            float sign) {
   float cor[2][4] = {};   // the correction terms, in their own accumulators
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     uint32_t ah[4], al[4];
 #pragma unroll
     for (int r = 0; r < 4; ++r) split_tf32(sign * col[4 * ks + r], ah[r], al[r]);
-    const uint4 bh = *reinterpret_cast<const uint4*>(vh + (vf_chunk(ks, lane) << 2));
-    const uint4 bl = *reinterpret_cast<const uint4*>(vl + (vf_chunk(ks, lane) << 2));
+    uint4 bh, bl;
+    split4(*reinterpret_cast<const float4*>(vs + (vf_chunk(ks, lane) << 2)), bh, bl);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const uint32_t h0 = nt ? bh.z : bh.x, h1 = nt ? bh.w : bh.y;
@@ -536,7 +538,7 @@ __device__ __forceinline__ float4 ldg4(const float* p) { return __ldg(reinterpre
 // tf32).  Grid (N Hv, 8), 256 threads.
 template <bool KEXACT>
 __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const float* h0, int NC) {
-  __shared__ __align__(16) float xh[kXF], xl[kXF], vh[kVF], vl[kVF];
+  __shared__ __align__(16) float xs[kXF], vs[kVF];
   const int64_t chain = blockIdx.x;
   int64_t b0 = chain * NC;
   int nc = NC;
@@ -556,7 +558,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
     for (int r = 0; r < 4; ++r) {
       const int d = st_row(w, g, r), c = st_col(t, nt, r);
       st[nt][r] = h0 ? h0[(chain * kDh + d) * kDh + e0 + c] : 0.f;   // h0 may be 4-byte aligned only
-      put_split(xh, xl, xf_index(d, c), st[nt][r]);
+      xs[xf_index(d, c)] = st[nt][r];
     }
   auto put_s0 = [&](int64_t b) {
 #pragma unroll
@@ -602,16 +604,16 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
     {
       // V' = U - W S0 at rows i0, i0 + 1 and columns g, g + 8
       float o[4];
-      row_product<false>(wr, xh, xl, lane, o);
+      row_product<false>(wr, xs, lane, o);
       const float v[4] = {ur[0] - o[0], ur[1] - o[1], ur[2] - o[2], ur[3] - o[3]};
       const float d0 = dr[0], d1 = dr[1];
       if (c + 1 < nc) load_r(b + 1);
       float* vp = L.Vp + (b * kC + i0) * kDh + e0 + g;
       vp[0] = v[0], vp[kDh] = v[1], vp[8] = v[2], vp[kDh + 8] = v[3];
-      put_split(vh, vl, vf_index(i0, g), d0 * v[0]);
-      put_split(vh, vl, vf_index(i0 + 1, g), d1 * v[1]);
-      put_split(vh, vl, vf_index(i0, g + 8), d0 * v[2]);
-      put_split(vh, vl, vf_index(i0 + 1, g + 8), d1 * v[3]);
+      vs[vf_index(i0, g)] = d0 * v[0];
+      vs[vf_index(i0 + 1, g)] = d1 * v[1];
+      vs[vf_index(i0, g + 8)] = d0 * v[2];
+      vs[vf_index(i0 + 1, g + 8)] = d1 * v[3];
     }
     __syncthreads();
     {
@@ -620,14 +622,14 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) st[nt][r] *= el;
-      col_product<KEXACT>(st, kc, vh, vl, lane, 1.f);
+      col_product<KEXACT>(st, kc, vs, lane, 1.f);
       if (c + 1 < nc) {
         load_c(b + 1);
         put_s0(b + 1);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) put_split(xh, xl, xf_index(st_row(w, g, r), st_col(t, nt, r)), st[nt][r]);
+          for (int r = 0; r < 4; ++r) xs[xf_index(st_row(w, g, r), st_col(t, nt, r))] = st[nt][r];
       }
     }
     __syncthreads();
@@ -642,7 +644,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_fwd_states(const Lay L, const flo
 // (N Hv, 8), 256 threads.
 template <bool KEXACT>
 __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht, float* dh0, int NC) {
-  __shared__ __align__(16) float xh[kXF], xl[kXF], vh[kVF], vl[kVF];
+  __shared__ __align__(16) float xs[kXF], vs[kVF];
   const int64_t chain = blockIdx.x;
   int64_t b0 = chain * NC;
   int nc = NC;
@@ -670,7 +672,7 @@ __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht
     for (int r = 0; r < 4; ++r) {
       const int d = st_row(w, g, r), cc = st_col(t, nt, r);
       st[nt][r] = dht ? dht[(chain * kDh + d) * kDh + e0 + cc] : 0.f;   // dht may be 4-byte aligned only
-      put_split(xh, xl, xf_index(d, cc), st[nt][r]);
+      xs[xf_index(d, cc)] = st[nt][r];
     }
   auto put_g = [&](int64_t b) {
 #pragma unroll
@@ -725,16 +727,16 @@ __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht
       // dV' = D (K G) + X at rows i0, i0 + 1 and columns g, g + 8 (X was read
       // by this lane from the places dV' now overwrites)
       float o[4];
-      row_product<KEXACT>(kr, xh, xl, lane, o);
+      row_product<KEXACT>(kr, xs, lane, o);
       const float v[4] = {fmaf(dr[0], o[0], xr[0]), fmaf(dr[1], o[1], xr[1]), fmaf(dr[0], o[2], xr[2]),
                           fmaf(dr[1], o[3], xr[3])};
       if (c > 0) load_r(b - 1);
       float* vp = L.dVp + (b * kC + i0) * kDh + e0 + g;
       vp[0] = v[0], vp[kDh] = v[1], vp[8] = v[2], vp[kDh + 8] = v[3];
-      put_split(vh, vl, vf_index(i0, g), v[0]);
-      put_split(vh, vl, vf_index(i0 + 1, g), v[1]);
-      put_split(vh, vl, vf_index(i0, g + 8), v[2]);
-      put_split(vh, vl, vf_index(i0 + 1, g + 8), v[3]);
+      vs[vf_index(i0, g)] = v[0];
+      vs[vf_index(i0 + 1, g)] = v[1];
+      vs[vf_index(i0, g + 8)] = v[2];
+      vs[vf_index(i0 + 1, g + 8)] = v[3];
     }
     __syncthreads();
     {
@@ -743,14 +745,14 @@ __global__ void __launch_bounds__(256, 2) bwdc_rev(const Lay L, const float* dht
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int r = 0; r < 4; ++r) st[nt][r] = fmaf(el, st[nt][r], hr[nt][r]);
-      col_product<false>(st, wc, vh, vl, lane, -1.f);
+      col_product<false>(st, wc, vs, lane, -1.f);
       if (c > 0) {
         load_c(b - 1);
         put_g(b - 1);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) put_split(xh, xl, xf_index(st_row(w, g, r), st_col(t, nt, r)), st[nt][r]);
+          for (int r = 0; r < 4; ++r) xs[xf_index(st_row(w, g, r), st_col(t, nt, r))] = st[nt][r];
       } else if (dh0) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
