@@ -757,7 +757,6 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         continue;
       }
       wait_commit(bar_mma, ph_mma, mma_pending);   // S^T Q^T (committed in M3)
-      wait_commit(bar_q, ph_q, q_pending);         // V'^T P^T
       if (!sync_ok()) break;
 
       // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
@@ -770,11 +769,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
         const bool odd = lane & 1;
         uint8_t* lbase = sm + OFF_OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
         const uint32_t xsw = (static_cast<uint32_t>((ecol >> 3) ^ (odd ? 1 : 0))) << 4;
-#pragma unroll 1
+        // OQ while V'^T P^T is still in the tensor pipe, then OP
+        float oq[2][16];
+        tmem_ld16(R_a + lane_off + 32 * hf, oq[0]);
+        tmem_ld16(R_a + lane_off + 32 * hf + 16, oq[1]);
+        wait_commit(bar_q, ph_q, q_pending);   // V'^T P^T
+        tc_fence_after();
+#pragma unroll
         for (int q = 0; q < 2; ++q) {
-          float a[16], b[16];
+          float b[16];
+          const float* a = oq[q];
           const uint32_t col = 32 * hf + 16 * q;
-          tmem_ld16(R_a + lane_off + col, a);
           tmem_ld16(R_b + lane_off + col, b);
           float e[16];
 #pragma unroll
