@@ -273,31 +273,66 @@ const char* gdn_version(void) { return "gdn 0.1 sm_103a"; }
 // implicit device-wide synchronisation of cudaMalloc/cudaFree between its
 // launches.  For them the staged forward pass runs with its intermediates in
 // one file-scope device array, kStaticScratchBytes (32 MiB) per GPU, which
-// every GPU that loads this library holds until the process exits.
+// every GPU that loads this library holds until the process exits.  The first
+// kAlign bytes of the array hold the status word of the last call (copied
+// there from the staged workspace, which starts right after it), so that
+// gdn_chunk_fwd_noalloc_get_device_status can read it without the problem.
+#include <cudaTypedefs.h>
 #include <mutex>
 
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(32) << 20;
+constexpr size_t kStaticStagedBytes = kStaticScratchBytes - kAlign;   // after the status slot
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
 std::mutex g_static_mu;
 void* g_static_ptr[kMaxDevices] = {};
+unsigned long long g_static_ctx[kMaxDevices] = {};   // context the cached address belongs to
+
+// Unique id of the current CUDA context (0 when the driver cannot tell), through
+// the driver entry points that the runtime hands out.
+unsigned long long current_context_id() {
+  static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_cur || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_cur(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
 
 // Device address of g_static_scratch on the current device.  The host-side
-// name of the array is only a stand-in, so the address is fetched once per
-// device with cudaGetSymbolAddress (with that device current) and cached.
+// name of the array is only a stand-in, so the address is fetched with
+// cudaGetSymbolAddress (with that device current) once per device and
+// context, and cached: a device reset that replaces the context makes the
+// next call look the address up again.
 gdn_status static_scratch(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return GDN_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return GDN_ERR_UNSUPPORTED;
+  // 0 before the runtime has made the device's context current: then the
+  // look-up below creates it, and the id is read again afterwards
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_static_mu);
-  if (!g_static_ptr[dev]) {
+  if (!g_static_ptr[dev] || ctx == 0 || g_static_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
     g_static_ptr[dev] = p;
+    g_static_ctx[dev] = current_context_id();
   }
   *out = g_static_ptr[dev];
   return GDN_OK;

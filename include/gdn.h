@@ -220,20 +220,28 @@ gdn_status gdn_selftest_umma(int variant, const void* A, const void* B, float* D
  *   Arguments as gdn_chunk_fwd (the caller still passes inputs and outputs).
  *   Returns GDN_ERR_SCRATCH_LIMIT, launching nothing, when the problem's
  *   staged workspace (gdn_chunk_fwd_workspace_size with GDN_PATH_STAGED)
- *   exceeds 32 MiB.
- *   The first call on a device looks up the array's device address with
- *   cudaGetSymbolAddress (with that device current); make that first call
+ *   exceeds 32 MiB - 256 bytes (the array's first 256 bytes hold the status
+ *   word).
+ *   The first call on a device (and the first after a device reset replaced
+ *   its context) looks up the array's device address with
+ *   cudaGetSymbolAddress, with that device current; make that first call
  *   before any stream capture.
  *   All calls share the one array: calls whose executions overlap on the GPU
  *   (other streams, other host threads) race on it and must be serialised by
- *   the caller.  The device status word lives in the array too and is not
- *   exposed.
+ *   the caller.
+ *   Errors found on the device (malformed cu_seqlens) leave o and ht
+ *   incomplete and are recorded in the array's status word, which
+ *   gdn_chunk_fwd_noalloc_get_device_status reads: it waits for `stream`,
+ *   then returns the status (GDN_DEV_*) of the last gdn_chunk_fwd_noalloc call
+ *   on the current device in *dev_status and clears it.  It allocates
+ *   nothing either.
  */
 gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* p,
                                  const void* q, const void* k, const void* v,
                                  const float* g, const float* beta, float scale,
                                  const float* h0, const int32_t* cu_seqlens,
                                  void* o, float* ht, void* stream);
+gdn_status gdn_chunk_fwd_noalloc_get_device_status(void* stream, int* dev_status);
 
 /*
  * Fused recurrent (decode) step with sigmoid gating (TileLang x xLLM page,
