@@ -154,6 +154,20 @@ gdn_status gdn_get_device_status(const gdn_problem* pp, gdn_path path, void* wor
   return GDN_OK;
 }
 
+gdn_status gdn_selftest_handover_timeout(const gdn_problem* pp, const void* q, const void* k, const void* v,
+                                         const float* g, const float* beta, float scale, const float* h0, void* o,
+                                         float* ht, void* workspace, size_t workspace_bytes, int drop_window,
+                                         long long wait_ns, void* stream) {
+  gdn_problem p;
+  if (!problem_ok(pp, &p) || p.varlen || wait_ns <= 0) return GDN_ERR_INVALID_ARG;
+  if (!fused_handover_window(p, drop_window)) return GDN_ERR_UNSUPPORTED;
+  gdn_status st = check_call(p, q, k, v, g, beta, h0, nullptr, o, ht, workspace, workspace_bytes,
+                             workspace_for(p, GDN_PATH_FUSED));
+  if (st != GDN_OK) return st;
+  return run_fused(p, q, k, v, g, beta, scale, h0, nullptr, o, ht, workspace, static_cast<cudaStream_t>(stream),
+                   drop_window, static_cast<unsigned long long>(wait_ns));
+}
+
 gdn_status gdn_recurrent_fwd(const gdn_problem* pp, const void* q, const void* k, const void* v, const float* a,
                              const float* b, const float* A_log, const float* dt_bias, float scale, float* state,
                              const int32_t* state_indices, int state_slots, const int32_t* cu_seqlens, void* o,
@@ -346,14 +360,35 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* pp, const void* q
   gdn_problem p;
   if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
   const size_t need = workspace_for(p, GDN_PATH_STAGED);
-  if (need > kStaticScratchBytes) return GDN_ERR_SCRATCH_LIMIT;
+  if (need > kStaticStagedBytes) return GDN_ERR_SCRATCH_LIMIT;
   void* scratch = nullptr;
   gdn_status st = static_scratch(&scratch);
   if (st != GDN_OK) return st;
-  st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, scratch, kStaticScratchBytes, need);
+  uint8_t* ws = static_cast<uint8_t*>(scratch) + kAlign;
+  st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, ws, kStaticStagedBytes, need);
   if (st != GDN_OK) return st;
   // run_staged clears the status word it uses; every other intermediate is
   // rewritten before it is read, so stale contents of earlier calls are harmless.
-  return run_staged(p, 6, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, scratch,
-                    static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = run_staged(p, 6, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, ws, s);
+  if (st != GDN_OK) return st;
+  // the call's status word goes to the fixed slot at the array's start
+  gdn_staged_layout_t L;
+  staged_layout(p, &L);
+  if (cudaMemcpyAsync(scratch, ws + L.status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
+}
+
+extern "C" gdn_status gdn_chunk_fwd_noalloc_get_device_status(void* stream, int* dev_status) {
+  if (!dev_status) return GDN_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  gdn_status st = static_scratch(&scratch);
+  if (st != GDN_OK) return st;
+  int32_t host = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemcpy(&host, scratch, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemset(scratch, 0, sizeof(int32_t)) != cudaSuccess) return GDN_ERR_CUDA;
+  *dev_status = host;
+  return GDN_OK;
 }

@@ -58,7 +58,8 @@ struct GemmArgs {
 
 // x = hi + lo, hi = x cut to its top 10 mantissa bits (exact tf32), lo = x - hi
 // (exact in fp32); the three-term products hi hi + hi lo + lo hi leave about
-// 2^-19 of each product (the lo lo term and the unit's truncation of lo).
+// 2^-19 of each product (the lo lo term and the unit's truncation of lo, whose
+// low 13 bits it ignores).
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
   hi = __float_as_uint(x) & 0xffffe000u;
   lo = __float_as_uint(x - __uint_as_float(hi));

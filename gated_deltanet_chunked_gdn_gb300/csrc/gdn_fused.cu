@@ -103,6 +103,10 @@ struct FusedParams {
   int* sched;
   float* hand;
   int nwin, W;
+  // limit of the wait for a hand-over flag, and a window whose flag is never
+  // raised (-1: none; a test hook that makes one wait run out)
+  unsigned long long wait_ns;
+  int drop_flag;
 };
 
 // Kernel modes: the full forward pass, or final states only (no q, no o).
@@ -126,6 +130,9 @@ constexpr int kStates = 1;
 //     relative per operand); measured end to end against the fp64 oracle,
 //     this leaves the error of o and ht where rounding to tf32 puts it, far
 //     below the bf16 rounding T receives as an MMA operand afterwards.
+//     Rounding the operands first (cvt.rna, or an integer round-half-away of
+//     the bit pattern) lengthens this serial phase enough to cost 7 % (3 %)
+//     of the whole step at 16 x 8192, 32 heads.
 
 // d[16x8] += A[16 x KK] B[KK x 8]; A(r, c) = A[r * lda + c], B(r, c) = B[r * ldb + c]
 // (shared memory).  A's fragments come from one ldmatrix.x4 per k-step (four
@@ -460,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       break;
     }
     if (from_hand) {
-      if (tid == 0 && !flag_wait(hflag + win + 1, prm.status)) flags[1] = 1;
+      if (tid == 0 && !flag_wait(hflag + win + 1, prm.status, prm.wait_ns)) flags[1] = 1;
       __syncthreads();
       if (flags[1]) break;
     }
@@ -842,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
       __syncthreads();
       if (tid == 0) {
         __threadfence();
-        atomicExch(hflag + win, 1);
+        if (win != prm.drop_flag) atomicExch(hflag + win, 1);
       }
     }
   }   // pieces
@@ -922,7 +929,7 @@ size_t fused_status_offset(const gdn_problem&) { return 0; }
 gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const void* k, const void* v, const float* g,
                         const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
                         float* ht2, int32_t* status, cudaStream_t s, int* sched, float* hand, int64_t nwin,
-                        int64_t W) {
+                        int64_t W, int drop_flag, unsigned long long wait_ns) {
   const int64_t Ttot = (int64_t)p.B * p.T;
   CUtensorMap tq, tk, tv, to;
   memset(&to, 0, sizeof(to));
@@ -962,6 +969,8 @@ gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const voi
   prm.hand = hand;
   prm.nwin = (int)nwin;
   prm.W = (int)W;
+  prm.wait_ns = wait_ns;
+  prm.drop_flag = drop_flag;
   const unsigned chains = (unsigned)((int64_t)p.N * p.Hv);
   auto kernel = mode == kStates ? gdn_fused_kernel<kStates, false>
                : (prm.sched ? gdn_fused_kernel<kFull, true> : gdn_fused_kernel<kFull, false>);
@@ -974,7 +983,7 @@ gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const voi
 
 gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
                      const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
-                     void* ws, cudaStream_t s) {
+                     void* ws, cudaStream_t s, int drop_flag, unsigned long long wait_ns) {
   if (!fused_supported(p)) return GDN_ERR_UNSUPPORTED;
   int32_t* status = static_cast<int32_t*>(ws);
   const Windows w = fused_windows(p);
@@ -993,7 +1002,16 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
   if (!w.handover()) return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s);
   float* hand = cuts_chains(p, w) ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sched_bytes(w)) : nullptr;
   return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s, status + 1, hand, w.nwin,
-                      w.W);
+                      w.W, drop_flag, wait_ns);
+}
+
+bool fused_handover_window(const gdn_problem& p, int window) {
+  if (!fused_supported(p)) return false;
+  const Windows w = fused_windows(p);
+  if (!cuts_chains(p, w) || window < 1 || window >= w.nwin) return false;
+  // window - 1 ends with the suffix of a chain whose prefix `window` runs
+  const int64_t nch = ((int64_t)p.T + kChunk - 1) / kChunk;
+  return ((int64_t)window * w.W) % nch != 0;
 }
 
 gdn_status run_fused_states(const gdn_problem& p, const void* k, const void* v, const float* g, const float* beta,

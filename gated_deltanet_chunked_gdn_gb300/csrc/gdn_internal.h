@@ -81,9 +81,16 @@ gdn_status run_recurrent(const gdn_problem& p, const void* q, const void* k, con
 bool fused_supported(const gdn_problem& p);
 size_t fused_workspace_bytes(const gdn_problem& p);
 size_t fused_status_offset(const gdn_problem& p);
+// drop_flag / wait_ns: test hook of the window schedule -- the hand-over flag
+// of window drop_flag is never raised, and a window waits at most wait_ns for
+// its flag (then records GDN_DEV_WAIT_TIMEOUT and stops).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
                      const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
-                     void* ws, cudaStream_t s);
+                     void* ws, cudaStream_t s, int drop_flag = -1, unsigned long long wait_ns = kWaitLimitNs);
+// True when the fused pass over p cuts a chain at the start of window
+// `window` (so window - 1 waits for the hand-over flag of `window`).
+bool fused_handover_window(const gdn_problem& p, int window);
 // States-only launch over the chains of p (p.varlen with cu): chains started
 // from a zero state write their final states to ht_zero, the same chains
 // started from the identity with v = 0 write their transition matrices to
@@ -124,7 +131,8 @@ bool cp_preferred(const gdn_problem& p);
 gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const void* k, const void* v, const float* g,
                         const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
                         float* ht2, int32_t* status, cudaStream_t s, int* sched = nullptr, float* hand = nullptr,
-                        int64_t nwin = 0, int64_t W = 0);
+                        int64_t nwin = 0, int64_t W = 0, int drop_flag = -1,
+                        unsigned long long wait_ns = kWaitLimitNs);
 // Streaming multiprocessors of the current device (148 when none can be queried).
 int sm_count();
 // Byte offset of the device status word inside a forward workspace for `path`

@@ -209,6 +209,29 @@ gdn_status gdn_selftest_umma(int variant, const void* A, const void* B, float* D
                              void* stream);
 
 /*
+ * Test hook of the fused path's bounded waits (no counterpart on the pages).
+ * Runs gdn_chunk_fwd(p, GDN_PATH_FUSED, ...) on an equal-length batch whose
+ * chains the fused kernel deals out as windows that hand a cut chain's state
+ * over from one CTA to another, except that window `drop_window` never raises
+ * its hand-over flag and every window waits at most `wait_ns` nanoseconds for
+ * the flag it needs.  Window drop_window - 1 therefore gives up: it records
+ * GDN_DEV_WAIT_TIMEOUT in the workspace's status word (read it with
+ * gdn_get_device_status, path GDN_PATH_FUSED) and stops, leaving the o rows
+ * and the final state of the chain it was waiting for unwritten; every other
+ * window completes and the launch ends.  The failure is made on purpose in a
+ * wait that has a limit: nothing faults and nothing hangs.
+ *   Arguments as gdn_chunk_fwd (no cu_seqlens).  Returns GDN_ERR_UNSUPPORTED
+ *   when the fused pass over p hands no chain over at the start of window
+ *   drop_window (then nothing is launched).
+ */
+gdn_status gdn_selftest_handover_timeout(const gdn_problem* p,
+                                         const void* q, const void* k, const void* v,
+                                         const float* g, const float* beta, float scale,
+                                         const float* h0, void* o, float* ht,
+                                         void* workspace, size_t workspace_bytes,
+                                         int drop_window, long long wait_ns, void* stream);
+
+/*
  * Forward pass for callers that cannot allocate device memory (no counterpart
  * on the pages).  Some callers cannot call cudaMalloc in their call path: an
  * op inside a host framework that owns every device buffer and passes the op
