@@ -294,6 +294,44 @@ def test_stage_intermediates(oracle_mod):
     assert np.all(st["W"][-1, tail:] == 0) and np.all(st["Vn"][-1, tail:] == 0)
 
 
+def test_stage_wy_terms_against_the_recurrence(oracle_mod):
+    """W, U and V' of every chunk, pinned by the token recurrence rather than
+    by their own formulas.  Unrolling S_t = e^{g_t} S_{t-1} + k_t d_t^T with
+    d_t = beta_t (v_t - e^{g_t} S_{t-1}^T k_t) over a chunk gives V' = U - W S0
+    with V'_t = d_t: so the dumped V' must equal d_t computed from the
+    recurrence's own states S_{t-1}, and U - W S0 must equal it for two
+    different initial states h0 (whose chunk-start states differ by a
+    full-rank K x V matrix, K <= V), which fixes W and U uniquely."""
+    rng = np.random.default_rng(37)
+    C, T, K, V, h = 16, 45, 6, 8, 1
+    q, k, v, g, beta, h0 = rand_inputs(rng, 1, T, 1, 2, K, V)
+
+    def run(init):
+        st = oracle_mod.chunked_stages(q, k, v, g, beta, 0.5, C, 0, h, h0=init)
+        d = np.zeros((T, V))
+        for t in range(T):
+            if t == 0:
+                S = init[0, h] if init is not None else np.zeros((K, V))
+            else:
+                _, ht = oracle_mod.recurrent(q[:, :t], k[:, :t], v[:, :t], g[:, :t], beta[:, :t], 0.5, h0=init)
+                S = ht[0, h]
+            d[t] = beta[0, t, h] * (v[0, t, h] - math.exp(g[0, t, h]) * (S.T @ k[0, t, 0]))
+        return st, d
+
+    a, da = run(h0)
+    b, db = run(None)
+    for c in range(a["gamma"].shape[0]):
+        n = min(C, T - c * C)
+        rows = slice(c * C, c * C + n)
+        for st, d in ((a, da), (b, db)):
+            assert rel_fro(st["Vn"][c, :n], d[rows]) < TOL
+            assert rel_fro(st["U"][c, :n] - st["W"][c, :n] @ st["S0"][c], d[rows]) < TOL
+        # the dumps of U and W do not depend on the initial state
+        np.testing.assert_array_equal(a["W"][c], b["W"][c])
+        np.testing.assert_array_equal(a["U"][c], b["U"][c])
+        assert np.linalg.matrix_rank(a["S0"][c] - b["S0"][c]) == K
+
+
 # -------------------------------------------------------- decode (gated) step
 
 def test_gated_decode_hand_example(oracle_mod):
