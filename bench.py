@@ -47,11 +47,18 @@ def peaks() -> dict:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def measured_traffic(op: str, units: float):
+def measured_traffic(op: str, units: float, fixed_bytes: float = 0.0):
     """DRAM bytes (read + write) per launch of op's kernels, from the committed
-    ncu summary table (profiles/traffic.json), scaled linearly from the
-    captured case to `units` (sequences, or pool entries for decode); None
-    when any of the kernels' sources changed since that capture."""
+    ncu summary table (profiles/traffic.json); None when any of the kernels'
+    sources changed since that capture.
+
+    One formula: traffic = fixed_bytes + (D - F) * units / U, where D is the
+    captured launch's DRAM bytes, U its size in units (sequences of 8192
+    tokens, or pool entries for decode) and F the bytes of that launch that do
+    not grow with its size (the record's ``fixed_bytes``: initial and final
+    states); fixed_bytes is the same for the bench's own launch.  A capture
+    taken at the bench's own size (units == U, F == fixed_bytes) is used as
+    it is."""
     import hashlib
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
@@ -62,7 +69,8 @@ def measured_traffic(op: str, units: float):
                     return None
     except (OSError, KeyError, ValueError):
         return None
-    return rec["dram_bytes_per_launch"] * units / rec["units"]
+    F = float(rec.get("fixed_bytes", 0.0))
+    return fixed_bytes + (rec["dram_bytes_per_launch"] - F) * units / rec["units"]
 
 
 def algorithmic(B, T, Hqk, Hv, K, V, C, elem=2, h0=True, N=None):
@@ -601,7 +609,13 @@ def main():
     e2e_value, _ = aggregate(time.perf_counter() - t0, tokens_step, args.e2e_steps, world, dev)
 
     pk = peaks()
-    nbytes, flops = algorithmic(Bx, Tx, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None, N=x["N"])
+    # the fused and chunk-parallel kernels run 64-token chunks whatever C the
+    # call asks for (the result does not depend on C): their FLOPs are counted
+    # at the chunk length they execute
+    C_exec = 64 if path in ("fused", "cp") else w.C
+    nbytes, flops = algorithmic(Bx, Tx, w.Hqk, w.Hv, w.K, w.V, C_exec, 2, h0=x["h0"] is not None, N=x["N"])
+    _, flops_req = algorithmic(Bx, Tx, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None, N=x["N"])
+    state_bytes = x["N"] * w.Hv * w.K * w.V * 4 * (2 if x["h0"] is not None else 1)
     t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
     t_tc = flops / (pk["bf16_tflops"] * 1e12)
     bound = "hbm" if t_hbm >= t_tc else "tensor"
@@ -617,16 +631,17 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wname, "B": Bx, "T": Tx, "N": x["N"], "Hqk": w.Hqk, "Hv": w.Hv,
-                   "K": w.K, "V": w.V, "C": w.C, "path": path, "parallelism": f"dp{world} (independent batches)",
+                   "K": w.K, "V": w.V, "C": w.C, "C_executed": C_exec, "path": path,
+                   "parallelism": f"dp{world} (independent batches)",
                    "l2": (f"inputs larger than L2 ({nbytes / 1e9:.2f} GB compulsory traffic per step)"
                           if flush is None else "L2 flushed (512 MB write) before every timed step")},
         "tflops_alg": flops / sec / 1e12,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": (measured_traffic("fused", w.B * w.T / 8192)
+                     "traffic": (measured_traffic("fused", w.B * w.T / 8192 * w.Hv / 32, state_bytes)
                                  if path == "fused" and args.workload == "batched_16x8192" else None), "peak_source": pk["source"],
                      "kernel": "gdn_fused_kernel (the step's only launch)" if path == "fused"
                      else "gdn_chunk_fwd call (all launches of one step)",
-                     "alg_bytes": nbytes, "alg_flops": flops,
+                     "alg_bytes": nbytes, "alg_flops": flops, "alg_flops_at_requested_C": flops_req,
                      "t_hbm_ms": 1e3 * t_hbm, "t_tensor_ms": 1e3 * t_tc},
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": args.e2e_steps, "call": f"gdn_chunk_fwd_host, {args.e2e_split} sub-batches"},
