@@ -477,10 +477,11 @@ def main():
     ap.add_argument("--T", type=int, default=8192,
                     help="sequence length override of the batched workload (profiling runs only; the metric is T=8192)")
     ap.add_argument("--workload", default="batched_16x8192",
-                    choices=["batched_16x8192", "gqa_prefill_1x4096", "long_1x32768", "varlen_64"],
+                    choices=["batched_16x8192", "gqa_prefill_1x4096", "long_1x32768", "varlen_64", "long_d256"],
                     help="chunk_fwd shape: the headline 16 x 8192 batch, one long GQA sequence (1 x 4096 or "
-                         "1 x 32768 tokens, 16 qk / 32 value heads), where AUTO takes the chunk-parallel path, or "
-                         "64 packed sequences of log-uniform lengths in [1, 16384] (16 qk / 32 value heads)")
+                         "1 x 32768 tokens, 16 qk / 32 value heads), where AUTO takes the chunk-parallel path, "
+                         "64 packed sequences of log-uniform lengths in [1, 16384] (16 qk / 32 value heads), or "
+                         "the large-head-dim prefill: 4 x 32768 tokens, 8 qk / 32 value heads, K = V = 256")
     ap.add_argument("--op", default="chunk_fwd", choices=["chunk_fwd", "conv1d", "decode", "bwd"],
                     help="chunk_fwd: the GDN chunked forward (the headline); conv1d / decode: the neighbouring "
                          "ops of the same layer, each with its own JSON line")
@@ -515,6 +516,9 @@ def main():
         wname = f"batched_{w.B}x{w.T}_H{args.H}"
     elif args.workload == "varlen_64":
         w = I.WORKLOADS[3].with_(seed=3 + rank)
+    elif args.workload == "long_d256":
+        w = I.WORKLOADS[4].with_(seed=4 + rank)
+        wname = f"long_d256_{w.B}x{w.T}_Hqk{w.Hqk}_Hv{w.Hv}"
     else:
         T = 4096 if args.workload == "gqa_prefill_1x4096" else 32768
         w = I.WORKLOADS[1].with_(T=T, seed=1 + rank)
@@ -622,8 +626,11 @@ def main():
     sec = ms_step / 1000.0
     if bound == "hbm":
         achieved, peak, unit = nbytes / sec / 1e9, pk["hbm_gbs"], "GB/s"
+        peak_kind = "HBM copy"
     else:
-        achieved, peak, unit = flops / sec / 1e12, pk["bf16_tflops"], "TFLOP/s"
+        # a tensor-bound step is one long launch: the sustained bf16 figure
+        achieved, peak, unit = flops / sec / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
+        peak_kind = "bf16 sustained"
     launches = {"staged": 7, "fused": 1, "cp": 4}[path]
     line = {
         "metric": METRIC if args.workload == "batched_16x8192" else f"GDN chunk-fwd tokens/s ({wname}, bf16); % roofline",
@@ -638,8 +645,12 @@ def main():
         "tflops_alg": flops / sec / 1e12,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": (measured_traffic("fused", w.B * w.T / 8192 * w.Hv / 32, state_bytes)
-                                 if path == "fused" and args.workload == "batched_16x8192" else None), "peak_source": pk["source"],
-                     "kernel": "gdn_fused_kernel (the step's only launch)" if path == "fused"
+                                 if path == "fused" and args.workload == "batched_16x8192" else
+                                 measured_traffic("fused256", w.B * w.T / 32768, state_bytes)
+                                 if path == "fused" and args.workload == "long_d256" else None),
+                     "peak_source": f"{pk['source']} ({peak_kind})",
+                     "kernel": (("gdn_fused256_kernel" if w.K == 256 else "gdn_fused_kernel") +
+                                " (the step's only launch)") if path == "fused"
                      else "gdn_chunk_fwd call (all launches of one step)",
                      "alg_bytes": nbytes, "alg_flops": flops, "alg_flops_at_requested_C": flops_req,
                      "t_hbm_ms": 1e3 * t_hbm, "t_tensor_ms": 1e3 * t_tc},

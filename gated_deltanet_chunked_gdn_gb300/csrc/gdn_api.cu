@@ -89,7 +89,8 @@ size_t gdn_chunk_fwd_workspace_size(const gdn_problem* pp, gdn_path path) {
   if (!problem_ok(pp, &p)) return 0;
   if (!path_ok(path)) return 0;
   path = resolve(p, path);
-  if ((path == GDN_PATH_FUSED || path == GDN_PATH_CP) && !fused_supported(p)) return 0;
+  if (path == GDN_PATH_FUSED && !fused_supported(p)) return 0;
+  if (path == GDN_PATH_CP && !fused128_supported(p)) return 0;
   return workspace_for(p, path);
 }
 
@@ -107,7 +108,8 @@ gdn_status gdn_chunk_fwd(const gdn_problem* pp, gdn_path path, const void* q, co
   if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
   if (!path_ok(path)) return GDN_ERR_INVALID_ARG;
   path = resolve(p, path);
-  if ((path == GDN_PATH_FUSED || path == GDN_PATH_CP) && !fused_supported(p)) return GDN_ERR_UNSUPPORTED;
+  if (path == GDN_PATH_FUSED && !fused_supported(p)) return GDN_ERR_UNSUPPORTED;
+  if (path == GDN_PATH_CP && !fused128_supported(p)) return GDN_ERR_UNSUPPORTED;
   gdn_status st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, workspace, workspace_bytes,
                              workspace_for(p, path));
   if (st != GDN_OK) return st;

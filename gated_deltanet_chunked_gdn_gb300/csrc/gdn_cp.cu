@@ -243,14 +243,14 @@ size_t cp_workspace_bytes(const gdn_problem& p) { return cp_layout(p, cp_segment
 bool cp_preferred(const gdn_problem& p) {
   const int64_t Ttot = (int64_t)p.B * p.T;
   const int64_t chains = (int64_t)p.N * p.Hv;
-  if (chains <= 0 || Ttot <= 0) return false;
+  if (chains <= 0 || Ttot <= 0 || !fused128_supported(p)) return false;
   return 2 * chains <= sm_count() && Ttot / p.N >= 2048;
 }
 
 gdn_status run_cp(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
                   const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht, void* ws,
                   size_t ws_bytes, cudaStream_t s) {
-  if (!fused_supported(p)) return GDN_ERR_UNSUPPORTED;
+  if (!fused128_supported(p)) return GDN_ERR_UNSUPPORTED;
   const int seg_len = cp_segment_length(p);
   const CpLayout L = cp_layout(p, seg_len);
   if (ws_bytes < L.total) return GDN_ERR_INVALID_ARG;

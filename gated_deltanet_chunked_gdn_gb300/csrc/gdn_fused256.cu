@@ -1,0 +1,757 @@
+// gdn_fused256.cu -- the fused path for head dimension K = 256 (V a multiple
+// of 128): the whole chunk pipeline (cumsum, scaled_dot_kkt, solve_tril,
+// wy_fast, chunk_h, chunk_o; MegaGDN-PTO walkthrough, sections 1.1 and 4.5) in
+// ONE sm_103a launch, as for K = V = 128, for the large-head-dim shapes the
+// pages specialise for (TileLang x xLLM page, the build-specialisation step:
+// H = 32 value heads on 8 qk groups, D = 256).
+//
+// A 256 x 256 fp32 state is the whole of an SM's tensor memory, so the value
+// dimension is cut into slices of 128 columns: a CTA owns one slice of one
+// (sequence, value head) chain -- its 256 x 128 fp32 state slice S^T[e][d]
+// lives in TMEM (256 of the 512 columns) for the whole chain -- and walks the
+// chain's 64-token chunks in order.  Everything of a chunk that does not depend
+// on V (K K^T, Q K^T, gating, the triangular solve, W) is recomputed by each
+// slice of a chain; v, U, V', o and the state are the slice's own.  One CTA per
+// SM (about 187 KB of shared memory, all 512 TMEM columns); equal-length
+// problems deal the (chain, slice) units' chunks out as windows of equal
+// length over the SMs, handing a cut unit's state slice over through the
+// workspace, exactly as the K = V = 128 kernel does.
+//
+// Products (M = 128 on the slice's value columns e, or on 128 key columns d,
+// or on the 64 k rows stacked over the 64 q rows):
+//
+//   M1  [K;Q] K^T                 -> R_A   (M128 N64, 16 k-steps over d)
+//   S1  A = strict-lower(beta_i e^{g_i - g_j} K K^T) -> smem fp32, P -> smem bf16
+//   S2  T = (I + A)^{-1}; T diag(beta), T diag(beta e^g) -> bf16
+//   M2  W^T = K^T (T diag(beta e^g))^T -> R_W (two M128 halves of d)
+//       U^T = V^T (T diag(beta))^T     -> R_B
+//   S4  S^T (fp32, TMEM) -> bf16 [e][d]; S^T *= e^{g_last}
+//   S3  W^T -> bf16 [d][i]
+//   M3  V'^T = U^T - S^T W^T -> R_B;  OQ^T = S^T Q^T -> R_A   (16 k-steps each)
+//   S5  V'^T -> bf16, V''^T = V'^T diag(e^{g_last - g}) -> bf16
+//   M4  OP^T = V'^T P^T -> R_B;  S^T += V''^T K (N = 256) -> R_S
+//   S6  o_i = scale e^{g_i} OQ_i + OP_i -> staging -> TMA store
+#include <string.h>
+
+#include "gdn_solve64.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace sm100;
+using namespace solve64;
+
+constexpr int kDK = 256;         // K
+constexpr int kVS = 128;         // value columns of one slice
+constexpr int kTmemCols = 512;
+
+// TMEM columns (lane = slice column e, key column d mod 128, or chunk row)
+constexpr uint32_t R_S = 0;      // S^T[e][d], d = 0..255
+constexpr uint32_t R_A = 256;    // [K;Q] K^T, then OQ^T[e][i]
+constexpr uint32_t R_W = 320;    // W^T[d][i]: d < 128 at 320, d >= 128 at 384
+constexpr uint32_t R_B = 448;    // U^T[e][i] -> V'^T -> OP^T
+
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_KQ = 0;          // 4 atom columns (d 64a..64a+63) of [k rows 0..63; q rows 64..127], 16 KB each
+constexpr uint32_t OFF_V = 65536;       // v slice rows 0..63 x 128 e, 2 atom columns of 8 KB
+constexpr uint32_t OFF_Y = 81920;       // T diag(beta) | T diag(beta e^g) (8 KB each), then W^T (32 KB), then V''^T
+constexpr uint32_t OFF_TB = OFF_Y;
+constexpr uint32_t OFF_TBE = OFF_Y + 8192;
+constexpr uint32_t OFF_W = OFF_Y;       // W^T bf16 [d][i], 256 rows of 128 B
+constexpr uint32_t OFF_VPP = OFF_Y;     // V''^T bf16 [e][j], 16 KB (W^T is dead once V' is complete)
+constexpr uint32_t OFF_P = 114688;      // P [i][j] bf16, 8 KB
+constexpr uint32_t OFF_X = 122880;      // 64 KB, reused: A/T fp32 + scratch | S^T bf16 | V'^T | o staging
+constexpr uint32_t OFF_AS = OFF_X;      // fp32 [64][68]
+constexpr uint32_t OFF_TMP = OFF_X + 64 * 68 * 4;
+constexpr uint32_t OFF_ST = OFF_X;      // S^T bf16 [e][d], 4 atom columns of 16 KB
+constexpr uint32_t OFF_VP = OFF_X;      // V'^T bf16 [e][j] (the S^T atom that M3 reads first)
+constexpr uint32_t OFF_OS = OFF_X;      // o staging bf16: 2 boxes [64 rows][64 e]
+constexpr uint32_t OFF_MISC = 188416;
+constexpr uint32_t OFF_GAM = OFF_MISC;
+constexpr uint32_t OFF_BET = OFF_MISC + 256;
+constexpr uint32_t OFF_BE = OFF_MISC + 512;
+constexpr uint32_t OFF_DL = OFF_MISC + 768;
+constexpr uint32_t OFF_EG = OFF_MISC + 1024;
+constexpr uint32_t OFF_BAR = OFF_MISC + 1280;    // 6 mbarriers: k/q, v, three MMA commit groups, first quarter of OQ
+constexpr uint32_t OFF_FLAGS = OFF_MISC + 1328;  // [0] tmem base, [1] abort, [2] window
+constexpr uint32_t OFF_GRAW = OFF_MISC + 1344;   // float[2][2][64]: raw g, beta of two chunks
+constexpr uint32_t kSmemUsed = OFF_MISC + 2368;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
+
+static_assert(OFF_TMP + 32 * 40 * 4 <= OFF_X + 65536, "solve scratch overflows region X");
+static_assert(kSmemBytes <= 232448, "one CTA must fit an SM");
+static_assert(OFF_X % 1024 == 0 && OFF_Y % 1024 == 0 && OFF_P % 1024 == 0 && OFF_V % 1024 == 0, "atom alignment");
+
+struct Params {
+  const float* g;
+  const float* beta;
+  const float* h0;
+  const int32_t* cu;
+  __nv_bfloat16* o;
+  float* ht;
+  int32_t* status;
+  int N, Tseq, Ttot, Hqk, Hv, V, NS, varlen;   // NS = V / kVS slices per chain
+  float scale;
+  // window schedule over (chain, slice) units (null sched: one unit per CTA);
+  // the same dealing as the K = V = 128 kernel, with units in place of chains
+  int* sched;
+  float* hand;   // nwin slots of kDK x kVS fp32
+  int nwin, W;
+  unsigned long long wait_ns;
+  int drop_flag;
+};
+
+template <bool WIN>
+__global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                   const __grid_constant__ CUtensorMap tm_k,
+                                                                   const __grid_constant__ CUtensorMap tm_v,
+                                                                   const __grid_constant__ CUtensorMap tm_o,
+                                                                   const Params prm) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(sm);
+  float* As = reinterpret_cast<float*>(sm + OFF_AS);
+  float* tmp = reinterpret_cast<float*>(sm + OFF_TMP);
+  float* gam = reinterpret_cast<float*>(sm + OFF_GAM);
+  float* bet = reinterpret_cast<float*>(sm + OFF_BET);
+  float* be = reinterpret_cast<float*>(sm + OFF_BE);
+  float* dl = reinterpret_cast<float*>(sm + OFF_DL);
+  float* eg = reinterpret_cast<float*>(sm + OFF_EG);
+  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint64_t* bar_v = bar_kq + 1;
+  uint64_t* bar_mma = bar_kq + 2;   // M1, M2, then OQ^T (M3)
+  uint64_t* bar_x = bar_kq + 3;     // V'^T (M3), then the state update (M4)
+  uint64_t* bar_q = bar_kq + 4;     // OP^T (M4)
+  uint64_t* bar_o1 = bar_kq + 5;    // the OQ^T k-steps that read S^T's first atom
+  volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sm + OFF_FLAGS);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qd = warp & 3, hf = warp >> 2;   // TMEM lane quadrant, column half
+  const int G = prm.Hv / prm.Hqk;
+  // the unit of the current piece: sequence n, value head h, qk head hq, value
+  // columns [e0, e0 + 128), first token, length and chunks
+  int n = 0, h = 0, hq = 0, e0 = 0, nchunks = 0;
+  int64_t tok0 = 0, L = 0;
+
+  if (!WIN) {
+    const int unit = (int)blockIdx.x;
+    const int chain = unit / prm.NS;
+    e0 = (unit % prm.NS) * kVS;
+    n = chain / prm.Hv;
+    h = chain % prm.Hv;
+    hq = h / G;
+    if (prm.varlen) {
+      const int64_t a = prm.cu[n], b = prm.cu[n + 1];
+      bool ok = (0 <= a) && (a <= b) && (b <= prm.Ttot);
+      if (unit == 0 && (prm.cu[0] != 0 || prm.cu[prm.N] != prm.Ttot)) ok = false;
+      if (!ok) {
+        if (tid == 0) atomicExch(prm.status, GDN_DEV_BAD_CU_SEQLENS);
+        return;
+      }
+      tok0 = a;
+      L = b - a;
+    } else {
+      tok0 = (int64_t)n * prm.Tseq;
+      L = prm.Tseq;
+    }
+    nchunks = (int)((L + kChunk - 1) / kChunk);
+  }
+
+  if (tid == 0) {
+    flags[2] = WIN ? prm.nwin - 1 - atomicAdd(prm.sched, 1) : 0;
+    mbar_init(bar_kq, 1);
+    mbar_init(bar_v, 1);
+    mbar_init(bar_mma, 1);
+    mbar_init(bar_x, 1);
+    mbar_init(bar_q, 1);
+    mbar_init(bar_o1, 1);
+    mbar_fence_init();
+    flags[1] = 0;
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_o);
+  }
+  if (warp == 0) tmem_alloc(const_cast<uint32_t*>(flags), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = flags[0];
+  const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
+  const int row = 32 * qd + lane;   // this thread's TMEM lane
+
+  uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_x = 0, ph_q = 0, ph_o1 = 0;
+  bool kq_pending = false, v_pending = false;   // thread 0
+  int mma_pending = 0, x_pending = 0, q_pending = 0, o1_pending = 0;
+  auto issue_kq = [&](int c) {
+    const int t = (int)(tok0 + (int64_t)kChunk * c);
+    mbar_arrive_expect_tx(bar_kq, 65536);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      tma_load_3d(sm + OFF_KQ + a * 16384, &tm_k, bar_kq, 64 * a, hq, t);
+      tma_load_3d(sm + OFF_KQ + a * 16384 + 8192, &tm_q, bar_kq, 64 * a, hq, t);
+    }
+    kq_pending = true;
+  };
+  auto issue_v = [&](int c) {
+    const int t = (int)(tok0 + (int64_t)kChunk * c);
+    mbar_arrive_expect_tx(bar_v, 16384);
+    tma_load_3d(sm + OFF_V, &tm_v, bar_v, e0, h, t);
+    tma_load_3d(sm + OFF_V + 8192, &tm_v, bar_v, e0 + 64, h, t);
+    v_pending = true;
+  };
+  auto wait_commit = [&](uint64_t* bar, uint32_t& ph, int& pending) {
+    if (!mbar_wait(bar, ph, prm.status)) flags[1] = 1;
+    ph ^= 1;
+    if (tid == 0) --pending;
+  };
+  auto sync_ok = [&]() -> bool {
+    __syncthreads();
+    tc_fence_after();
+    return flags[1] == 0;
+  };
+  auto wait_mma = [&]() -> bool {
+    wait_commit(bar_mma, ph_mma, mma_pending);
+    return sync_ok();
+  };
+  const uint32_t s4 = (sbase & 0x3FFFFu) >> 4;
+
+  float* graw = reinterpret_cast<float*>(sm + OFF_GRAW);
+  auto fetch_gb = [&](int cc) {
+    float* dst = graw + (cc & 1) * 128;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int rr = 2 * lane + r;
+      const int64_t tn = tok0 + (int64_t)kChunk * cc + rr;
+      if (tn < tok0 + L) {
+        cp_async4(dst + rr, prm.g + tn * prm.Hv + h);
+        cp_async4(dst + 64 + rr, prm.beta + tn * prm.Hv + h);
+      } else {
+        dst[rr] = 0.f;
+        dst[64 + rr] = 0.f;
+      }
+    }
+    cp_async_commit();
+  };
+  const int nch = (prm.Tseq + kChunk - 1) / kChunk;   // chunks per unit (window schedule)
+  const int win = (int)flags[2];
+  int64_t wpos = 0, wend = 0;
+  if (WIN) {
+    const int64_t U = (int64_t)prm.N * prm.Hv * prm.NS * nch;
+    wpos = (int64_t)win * prm.W;
+    wend = wpos + prm.W < U ? wpos + prm.W : U;
+  }
+  int* hflag = WIN ? prm.sched + 1 : nullptr;
+  constexpr int64_t kSlot = (int64_t)kDK * kVS;   // floats of one hand-over slot
+
+#pragma unroll 1
+  for (bool first = true;; first = false) {
+    int c_begin = 0, c_end = nchunks;
+    bool from_hand = false, to_hand = false;
+    if (WIN) {
+      if (wpos >= wend) break;
+      const int64_t j = wpos / nch, off = wpos - j * nch;
+      const int64_t len = (wend < (j + 1) * nch ? wend : (j + 1) * nch) - wpos;
+      const int chain = (int)(j / prm.NS);
+      e0 = (int)(j % prm.NS) * kVS;
+      n = chain / prm.Hv;
+      h = chain % prm.Hv;
+      hq = h / G;
+      tok0 = (int64_t)n * prm.Tseq;
+      L = prm.Tseq;
+      nchunks = nch;
+      c_begin = (int)(nch - off - len);
+      c_end = (int)(nch - off);
+      from_hand = c_begin > 0;
+      to_hand = c_end < nch;
+      wpos += len;
+    } else if (!first) {
+      break;
+    }
+    if (from_hand) {
+      if (tid == 0 && !flag_wait(hflag + win + 1, prm.status, prm.wait_ns)) flags[1] = 1;
+      __syncthreads();
+      if (flags[1]) break;
+    }
+
+    // state slice S^T[e][d] = h0[d][e0 + e] (or the handed-over slot [d][e])
+    {
+      const float* h0p = from_hand ? prm.hand + (int64_t)(win + 1) * kSlot
+                                   : (prm.h0 ? prm.h0 + ((int64_t)n * prm.Hv + h) * kDK * prm.V + e0 : nullptr);
+      const int64_t ld = from_hand ? kVS : prm.V;
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float v[32];
+        const int d0 = 128 * hf + 32 * q4;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int64_t at = (int64_t)(d0 + i) * ld + row;
+          v[i] = !h0p ? 0.f : (from_hand ? __ldcg(h0p + at) : h0p[at]);
+        }
+        tmem_st32(tmem + R_S + lane_off + d0, v);
+      }
+      tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && c_begin < c_end) {
+      issue_kq(c_begin);
+      issue_v(c_begin);
+    }
+    if (warp == 1 && c_begin < c_end) fetch_gb(c_begin);
+
+#pragma unroll 1
+    for (int c = c_begin; c < c_end; ++c) {
+      const int64_t t0 = tok0 + (int64_t)kChunk * c;
+      const int Lc = (int)((L - (int64_t)kChunk * c) < kChunk ? (L - (int64_t)kChunk * c) : kChunk);
+
+      // ---- S0 (warp 1): gamma, beta and the decay factors of this chunk
+      if (warp == 1) {
+        cp_async_wait_all();
+        const float* cur = graw + (c & 1) * 128;
+        const float ga = cur[2 * lane], gb = cur[2 * lane + 1], ba = cur[64 + 2 * lane], bb = cur[64 + 2 * lane + 1];
+        if (c + 1 < c_end) fetch_gb(c + 1);
+        float sum = ga + gb;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float t = __shfl_up_sync(0xffffffffu, sum, off);
+          if (lane >= off) sum += t;
+        }
+        const float g0 = (sum - gb) * kLog2e, g1 = sum * kLog2e;
+        const float gl = __shfl_sync(0xffffffffu, sum, 31) * kLog2e;
+        *reinterpret_cast<float2*>(gam + 2 * lane) = make_float2(g0, g1);
+        *reinterpret_cast<float2*>(bet + 2 * lane) = make_float2(ba, bb);
+        *reinterpret_cast<float2*>(be + 2 * lane) = make_float2(ba * ex2_fast(g0), bb * ex2_fast(g1));
+        *reinterpret_cast<float2*>(dl + 2 * lane) = make_float2(ex2_fast(gl - g0), ex2_fast(gl - g1));
+        *reinterpret_cast<float2*>(eg + 2 * lane) = make_float2(prm.scale * ex2_fast(g0), prm.scale * ex2_fast(g1));
+      }
+
+      // ---- M1: [K;Q] K^T -> R_A (16 k-steps over d)
+      if (tid == 0) {
+        if (!mbar_wait(bar_kq, ph_kq, prm.status)) {
+          flags[1] = 1;
+        } else {
+          ph_kq ^= 1;
+          kq_pending = false;
+          tc_fence_after();
+          const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+          for (int s = 0; s < 16; ++s) {
+            const uint32_t a = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
+            mma_bf16(tmem + R_A, dsw(s4, a, 16), dsw(s4, a, 16), id, s > 0);
+          }
+          mma_commit(bar_mma);
+          ++mma_pending;
+        }
+        if (c + 1 < c_end) {
+          const int tn = (int)(t0 + kChunk);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            tma_prefetch_3d(&tm_k, 64 * a, hq, tn);
+            tma_prefetch_3d(&tm_q, 64 * a, hq, tn);
+          }
+        }
+        bulk_wait_read();   // the previous chunk's o staging (region X) has been read
+      }
+      if (!wait_mma()) break;
+
+      // ---- S1: A rows (lanes 0..63) and P rows (lanes 64..127)
+      {
+        float v[32];
+        const bool upper = (qd & 1) == 0 && hf == 1;
+        const int i = qd < 2 ? row : row - 64;
+        if (upper) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) v[jj] = 0.f;
+        } else {
+          tmem_ld32(tmem + R_A + lane_off + 32 * hf, v);
+          const float ri = qd < 2 ? bet[i] : prm.scale;
+          const float gi = gam[i];
+          const int lim = qd < 2 ? i : i + 1;
+#pragma unroll
+          for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 gj = *reinterpret_cast<const float4*>(gam + 32 * hf + 4 * k4);
+            const float gjs[4] = {gj.x, gj.y, gj.z, gj.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int j = 32 * hf + 4 * k4 + u;
+              v[4 * k4 + u] = j < lim ? ri * ex2_fast(gi - gjs[u]) * v[4 * k4 + u] : 0.f;
+            }
+          }
+        }
+        if (qd < 2) {
+          float4* dst = reinterpret_cast<float4*>(As + i * kAsLd + 32 * hf);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
+        }
+      }
+
+      // ---- S2: solve_tril (the same warp assignment as the K = V = 128 kernel)
+      if (warp == 0 || warp == 5) {
+        const int o = warp == 5 ? 32 : 0;
+        __syncwarp();
+        diag_pair(As, o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+        if (warp == 5) {
+          named_bar64<2>();
+          merge16_half<2>(As, tmp + 16 * 24, o, 0, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+        } else {
+          named_bar64<1>();
+          merge16_half<1>(As, tmp, o, 0, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+        }
+      } else {
+        const int u = 32 * (warp - 1 - (warp > 5 ? 1 : 0)) + lane;
+        const int blk = u >> 5, r = (u >> 1) & 15, half = u & 1;
+        const int rb = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
+        *reinterpret_cast<uint4*>(sm + OFF_TB + off) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sm + OFF_TBE + off) = make_uint4(0u, 0u, 0u, 0u);
+        if (warp == 2 || warp == 7) {
+          if (warp == 7) {
+            named_bar64<2>();
+            merge16_half<2>(As, tmp + 16 * 24, 32, 1, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+          } else {
+            named_bar64<1>();
+            merge16_half<1>(As, tmp, 0, 1, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncthreads();
+      merge_level<32>(As, tmp, warp, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+
+      // ---- M2: W^T (two halves of d) -> R_W ; U^T -> R_B
+      if (tid == 0) {
+        if (!mbar_wait(bar_v, ph_v, prm.status)) {
+          flags[1] = 1;
+        } else {
+          ph_v ^= 1;
+          v_pending = false;
+          tc_fence_after();
+          const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+              mma_bf16(tmem + R_W + 64 * hh, dsw(s4, OFF_KQ + 2 * hh * 16384 + s * 2048, 16384),
+                       dsw(s4, OFF_TBE + s * 32, 16), id, s > 0);
+          }
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem + R_B, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), id, s > 0);
+          mma_commit(bar_mma);
+          ++mma_pending;
+        }
+      }
+      // ---- S4 (while M2 runs): S^T -> bf16 [e][d] (K-major A), S^T *= e^{g_last}
+      {
+        float v[32];
+        const float dec = ex2_fast(gam[kChunk - 1]);
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const uint32_t col = 128 * hf + 32 * q4;
+          tmem_ld32(tmem + R_S + lane_off + col, v);
+          uint8_t* atom = sm + OFF_ST + (col >> 6) * 16384;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) store8_bf16(atom + sw128_chunk(row, 4 * (q4 & 1) + cc), v + 8 * cc);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= dec;
+          tmem_st32(tmem + R_S + lane_off + col, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      if (!wait_mma()) break;
+      if (tid == 0 && c + 1 < c_end) issue_v(c + 1);   // v tile consumed
+
+      // ---- S3: W^T -> bf16 [d][i] (MN-major B); this thread: d = 128 hf + row
+      {
+        float v[32];
+        const int d = 128 * hf + row;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(tmem + R_W + 64 * hf + 32 * half + lane_off, v);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_W + sw128_chunk(d, 4 * half + cc), v + 8 * cc);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+
+      // ---- M3: V'^T = U^T - S^T W^T (R_B) ; OQ^T = S^T Q^T (R_A).  S5 overwrites
+      // S^T's first atom with V'^T: the OQ k-steps that read it commit to bar_o1.
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idv = idesc_bf16(128, 64, 0, 1, 1);
+        const uint32_t ido = idesc_bf16(128, 64, 0, 0, 0);
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+          const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+          mma_bf16(tmem + R_B, dsw(s4, a, 16), dsw(s4, OFF_W + s * 2048, 16384), idv, 1u);
+        }
+        mma_commit(bar_x);
+        ++x_pending;
+#pragma unroll
+        for (int s = 0; s < 16; ++s) {
+          const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+          const uint32_t b = OFF_KQ + (s >> 2) * 16384 + 8192 + (s & 3) * 32;
+          mma_bf16(tmem + R_A, dsw(s4, a, 16), dsw(s4, b, 16), ido, s > 0);
+          if (s == 3) {
+            mma_commit(bar_o1);
+            ++o1_pending;
+          }
+        }
+        mma_commit(bar_mma);
+        ++mma_pending;
+      }
+      wait_commit(bar_x, ph_x, x_pending);
+      if (!sync_ok()) break;
+
+      // ---- S5: V'^T -> bf16 [e][j] ; V''^T = V'^T diag(e^{g_last - g}) -> bf16
+      {
+        float v[32], w[32];
+        tmem_ld32(tmem + R_B + lane_off + 32 * hf, v);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) w[jj] = v[jj] * dl[32 * hf + jj];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
+        wait_commit(bar_o1, ph_o1, o1_pending);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+
+      // ---- M4: OP^T = V'^T P^T (R_B) ; S^T += V''^T K (R_S, N = 256)
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idp = idesc_bf16(128, 64, 0, 0, 0);
+        const uint32_t ids = idesc_bf16(128, 256, 0, 1, 0);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(tmem + R_B, dsw(s4, OFF_VP + s * 32, 16), dsw(s4, OFF_P + s * 32, 16), idp, s > 0);
+        mma_commit(bar_q);
+        ++q_pending;
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          mma_bf16(tmem + R_S, dsw(s4, OFF_VPP + s * 32, 16), dsw(s4, OFF_KQ + s * 2048, 16384), ids, 1);
+        mma_commit(bar_x);
+        ++x_pending;
+      }
+      wait_commit(bar_mma, ph_mma, mma_pending);   // OQ^T (committed in M3)
+      if (!sync_ok()) break;
+
+      // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
+      {
+        const int ecol = (row & 63) & ~1;
+        const bool odd = lane & 1;
+        uint8_t* lbase = sm + OFF_OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
+        const uint32_t xsw = (static_cast<uint32_t>((ecol >> 3) ^ (odd ? 1 : 0))) << 4;
+        float oq[2][16];
+        tmem_ld16(tmem + R_A + lane_off + 32 * hf, oq[0]);
+        tmem_ld16(tmem + R_A + lane_off + 32 * hf + 16, oq[1]);
+        wait_commit(bar_q, ph_q, q_pending);   // OP^T
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float b[16];
+          const float* a = oq[q];
+          const uint32_t col = 32 * hf + 16 * q;
+          tmem_ld16(tmem + R_B + lane_off + col, b);
+          float e[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 x = *reinterpret_cast<const float4*>(eg + col + 4 * k4);
+            e[4 * k4] = x.x, e[4 * k4 + 1] = x.y, e[4 * k4 + 2] = x.z, e[4 * k4 + 3] = x.w;
+          }
+          uint8_t* qb = lbase + col * 128;
+#pragma unroll
+          for (int pp = 0; pp < 8; ++pp) {
+            const float v0 = fmaf(e[2 * pp], a[2 * pp], b[2 * pp]);
+            const float v1 = fmaf(e[2 * pp + 1], a[2 * pp + 1], b[2 * pp + 1]);
+            const float other = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
+            const uint32_t word = odd ? pack_bf16(other, v1) : pack_bf16(v0, other);
+            const uint32_t off = (2 * pp) * 128 + (xsw ^ (static_cast<uint32_t>((2 * pp) & 7) << 4));
+            *reinterpret_cast<uint32_t*>(qb + off) = word;
+          }
+        }
+      }
+      // the state update ran under S6; its completion frees the k / q tile
+      wait_commit(bar_x, ph_x, x_pending);
+      if (tid == 0 && c + 1 < c_end && !flags[1]) issue_kq(c + 1);
+      fence_proxy_async();
+      tc_fence_before();
+      __syncthreads();
+      if (Lc == kChunk) {
+        if (tid == 0) {
+          tma_store_3d(&tm_o, sm + OFF_OS, e0, h, (int)t0);
+          tma_store_3d(&tm_o, sm + OFF_OS + 8192, e0 + 64, h, (int)t0);
+          bulk_commit();
+        }
+      } else {
+        for (int u = tid; u < kChunk * 16; u += kThreads) {
+          const int i = u >> 4, cc = u & 15;
+          if (i < Lc) {
+            const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OS + (cc >> 3) * 8192 + sw128_chunk(i, cc & 7));
+            *reinterpret_cast<uint4*>(prm.o + ((t0 + i) * prm.Hv + h) * prm.V + e0 + cc * 8) = val;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    if (flags[1]) break;
+    if (to_hand || prm.ht != nullptr) {
+      // final state slice ht[d][e0 + e] = S^T[e][d] (or the hand-over slot [d][e])
+      float* htp = to_hand ? prm.hand + (int64_t)win * kSlot : prm.ht + ((int64_t)n * prm.Hv + h) * kDK * prm.V + e0;
+      const int64_t ld = to_hand ? kVS : prm.V;
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        float v[32];
+        const int d0 = 128 * hf + 32 * q4;
+        tmem_ld32(tmem + R_S + lane_off + d0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) htp[(int64_t)(d0 + i) * ld + row] = v[i];
+      }
+    }
+    if (to_hand) {
+      __syncthreads();
+      if (tid == 0) {
+        __threadfence();
+        if (win != prm.drop_flag) atomicExch(hflag + win, 1);
+      }
+    }
+  }   // pieces
+
+  if (tid == 0) bulk_wait_read();
+  if (warp == 1) cp_async_wait_all();
+
+  if (flags[1]) {
+    if (tid == 0) {
+      if (kq_pending) mbar_wait(bar_kq, ph_kq, prm.status, 100000000ull);
+      if (v_pending) mbar_wait(bar_v, ph_v, prm.status, 100000000ull);
+      for (; mma_pending > 0; --mma_pending, ph_mma ^= 1) mbar_wait(bar_mma, ph_mma, prm.status, 100000000ull);
+      for (; x_pending > 0; --x_pending, ph_x ^= 1) mbar_wait(bar_x, ph_x, prm.status, 100000000ull);
+      for (; q_pending > 0; --q_pending, ph_q ^= 1) mbar_wait(bar_q, ph_q, prm.status, 100000000ull);
+      for (; o1_pending > 0; --o1_pending, ph_o1 ^= 1) mbar_wait(bar_o1, ph_o1, prm.status, 100000000ull);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Window schedule over the (chain, slice) units of an equal-length problem:
+// one CTA per SM.
+struct Windows {
+  int64_t W = 0, nwin = 0;
+};
+
+Windows windows_of(const gdn_problem& p) {
+  Windows w;
+  if (p.varlen) return w;
+  const int64_t nch = ((int64_t)p.T + kChunk - 1) / kChunk;
+  const int64_t U = (int64_t)p.N * p.Hv * (p.V / kVS) * nch;
+  if (U == 0) return w;
+  const int64_t G = sm_count();
+  w.W = (U + G - 1) / G;
+  if (w.W < nch) w.W = nch;
+  w.nwin = (U + w.W - 1) / w.W;
+  return w;
+}
+
+size_t sched_bytes(const Windows& w) { return ((sizeof(int32_t) * (2 + w.nwin) + kAlign - 1) / kAlign) * kAlign; }
+
+bool cuts_units(const gdn_problem& p, const Windows& w) {
+  return w.nwin > 0 && w.W != ((int64_t)p.T + kChunk - 1) / kChunk;
+}
+
+}  // namespace
+
+bool fused256_supported(const gdn_problem& p) {
+  return p.dt == GDN_BF16 && p.K == kDK && p.V % kVS == 0 && p.V <= 256 && (p.C == 64 || p.C == 128);
+}
+
+size_t fused256_workspace_bytes(const gdn_problem& p) {
+  const Windows w = windows_of(p);
+  if (w.nwin == 0) return kAlign;
+  return sched_bytes(w) + (cuts_units(p, w) ? (size_t)w.nwin * kDK * kVS * sizeof(float) : 0);
+}
+
+bool fused256_handover_window(const gdn_problem& p, int window) {
+  if (!fused256_supported(p)) return false;
+  const Windows w = windows_of(p);
+  if (!cuts_units(p, w) || window < 1 || window >= w.nwin) return false;
+  const int64_t nch = ((int64_t)p.T + kChunk - 1) / kChunk;
+  return ((int64_t)window * w.W) % nch != 0;
+}
+
+gdn_status run_fused256(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                        void* ws, cudaStream_t s, int drop_flag, unsigned long long wait_ns) {
+  if (!fused256_supported(p)) return GDN_ERR_UNSUPPORTED;
+  int32_t* status = static_cast<int32_t*>(ws);
+  const Windows w = windows_of(p);
+  if (cudaMemsetAsync(status, 0, w.nwin > 0 ? sizeof(int32_t) * (2 + w.nwin) : sizeof(int32_t), s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  const int64_t Ttot = (int64_t)p.B * p.T;
+  if (Ttot == 0 || (int64_t)p.N * p.Hv == 0) {
+    if (ht) {
+      const size_t bytes = sizeof(float) * (size_t)p.N * p.Hv * p.K * p.V;
+      cudaError_t e = h0 ? cudaMemcpyAsync(ht, h0, bytes, cudaMemcpyDeviceToDevice, s) : cudaMemsetAsync(ht, 0, bytes, s);
+      if (e != cudaSuccess) return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+  }
+  CUtensorMap tq, tk, tv, to;
+  memset(&tq, 0, sizeof(tq));
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  memset(&to, 0, sizeof(to));
+  const uint32_t box[3] = {64, 1, kChunk};
+  {
+    const uint64_t dims[3] = {(uint64_t)p.K, (uint64_t)p.Hqk, (uint64_t)Ttot};
+    const uint64_t str[2] = {(uint64_t)p.K * 2, (uint64_t)p.Hqk * p.K * 2};
+    if (!make_tmap_bf16(&tq, q, 3, dims, str, box) || !make_tmap_bf16(&tk, k, 3, dims, str, box)) return GDN_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {(uint64_t)p.V, (uint64_t)p.Hv, (uint64_t)Ttot};
+    const uint64_t str[2] = {(uint64_t)p.V * 2, (uint64_t)p.Hv * p.V * 2};
+    if (!make_tmap_bf16(&tv, v, 3, dims, str, box) || !make_tmap_bf16(&to, o, 3, dims, str, box)) return GDN_ERR_CUDA;
+  }
+  Params prm;
+  prm.g = g;
+  prm.beta = beta;
+  prm.h0 = h0;
+  prm.cu = p.varlen ? cu : nullptr;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.ht = ht;
+  prm.status = status;
+  prm.N = p.N;
+  prm.Tseq = p.T;
+  prm.Ttot = (int)Ttot;
+  prm.Hqk = p.Hqk;
+  prm.Hv = p.Hv;
+  prm.V = p.V;
+  prm.NS = p.V / kVS;
+  prm.varlen = p.varlen;
+  prm.scale = scale;
+  prm.sched = w.nwin > 0 ? status + 1 : nullptr;
+  prm.hand = cuts_units(p, w) ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sched_bytes(w)) : nullptr;
+  prm.nwin = (int)w.nwin;
+  prm.W = (int)w.W;
+  prm.wait_ns = wait_ns;
+  prm.drop_flag = drop_flag;
+  auto kernel = prm.sched ? gdn_fused256_kernel<true> : gdn_fused256_kernel<false>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  const unsigned grid = prm.sched ? (unsigned)w.nwin : (unsigned)((int64_t)p.N * p.Hv * prm.NS);
+  kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace gdn

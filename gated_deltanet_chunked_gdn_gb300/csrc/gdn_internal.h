@@ -77,8 +77,16 @@ gdn_status run_recurrent(const gdn_problem& p, const void* q, const void* k, con
                          const int32_t* state_indices, int state_slots, const int32_t* cu, void* o,
                          cudaStream_t s);
 
-// Fused path (gdn_fused.cu).
+// Fused path (gdn_fused.cu: K = V = 128; gdn_fused256.cu: K = 256, V = 128 or
+// 256, value slices of 128 columns).  fused_supported: either kernel.
 bool fused_supported(const gdn_problem& p);
+bool fused128_supported(const gdn_problem& p);
+bool fused256_supported(const gdn_problem& p);
+size_t fused256_workspace_bytes(const gdn_problem& p);
+bool fused256_handover_window(const gdn_problem& p, int window);
+gdn_status run_fused256(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                        const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                        void* ws, cudaStream_t s, int drop_flag, unsigned long long wait_ns);
 size_t fused_workspace_bytes(const gdn_problem& p);
 size_t fused_status_offset(const gdn_problem& p);
 // drop_flag / wait_ns: test hook of the window schedule -- the hand-over flag

@@ -187,6 +187,15 @@ FUSED_CASES = {
     # 150 packed sequences of 0..299 tokens (empty ones included), GQA 2 -> 4
     "varlen_many_short": (I.WORKLOADS[3].with_(Hqk=2, Hv=4),
                           [int(n) for n in np.random.default_rng(5).integers(0, 300, 150)]),
+    # K = V = 256 (value slices of 128 columns): ragged tail with GQA 4, h0,
+    # short and empty packed sequences, V = 128, and windows that cut units
+    "d256_fixed_ragged_gqa4": (I.WORKLOADS[4].with_(B=2, T=333, Hqk=1, Hv=4), None),
+    "d256_gqa4_h0": (I.WORKLOADS[4].with_(B=1, T=200, Hqk=2, Hv=8, h0=True), None),
+    "d256_varlen_short_and_empty": (I.WORKLOADS[4].with_(B=1, T=0, Hqk=1, Hv=4, h0=True, varlen_n=8),
+                                    [5, 64, 200, 1, 0, 129, 63, 65]),
+    "d256_V128_h0": (I.WORKLOADS[4].with_(B=2, T=150, Hqk=2, Hv=4, V=128, h0=True), None),
+    # 320 (chain, slice) units of 3 chunks over 152 SMs: windows of 7 chunks
+    "d256_windows_cut_units": (I.WORKLOADS[4].with_(B=20, T=190, Hqk=2, Hv=8, h0=True), None),
 }
 
 

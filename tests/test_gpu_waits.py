@@ -31,10 +31,18 @@ def gdn():
     return binding
 
 
-def test_handover_wait_times_out_and_the_next_call_is_exact(gdn):
+CASES = {
     # 512 chains of 4 chunks over the 2 x SMs CTA slots: windows of more than
     # one chain's chunks, so window boundaries cut chains
-    w = I.WORKLOADS[2].with_(B=4, T=256, Hqk=128, Hv=128)
+    "d128": I.WORKLOADS[2].with_(B=4, T=256, Hqk=128, Hv=128),
+    # K = V = 256: 320 (chain, value slice) units of 3 chunks over one CTA per SM
+    "d256": I.WORKLOADS[4].with_(B=20, T=190, Hqk=2, Hv=8, h0=True),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_handover_wait_times_out_and_the_next_call_is_exact(gdn, name):
+    w = CASES[name]
     x = I.make_inputs(w, "cuda")
     p = gdn.problem_of(x["q"], x["v"], w.C)
     ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, "fused"), dtype=torch.uint8, device="cuda")
