@@ -10,24 +10,26 @@
 // (sequence, value head) chain -- its 256 x 128 fp32 state slice S^T[e][d]
 // lives in TMEM (256 of the 512 columns) for the whole chain -- and walks the
 // chain's 64-token chunks in order.  Everything of a chunk that does not depend
-// on V (K K^T, Q K^T, gating, the triangular solve, W) is recomputed by each
-// slice of a chain; v, U, V', o and the state are the slice's own.  One CTA per
-// SM (about 187 KB of shared memory, all 512 TMEM columns); equal-length
+// on V (K K^T, Q K^T, gating, the triangular solve) is recomputed by each slice
+// of a chain; v, Y, U, V', o and the state are the slice's own.  One CTA per SM
+// (about 194 KB of shared memory, all 512 TMEM columns); equal-length
 // problems deal the (chain, slice) units' chunks out as windows of equal
 // length over the SMs, handing a cut unit's state slice over through the
 // workspace, exactly as the K = V = 128 kernel does.
 //
-// Products (M = 128 on the slice's value columns e, or on 128 key columns d,
-// or on the 64 k rows stacked over the 64 q rows):
+// Products (M = 128 on the slice's value columns e, or on the 64 k rows
+// stacked over the 64 q rows).  The WY term is applied to the state through
+// Y = K S (Y[j][e] = k_j . S[:, e], the state's current value for key j):
+// V' = U - T diag(beta e^g) K S = U - (T diag(beta e^g)) Y, so no W = T diag(beta
+// e^g) K is formed, and Y comes out of the same product as the query term:
 //
-//   M1  [K;Q] K^T                 -> R_A   (M128 N64, 16 k-steps over d)
+//   M1  [K;Q] K^T                  -> R_A   (M128 N64, 16 k-steps over d)
 //   S1  A = strict-lower(beta_i e^{g_i - g_j} K K^T) -> smem fp32, P -> smem bf16
-//   S2  T = (I + A)^{-1}; T diag(beta), T diag(beta e^g) -> bf16
-//   M2  W^T = K^T (T diag(beta e^g))^T -> R_W (two M128 halves of d)
-//       U^T = V^T (T diag(beta))^T     -> R_B
-//   S4  S^T (fp32, TMEM) -> bf16 [e][d]; S^T *= e^{g_last}
-//   S3  W^T -> bf16 [d][i]
-//   M3  V'^T = U^T - S^T W^T -> R_B;  OQ^T = S^T Q^T -> R_A   (16 k-steps each)
+//   S2  T = (I + A)^{-1}; T diag(beta), T diag(beta e^g) -> bf16       (warps 0, 2, 5, 7, then all)
+//   S4  S^T (fp32, TMEM) -> bf16 [e][d]; S^T *= e^{g_last}            (warps 1, 3, 4, 6, beside S2)
+//   M3a [Y^T | OQ^T] = S^T [K;Q]^T -> R_Y   (M128 N128, 16 k-steps; runs under the solve's merges)
+//   S3  Y^T -> bf16 [e][j]
+//   M3b V'^T = V^T (T diag(beta))^T - Y^T (T diag(beta e^g))^T -> R_B  (8 k-steps)
 //   S5  V'^T -> bf16, V''^T = V'^T diag(e^{g_last - g}) -> bf16
 //   M4  OP^T = V'^T P^T -> R_B;  S^T += V''^T K (N = 256) -> R_S
 //   S6  o_i = scale e^{g_i} OQ_i + OP_i -> staging -> TMA store
@@ -45,43 +47,40 @@ constexpr int kDK = 256;         // K
 constexpr int kVS = 128;         // value columns of one slice
 constexpr int kTmemCols = 512;
 
-// TMEM columns (lane = slice column e, key column d mod 128, or chunk row)
+// TMEM columns (lane = slice column e, or chunk row)
 constexpr uint32_t R_S = 0;      // S^T[e][d], d = 0..255
-constexpr uint32_t R_A = 256;    // [K;Q] K^T, then OQ^T[e][i]
-constexpr uint32_t R_W = 320;    // W^T[d][i]: d < 128 at 320, d >= 128 at 384
-constexpr uint32_t R_B = 448;    // U^T[e][i] -> V'^T -> OP^T
+constexpr uint32_t R_A = 256;    // [K;Q] K^T
+constexpr uint32_t R_Y = 320;    // Y^T[e][j] (320..383) | OQ^T[e][i] (384..447)
+constexpr uint32_t R_B = 448;    // V'^T[e][i] -> OP^T
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_KQ = 0;          // 4 atom columns (d 64a..64a+63) of [k rows 0..63; q rows 64..127], 16 KB each
 constexpr uint32_t OFF_V = 65536;       // v slice rows 0..63 x 128 e, 2 atom columns of 8 KB
-constexpr uint32_t OFF_Y = 81920;       // T diag(beta) | T diag(beta e^g) (8 KB each), then W^T (32 KB), then V''^T
-constexpr uint32_t OFF_TB = OFF_Y;
-constexpr uint32_t OFF_TBE = OFF_Y + 8192;
-constexpr uint32_t OFF_W = OFF_Y;       // W^T bf16 [d][i], 256 rows of 128 B
-constexpr uint32_t OFF_VPP = OFF_Y;     // V''^T bf16 [e][j], 16 KB (W^T is dead once V' is complete)
-constexpr uint32_t OFF_P = 114688;      // P [i][j] bf16, 8 KB
-constexpr uint32_t OFF_X = 122880;      // 64 KB, reused: A/T fp32 + scratch | S^T bf16 | V'^T | o staging
-constexpr uint32_t OFF_AS = OFF_X;      // fp32 [64][68]
-constexpr uint32_t OFF_TMP = OFF_X + 64 * 68 * 4;
-constexpr uint32_t OFF_ST = OFF_X;      // S^T bf16 [e][d], 4 atom columns of 16 KB
-constexpr uint32_t OFF_VP = OFF_X;      // V'^T bf16 [e][j] (the S^T atom that M3 reads first)
-constexpr uint32_t OFF_OS = OFF_X;      // o staging bf16: 2 boxes [64 rows][64 e]
-constexpr uint32_t OFF_MISC = 188416;
+constexpr uint32_t OFF_TB = 81920;      // T diag(beta) [i][j] bf16, 8 KB
+constexpr uint32_t OFF_TBE = 90112;     // T diag(beta e^g) [i][j] bf16, 8 KB
+constexpr uint32_t OFF_P = 98304;       // P [i][j] bf16, 8 KB
+constexpr uint32_t OFF_AS = 106496;     // A / T fp32 [64][68] and the merges' scratch
+constexpr uint32_t OFF_TMP = OFF_AS + 64 * 68 * 4;
+constexpr uint32_t OFF_ST = 129024;     // S^T bf16 [e][d], 4 atom columns of 16 KB; after M3a reused:
+constexpr uint32_t OFF_YT = OFF_ST;            //   Y^T bf16 [e][j]
+constexpr uint32_t OFF_VP = OFF_ST + 16384;    //   V'^T bf16 [e][j]
+constexpr uint32_t OFF_VPP = OFF_ST + 32768;   //   V''^T bf16 [e][j]
+constexpr uint32_t OFF_OS = OFF_ST + 49152;    //   o staging bf16: 2 boxes [64 rows][64 e]
+constexpr uint32_t OFF_MISC = 194560;
 constexpr uint32_t OFF_GAM = OFF_MISC;
 constexpr uint32_t OFF_BET = OFF_MISC + 256;
 constexpr uint32_t OFF_BE = OFF_MISC + 512;
 constexpr uint32_t OFF_DL = OFF_MISC + 768;
 constexpr uint32_t OFF_EG = OFF_MISC + 1024;
-constexpr uint32_t OFF_BAR = OFF_MISC + 1280;    // 6 mbarriers: k/q, v, three MMA commit groups, first quarter of OQ
+constexpr uint32_t OFF_BAR = OFF_MISC + 1280;    // 6 mbarriers: k/q, v, M1, M3a, M3b / M4 state, OP
 constexpr uint32_t OFF_FLAGS = OFF_MISC + 1328;  // [0] tmem base, [1] abort, [2] window
 constexpr uint32_t OFF_GRAW = OFF_MISC + 1344;   // float[2][2][64]: raw g, beta of two chunks
 constexpr uint32_t kSmemUsed = OFF_MISC + 2368;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 
-static_assert(OFF_TMP + 32 * 40 * 4 <= OFF_X + 65536, "solve scratch overflows region X");
+static_assert(OFF_TMP + 32 * 40 * 4 <= OFF_ST, "solve scratch overflows into S^T");
 static_assert(kSmemBytes <= 232448, "one CTA must fit an SM");
-static_assert(OFF_X % 1024 == 0 && OFF_Y % 1024 == 0 && OFF_P % 1024 == 0 && OFF_V % 1024 == 0, "atom alignment");
-
+static_assert(OFF_ST % 1024 == 0 && OFF_TB % 1024 == 0 && OFF_P % 1024 == 0 && OFF_V % 1024 == 0, "atom alignment");
 struct Params {
   const float* g;
   const float* beta;
@@ -119,14 +118,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   float* eg = reinterpret_cast<float*>(sm + OFF_EG);
   uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
   uint64_t* bar_v = bar_kq + 1;
-  uint64_t* bar_mma = bar_kq + 2;   // M1, M2, then OQ^T (M3)
-  uint64_t* bar_x = bar_kq + 3;     // V'^T (M3), then the state update (M4)
-  uint64_t* bar_q = bar_kq + 4;     // OP^T (M4)
-  uint64_t* bar_o1 = bar_kq + 5;    // the OQ^T k-steps that read S^T's first atom
+  // MMA commit groups; every thread waits for every commit, in order, so all
+  // threads track the same phases
+  uint64_t* bar_mma = bar_kq + 2;   // M1
+  uint64_t* bar_y = bar_kq + 3;     // M3a (issued by thread kYIssuer)
+  uint64_t* bar_x = bar_kq + 4;     // M3b, then the state update (M4)
+  uint64_t* bar_q = bar_kq + 5;     // OP^T (M4)
   volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sm + OFF_FLAGS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, hf = warp >> 2;   // TMEM lane quadrant, column half
+  constexpr int kYIssuer = 32;               // warp 1, lane 0: issues M3a after S4
   const int G = prm.Hv / prm.Hqk;
   // the unit of the current piece: sequence n, value head h, qk head hq, value
   // columns [e0, e0 + 128), first token, length and chunks
@@ -162,9 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     mbar_init(bar_kq, 1);
     mbar_init(bar_v, 1);
     mbar_init(bar_mma, 1);
+    mbar_init(bar_y, 1);
     mbar_init(bar_x, 1);
     mbar_init(bar_q, 1);
-    mbar_init(bar_o1, 1);
     mbar_fence_init();
     flags[1] = 0;
     prefetch_tmap(&tm_q);
@@ -180,9 +182,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
   const int row = 32 * qd + lane;   // this thread's TMEM lane
 
-  uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_x = 0, ph_q = 0, ph_o1 = 0;
-  bool kq_pending = false, v_pending = false;   // thread 0
-  int mma_pending = 0, x_pending = 0, q_pending = 0, o1_pending = 0;
+  uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_y = 0, ph_x = 0, ph_q = 0;
+  bool kq_pending = false, v_pending = false;          // thread 0
+  int mma_pending = 0, x_pending = 0, q_pending = 0;   // commits of thread 0 not yet waited for
+  int y_pending = 0;                                   // commits of kYIssuer not yet waited for
   auto issue_kq = [&](int c) {
     const int t = (int)(tok0 + (int64_t)kChunk * c);
     mbar_arrive_expect_tx(bar_kq, 65536);
@@ -200,19 +203,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     tma_load_3d(sm + OFF_V + 8192, &tm_v, bar_v, e0 + 64, h, t);
     v_pending = true;
   };
-  auto wait_commit = [&](uint64_t* bar, uint32_t& ph, int& pending) {
+  auto wait_commit = [&](uint64_t* bar, uint32_t& ph, int& pending, int owner) {
     if (!mbar_wait(bar, ph, prm.status)) flags[1] = 1;
     ph ^= 1;
-    if (tid == 0) --pending;
+    if (tid == owner) --pending;
   };
   auto sync_ok = [&]() -> bool {
     __syncthreads();
     tc_fence_after();
     return flags[1] == 0;
-  };
-  auto wait_mma = [&]() -> bool {
-    wait_commit(bar_mma, ph_mma, mma_pending);
-    return sync_ok();
   };
   const uint32_t s4 = (sbase & 0x3FFFFu) >> 4;
 
@@ -351,9 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
             tma_prefetch_3d(&tm_q, 64 * a, hq, tn);
           }
         }
-        bulk_wait_read();   // the previous chunk's o staging (region X) has been read
+        bulk_wait_read();   // the previous chunk's o staging has been read by its TMA store
       }
-      if (!wait_mma()) break;
+      wait_commit(bar_mma, ph_mma, mma_pending, 0);
+      if (!sync_ok()) break;
 
       // ---- S1: A rows (lanes 0..63) and P rows (lanes 64..127)
       {
@@ -389,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         }
       }
 
-      // ---- S2: solve_tril (the same warp assignment as the K = V = 128 kernel)
+      // ---- S2 (warps 0, 2, 5, 7: diagonal blocks and 16-merges) beside
+      //      S4 (warps 1, 3, 4, 6: the state) and M3a (issued by kYIssuer once S4 is done)
       if (warp == 0 || warp == 5) {
         const int o = warp == 5 ? 32 : 0;
         __syncwarp();
@@ -417,13 +418,59 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
             named_bar64<1>();
             merge16_half<1>(As, tmp, 0, 1, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
           }
+        } else {
+          // S4: S^T -> bf16 [e][d] (K-major A of M3a), S^T *= e^{g_last}; this
+          // warp's lane quadrant, all 256 columns
+          float v[32];
+          const float dec = ex2_fast(gam[kChunk - 1]);
+#pragma unroll 1
+          for (int q8 = 0; q8 < 8; ++q8) {
+            const uint32_t col = 32 * q8;
+            tmem_ld32(tmem + R_S + lane_off + col, v);
+            uint8_t* atom = sm + OFF_ST + (col >> 6) * 16384;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) store8_bf16(atom + sw128_chunk(row, 4 * (q8 & 1) + cc), v + 8 * cc);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= dec;
+            tmem_st32(tmem + R_S + lane_off + col, v);
+          }
+          tmem_wait_st();
+          fence_proxy_async();   // S^T bf16 feeds tcgen05.mma
+          tc_fence_before();
+          named_bar128<3>();     // the four S4 warps are done
+          // ---- M3a: [Y^T | OQ^T] = S^T [K;Q]^T -> R_Y (M128 N128)
+          if (tid == kYIssuer) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 128, 0, 0, 0);
+#pragma unroll
+            for (int s = 0; s < 16; ++s) {
+              const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
+              const uint32_t b = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
+              mma_bf16(tmem + R_Y, dsw(s4, a, 16), dsw(s4, b, 16), id, s > 0);
+            }
+            mma_commit(bar_y);
+            ++y_pending;
+          }
         }
       }
       tc_fence_before();
       __syncthreads();
       merge_level<32>(As, tmp, warp, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
 
-      // ---- M2: W^T (two halves of d) -> R_W ; U^T -> R_B
+      // ---- S3: Y^T -> bf16 [e][j] (K-major A of M3b), over S^T's first atom
+      wait_commit(bar_y, ph_y, y_pending, kYIssuer);
+      tc_fence_after();
+      {
+        float v[32];
+        tmem_ld32(tmem + R_Y + lane_off + 32 * hf, v);
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_YT + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      if (!sync_ok()) break;
+
+      // ---- M3b: V'^T = V^T (T diag(beta))^T - Y^T (T diag(beta e^g))^T -> R_B
       if (tid == 0) {
         if (!mbar_wait(bar_v, ph_v, prm.status)) {
           flags[1] = 1;
@@ -431,85 +478,21 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
           ph_v ^= 1;
           v_pending = false;
           tc_fence_after();
-          const uint32_t id = idesc_bf16(128, 64, 1, 0, 0);
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-            for (int s = 0; s < 4; ++s)
-              mma_bf16(tmem + R_W + 64 * hh, dsw(s4, OFF_KQ + 2 * hh * 16384 + s * 2048, 16384),
-                       dsw(s4, OFF_TBE + s * 32, 16), id, s > 0);
-          }
+          const uint32_t idu = idesc_bf16(128, 64, 1, 0, 0);
+          const uint32_t idy = idesc_bf16(128, 64, 0, 0, 1);
 #pragma unroll
           for (int s = 0; s < 4; ++s)
-            mma_bf16(tmem + R_B, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), id, s > 0);
-          mma_commit(bar_mma);
-          ++mma_pending;
+            mma_bf16(tmem + R_B, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), idu, s > 0);
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem + R_B, dsw(s4, OFF_YT + s * 32, 16), dsw(s4, OFF_TBE + s * 32, 16), idy, 1u);
+          mma_commit(bar_x);
+          ++x_pending;
         }
       }
-      // ---- S4 (while M2 runs): S^T -> bf16 [e][d] (K-major A), S^T *= e^{g_last}
-      {
-        float v[32];
-        const float dec = ex2_fast(gam[kChunk - 1]);
-#pragma unroll 1
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const uint32_t col = 128 * hf + 32 * q4;
-          tmem_ld32(tmem + R_S + lane_off + col, v);
-          uint8_t* atom = sm + OFF_ST + (col >> 6) * 16384;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) store8_bf16(atom + sw128_chunk(row, 4 * (q4 & 1) + cc), v + 8 * cc);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= dec;
-          tmem_st32(tmem + R_S + lane_off + col, v);
-        }
-        tmem_wait_st();
-        tc_fence_before();
-      }
-      if (!wait_mma()) break;
-      if (tid == 0 && c + 1 < c_end) issue_v(c + 1);   // v tile consumed
-
-      // ---- S3: W^T -> bf16 [d][i] (MN-major B); this thread: d = 128 hf + row
-      {
-        float v[32];
-        const int d = 128 * hf + row;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          tmem_ld32(tmem + R_W + 64 * hf + 32 * half + lane_off, v);
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_W + sw128_chunk(d, 4 * half + cc), v + 8 * cc);
-        }
-      }
-      fence_proxy_async();
-      tc_fence_before();
-      __syncthreads();
-
-      // ---- M3: V'^T = U^T - S^T W^T (R_B) ; OQ^T = S^T Q^T (R_A).  S5 overwrites
-      // S^T's first atom with V'^T: the OQ k-steps that read it commit to bar_o1.
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t idv = idesc_bf16(128, 64, 0, 1, 1);
-        const uint32_t ido = idesc_bf16(128, 64, 0, 0, 0);
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-          mma_bf16(tmem + R_B, dsw(s4, a, 16), dsw(s4, OFF_W + s * 2048, 16384), idv, 1u);
-        }
-        mma_commit(bar_x);
-        ++x_pending;
-#pragma unroll
-        for (int s = 0; s < 16; ++s) {
-          const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-          const uint32_t b = OFF_KQ + (s >> 2) * 16384 + 8192 + (s & 3) * 32;
-          mma_bf16(tmem + R_A, dsw(s4, a, 16), dsw(s4, b, 16), ido, s > 0);
-          if (s == 3) {
-            mma_commit(bar_o1);
-            ++o1_pending;
-          }
-        }
-        mma_commit(bar_mma);
-        ++mma_pending;
-      }
-      wait_commit(bar_x, ph_x, x_pending);
+      wait_commit(bar_x, ph_x, x_pending, 0);
       if (!sync_ok()) break;
+      if (tid == 0 && c + 1 < c_end) issue_v(c + 1);   // v tile consumed
 
       // ---- S5: V'^T -> bf16 [e][j] ; V''^T = V'^T diag(e^{g_last - g}) -> bf16
       {
@@ -519,7 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         for (int jj = 0; jj < 32; ++jj) w[jj] = v[jj] * dl[32 * hf + jj];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
-        wait_commit(bar_o1, ph_o1, o1_pending);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
       }
@@ -543,8 +525,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         mma_commit(bar_x);
         ++x_pending;
       }
-      wait_commit(bar_mma, ph_mma, mma_pending);   // OQ^T (committed in M3)
-      if (!sync_ok()) break;
 
       // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
       {
@@ -553,9 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         uint8_t* lbase = sm + OFF_OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
         const uint32_t xsw = (static_cast<uint32_t>((ecol >> 3) ^ (odd ? 1 : 0))) << 4;
         float oq[2][16];
-        tmem_ld16(tmem + R_A + lane_off + 32 * hf, oq[0]);
-        tmem_ld16(tmem + R_A + lane_off + 32 * hf + 16, oq[1]);
-        wait_commit(bar_q, ph_q, q_pending);   // OP^T
+        tmem_ld16(tmem + R_Y + 64 + lane_off + 32 * hf, oq[0]);
+        tmem_ld16(tmem + R_Y + 64 + lane_off + 32 * hf + 16, oq[1]);
+        wait_commit(bar_q, ph_q, q_pending, 0);   // OP^T
         tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -582,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         }
       }
       // the state update ran under S6; its completion frees the k / q tile
-      wait_commit(bar_x, ph_x, x_pending);
+      wait_commit(bar_x, ph_x, x_pending, 0);
       if (tid == 0 && c + 1 < c_end && !flags[1]) issue_kq(c + 1);
       fence_proxy_async();
       tc_fence_before();
@@ -631,14 +611,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   if (warp == 1) cp_async_wait_all();
 
   if (flags[1]) {
+    // abort: copies and MMAs already in flight finish (bounded) before the
+    // shared memory and TMEM are released; each issuing thread waits for its own
     if (tid == 0) {
       if (kq_pending) mbar_wait(bar_kq, ph_kq, prm.status, 100000000ull);
       if (v_pending) mbar_wait(bar_v, ph_v, prm.status, 100000000ull);
       for (; mma_pending > 0; --mma_pending, ph_mma ^= 1) mbar_wait(bar_mma, ph_mma, prm.status, 100000000ull);
       for (; x_pending > 0; --x_pending, ph_x ^= 1) mbar_wait(bar_x, ph_x, prm.status, 100000000ull);
       for (; q_pending > 0; --q_pending, ph_q ^= 1) mbar_wait(bar_q, ph_q, prm.status, 100000000ull);
-      for (; o1_pending > 0; --o1_pending, ph_o1 ^= 1) mbar_wait(bar_o1, ph_o1, prm.status, 100000000ull);
     }
+    if (tid == kYIssuer)
+      for (; y_pending > 0; --y_pending, ph_y ^= 1) mbar_wait(bar_y, ph_y, prm.status, 100000000ull);
   }
   tc_fence_before();
   __syncthreads();

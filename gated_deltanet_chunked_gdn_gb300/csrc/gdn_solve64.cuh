@@ -149,6 +149,12 @@ __device__ __forceinline__ void named_bar64() {
   asm volatile("bar.sync %0, 64;" :: "n"(ID) : "memory");
 }
 
+// Named barrier ID over 128 threads (four warps).
+template <int ID>
+__device__ __forceinline__ void named_bar128() {
+  asm volatile("bar.sync %0, 128;" :: "n"(ID) : "memory");
+}
+
 // 16-level merge of the 32x32 diagonal block at o, T21 = -T22 (A21 T11),
 // split over two warps: this one computes the 8-column tile nt of T21, the
 // product A21 T11 passing through the pair's scratch (16 x 16, leading
