@@ -33,6 +33,13 @@
 //   S5  V'^T -> bf16, V''^T = V'^T diag(e^{g_last - g}) -> bf16
 //   M4  OP^T = V'^T P^T -> R_B;  S^T += V''^T K (N = 256) -> R_S
 //   S6  o_i = scale e^{g_i} OQ_i + OP_i -> staging -> TMA store
+//
+// The k rows are double-buffered inside the [k; q] tile (per 64-column atom:
+// k of even chunks, q, k of odd chunks), so the next chunk's k is loaded while
+// this chunk runs and its q as soon as M3a has read this chunk's q: the next
+// M1 no longer waits for a 64 KB load issued at the end of the chunk.  Odd
+// chunks read the stacked operand as [q; k]: their M1 rows and M3a columns
+// come out in the other order.
 #include <string.h>
 
 #include "gdn_solve64.cuh"
@@ -49,24 +56,26 @@ constexpr int kTmemCols = 512;
 
 // TMEM columns (lane = slice column e, or chunk row)
 constexpr uint32_t R_S = 0;      // S^T[e][d], d = 0..255
-constexpr uint32_t R_A = 256;    // [K;Q] K^T
-constexpr uint32_t R_Y = 320;    // Y^T[e][j] (320..383) | OQ^T[e][i] (384..447)
+constexpr uint32_t R_A = 256;    // [K;Q] K^T (even chunks) or [Q;K] K^T (odd chunks)
+constexpr uint32_t R_Y = 320;    // [Y^T | OQ^T] (even chunks) or [OQ^T | Y^T] (odd chunks), 64 columns each
 constexpr uint32_t R_B = 448;    // V'^T[e][i] -> OP^T
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_KQ = 0;          // 4 atom columns (d 64a..64a+63) of [k rows 0..63; q rows 64..127], 16 KB each
-constexpr uint32_t OFF_V = 65536;       // v slice rows 0..63 x 128 e, 2 atom columns of 8 KB
-constexpr uint32_t OFF_TB = 81920;      // T diag(beta) [i][j] bf16, 8 KB
-constexpr uint32_t OFF_TBE = 90112;     // T diag(beta e^g) [i][j] bf16, 8 KB
-constexpr uint32_t OFF_P = 98304;       // P [i][j] bf16, 8 KB
-constexpr uint32_t OFF_AS = 106496;     // A / T fp32 [64][68] and the merges' scratch
+constexpr uint32_t OFF_KQ = 0;          // 4 atom columns (d 64a..64a+63) of [k even ; q ; k odd], 24 KB each
+constexpr uint32_t kAtomKQ = 24576;
+constexpr uint32_t kRowsQ = 8192;       // byte offset of the q rows in an atom (k of odd chunks: 2 kRowsQ)
+constexpr uint32_t OFF_V = 98304;       // v slice rows 0..63 x 128 e, 2 atom columns of 8 KB
+constexpr uint32_t OFF_TB = 114688;     // T diag(beta) [i][j] bf16, 8 KB
+constexpr uint32_t OFF_TBE = 122880;    // T diag(beta e^g) [i][j] bf16, 8 KB
+constexpr uint32_t OFF_P = 131072;      // P [i][j] bf16, 8 KB
+constexpr uint32_t OFF_AS = 139264;     // A / T fp32 [64][68] and the merges' scratch
 constexpr uint32_t OFF_TMP = OFF_AS + 64 * 68 * 4;
-constexpr uint32_t OFF_ST = 129024;     // S^T bf16 [e][d], 4 atom columns of 16 KB; after M3a reused:
+constexpr uint32_t OFF_ST = 161792;     // S^T bf16 [e][d], 4 atom columns of 16 KB; after M3a reused:
 constexpr uint32_t OFF_YT = OFF_ST;            //   Y^T bf16 [e][j]
 constexpr uint32_t OFF_VP = OFF_ST + 16384;    //   V'^T bf16 [e][j]
 constexpr uint32_t OFF_VPP = OFF_ST + 32768;   //   V''^T bf16 [e][j]
 constexpr uint32_t OFF_OS = OFF_ST + 49152;    //   o staging bf16: 2 boxes [64 rows][64 e]
-constexpr uint32_t OFF_MISC = 194560;
+constexpr uint32_t OFF_MISC = 227328;
 constexpr uint32_t OFF_GAM = OFF_MISC;
 constexpr uint32_t OFF_BET = OFF_MISC + 256;
 constexpr uint32_t OFF_BE = OFF_MISC + 512;
@@ -182,19 +191,47 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   const uint32_t lane_off = static_cast<uint32_t>(32 * qd) << 16;
   const int row = 32 * qd + lane;   // this thread's TMEM lane
 
+  const uint32_t s4 = (sbase & 0x3FFFFu) >> 4;
   uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_y = 0, ph_x = 0, ph_q = 0;
   bool kq_pending = false, v_pending = false;          // thread 0
+  bool q_owed = false;                                 // thread 0: k issued without its q
   int mma_pending = 0, x_pending = 0, q_pending = 0;   // commits of thread 0 not yet waited for
   int y_pending = 0;                                   // commits of kYIssuer not yet waited for
-  auto issue_kq = [&](int c) {
+  // k rows of chunk c into buffer c & 1: raises the phase's byte count only
+  // (the arrive comes with the q rows), so the phase completes once both are in
+  auto issue_k = [&](int c) {
     const int t = (int)(tok0 + (int64_t)kChunk * c);
-    mbar_arrive_expect_tx(bar_kq, 65536);
+    mbar_expect_tx(bar_kq, 32768);
 #pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      tma_load_3d(sm + OFF_KQ + a * 16384, &tm_k, bar_kq, 64 * a, hq, t);
-      tma_load_3d(sm + OFF_KQ + a * 16384 + 8192, &tm_q, bar_kq, 64 * a, hq, t);
-    }
+    for (int a = 0; a < 4; ++a)
+      tma_load_3d(sm + OFF_KQ + a * kAtomKQ + (c & 1) * 2 * kRowsQ, &tm_k, bar_kq, 64 * a, hq, t);
     kq_pending = true;
+    q_owed = true;
+  };
+  auto issue_q = [&](int c) {
+    const int t = (int)(tok0 + (int64_t)kChunk * c);
+    mbar_arrive_expect_tx(bar_kq, 32768);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) tma_load_3d(sm + OFF_KQ + a * kAtomKQ + kRowsQ, &tm_q, bar_kq, 64 * a, hq, t);
+    q_owed = false;
+  };
+  // M1 of chunk c: [K;Q] K^T (even c) or [Q;K] K^T (odd c) -> R_A; false if its
+  // tiles never arrived
+  auto issue_m1 = [&](int c) -> bool {
+    if (!mbar_wait(bar_kq, ph_kq, prm.status)) return false;
+    ph_kq ^= 1;
+    kq_pending = false;
+    tc_fence_after();
+    const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
+    const uint32_t sb = (c & 1) * kRowsQ, kb = (c & 1) * 2 * kRowsQ;
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const uint32_t at = OFF_KQ + (s >> 2) * kAtomKQ + (s & 3) * 32;
+      mma_bf16(tmem + R_A, dsw(s4, at + sb, 16), dsw(s4, at + kb, 16), id, s > 0);
+    }
+    mma_commit(bar_mma);
+    ++mma_pending;
+    return true;
   };
   auto issue_v = [&](int c) {
     const int t = (int)(tok0 + (int64_t)kChunk * c);
@@ -213,7 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     tc_fence_after();
     return flags[1] == 0;
   };
-  const uint32_t s4 = (sbase & 0x3FFFFu) >> 4;
 
   float* graw = reinterpret_cast<float*>(sm + OFF_GRAW);
   auto fetch_gb = [&](int cc) {
@@ -294,7 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && c_begin < c_end) {
-      issue_kq(c_begin);
+      issue_k(c_begin);
+      issue_q(c_begin);
       issue_v(c_begin);
     }
     if (warp == 1 && c_begin < c_end) fetch_gb(c_begin);
@@ -325,30 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         *reinterpret_cast<float2*>(eg + 2 * lane) = make_float2(prm.scale * ex2_fast(g0), prm.scale * ex2_fast(g1));
       }
 
-      // ---- M1: [K;Q] K^T -> R_A (16 k-steps over d)
+      // ---- M1; then the next chunk's k into the other buffer (its last
+      // reader, the previous chunk's state update, is complete)
       if (tid == 0) {
-        if (!mbar_wait(bar_kq, ph_kq, prm.status)) {
-          flags[1] = 1;
-        } else {
-          ph_kq ^= 1;
-          kq_pending = false;
-          tc_fence_after();
-          const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
+        if (!issue_m1(c)) flags[1] = 1;
+        if (c + 1 < c_end && !flags[1]) issue_k(c + 1);
+        const int tn = (int)(t0 + kChunk);
 #pragma unroll
-          for (int s = 0; s < 16; ++s) {
-            const uint32_t a = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
-            mma_bf16(tmem + R_A, dsw(s4, a, 16), dsw(s4, a, 16), id, s > 0);
-          }
-          mma_commit(bar_mma);
-          ++mma_pending;
-        }
-        if (c + 1 < c_end) {
-          const int tn = (int)(t0 + kChunk);
-#pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            tma_prefetch_3d(&tm_k, 64 * a, hq, tn);
-            tma_prefetch_3d(&tm_q, 64 * a, hq, tn);
-          }
+        for (int a = 0; a < 4; ++a) {
+          if (c + 1 < c_end) tma_prefetch_3d(&tm_q, 64 * a, hq, tn);
+          if (c + 2 < c_end) tma_prefetch_3d(&tm_k, 64 * a, hq, tn + kChunk);
         }
         bulk_wait_read();   // the previous chunk's o staging has been read by its TMA store
       }
@@ -359,15 +382,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       {
         float v[32];
         const bool upper = (qd & 1) == 0 && hf == 1;
-        const int i = qd < 2 ? row : row - 64;
+        const bool isA = (qd < 2) != static_cast<bool>(c & 1);   // lanes of K K^T
+        const int i = row & 63;
         if (upper) {
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) v[jj] = 0.f;
         } else {
           tmem_ld32(tmem + R_A + lane_off + 32 * hf, v);
-          const float ri = qd < 2 ? bet[i] : prm.scale;
+          const float ri = isA ? bet[i] : prm.scale;
           const float gi = gam[i];
-          const int lim = qd < 2 ? i : i + 1;
+          const int lim = isA ? i : i + 1;
 #pragma unroll
           for (int k4 = 0; k4 < 8; ++k4) {
             const float4 gj = *reinterpret_cast<const float4*>(gam + 32 * hf + 4 * k4);
@@ -379,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
             }
           }
         }
-        if (qd < 2) {
+        if (isA) {
           float4* dst = reinterpret_cast<float4*>(As + i * kAsLd + 32 * hf);
 #pragma unroll
           for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -389,13 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         }
       }
 
-      // ---- S2 (warps 0, 2, 5, 7: diagonal blocks and 16-merges) beside
-      //      S4 (warps 1, 3, 4, 6: the state) and M3a (issued by kYIssuer once S4 is done)
-      if (warp == 0 || warp == 5) {
-        const int o = warp == 5 ? 32 : 0;
+      // ---- S2 beside S4 and M3a.  The two warps that wrote the 32 x 32
+      // diagonal blocks of A in S1 (warps 0 and 5 for even chunks, 2 and 7 for
+      // odd ones, whose A rows sit in the other TMEM lanes) solve their 16 x 16
+      // diagonal blocks and merge them with a partner warp (2 and 7, or 0 and
+      // 5); warps 1, 3, 4 and 6 convert the state (S4), and kYIssuer then
+      // issues M3a.
+      const bool oddc = c & 1;
+      const int w_sa = oddc ? 2 : 0, w_sb = oddc ? 7 : 5, w_pa = oddc ? 0 : 2, w_pb = oddc ? 5 : 7;
+      if (warp == w_sa || warp == w_sb) {
+        const int o = warp == w_sb ? 32 : 0;
         __syncwarp();
         diag_pair(As, o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
-        if (warp == 5) {
+        if (warp == w_sb) {
           named_bar64<2>();
           merge16_half<2>(As, tmp + 16 * 24, o, 0, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
         } else {
@@ -403,15 +433,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
           merge16_half<1>(As, tmp, o, 0, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
         }
       } else {
-        const int u = 32 * (warp - 1 - (warp > 5 ? 1 : 0)) + lane;
+        // the six other warps zero the upper 16 x 16 blocks of both operands
+        const int z = oddc ? warp - (warp > 2 ? 1 : 0) : warp - 1 - (warp > 5 ? 1 : 0);
+        const int u = 32 * z + lane;
         const int blk = u >> 5, r = (u >> 1) & 15, half = u & 1;
         const int rb = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
         const int cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
         const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
         *reinterpret_cast<uint4*>(sm + OFF_TB + off) = make_uint4(0u, 0u, 0u, 0u);
         *reinterpret_cast<uint4*>(sm + OFF_TBE + off) = make_uint4(0u, 0u, 0u, 0u);
-        if (warp == 2 || warp == 7) {
-          if (warp == 7) {
+        if (warp == w_pa || warp == w_pb) {
+          if (warp == w_pb) {
             named_bar64<2>();
             merge16_half<2>(As, tmp + 16 * 24, 32, 1, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
           } else {
@@ -445,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
 #pragma unroll
             for (int s = 0; s < 16; ++s) {
               const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-              const uint32_t b = OFF_KQ + (s >> 2) * 16384 + (s & 3) * 32;
+              const uint32_t b = OFF_KQ + (s >> 2) * kAtomKQ + (c & 1) * kRowsQ + (s & 3) * 32;
               mma_bf16(tmem + R_Y, dsw(s4, a, 16), dsw(s4, b, 16), id, s > 0);
             }
             mma_commit(bar_y);
@@ -460,9 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       // ---- S3: Y^T -> bf16 [e][j] (K-major A of M3b), over S^T's first atom
       wait_commit(bar_y, ph_y, y_pending, kYIssuer);
       tc_fence_after();
+      if (tid == 0 && c + 1 < c_end && !flags[1]) issue_q(c + 1);   // this chunk's q has been read
+      __syncwarp();
+      const uint32_t col_y = (c & 1) ? 64 : 0, col_oq = 64 - col_y;
       {
         float v[32];
-        tmem_ld32(tmem + R_Y + lane_off + 32 * hf, v);
+        tmem_ld32(tmem + R_Y + col_y + lane_off + 32 * hf, v);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_YT + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
       }
@@ -493,6 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       wait_commit(bar_x, ph_x, x_pending, 0);
       if (!sync_ok()) break;
       if (tid == 0 && c + 1 < c_end) issue_v(c + 1);   // v tile consumed
+      __syncwarp();
 
       // ---- S5: V'^T -> bf16 [e][j] ; V''^T = V'^T diag(e^{g_last - g}) -> bf16
       {
@@ -521,10 +557,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         ++q_pending;
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma_bf16(tmem + R_S, dsw(s4, OFF_VPP + s * 32, 16), dsw(s4, OFF_KQ + s * 2048, 16384), ids, 1);
+          mma_bf16(tmem + R_S, dsw(s4, OFF_VPP + s * 32, 16),
+                   dsw(s4, OFF_KQ + (c & 1) * 2 * kRowsQ + s * 2048, kAtomKQ), ids, 1);
         mma_commit(bar_x);
         ++x_pending;
       }
+      __syncwarp();   // warp 0 reconverges before the warp-collective TMEM loads
 
       // ---- S6: o_i = scale (e^{g_i} OQ_i + OP_i) -> staging -> global
       {
@@ -533,9 +571,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         uint8_t* lbase = sm + OFF_OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
         const uint32_t xsw = (static_cast<uint32_t>((ecol >> 3) ^ (odd ? 1 : 0))) << 4;
         float oq[2][16];
-        tmem_ld16(tmem + R_Y + 64 + lane_off + 32 * hf, oq[0]);
-        tmem_ld16(tmem + R_Y + 64 + lane_off + 32 * hf + 16, oq[1]);
+        tmem_ld16(tmem + R_Y + col_oq + lane_off + 32 * hf, oq[0]);
+        tmem_ld16(tmem + R_Y + col_oq + lane_off + 32 * hf + 16, oq[1]);
         wait_commit(bar_q, ph_q, q_pending, 0);   // OP^T
+        __syncwarp();
         tc_fence_after();
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -563,7 +602,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       }
       // the state update ran under S6; its completion frees the k / q tile
       wait_commit(bar_x, ph_x, x_pending, 0);
-      if (tid == 0 && c + 1 < c_end && !flags[1]) issue_kq(c + 1);
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
@@ -614,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     // abort: copies and MMAs already in flight finish (bounded) before the
     // shared memory and TMEM are released; each issuing thread waits for its own
     if (tid == 0) {
+      if (q_owed) mbar_arrive_expect_tx(bar_kq, 0);   // the phase's arrive, so that it can complete
       if (kq_pending) mbar_wait(bar_kq, ph_kq, prm.status, 100000000ull);
       if (v_pending) mbar_wait(bar_v, ph_v, prm.status, 100000000ull);
       for (; mma_pending > 0; --mma_pending, ph_mma ^= 1) mbar_wait(bar_mma, ph_mma, prm.status, 100000000ull);
