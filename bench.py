@@ -474,8 +474,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--B", type=int, default=16, help="batch override (profiling runs only; the metric is B=16)")
-    ap.add_argument("--T", type=int, default=8192,
-                    help="sequence length override of the batched workload (profiling runs only; the metric is T=8192)")
+    ap.add_argument("--T", type=int, default=None,
+                    help="sequence length override of the batched (8192) or long_d256 (32768) workload "
+                         "(profiling runs only)")
     ap.add_argument("--workload", default="batched_16x8192",
                     choices=["batched_16x8192", "gqa_prefill_1x4096", "long_1x32768", "varlen_64", "long_d256"],
                     help="chunk_fwd shape: the headline 16 x 8192 batch, one long GQA sequence (1 x 4096 or "
@@ -512,12 +513,12 @@ def main():
             dist.destroy_process_group()
         return
     if args.workload == "batched_16x8192":
-        w = I.WORKLOADS[2].with_(B=args.B, T=args.T, Hqk=args.H, Hv=args.H, seed=2 + rank)
+        w = I.WORKLOADS[2].with_(B=args.B, T=args.T or 8192, Hqk=args.H, Hv=args.H, seed=2 + rank)
         wname = f"batched_{w.B}x{w.T}_H{args.H}"
     elif args.workload == "varlen_64":
         w = I.WORKLOADS[3].with_(seed=3 + rank)
     elif args.workload == "long_d256":
-        w = I.WORKLOADS[4].with_(seed=4 + rank)
+        w = I.WORKLOADS[4].with_(T=args.T or 32768, seed=4 + rank)
         wname = f"long_d256_{w.B}x{w.T}_Hqk{w.Hqk}_Hv{w.Hv}"
     else:
         T = 4096 if args.workload == "gqa_prefill_1x4096" else 32768

@@ -12,10 +12,13 @@
 // chain's 64-token chunks in order.  Everything of a chunk that does not depend
 // on V (K K^T, Q K^T, gating, the triangular solve) is recomputed by each slice
 // of a chain; v, Y, U, V', o and the state are the slice's own.  One CTA per SM
-// (about 194 KB of shared memory, all 512 TMEM columns); equal-length
-// problems deal the (chain, slice) units' chunks out as windows of equal
-// length over the SMs, handing a cut unit's state slice over through the
-// workspace, exactly as the K = V = 128 kernel does.
+// (about 225 KB of shared memory, all 512 TMEM columns).  Equal-length
+// problems deal the chunks out as windows of equal length over the SMs,
+// handing a cut unit's state slice over through the workspace as the
+// K = V = 128 kernel does, but group-aligned: the G value heads x V / 128
+// slices of one qk head (UG units that read the same q and k) run in lockstep
+// on UG CTAs, window w taking unit w % UG of every qk head in its group's
+// range, so each q / k chunk comes from DRAM once and from L2 for the others.
 //
 // Products (M = 128 on the slice's value columns e, or on the 64 k rows
 // stacked over the 64 q rows).  The WY term is applied to the state through
@@ -100,11 +103,14 @@ struct Params {
   int32_t* status;
   int N, Tseq, Ttot, Hqk, Hv, V, NS, varlen;   // NS = V / kVS slices per chain
   float scale;
-  // window schedule over (chain, slice) units (null sched: one unit per CTA);
-  // the same dealing as the K = V = 128 kernel, with units in place of chains
+  // group-aligned window schedule (null sched: one unit per CTA): nwin = UG x
+  // window groups; group m covers positions [m W, (m + 1) W) of the qk heads'
+  // chunks laid end to end (each head's in reverse), window w = UG m + k runs
+  // unit k of those heads; a unit cut between groups m + 1 and m hands its
+  // state from window w + UG to window w
   int* sched;
   float* hand;   // nwin slots of kDK x kVS fp32
-  int nwin, W;
+  int nwin, W, UG;
   unsigned long long wait_ns;
   int drop_flag;
 };
@@ -270,10 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   };
   const int nch = (prm.Tseq + kChunk - 1) / kChunk;   // chunks per unit (window schedule)
   const int win = (int)flags[2];
+  const int wunit = WIN ? win % prm.UG : 0;             // this window's unit within each qk head
   int64_t wpos = 0, wend = 0;
   if (WIN) {
-    const int64_t U = (int64_t)prm.N * prm.Hv * prm.NS * nch;
-    wpos = (int64_t)win * prm.W;
+    const int64_t U = (int64_t)prm.N * prm.Hqk * nch;
+    wpos = (int64_t)(win / prm.UG) * prm.W;
     wend = wpos + prm.W < U ? wpos + prm.W : U;
   }
   int* hflag = WIN ? prm.sched + 1 : nullptr;
@@ -285,13 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     bool from_hand = false, to_hand = false;
     if (WIN) {
       if (wpos >= wend) break;
-      const int64_t j = wpos / nch, off = wpos - j * nch;
+      const int64_t j = wpos / nch, off = wpos - j * nch;   // j: qk head of the sequences' heads
       const int64_t len = (wend < (j + 1) * nch ? wend : (j + 1) * nch) - wpos;
-      const int chain = (int)(j / prm.NS);
-      e0 = (int)(j % prm.NS) * kVS;
-      n = chain / prm.Hv;
-      h = chain % prm.Hv;
-      hq = h / G;
+      n = (int)(j / prm.Hqk);
+      hq = (int)(j % prm.Hqk);
+      h = hq * G + wunit / prm.NS;
+      e0 = (wunit % prm.NS) * kVS;
       tok0 = (int64_t)n * prm.Tseq;
       L = prm.Tseq;
       nchunks = nch;
@@ -304,14 +310,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       break;
     }
     if (from_hand) {
-      if (tid == 0 && !flag_wait(hflag + win + 1, prm.status, prm.wait_ns)) flags[1] = 1;
+      if (tid == 0 && !flag_wait(hflag + win + prm.UG, prm.status, prm.wait_ns)) flags[1] = 1;
       __syncthreads();
       if (flags[1]) break;
     }
 
     // state slice S^T[e][d] = h0[d][e0 + e] (or the handed-over slot [d][e])
     {
-      const float* h0p = from_hand ? prm.hand + (int64_t)(win + 1) * kSlot
+      const float* h0p = from_hand ? prm.hand + (int64_t)(win + prm.UG) * kSlot
                                    : (prm.h0 ? prm.h0 + ((int64_t)n * prm.Hv + h) * kDK * prm.V + e0 : nullptr);
       const int64_t ld = from_hand ? kVS : prm.V;
 #pragma unroll 1
@@ -667,22 +673,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
-// Window schedule over the (chain, slice) units of an equal-length problem:
-// one CTA per SM.
+// Group-aligned window schedule of an equal-length problem: UG = G x V / 128
+// units per qk head, as many groups of UG windows as the SMs hold (at least
+// one), W chunks of the qk heads' chunk order per group (at least one unit's).
 struct Windows {
-  int64_t W = 0, nwin = 0;
+  int64_t W = 0, nwin = 0, UG = 0;
 };
 
 Windows windows_of(const gdn_problem& p) {
   Windows w;
   if (p.varlen) return w;
   const int64_t nch = ((int64_t)p.T + kChunk - 1) / kChunk;
-  const int64_t U = (int64_t)p.N * p.Hv * (p.V / kVS) * nch;
+  const int64_t U = (int64_t)p.N * p.Hqk * nch;
   if (U == 0) return w;
-  const int64_t G = sm_count();
-  w.W = (U + G - 1) / G;
+  w.UG = (int64_t)(p.Hv / p.Hqk) * (p.V / kVS);
+  int64_t groups = sm_count() / w.UG;
+  if (groups < 1) groups = 1;
+  w.W = (U + groups - 1) / groups;
   if (w.W < nch) w.W = nch;
-  w.nwin = (U + w.W - 1) / w.W;
+  w.nwin = w.UG * ((U + w.W - 1) / w.W);
   return w;
 }
 
@@ -707,9 +716,10 @@ size_t fused256_workspace_bytes(const gdn_problem& p) {
 bool fused256_handover_window(const gdn_problem& p, int window) {
   if (!fused256_supported(p)) return false;
   const Windows w = windows_of(p);
-  if (!cuts_units(p, w) || window < 1 || window >= w.nwin) return false;
+  if (!cuts_units(p, w) || window < w.UG || window >= w.nwin) return false;
+  // window - UG ends with the suffix of a unit whose prefix `window` runs
   const int64_t nch = ((int64_t)p.T + kChunk - 1) / kChunk;
-  return ((int64_t)window * w.W) % nch != 0;
+  return ((int64_t)(window / w.UG) * w.W) % nch != 0;
 }
 
 gdn_status run_fused256(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
@@ -766,6 +776,7 @@ gdn_status run_fused256(const gdn_problem& p, const void* q, const void* k, cons
   prm.hand = cuts_units(p, w) ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sched_bytes(w)) : nullptr;
   prm.nwin = (int)w.nwin;
   prm.W = (int)w.W;
+  prm.UG = (int)w.UG;
   prm.wait_ns = wait_ns;
   prm.drop_flag = drop_flag;
   auto kernel = prm.sched ? gdn_fused256_kernel<true> : gdn_fused256_kernel<false>;
