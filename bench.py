@@ -467,7 +467,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--H", type=int, default=32, choices=[16, 32, 48, 64])
-    ap.add_argument("--path", default="auto", choices=["auto", "staged", "fused"])
+    ap.add_argument("--path", default="auto", choices=["auto", "staged", "fused", "fused1"])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-split", type=int, default=8,
                     help="sub-batches of the end-to-end leg (host buffers streamed through the GPU)")
@@ -632,7 +632,7 @@ def main():
         # a tensor-bound step is one long launch: the sustained bf16 figure
         achieved, peak, unit = flops / sec / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
         peak_kind = "bf16 sustained"
-    launches = {"staged": 7, "fused": 1, "cp": 4}[path]
+    launches = {"staged": 7, "fused": 1, "fused1": 1, "cp": 4}[path]
     line = {
         "metric": METRIC if args.workload == "batched_16x8192" else f"GDN chunk-fwd tokens/s ({wname}, bf16); % roofline",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -647,11 +647,11 @@ def main():
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": (measured_traffic("fused", w.B * w.T / 8192 * w.Hv / 32, state_bytes)
                                  if path == "fused" and args.workload == "batched_16x8192" else
-                                 measured_traffic("fused256", w.B * w.T / 32768, state_bytes)
-                                 if path == "fused" and args.workload == "long_d256" else None),
+                                 measured_traffic("fused1_d256", w.B * w.T / 32768, state_bytes)
+                                 if path in ("fused", "fused1") and args.workload == "long_d256" else None),
                      "peak_source": f"{pk['source']} ({peak_kind})",
-                     "kernel": (("gdn_fused256_kernel" if w.K == 256 else "gdn_fused_kernel") +
-                                " (the step's only launch)") if path == "fused"
+                     "kernel": (("gdn_fused1_kernel" if (w.K == 256 or path == "fused1") else "gdn_fused_kernel") +
+                                " (the step's only launch)") if path in ("fused", "fused1")
                      else "gdn_chunk_fwd call (all launches of one step)",
                      "alg_bytes": nbytes, "alg_flops": flops, "alg_flops_at_requested_C": flops_req,
                      "t_hbm_ms": 1e3 * t_hbm, "t_tensor_ms": 1e3 * t_tc},

@@ -17,7 +17,7 @@ import torch
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_DEVICE = range(5)
 GDN_F32, GDN_BF16 = 0, 1
-PATHS = {"auto": 0, "staged": 1, "fused": 2, "cp": 3}
+PATHS = {"auto": 0, "staged": 1, "fused": 2, "cp": 3, "fused1": 4}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 DEV_OK, DEV_BAD_CU_SEQLENS, DEV_WAIT_TIMEOUT = 0, 1, 2
 STAGES = {"prepare": 0, "cumsum": 1, "kkt": 2, "solve_tril": 3, "wy_fast": 4, "chunk_h": 5, "chunk_o": 6}
@@ -207,7 +207,7 @@ def gdn_chunk_fwd(q, k, v, g, beta, scale: Optional[float] = None, h0=None, cu_s
         ht = torch.empty((p.N, p.Hv, p.K, p.V), dtype=torch.float32, device=q.device)
     need = gdn_chunk_fwd_workspace_size(p, path)
     if need == 0:
-        raise GDNError(GDN_ERR_UNSUPPORTED if path in ("fused", "cp") else GDN_ERR_INVALID_ARG, "gdn_chunk_fwd_workspace_size")
+        raise GDNError(GDN_ERR_UNSUPPORTED if path in ("fused", "cp", "fused1") else GDN_ERR_INVALID_ARG, "gdn_chunk_fwd_workspace_size")
     if workspace is None:
         workspace = _alloc_ws(need, q.device)
     s = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream

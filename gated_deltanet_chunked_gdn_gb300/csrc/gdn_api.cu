@@ -35,17 +35,28 @@ bool problem_ok(const gdn_problem* pp, gdn_problem* out) {
 
 gdn_path resolve(const gdn_problem& p, gdn_path path) {
   if (path == GDN_PATH_AUTO) {
-    if (!fused_supported(p)) return GDN_PATH_STAGED;
-    return cp_preferred(p) ? GDN_PATH_CP : GDN_PATH_FUSED;
+    if (!fused_supported(p) && !fused1_supported(p)) return GDN_PATH_STAGED;
+    if (!fused128_supported(p)) return GDN_PATH_FUSED1;
+    if (cp_preferred(p)) return GDN_PATH_CP;
+    return fused1_preferred(p) ? GDN_PATH_FUSED1 : GDN_PATH_FUSED;
   }
   return path;
 }
 
 bool path_ok(gdn_path path) {
-  return path == GDN_PATH_AUTO || path == GDN_PATH_STAGED || path == GDN_PATH_FUSED || path == GDN_PATH_CP;
+  return path == GDN_PATH_AUTO || path == GDN_PATH_STAGED || path == GDN_PATH_FUSED || path == GDN_PATH_CP ||
+         path == GDN_PATH_FUSED1;
+}
+
+bool path_supported(const gdn_problem& p, gdn_path path) {
+  if (path == GDN_PATH_FUSED) return fused_supported(p);
+  if (path == GDN_PATH_FUSED1) return fused1_supported(p);
+  if (path == GDN_PATH_CP) return fused128_supported(p);
+  return true;
 }
 
 size_t workspace_for(const gdn_problem& p, gdn_path path) {
+  if (path == GDN_PATH_FUSED1) return fused1_workspace_bytes(p);
   if (path == GDN_PATH_FUSED) return fused_workspace_bytes(p);
   if (path == GDN_PATH_CP) return cp_workspace_bytes(p);
   gdn_staged_layout_t L;
@@ -54,7 +65,7 @@ size_t workspace_for(const gdn_problem& p, gdn_path path) {
 }
 
 size_t status_offset(const gdn_problem& p, gdn_path path) {
-  if (path == GDN_PATH_FUSED) return fused_status_offset(p);
+  if (path == GDN_PATH_FUSED || path == GDN_PATH_FUSED1) return fused_status_offset(p);
   if (path == GDN_PATH_CP) return 0;
   gdn_staged_layout_t L;
   staged_layout(p, &L);
@@ -89,8 +100,7 @@ size_t gdn_chunk_fwd_workspace_size(const gdn_problem* pp, gdn_path path) {
   if (!problem_ok(pp, &p)) return 0;
   if (!path_ok(path)) return 0;
   path = resolve(p, path);
-  if (path == GDN_PATH_FUSED && !fused_supported(p)) return 0;
-  if (path == GDN_PATH_CP && !fused128_supported(p)) return 0;
+  if (!path_supported(p, path)) return 0;
   return workspace_for(p, path);
 }
 
@@ -108,13 +118,13 @@ gdn_status gdn_chunk_fwd(const gdn_problem* pp, gdn_path path, const void* q, co
   if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
   if (!path_ok(path)) return GDN_ERR_INVALID_ARG;
   path = resolve(p, path);
-  if (path == GDN_PATH_FUSED && !fused_supported(p)) return GDN_ERR_UNSUPPORTED;
-  if (path == GDN_PATH_CP && !fused128_supported(p)) return GDN_ERR_UNSUPPORTED;
+  if (!path_supported(p, path)) return GDN_ERR_UNSUPPORTED;
   gdn_status st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, workspace, workspace_bytes,
                              workspace_for(p, path));
   if (st != GDN_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (path == GDN_PATH_FUSED) return run_fused(p, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, s);
+  if (path == GDN_PATH_FUSED1) return run_fused1(p, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, s);
   if (path == GDN_PATH_CP)
     return run_cp(p, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, workspace_bytes, s);
   return run_staged(p, 6, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, workspace, s);
@@ -156,18 +166,24 @@ gdn_status gdn_get_device_status(const gdn_problem* pp, gdn_path path, void* wor
   return GDN_OK;
 }
 
-gdn_status gdn_selftest_handover_timeout(const gdn_problem* pp, const void* q, const void* k, const void* v,
+gdn_status gdn_selftest_handover_timeout(const gdn_problem* pp, gdn_path path, const void* q, const void* k,
+                                         const void* v,
                                          const float* g, const float* beta, float scale, const float* h0, void* o,
                                          float* ht, void* workspace, size_t workspace_bytes, int drop_window,
                                          long long wait_ns, void* stream) {
   gdn_problem p;
   if (!problem_ok(pp, &p) || p.varlen || wait_ns <= 0) return GDN_ERR_INVALID_ARG;
-  if (!fused_handover_window(p, drop_window)) return GDN_ERR_UNSUPPORTED;
+  if (path != GDN_PATH_FUSED && path != GDN_PATH_FUSED1) return GDN_ERR_INVALID_ARG;
+  const bool one = path == GDN_PATH_FUSED1;
+  if (!(one ? fused1_supported(p) && fused1_handover_window(p, drop_window) : fused_handover_window(p, drop_window)))
+    return GDN_ERR_UNSUPPORTED;
   gdn_status st = check_call(p, q, k, v, g, beta, h0, nullptr, o, ht, workspace, workspace_bytes,
-                             workspace_for(p, GDN_PATH_FUSED));
+                             workspace_for(p, path));
   if (st != GDN_OK) return st;
-  return run_fused(p, q, k, v, g, beta, scale, h0, nullptr, o, ht, workspace, static_cast<cudaStream_t>(stream),
-                   drop_window, static_cast<unsigned long long>(wait_ns));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const unsigned long long lim = static_cast<unsigned long long>(wait_ns);
+  return one ? run_fused1(p, q, k, v, g, beta, scale, h0, nullptr, o, ht, workspace, s, drop_window, lim)
+             : run_fused(p, q, k, v, g, beta, scale, h0, nullptr, o, ht, workspace, s, drop_window, lim);
 }
 
 gdn_status gdn_recurrent_fwd(const gdn_problem* pp, const void* q, const void* k, const void* v, const float* a,

@@ -709,7 +709,9 @@ bool fused128_supported(const gdn_problem& p) {
   return p.dt == GDN_BF16 && p.K == kD && p.V == kD && (p.C == 64 || p.C == 128);
 }
 
-bool fused_supported(const gdn_problem& p) { return fused128_supported(p) || fused256_supported(p); }
+bool fused_supported(const gdn_problem& p) { return fused128_supported(p) || (fused1_supported(p) && p.K == 256); }
+
+
 
 namespace {
 
@@ -748,8 +750,22 @@ bool cuts_chains(const gdn_problem& p, const Windows& w) {
 
 }  // namespace
 
+// K = V = 128: the one-CTA-per-SM kernel when the chains do not fill the SMs
+// (each chain has an SM to itself either way, and its chunks are about twice as
+// fast there), and for packed batches small enough (at most 128 chunks a CTA
+// slot of the two-CTA kernel, counting ceil(T / 64) + N chunks a value head)
+// that their longest sequence, not their total work, is what bounds the step.
+bool fused1_preferred(const gdn_problem& p) {
+  if (!fused1_supported(p) || p.K != 128) return false;
+  const int64_t chains = (int64_t)p.N * p.Hv;
+  if (chains <= sm_count()) return true;
+  if (!p.varlen) return false;
+  const int64_t chunk_heads = (((int64_t)p.T + kChunk - 1) / kChunk + p.N) * p.Hv;
+  return chunk_heads <= (int64_t)kCtasPerSm * sm_count() * 128;
+}
+
 size_t fused_workspace_bytes(const gdn_problem& p) {
-  if (fused256_supported(p)) return fused256_workspace_bytes(p);
+  if (!fused128_supported(p)) return fused1_workspace_bytes(p);
   const Windows w = fused_windows(p);
   if (!w.handover()) return kAlign;   // the status word
   return sched_bytes(w) + (cuts_chains(p, w) ? (size_t)w.nwin * kD * kD * sizeof(float) : 0);
@@ -816,9 +832,10 @@ gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const voi
 gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
                      const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
                      void* ws, cudaStream_t s, int drop_flag, unsigned long long wait_ns) {
-  if (fused256_supported(p))
-    return run_fused256(p, q, k, v, g, beta, scale, h0, cu, o, ht, ws, s, drop_flag, wait_ns);
-  if (!fused128_supported(p)) return GDN_ERR_UNSUPPORTED;
+  if (!fused128_supported(p)) {
+    if (!fused_supported(p)) return GDN_ERR_UNSUPPORTED;
+    return run_fused1(p, q, k, v, g, beta, scale, h0, cu, o, ht, ws, s, drop_flag, wait_ns);
+  }
   int32_t* status = static_cast<int32_t*>(ws);
   const Windows w = fused_windows(p);
   if (cudaMemsetAsync(status, 0, w.handover() ? sizeof(int32_t) * (2 + w.nwin) : sizeof(int32_t), s) != cudaSuccess)
@@ -840,8 +857,7 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
 }
 
 bool fused_handover_window(const gdn_problem& p, int window) {
-  if (fused256_supported(p)) return fused256_handover_window(p, window);
-  if (!fused128_supported(p)) return false;
+  if (!fused128_supported(p)) return fused_supported(p) && fused1_handover_window(p, window);
   const Windows w = fused_windows(p);
   if (!cuts_chains(p, w) || window < 1 || window >= w.nwin) return false;
   // window - 1 ends with the suffix of a chain whose prefix `window` runs

@@ -1,24 +1,25 @@
-// gdn_fused256.cu -- the fused path for head dimension K = 256 (V a multiple
-// of 128): the whole chunk pipeline (cumsum, scaled_dot_kkt, solve_tril,
+// gdn_fused1.cu -- the fused forward pass with ONE CTA per SM (all 512 TMEM
+// columns): the whole chunk pipeline (cumsum, scaled_dot_kkt, solve_tril,
 // wy_fast, chunk_h, chunk_o; MegaGDN-PTO walkthrough, sections 1.1 and 4.5) in
-// ONE sm_103a launch, as for K = V = 128, for the large-head-dim shapes the
-// pages specialise for (TileLang x xLLM page, the build-specialisation step:
-// H = 32 value heads on 8 qk groups, D = 256).
+// one sm_103a launch, for key dimension DK = 256 (the large-head-dim shapes the
+// pages specialise for: TileLang x xLLM page, the build-specialisation step, H
+// = 32 value heads on 8 qk groups, D = 256) and DK = 128 (the latency form of
+// the K = V = 128 pass: for chains that do not share an SM, its chunks take
+// about half the time of the two-CTA kernel's).
 //
-// A 256 x 256 fp32 state is the whole of an SM's tensor memory, so the value
-// dimension is cut into slices of 128 columns: a CTA owns one slice of one
-// (sequence, value head) chain -- its 256 x 128 fp32 state slice S^T[e][d]
-// lives in TMEM (256 of the 512 columns) for the whole chain -- and walks the
-// chain's 64-token chunks in order.  Everything of a chunk that does not depend
-// on V (K K^T, Q K^T, gating, the triangular solve) is recomputed by each slice
-// of a chain; v, Y, U, V', o and the state are the slice's own.  One CTA per SM
-// (about 225 KB of shared memory, all 512 TMEM columns).  Equal-length
-// problems deal the chunks out as windows of equal length over the SMs,
-// handing a cut unit's state slice over through the workspace as the
-// K = V = 128 kernel does, but group-aligned: the G value heads x V / 128
-// slices of one qk head (UG units that read the same q and k) run in lockstep
-// on UG CTAs, window w taking unit w % UG of every qk head in its group's
-// range, so each q / k chunk comes from DRAM once and from L2 for the others.
+// The value dimension is cut into slices of 128 columns (a 256 x 256 fp32
+// state is all of an SM's tensor memory): a CTA owns one slice of one
+// (sequence, value head) chain -- its DK x 128 fp32 state slice S^T[e][d]
+// lives in TMEM for the whole chain -- and walks the chain's 64-token chunks
+// in order.  Everything of a chunk that does not depend on V (K K^T, Q K^T,
+// gating, the triangular solve) is recomputed by each slice of a chain; v, Y,
+// U, V', o and the state are the slice's own.  Equal-length problems deal the
+// chunks out as windows of equal length over the SMs, handing a cut unit's
+// state slice over through the workspace as the two-CTA kernel does, but
+// group-aligned: the G value heads x V / 128 slices of one qk head (UG units
+// that read the same q and k) run in lockstep on UG CTAs, window w taking unit
+// w % UG of every qk head in its group's range, so each q / k chunk comes from
+// DRAM once and from L2 for the others.
 //
 // Products (M = 128 on the slice's value columns e, or on the 64 k rows
 // stacked over the 64 q rows).  The WY term is applied to the state through
@@ -26,21 +27,21 @@
 // V' = U - T diag(beta e^g) K S = U - (T diag(beta e^g)) Y, so no W = T diag(beta
 // e^g) K is formed, and Y comes out of the same product as the query term:
 //
-//   M1  [K;Q] K^T                  -> R_A   (M128 N64, 16 k-steps over d)
+//   M1  [K;Q] K^T                  -> R_A   (M128 N64, DK / 16 k-steps over d)
 //   S1  A = strict-lower(beta_i e^{g_i - g_j} K K^T) -> smem fp32, P -> smem bf16
 //   S2  T = (I + A)^{-1}; T diag(beta), T diag(beta e^g) -> bf16       (warps 0, 2, 5, 7, then all)
 //   S4  S^T (fp32, TMEM) -> bf16 [e][d]; S^T *= e^{g_last}            (warps 1, 3, 4, 6, beside S2)
-//   M3a [Y^T | OQ^T] = S^T [K;Q]^T -> R_Y   (M128 N128, 16 k-steps; runs under the solve's merges)
+//   M3a [Y^T | OQ^T] = S^T [K;Q]^T -> R_Y   (M128 N128, DK / 16 k-steps; runs under the solve's merges)
 //   S3  Y^T -> bf16 [e][j]
 //   M3b V'^T = V^T (T diag(beta))^T - Y^T (T diag(beta e^g))^T -> R_B  (8 k-steps)
 //   S5  V'^T -> bf16, V''^T = V'^T diag(e^{g_last - g}) -> bf16
-//   M4  OP^T = V'^T P^T -> R_B;  S^T += V''^T K (N = 256) -> R_S
+//   M4  OP^T = V'^T P^T -> R_B;  S^T += V''^T K (N = DK) -> R_S
 //   S6  o_i = scale e^{g_i} OQ_i + OP_i -> staging -> TMA store
 //
 // The k rows are double-buffered inside the [k; q] tile (per 64-column atom:
 // k of even chunks, q, k of odd chunks), so the next chunk's k is loaded while
 // this chunk runs and its q as soon as M3a has read this chunk's q: the next
-// M1 no longer waits for a 64 KB load issued at the end of the chunk.  Odd
+// M1 no longer waits for the whole tile, loaded at the end of the chunk.  Odd
 // chunks read the stacked operand as [q; k]: their M1 rows and M3a columns
 // come out in the other order.
 #include <string.h>
@@ -53,46 +54,46 @@ namespace {
 using namespace sm100;
 using namespace solve64;
 
-constexpr int kDK = 256;         // K
 constexpr int kVS = 128;         // value columns of one slice
 constexpr int kTmemCols = 512;
-
-// TMEM columns (lane = slice column e, or chunk row)
-constexpr uint32_t R_S = 0;      // S^T[e][d], d = 0..255
-constexpr uint32_t R_A = 256;    // [K;Q] K^T (even chunks) or [Q;K] K^T (odd chunks)
-constexpr uint32_t R_Y = 320;    // [Y^T | OQ^T] (even chunks) or [OQ^T | Y^T] (odd chunks), 64 columns each
-constexpr uint32_t R_B = 448;    // V'^T[e][i] -> OP^T
-
-// shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_KQ = 0;          // 4 atom columns (d 64a..64a+63) of [k even ; q ; k odd], 24 KB each
-constexpr uint32_t kAtomKQ = 24576;
+constexpr uint32_t kAtomKQ = 24576;     // one 64-column atom of the [k even ; q ; k odd] tile
 constexpr uint32_t kRowsQ = 8192;       // byte offset of the q rows in an atom (k of odd chunks: 2 kRowsQ)
-constexpr uint32_t OFF_V = 98304;       // v slice rows 0..63 x 128 e, 2 atom columns of 8 KB
-constexpr uint32_t OFF_TB = 114688;     // T diag(beta) [i][j] bf16, 8 KB
-constexpr uint32_t OFF_TBE = 122880;    // T diag(beta e^g) [i][j] bf16, 8 KB
-constexpr uint32_t OFF_P = 131072;      // P [i][j] bf16, 8 KB
-constexpr uint32_t OFF_AS = 139264;     // A / T fp32 [64][68] and the merges' scratch
-constexpr uint32_t OFF_TMP = OFF_AS + 64 * 68 * 4;
-constexpr uint32_t OFF_ST = 161792;     // S^T bf16 [e][d], 4 atom columns of 16 KB; after M3a reused:
-constexpr uint32_t OFF_YT = OFF_ST;            //   Y^T bf16 [e][j]
-constexpr uint32_t OFF_VP = OFF_ST + 16384;    //   V'^T bf16 [e][j]
-constexpr uint32_t OFF_VPP = OFF_ST + 32768;   //   V''^T bf16 [e][j]
-constexpr uint32_t OFF_OS = OFF_ST + 49152;    //   o staging bf16: 2 boxes [64 rows][64 e]
-constexpr uint32_t OFF_MISC = 227328;
-constexpr uint32_t OFF_GAM = OFF_MISC;
-constexpr uint32_t OFF_BET = OFF_MISC + 256;
-constexpr uint32_t OFF_BE = OFF_MISC + 512;
-constexpr uint32_t OFF_DL = OFF_MISC + 768;
-constexpr uint32_t OFF_EG = OFF_MISC + 1024;
-constexpr uint32_t OFF_BAR = OFF_MISC + 1280;    // 6 mbarriers: k/q, v, M1, M3a, M3b / M4 state, OP
-constexpr uint32_t OFF_FLAGS = OFF_MISC + 1328;  // [0] tmem base, [1] abort, [2] window
-constexpr uint32_t OFF_GRAW = OFF_MISC + 1344;   // float[2][2][64]: raw g, beta of two chunks
-constexpr uint32_t kSmemUsed = OFF_MISC + 2368;
-constexpr uint32_t kSmemBytes = kSmemUsed + 1024;   // + alignment slack
 
-static_assert(OFF_TMP + 32 * 40 * 4 <= OFF_ST, "solve scratch overflows into S^T");
-static_assert(kSmemBytes <= 232448, "one CTA must fit an SM");
-static_assert(OFF_ST % 1024 == 0 && OFF_TB % 1024 == 0 && OFF_P % 1024 == 0 && OFF_V % 1024 == 0, "atom alignment");
+__host__ __device__ constexpr uint32_t up1024(uint32_t x) { return (x + 1023u) / 1024u * 1024u; }
+
+// Shared-memory map (bytes from a 1024-aligned base) and TMEM columns of the
+// kernel for key dimension DK (128 or 256).
+template <int DK>
+struct Map {
+  static constexpr int NA = DK / 64;                      // 64-column atoms of the key dimension
+  static constexpr uint32_t KQ = 0;                       // NA atoms of [k even ; q ; k odd]
+  static constexpr uint32_t V = NA * kAtomKQ;             // v slice rows 0..63 x 128 e, 2 atoms of 8 KB
+  static constexpr uint32_t TB = V + 16384;               // T diag(beta) [i][j] bf16, 8 KB
+  static constexpr uint32_t TBE = TB + 8192;              // T diag(beta e^g) [i][j] bf16, 8 KB
+  static constexpr uint32_t P = TBE + 8192;               // P [i][j] bf16, 8 KB
+  static constexpr uint32_t AS = P + 8192;                // A / T fp32 [64][68] and the merges' scratch
+  static constexpr uint32_t TMP = AS + 64 * 68 * 4;
+  static constexpr uint32_t ST = up1024(TMP + 32 * 40 * 4);   // S^T bf16 [e][d], NA atoms of 16 KB; after M3a:
+  static constexpr uint32_t YT = ST;                      //   Y^T bf16 [e][j]
+  static constexpr uint32_t VP = ST + 16384;              //   V'^T bf16 [e][j]
+  static constexpr uint32_t VPP = ST + 32768;             //   V''^T bf16 [e][j]
+  static constexpr uint32_t OS = ST + 49152;              //   o staging bf16: 2 boxes [64 rows][64 e]
+  static constexpr uint32_t MISC = ST + (NA * 16384 > 65536 ? NA * 16384 : 65536);
+  static constexpr uint32_t GAM = MISC, BET = MISC + 256, BE = MISC + 512, DL = MISC + 768, EG = MISC + 1024;
+  static constexpr uint32_t BAR = MISC + 1280;            // 6 mbarriers: k/q, v, M1, M3a, M3b / M4 state, OP
+  static constexpr uint32_t FLAGS = MISC + 1328;          // [0] tmem base, [1] abort, [2] window
+  static constexpr uint32_t GRAW = MISC + 1344;           // float[2][2][64]: raw g, beta of two chunks
+  static constexpr uint32_t SMEM = MISC + 2368 + 1024;    // + alignment slack
+  // TMEM columns (lane = slice column e, or chunk row)
+  static constexpr uint32_t R_S = 0;                      // S^T[e][d], d = 0..DK-1
+  static constexpr uint32_t R_A = DK;                     // [K;Q] K^T (even chunks) or [Q;K] K^T (odd)
+  static constexpr uint32_t R_Y = DK + 64;                // [Y^T | OQ^T] (even) or [OQ^T | Y^T] (odd)
+  static constexpr uint32_t R_B = DK + 192;               // V'^T[e][i] -> OP^T
+  static_assert(SMEM <= 232448, "one CTA must fit an SM");
+  static_assert(R_B + 64 <= kTmemCols, "TMEM");
+  static_assert(V % 1024 == 0 && TB % 1024 == 0 && P % 1024 == 0 && ST % 1024 == 0, "atom alignment");
+};
+
 struct Params {
   const float* g;
   const float* beta;
@@ -109,29 +110,31 @@ struct Params {
   // unit k of those heads; a unit cut between groups m + 1 and m hands its
   // state from window w + UG to window w
   int* sched;
-  float* hand;   // nwin slots of kDK x kVS fp32
+  float* hand;   // nwin slots of K x kVS fp32
   int nwin, W, UG;
   unsigned long long wait_ns;
   int drop_flag;
 };
 
-template <bool WIN>
-__global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_constant__ CUtensorMap tm_q,
+template <int DK, bool WIN>
+__global__ void __launch_bounds__(kThreads, 1) gdn_fused1_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                    const __grid_constant__ CUtensorMap tm_k,
                                                                    const __grid_constant__ CUtensorMap tm_v,
                                                                    const __grid_constant__ CUtensorMap tm_o,
                                                                    const Params prm) {
+  using M = Map<DK>;
+  constexpr int NA = M::NA;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(sm);
-  float* As = reinterpret_cast<float*>(sm + OFF_AS);
-  float* tmp = reinterpret_cast<float*>(sm + OFF_TMP);
-  float* gam = reinterpret_cast<float*>(sm + OFF_GAM);
-  float* bet = reinterpret_cast<float*>(sm + OFF_BET);
-  float* be = reinterpret_cast<float*>(sm + OFF_BE);
-  float* dl = reinterpret_cast<float*>(sm + OFF_DL);
-  float* eg = reinterpret_cast<float*>(sm + OFF_EG);
-  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  float* As = reinterpret_cast<float*>(sm + M::AS);
+  float* tmp = reinterpret_cast<float*>(sm + M::TMP);
+  float* gam = reinterpret_cast<float*>(sm + M::GAM);
+  float* bet = reinterpret_cast<float*>(sm + M::BET);
+  float* be = reinterpret_cast<float*>(sm + M::BE);
+  float* dl = reinterpret_cast<float*>(sm + M::DL);
+  float* eg = reinterpret_cast<float*>(sm + M::EG);
+  uint64_t* bar_kq = reinterpret_cast<uint64_t*>(sm + M::BAR);
   uint64_t* bar_v = bar_kq + 1;
   // MMA commit groups; every thread waits for every commit, in order, so all
   // threads track the same phases
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   uint64_t* bar_y = bar_kq + 3;     // M3a (issued by thread kYIssuer)
   uint64_t* bar_x = bar_kq + 4;     // M3b, then the state update (M4)
   uint64_t* bar_q = bar_kq + 5;     // OP^T (M4)
-  volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sm + OFF_FLAGS);
+  volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sm + M::FLAGS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3, hf = warp >> 2;   // TMEM lane quadrant, column half
@@ -207,21 +210,21 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   // (the arrive comes with the q rows), so the phase completes once both are in
   auto issue_k = [&](int c) {
     const int t = (int)(tok0 + (int64_t)kChunk * c);
-    mbar_expect_tx(bar_kq, 32768);
+    mbar_expect_tx(bar_kq, NA * 8192);
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-      tma_load_3d(sm + OFF_KQ + a * kAtomKQ + (c & 1) * 2 * kRowsQ, &tm_k, bar_kq, 64 * a, hq, t);
+    for (int a = 0; a < NA; ++a)
+      tma_load_3d(sm + M::KQ + a * kAtomKQ + (c & 1) * 2 * kRowsQ, &tm_k, bar_kq, 64 * a, hq, t);
     kq_pending = true;
     q_owed = true;
   };
   auto issue_q = [&](int c) {
     const int t = (int)(tok0 + (int64_t)kChunk * c);
-    mbar_arrive_expect_tx(bar_kq, 32768);
+    mbar_arrive_expect_tx(bar_kq, NA * 8192);
 #pragma unroll
-    for (int a = 0; a < 4; ++a) tma_load_3d(sm + OFF_KQ + a * kAtomKQ + kRowsQ, &tm_q, bar_kq, 64 * a, hq, t);
+    for (int a = 0; a < NA; ++a) tma_load_3d(sm + M::KQ + a * kAtomKQ + kRowsQ, &tm_q, bar_kq, 64 * a, hq, t);
     q_owed = false;
   };
-  // M1 of chunk c: [K;Q] K^T (even c) or [Q;K] K^T (odd c) -> R_A; false if its
+  // M1 of chunk c: [K;Q] K^T (even c) or [Q;K] K^T (odd c) -> M::R_A; false if its
   // tiles never arrived
   auto issue_m1 = [&](int c) -> bool {
     if (!mbar_wait(bar_kq, ph_kq, prm.status)) return false;
@@ -231,9 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     const uint32_t id = idesc_bf16(128, 64, 0, 0, 0);
     const uint32_t sb = (c & 1) * kRowsQ, kb = (c & 1) * 2 * kRowsQ;
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      const uint32_t at = OFF_KQ + (s >> 2) * kAtomKQ + (s & 3) * 32;
-      mma_bf16(tmem + R_A, dsw(s4, at + sb, 16), dsw(s4, at + kb, 16), id, s > 0);
+    for (int s = 0; s < DK / 16; ++s) {
+      const uint32_t at = M::KQ + (s >> 2) * kAtomKQ + (s & 3) * 32;
+      mma_bf16(tmem + M::R_A, dsw(s4, at + sb, 16), dsw(s4, at + kb, 16), id, s > 0);
     }
     mma_commit(bar_mma);
     ++mma_pending;
@@ -242,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
   auto issue_v = [&](int c) {
     const int t = (int)(tok0 + (int64_t)kChunk * c);
     mbar_arrive_expect_tx(bar_v, 16384);
-    tma_load_3d(sm + OFF_V, &tm_v, bar_v, e0, h, t);
-    tma_load_3d(sm + OFF_V + 8192, &tm_v, bar_v, e0 + 64, h, t);
+    tma_load_3d(sm + M::V, &tm_v, bar_v, e0, h, t);
+    tma_load_3d(sm + M::V + 8192, &tm_v, bar_v, e0 + 64, h, t);
     v_pending = true;
   };
   auto wait_commit = [&](uint64_t* bar, uint32_t& ph, int& pending, int owner) {
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     return flags[1] == 0;
   };
 
-  float* graw = reinterpret_cast<float*>(sm + OFF_GRAW);
+  float* graw = reinterpret_cast<float*>(sm + M::GRAW);
   auto fetch_gb = [&](int cc) {
     float* dst = graw + (cc & 1) * 128;
 #pragma unroll
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     wend = wpos + prm.W < U ? wpos + prm.W : U;
   }
   int* hflag = WIN ? prm.sched + 1 : nullptr;
-  constexpr int64_t kSlot = (int64_t)kDK * kVS;   // floats of one hand-over slot
+  constexpr int64_t kSlot = (int64_t)DK * kVS;   // floats of one hand-over slot
 
 #pragma unroll 1
   for (bool first = true;; first = false) {
@@ -318,18 +321,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     // state slice S^T[e][d] = h0[d][e0 + e] (or the handed-over slot [d][e])
     {
       const float* h0p = from_hand ? prm.hand + (int64_t)(win + prm.UG) * kSlot
-                                   : (prm.h0 ? prm.h0 + ((int64_t)n * prm.Hv + h) * kDK * prm.V + e0 : nullptr);
+                                   : (prm.h0 ? prm.h0 + ((int64_t)n * prm.Hv + h) * DK * prm.V + e0 : nullptr);
       const int64_t ld = from_hand ? kVS : prm.V;
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < DK / 64; ++q4) {
         float v[32];
-        const int d0 = 128 * hf + 32 * q4;
+        const int d0 = (DK / 2) * hf + 32 * q4;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int64_t at = (int64_t)(d0 + i) * ld + row;
           v[i] = !h0p ? 0.f : (from_hand ? __ldcg(h0p + at) : h0p[at]);
         }
-        tmem_st32(tmem + R_S + lane_off + d0, v);
+        tmem_st32(tmem + M::R_S + lane_off + d0, v);
       }
       tmem_wait_st();
     }
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         if (c + 1 < c_end && !flags[1]) issue_k(c + 1);
         const int tn = (int)(t0 + kChunk);
 #pragma unroll
-        for (int a = 0; a < 4; ++a) {
+        for (int a = 0; a < NA; ++a) {
           if (c + 1 < c_end) tma_prefetch_3d(&tm_q, 64 * a, hq, tn);
           if (c + 2 < c_end) tma_prefetch_3d(&tm_k, 64 * a, hq, tn + kChunk);
         }
@@ -394,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) v[jj] = 0.f;
         } else {
-          tmem_ld32(tmem + R_A + lane_off + 32 * hf, v);
+          tmem_ld32(tmem + M::R_A + lane_off + 32 * hf, v);
           const float ri = isA ? bet[i] : prm.scale;
           const float gi = gam[i];
           const int lim = isA ? i : i + 1;
@@ -415,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
           for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
         } else {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
+          for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + M::P + sw128_chunk(i, 4 * hf + cc), v + 8 * cc);
         }
       }
 
@@ -430,13 +433,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       if (warp == w_sa || warp == w_sb) {
         const int o = warp == w_sb ? 32 : 0;
         __syncwarp();
-        diag_pair(As, o, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+        diag_pair(As, o, lane, sm + M::TB, sm + M::TBE, bet, be);
         if (warp == w_sb) {
           named_bar64<2>();
-          merge16_half<2>(As, tmp + 16 * 24, o, 0, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+          merge16_half<2>(As, tmp + 16 * 24, o, 0, lane, sm + M::TB, sm + M::TBE, bet, be);
         } else {
           named_bar64<1>();
-          merge16_half<1>(As, tmp, o, 0, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+          merge16_half<1>(As, tmp, o, 0, lane, sm + M::TB, sm + M::TBE, bet, be);
         }
       } else {
         // the six other warps zero the upper 16 x 16 blocks of both operands
@@ -446,15 +449,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
         const int rb = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
         const int cb = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
         const uint32_t off = sw128_chunk(16 * rb + r, 2 * cb + half);
-        *reinterpret_cast<uint4*>(sm + OFF_TB + off) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(sm + OFF_TBE + off) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sm + M::TB + off) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(sm + M::TBE + off) = make_uint4(0u, 0u, 0u, 0u);
         if (warp == w_pa || warp == w_pb) {
           if (warp == w_pb) {
             named_bar64<2>();
-            merge16_half<2>(As, tmp + 16 * 24, 32, 1, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+            merge16_half<2>(As, tmp + 16 * 24, 32, 1, lane, sm + M::TB, sm + M::TBE, bet, be);
           } else {
             named_bar64<1>();
-            merge16_half<1>(As, tmp, 0, 1, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+            merge16_half<1>(As, tmp, 0, 1, lane, sm + M::TB, sm + M::TBE, bet, be);
           }
         } else {
           // S4: S^T -> bf16 [e][d] (K-major A of M3a), S^T *= e^{g_last}; this
@@ -462,29 +465,29 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
           float v[32];
           const float dec = ex2_fast(gam[kChunk - 1]);
 #pragma unroll 1
-          for (int q8 = 0; q8 < 8; ++q8) {
+          for (int q8 = 0; q8 < DK / 32; ++q8) {
             const uint32_t col = 32 * q8;
-            tmem_ld32(tmem + R_S + lane_off + col, v);
-            uint8_t* atom = sm + OFF_ST + (col >> 6) * 16384;
+            tmem_ld32(tmem + M::R_S + lane_off + col, v);
+            uint8_t* atom = sm + M::ST + (col >> 6) * 16384;
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) store8_bf16(atom + sw128_chunk(row, 4 * (q8 & 1) + cc), v + 8 * cc);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= dec;
-            tmem_st32(tmem + R_S + lane_off + col, v);
+            tmem_st32(tmem + M::R_S + lane_off + col, v);
           }
           tmem_wait_st();
           fence_proxy_async();   // S^T bf16 feeds tcgen05.mma
           tc_fence_before();
           named_bar128<3>();     // the four S4 warps are done
-          // ---- M3a: [Y^T | OQ^T] = S^T [K;Q]^T -> R_Y (M128 N128)
+          // ---- M3a: [Y^T | OQ^T] = S^T [K;Q]^T -> M::R_Y (M128 N128)
           if (tid == kYIssuer) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 128, 0, 0, 0);
 #pragma unroll
-            for (int s = 0; s < 16; ++s) {
-              const uint32_t a = OFF_ST + (s >> 2) * 16384 + (s & 3) * 32;
-              const uint32_t b = OFF_KQ + (s >> 2) * kAtomKQ + (c & 1) * kRowsQ + (s & 3) * 32;
-              mma_bf16(tmem + R_Y, dsw(s4, a, 16), dsw(s4, b, 16), id, s > 0);
+            for (int s = 0; s < DK / 16; ++s) {
+              const uint32_t a = M::ST + (s >> 2) * 16384 + (s & 3) * 32;
+              const uint32_t b = M::KQ + (s >> 2) * kAtomKQ + (c & 1) * kRowsQ + (s & 3) * 32;
+              mma_bf16(tmem + M::R_Y, dsw(s4, a, 16), dsw(s4, b, 16), id, s > 0);
             }
             mma_commit(bar_y);
             ++y_pending;
@@ -493,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       }
       tc_fence_before();
       __syncthreads();
-      merge_level<32>(As, tmp, warp, lane, sm + OFF_TB, sm + OFF_TBE, bet, be);
+      merge_level<32>(As, tmp, warp, lane, sm + M::TB, sm + M::TBE, bet, be);
 
       // ---- S3: Y^T -> bf16 [e][j] (K-major A of M3b), over S^T's first atom
       wait_commit(bar_y, ph_y, y_pending, kYIssuer);
@@ -503,15 +506,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       const uint32_t col_y = (c & 1) ? 64 : 0, col_oq = 64 - col_y;
       {
         float v[32];
-        tmem_ld32(tmem + R_Y + col_y + lane_off + 32 * hf, v);
+        tmem_ld32(tmem + M::R_Y + col_y + lane_off + 32 * hf, v);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_YT + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + M::YT + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
       }
       fence_proxy_async();
       tc_fence_before();
       if (!sync_ok()) break;
 
-      // ---- M3b: V'^T = V^T (T diag(beta))^T - Y^T (T diag(beta e^g))^T -> R_B
+      // ---- M3b: V'^T = V^T (T diag(beta))^T - Y^T (T diag(beta e^g))^T -> M::R_B
       if (tid == 0) {
         if (!mbar_wait(bar_v, ph_v, prm.status)) {
           flags[1] = 1;
@@ -523,10 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
           const uint32_t idy = idesc_bf16(128, 64, 0, 0, 1);
 #pragma unroll
           for (int s = 0; s < 4; ++s)
-            mma_bf16(tmem + R_B, dsw(s4, OFF_V + s * 2048, 8192), dsw(s4, OFF_TB + s * 32, 16), idu, s > 0);
+            mma_bf16(tmem + M::R_B, dsw(s4, M::V + s * 2048, 8192), dsw(s4, M::TB + s * 32, 16), idu, s > 0);
 #pragma unroll
           for (int s = 0; s < 4; ++s)
-            mma_bf16(tmem + R_B, dsw(s4, OFF_YT + s * 32, 16), dsw(s4, OFF_TBE + s * 32, 16), idy, 1u);
+            mma_bf16(tmem + M::R_B, dsw(s4, M::YT + s * 32, 16), dsw(s4, M::TBE + s * 32, 16), idy, 1u);
           mma_commit(bar_x);
           ++x_pending;
         }
@@ -539,32 +542,32 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       // ---- S5: V'^T -> bf16 [e][j] ; V''^T = V'^T diag(e^{g_last - g}) -> bf16
       {
         float v[32], w[32];
-        tmem_ld32(tmem + R_B + lane_off + 32 * hf, v);
+        tmem_ld32(tmem + M::R_B + lane_off + 32 * hf, v);
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) w[jj] = v[jj] * dl[32 * hf + jj];
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + M::VPP + sw128_chunk(row, 4 * hf + cc), w + 8 * cc);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + OFF_VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
+        for (int cc = 0; cc < 4; ++cc) store8_bf16(sm + M::VP + sw128_chunk(row, 4 * hf + cc), v + 8 * cc);
       }
       fence_proxy_async();
       tc_fence_before();
       __syncthreads();
 
-      // ---- M4: OP^T = V'^T P^T (R_B) ; S^T += V''^T K (R_S, N = 256)
+      // ---- M4: OP^T = V'^T P^T (M::R_B) ; S^T += V''^T K (M::R_S, N = 256)
       if (tid == 0) {
         tc_fence_after();
         const uint32_t idp = idesc_bf16(128, 64, 0, 0, 0);
-        const uint32_t ids = idesc_bf16(128, 256, 0, 1, 0);
+        const uint32_t ids = idesc_bf16(128, DK, 0, 1, 0);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma_bf16(tmem + R_B, dsw(s4, OFF_VP + s * 32, 16), dsw(s4, OFF_P + s * 32, 16), idp, s > 0);
+          mma_bf16(tmem + M::R_B, dsw(s4, M::VP + s * 32, 16), dsw(s4, M::P + s * 32, 16), idp, s > 0);
         mma_commit(bar_q);
         ++q_pending;
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma_bf16(tmem + R_S, dsw(s4, OFF_VPP + s * 32, 16),
-                   dsw(s4, OFF_KQ + (c & 1) * 2 * kRowsQ + s * 2048, kAtomKQ), ids, 1);
+          mma_bf16(tmem + M::R_S, dsw(s4, M::VPP + s * 32, 16),
+                   dsw(s4, M::KQ + (c & 1) * 2 * kRowsQ + s * 2048, kAtomKQ), ids, 1);
         mma_commit(bar_x);
         ++x_pending;
       }
@@ -574,11 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       {
         const int ecol = (row & 63) & ~1;
         const bool odd = lane & 1;
-        uint8_t* lbase = sm + OFF_OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
+        uint8_t* lbase = sm + M::OS + (row >> 6) * 8192 + (odd ? 128 : 0) + (ecol & 7) * 2;
         const uint32_t xsw = (static_cast<uint32_t>((ecol >> 3) ^ (odd ? 1 : 0))) << 4;
         float oq[2][16];
-        tmem_ld16(tmem + R_Y + col_oq + lane_off + 32 * hf, oq[0]);
-        tmem_ld16(tmem + R_Y + col_oq + lane_off + 32 * hf + 16, oq[1]);
+        tmem_ld16(tmem + M::R_Y + col_oq + lane_off + 32 * hf, oq[0]);
+        tmem_ld16(tmem + M::R_Y + col_oq + lane_off + 32 * hf + 16, oq[1]);
         wait_commit(bar_q, ph_q, q_pending, 0);   // OP^T
         __syncwarp();
         tc_fence_after();
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
           float b[16];
           const float* a = oq[q];
           const uint32_t col = 32 * hf + 16 * q;
-          tmem_ld16(tmem + R_B + lane_off + col, b);
+          tmem_ld16(tmem + M::R_B + lane_off + col, b);
           float e[16];
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
@@ -613,15 +616,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
       __syncthreads();
       if (Lc == kChunk) {
         if (tid == 0) {
-          tma_store_3d(&tm_o, sm + OFF_OS, e0, h, (int)t0);
-          tma_store_3d(&tm_o, sm + OFF_OS + 8192, e0 + 64, h, (int)t0);
+          tma_store_3d(&tm_o, sm + M::OS, e0, h, (int)t0);
+          tma_store_3d(&tm_o, sm + M::OS + 8192, e0 + 64, h, (int)t0);
           bulk_commit();
         }
       } else {
         for (int u = tid; u < kChunk * 16; u += kThreads) {
           const int i = u >> 4, cc = u & 15;
           if (i < Lc) {
-            const uint4 val = *reinterpret_cast<const uint4*>(sm + OFF_OS + (cc >> 3) * 8192 + sw128_chunk(i, cc & 7));
+            const uint4 val = *reinterpret_cast<const uint4*>(sm + M::OS + (cc >> 3) * 8192 + sw128_chunk(i, cc & 7));
             *reinterpret_cast<uint4*>(prm.o + ((t0 + i) * prm.Hv + h) * prm.V + e0 + cc * 8) = val;
           }
         }
@@ -631,13 +634,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused256_kernel(const __grid_
     if (flags[1]) break;
     if (to_hand || prm.ht != nullptr) {
       // final state slice ht[d][e0 + e] = S^T[e][d] (or the hand-over slot [d][e])
-      float* htp = to_hand ? prm.hand + (int64_t)win * kSlot : prm.ht + ((int64_t)n * prm.Hv + h) * kDK * prm.V + e0;
+      float* htp = to_hand ? prm.hand + (int64_t)win * kSlot : prm.ht + ((int64_t)n * prm.Hv + h) * DK * prm.V + e0;
       const int64_t ld = to_hand ? kVS : prm.V;
 #pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < DK / 64; ++q4) {
         float v[32];
-        const int d0 = 128 * hf + 32 * q4;
-        tmem_ld32(tmem + R_S + lane_off + d0, v);
+        const int d0 = (DK / 2) * hf + 32 * q4;
+        tmem_ld32(tmem + M::R_S + lane_off + d0, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) htp[(int64_t)(d0 + i) * ld + row] = v[i];
       }
@@ -703,18 +706,19 @@ bool cuts_units(const gdn_problem& p, const Windows& w) {
 
 }  // namespace
 
-bool fused256_supported(const gdn_problem& p) {
-  return p.dt == GDN_BF16 && p.K == kDK && p.V % kVS == 0 && p.V <= 256 && (p.C == 64 || p.C == 128);
+bool fused1_supported(const gdn_problem& p) {
+  return p.dt == GDN_BF16 && (p.K == 128 || p.K == 256) && p.V % kVS == 0 && p.V <= 256 &&
+         (p.C == 64 || p.C == 128);
 }
 
-size_t fused256_workspace_bytes(const gdn_problem& p) {
+size_t fused1_workspace_bytes(const gdn_problem& p) {
   const Windows w = windows_of(p);
   if (w.nwin == 0) return kAlign;
-  return sched_bytes(w) + (cuts_units(p, w) ? (size_t)w.nwin * kDK * kVS * sizeof(float) : 0);
+  return sched_bytes(w) + (cuts_units(p, w) ? (size_t)w.nwin * p.K * kVS * sizeof(float) : 0);
 }
 
-bool fused256_handover_window(const gdn_problem& p, int window) {
-  if (!fused256_supported(p)) return false;
+bool fused1_handover_window(const gdn_problem& p, int window) {
+  if (!fused1_supported(p)) return false;
   const Windows w = windows_of(p);
   if (!cuts_units(p, w) || window < w.UG || window >= w.nwin) return false;
   // window - UG ends with the suffix of a unit whose prefix `window` runs
@@ -722,10 +726,25 @@ bool fused256_handover_window(const gdn_problem& p, int window) {
   return ((int64_t)(window / w.UG) * w.W) % nch != 0;
 }
 
-gdn_status run_fused256(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
-                        const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
-                        void* ws, cudaStream_t s, int drop_flag, unsigned long long wait_ns) {
-  if (!fused256_supported(p)) return GDN_ERR_UNSUPPORTED;
+namespace {
+
+template <int DK>
+gdn_status launch_fused1(const Params& prm, unsigned grid, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const CUtensorMap& to, cudaStream_t s) {
+  auto kernel = prm.sched ? gdn_fused1_kernel<DK, true> : gdn_fused1_kernel<DK, false>;
+  const int smem = (int)Map<DK>::SMEM;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  kernel<<<grid, kThreads, smem, s>>>(tq, tk, tv, to, prm);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+gdn_status run_fused1(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                      void* ws, cudaStream_t s, int drop_flag, unsigned long long wait_ns) {
+  if (!fused1_supported(p)) return GDN_ERR_UNSUPPORTED;
   int32_t* status = static_cast<int32_t*>(ws);
   const Windows w = windows_of(p);
   if (cudaMemsetAsync(status, 0, w.nwin > 0 ? sizeof(int32_t) * (2 + w.nwin) : sizeof(int32_t), s) != cudaSuccess)
@@ -779,12 +798,8 @@ gdn_status run_fused256(const gdn_problem& p, const void* q, const void* k, cons
   prm.UG = (int)w.UG;
   prm.wait_ns = wait_ns;
   prm.drop_flag = drop_flag;
-  auto kernel = prm.sched ? gdn_fused256_kernel<true> : gdn_fused256_kernel<false>;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
-    return GDN_ERR_CUDA;
   const unsigned grid = prm.sched ? (unsigned)w.nwin : (unsigned)((int64_t)p.N * p.Hv * prm.NS);
-  kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, to, prm);
-  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  return p.K == 256 ? launch_fused1<256>(prm, grid, tq, tk, tv, to, s) : launch_fused1<128>(prm, grid, tq, tk, tv, to, s);
 }
 
 }  // namespace gdn

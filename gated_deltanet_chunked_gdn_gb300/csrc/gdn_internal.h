@@ -77,22 +77,28 @@ gdn_status run_recurrent(const gdn_problem& p, const void* q, const void* k, con
                          const int32_t* state_indices, int state_slots, const int32_t* cu, void* o,
                          cudaStream_t s);
 
-// Fused path (gdn_fused.cu: K = V = 128; gdn_fused256.cu: K = 256, V = 128 or
-// 256, value slices of 128 columns).  fused_supported: either kernel.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // default limit of the hand-over wait
+
+// Fused paths.  gdn_fused.cu: the two-CTA-per-SM kernel, K = V = 128
+// (GDN_PATH_FUSED).  gdn_fused1.cu: the one-CTA-per-SM kernel, K = 128 or 256,
+// V = 128 or 256 in value slices of 128 columns (GDN_PATH_FUSED1; also what
+// GDN_PATH_FUSED runs for K = 256).  fused_supported: the problems
+// GDN_PATH_FUSED accepts.  fused1_preferred: AUTO's choice between the two
+// kernels for K = V = 128.
 bool fused_supported(const gdn_problem& p);
 bool fused128_supported(const gdn_problem& p);
-bool fused256_supported(const gdn_problem& p);
-size_t fused256_workspace_bytes(const gdn_problem& p);
-bool fused256_handover_window(const gdn_problem& p, int window);
-gdn_status run_fused256(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
-                        const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
-                        void* ws, cudaStream_t s, int drop_flag, unsigned long long wait_ns);
+bool fused1_supported(const gdn_problem& p);
+bool fused1_preferred(const gdn_problem& p);
+size_t fused1_workspace_bytes(const gdn_problem& p);
+bool fused1_handover_window(const gdn_problem& p, int window);
+gdn_status run_fused1(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
+                      const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
+                      void* ws, cudaStream_t s, int drop_flag = -1, unsigned long long wait_ns = kWaitLimitNs);
 size_t fused_workspace_bytes(const gdn_problem& p);
 size_t fused_status_offset(const gdn_problem& p);
 // drop_flag / wait_ns: test hook of the window schedule -- the hand-over flag
 // of window drop_flag is never raised, and a window waits at most wait_ns for
 // its flag (then records GDN_DEV_WAIT_TIMEOUT and stops).
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const void* v, const float* g,
                      const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
                      void* ws, cudaStream_t s, int drop_flag = -1, unsigned long long wait_ns = kWaitLimitNs);

@@ -55,10 +55,17 @@ typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
 typedef enum {
   GDN_PATH_AUTO = 0,    /* cp or fused when supported, else staged */
   GDN_PATH_STAGED = 1,  /* one kernel per stage, intermediates in the workspace */
-  GDN_PATH_FUSED = 2,   /* single persistent tcgen05 kernel (bf16, K = V = 128) */
-  GDN_PATH_CP = 3       /* chunk-parallel: each sequence cut into segments run on separate SMs
+  GDN_PATH_FUSED = 2,   /* single persistent tcgen05 kernel: two CTAs per SM for bf16 K = V = 128
+                           (the throughput form), the one-CTA-per-SM kernel for bf16 K = V = 256 */
+  GDN_PATH_CP = 3,      /* chunk-parallel: each sequence cut into segments run on separate SMs
                            (bf16, K = V = 128); AUTO takes it for sequences of >= 2048 tokens
                            when the (sequence, value head) chains number at most half the SMs */
+  GDN_PATH_FUSED1 = 4   /* single tcgen05 kernel with one CTA per SM and the value dimension in
+                           slices of 128 columns (bf16, K in {128, 256}, V in {128, 256}); AUTO
+                           takes it for K = 256, and for K = V = 128 when the (sequence, value
+                           head) chains number at most the SMs or a packed batch is small enough
+                           (ceil(T / 64) + N chunks a value head, times Hv, at most 256 x SMs)
+                           that its longest sequence bounds the step */
 } gdn_path;
 
 /*
@@ -209,22 +216,25 @@ gdn_status gdn_selftest_umma(int variant, const void* A, const void* B, float* D
                              void* stream);
 
 /*
- * Test hook of the fused path's bounded waits (no counterpart on the pages).
- * Runs gdn_chunk_fwd(p, GDN_PATH_FUSED, ...) on an equal-length batch whose
- * chains the fused kernel deals out as windows that hand a cut chain's state
- * over from one CTA to another, except that window `drop_window` never raises
- * its hand-over flag and every window waits at most `wait_ns` nanoseconds for
- * the flag it needs.  Window drop_window - 1 therefore gives up: it records
- * GDN_DEV_WAIT_TIMEOUT in the workspace's status word (read it with
- * gdn_get_device_status, path GDN_PATH_FUSED) and stops, leaving the o rows
- * and the final state of the chain it was waiting for unwritten; every other
- * window completes and the launch ends.  The failure is made on purpose in a
- * wait that has a limit: nothing faults and nothing hangs.
+ * Test hook of the fused paths' bounded waits (no counterpart on the pages).
+ * Runs gdn_chunk_fwd(p, path, ...) (path GDN_PATH_FUSED or GDN_PATH_FUSED1)
+ * on an equal-length batch whose chains the fused kernel deals out as windows
+ * that hand a cut chain's state over from one CTA to another, except that
+ * window `drop_window` never raises its hand-over flag and every window waits
+ * at most `wait_ns` nanoseconds for the flag it needs.  The window that would
+ * continue that chain (drop_window - 1 for GDN_PATH_FUSED; for
+ * GDN_PATH_FUSED1, whose windows come in groups of G x V / 128, the window one
+ * group below) therefore gives up: it records GDN_DEV_WAIT_TIMEOUT in the
+ * workspace's status word (read it with gdn_get_device_status with the same
+ * path) and stops, leaving the o rows and the final state of the chain it was
+ * waiting for unwritten; every other window completes and the launch ends.
+ * The failure is made on purpose in a wait that has a limit: nothing faults
+ * and nothing hangs.
  *   Arguments as gdn_chunk_fwd (no cu_seqlens).  Returns GDN_ERR_UNSUPPORTED
  *   when the fused pass over p hands no chain over at the start of window
  *   drop_window (then nothing is launched).
  */
-gdn_status gdn_selftest_handover_timeout(const gdn_problem* p,
+gdn_status gdn_selftest_handover_timeout(const gdn_problem* p, gdn_path path,
                                          const void* q, const void* k, const void* v,
                                          const float* g, const float* beta, float scale,
                                          const float* h0, void* o, float* ht,

@@ -83,7 +83,7 @@ def test_full_varlen_64(gdn, oracle_mod):
 def test_full_long_d256(gdn, oracle_mod):
     w = I.WORKLOADS[4]
     x = I.make_inputs(w.with_(B=1, T=64), "cuda")
-    assert gdn.gdn_resolve_path(gdn.problem_of(x["q"], x["v"], w.C)) == "fused"
+    assert gdn.gdn_resolve_path(gdn.problem_of(x["q"], x["v"], w.C)) == "fused1"
     # chains of every qk group's first and last value head and of every
     # sequence; the fused schedule cuts some of them between two CTAs
     check_chains(gdn, oracle_mod, w, [(0, 0), (1, 7), (2, 20), (3, 31)], nthreads=4)

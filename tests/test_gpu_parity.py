@@ -200,16 +200,19 @@ FUSED_CASES = {
 
 
 @pytest.mark.parametrize("name", sorted(FUSED_CASES))
-def test_fused_parity(gdn, oracle_mod, name):
+@pytest.mark.parametrize("path", ["fused", "fused1"])
+def test_fused_parity(gdn, oracle_mod, name, path):
+    """Both fused kernels (two CTAs per SM, K = V = 128; one CTA per SM, K in
+    {128, 256}) on every case; for K = 256 both paths run the one-CTA kernel."""
     w, lens = FUSED_CASES[name]
     x = I.make_inputs(w, "cpu", lengths=lens)
     d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
     p = gdn.problem_of(d["q"], d["v"], w.C, d["cu_seqlens"])
-    assert gdn.gdn_resolve_path(p) == "fused"
-    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, "fused"), dtype=torch.uint8, device="cuda")
+    assert gdn.gdn_resolve_path(p) in ("fused", "fused1")
+    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, path), dtype=torch.uint8, device="cuda")
     o, ht = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
-                              cu_seqlens=d["cu_seqlens"], C=w.C, path="fused", workspace=ws)
-    assert gdn.gdn_get_device_status(p, "fused", ws) == gdn.DEV_OK
+                              cu_seqlens=d["cu_seqlens"], C=w.C, path=path, workspace=ws)
+    assert gdn.gdn_get_device_status(p, path, ws) == gdn.DEV_OK
     o_ref, ht_ref = oracle_mod.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
                                          cu_seqlens=x["cu_seqlens"])
     o, ht = o.float().cpu().numpy(), ht.cpu().numpy()
@@ -239,13 +242,14 @@ def _gate_pattern(kind, B, T, H, gen):
 
 
 @pytest.mark.parametrize("kind", ["strong", "weak_then_strong", "strong_then_weak", "no_decay", "near_span_limit"])
-def test_fused_gate_regimes(gdn, oracle_mod, kind):
+@pytest.mark.parametrize("path", ["fused", "fused1"])
+def test_fused_gate_regimes(gdn, oracle_mod, kind, path):
     w = I.WORKLOADS[2].with_(B=2, T=200, Hqk=2, Hv=2, C=64)
     x = I.make_inputs(w, "cpu")
     x["g"] = _gate_pattern(kind, w.B, w.T, w.Hv, torch.Generator().manual_seed(7)).float().contiguous()
     d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
     o, ht = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"], C=64,
-                              path="fused")
+                              path=path)
     o_ref, ht_ref = oracle_mod.recurrent(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"])
     o, ht = o.float().cpu().numpy(), ht.cpu().numpy()
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(ht))
@@ -272,29 +276,31 @@ def test_fused_leaves_rows_of_other_sequences_untouched(gdn):
     assert torch.equal(o0, o[:, :70])
 
 
-def test_fused_malformed_cu_seqlens(gdn):
+@pytest.mark.parametrize("path", ["fused", "fused1"])
+def test_fused_malformed_cu_seqlens(gdn, path):
     w = I.WORKLOADS[3].with_(Hqk=1, Hv=2)
     x = I.make_inputs(w, "cuda", lengths=[10, 20, 30])
     # sequence 1 runs past the end of the batch, sequence 2 has a negative length
     bad = torch.tensor([0, 10, 70, 60], dtype=torch.int32, device="cuda")
     p = gdn.problem_of(x["q"], x["v"], 64, bad)
-    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, "fused"), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, path), dtype=torch.uint8, device="cuda")
     o = torch.full_like(x["v"], 7.0)
-    gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], cu_seqlens=bad, C=64, path="fused",
+    gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], cu_seqlens=bad, C=64, path=path,
                       o=o, workspace=ws)
-    assert gdn.gdn_get_device_status(p, "fused", ws) == gdn.DEV_BAD_CU_SEQLENS
+    assert gdn.gdn_get_device_status(p, path, ws) == gdn.DEV_BAD_CU_SEQLENS
     # the malformed sequences wrote nothing; the valid one wrote its rows
     assert torch.all(o[:, 10:] == 7.0)
     assert not torch.any(o[:, :10] == 7.0)
 
 
-def test_fused_matches_staged(gdn):
+@pytest.mark.parametrize("path", ["fused", "fused1"])
+def test_fused_matches_staged(gdn, path):
     """Fused and staged paths agree with each other (both against the same
     seeded inputs) -- a cross-check independent of the oracle."""
     w = I.WORKLOADS[1].with_(T=500, Hqk=2, Hv=4)
     x = I.make_inputs(w, "cuda")
     args = (x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"])
-    of, hf = gdn.gdn_chunk_fwd(*args, C=64, path="fused")
+    of, hf = gdn.gdn_chunk_fwd(*args, C=64, path=path)
     os_, hs = gdn.gdn_chunk_fwd(*args, C=64, path="staged")
     torch.cuda.synchronize()
     assert rel_fro(of.float().cpu().numpy(), os_.float().cpu().numpy()) < 5e-3
