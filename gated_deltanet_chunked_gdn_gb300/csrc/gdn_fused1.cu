@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused1_kernel(const __grid_co
     for (int a = 0; a < NA; ++a) tma_load_3d(sm + M::KQ + a * kAtomKQ + kRowsQ, &tm_q, bar_kq, 64 * a, hq, t);
     q_owed = false;
   };
-  // M1 of chunk c: [K;Q] K^T (even c) or [Q;K] K^T (odd c) -> M::R_A; false if its
+  // M1 of chunk c: [K;Q] K^T (even c) or [Q;K] K^T (odd c) -> R_A; false if its
   // tiles never arrived
   auto issue_m1 = [&](int c) -> bool {
     if (!mbar_wait(bar_kq, ph_kq, prm.status)) return false;
@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused1_kernel(const __grid_co
           fence_proxy_async();   // S^T bf16 feeds tcgen05.mma
           tc_fence_before();
           named_bar128<3>();     // the four S4 warps are done
-          // ---- M3a: [Y^T | OQ^T] = S^T [K;Q]^T -> M::R_Y (M128 N128)
+          // ---- M3a: [Y^T | OQ^T] = S^T [K;Q]^T -> R_Y (M128 N128)
           if (tid == kYIssuer) {
             tc_fence_after();
             const uint32_t id = idesc_bf16(128, 128, 0, 0, 0);
@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused1_kernel(const __grid_co
       tc_fence_before();
       if (!sync_ok()) break;
 
-      // ---- M3b: V'^T = V^T (T diag(beta))^T - Y^T (T diag(beta e^g))^T -> M::R_B
+      // ---- M3b: V'^T = V^T (T diag(beta))^T - Y^T (T diag(beta e^g))^T -> R_B
       if (tid == 0) {
         if (!mbar_wait(bar_v, ph_v, prm.status)) {
           flags[1] = 1;
@@ -554,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused1_kernel(const __grid_co
       tc_fence_before();
       __syncthreads();
 
-      // ---- M4: OP^T = V'^T P^T (M::R_B) ; S^T += V''^T K (M::R_S, N = 256)
+      // ---- M4: OP^T = V'^T P^T (R_B) ; S^T += V''^T K (R_S, N = DK)
       if (tid == 0) {
         tc_fence_after();
         const uint32_t idp = idesc_bf16(128, 64, 0, 0, 0);

@@ -87,3 +87,32 @@ def test_full_long_d256(gdn, oracle_mod):
     # chains of every qk group's first and last value head and of every
     # sequence; the fused schedule cuts some of them between two CTAs
     check_chains(gdn, oracle_mod, w, [(0, 0), (1, 7), (2, 20), (3, 31)], nthreads=4)
+
+
+@pytest.mark.parametrize("path", ["auto", "fused", "fused1"])
+def test_packed_long_and_short_sequences(gdn, oracle_mod, path):
+    """A packed batch whose two 12 K-token sequences bound the step, mixed with
+    short, sub-chunk and empty sequences: AUTO takes the one-CTA-per-SM kernel
+    for it; both fused kernels are checked on the long and a few short chains."""
+    w = I.WORKLOADS[3].with_(Hqk=4, Hv=8)
+    lens = [12288, 5, 0, 700, 12001, 63, 1, 2000, 0, 130]
+    x = I.make_inputs(w, "cuda", lengths=lens)
+    p = gdn.problem_of(x["q"], x["v"], w.C, x["cu_seqlens"])
+    if path == "auto":
+        assert gdn.gdn_resolve_path(p) == "fused1"
+    o, ht = gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                              cu_seqlens=x["cu_seqlens"], C=w.C, path=path)
+    torch.cuda.synchronize()
+    cu = x["cu_seqlens"].cpu().tolist()
+    G = w.Hv // w.Hqk
+    for n, h in [(0, 0), (4, 7), (1, 3), (2, 5), (5, 2), (6, 1), (9, 6)]:
+        sl = slice(cu[n], cu[n + 1])
+        sub = lambda t, hh: t[:, sl, hh:hh + 1].contiguous().cpu()
+        o_ref, ht_ref = oracle_mod.recurrent(sub(x["q"], h // G), sub(x["k"], h // G), sub(x["v"], h), sub(x["g"], h),
+                                             sub(x["beta"], h), x["scale"], h0=x["h0"][n:n + 1, h:h + 1].cpu())
+        o_got = o[:, sl, h:h + 1].float().cpu().numpy()
+        ht_got = ht[n:n + 1, h:h + 1].cpu().numpy()
+        assert np.all(np.isfinite(o_got)) and np.all(np.isfinite(ht_got))
+        if o_ref.size:
+            assert rel_fro(o_got, o_ref) <= TOL["bf16"], (n, h, rel_fro(o_got, o_ref))
+        assert rel_fro(ht_got, ht_ref) <= TOL["bf16"], (n, h, rel_fro(ht_got, ht_ref))
