@@ -305,3 +305,22 @@ def test_fused_matches_staged(gdn, path):
     torch.cuda.synchronize()
     assert rel_fro(of.float().cpu().numpy(), os_.float().cpu().numpy()) < 5e-3
     assert rel_fro(hf.cpu().numpy(), hs.cpu().numpy()) < 5e-3
+
+
+@pytest.mark.parametrize("path,case", [("fused", "windows_cut_chains"), ("fused1", "windows_cut_chains"),
+                                       ("fused1", "d256_windows_cut_units"), ("fused1", "varlen_many_short"),
+                                       ("fused", "varlen_many_short")])
+def test_fused_runs_are_bit_identical(gdn, path, case):
+    """No chain's arithmetic depends on scheduling (which CTA runs it, where a
+    window boundary cuts it, what runs beside it), so repeated calls must agree
+    bit for bit; a race between warps or CTAs would show up here."""
+    w, lens = FUSED_CASES[case]
+    x = I.make_inputs(w, "cuda", lengths=lens)
+    runs = []
+    for _ in range(4):
+        o, ht = gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                                  cu_seqlens=x["cu_seqlens"], C=w.C, path=path)
+        torch.cuda.synchronize()
+        runs.append((o.clone(), ht.clone()))
+    for o, ht in runs[1:]:
+        assert torch.equal(o, runs[0][0]) and torch.equal(ht, runs[0][1])
