@@ -8,14 +8,15 @@
 // B its final state from S = 0.  Three steps:
 //   1. one states-only launch of the fused kernel over all segments x heads
 //      computes B (zero initial state) and M (initial state I, v = 0);
-//   2. a small fp32 kernel chains the segments of each (sequence, head):
-//      S_{j+1} = M_j S_j + B_j, starting from h0; it records every segment's
-//      initial state S_j and writes the sequence's final state (ht);
+//   2. a small kernel chains the segments of each (sequence, head):
+//      S_{j+1} = M_j S_j + B_j, starting from h0 (tcgen05 products in three
+//      bf16 terms); it records every segment's initial state S_j and writes
+//      the sequence's final state (ht);
 //   3. the fused kernel reruns every segment from its S_j and writes o.
 // Work is about three times that of the serial pass, spread over
 // (segments x heads) CTAs instead of (sequences x heads).
 #include "gdn_internal.h"
-#include "gdn_sm100.cuh"
+#include "gdn_solve64.cuh"
 
 namespace gdn {
 namespace {
@@ -111,103 +112,183 @@ __global__ void __launch_bounds__(kPrepThreads) cp_prepare_kernel(const int32_t*
   for (int i = total + tid; i <= ns_max; i += kPrepThreads) seg_cu[i] = (int32_t)Ttot;
 }
 
-// Chain the segments of (sequence n, value head h) for 16 state columns:
-// H0s[j] = S_j, S_{j+1} = M_j S_j + B_j from S_0 = h0, ht = the last S.
-// 128 threads, thread t owning rows t/4 + 32 r (r < 4) and 4 columns of the
-// 128 x 16 slice.  M_j is row-major in 32-column k-blocks, staged into a
-// double-buffered shared tile by cp.async one block ahead of the FMAs; a
-// step of the inner product reads four rows of M and four rows of S as
-// 16-byte loads for 64 FMAs (row stride 36 floats: the eight rows a warp
-// reads fall on distinct banks).
-constexpr int kCSlice = 16;
-constexpr int kKb = 32;
-constexpr int kMld = kKb + 4;
+// Chain the segments of (sequence n, value head h) for 64 state columns
+// [e0, e0 + 64): H0s[j] = S_j, S_{j+1} = M_j S_j + B_j from S_0 = h0, ht = the
+// last S.  One CTA of 128 threads per (sequence, head, column half); thread d
+// owns row d of the state slice (TMEM lane d).  Each step's product runs on the
+// tensor cores (tcgen05, fp32 accumulation in TMEM) in three bf16 terms: with
+// x = hi + lo (hi = x rounded to bf16, lo = the rest rounded to bf16),
+// M S = Mh Sh + Mh Sl + Ml Sh up to the dropped Ml Sl and the rounding of the
+// lo parts, about 2^-17 of each product.  While a step's product runs, M_{j+1}
+// and the slice of B_j are staged in shared memory by coalesced cp.async.
+//   A = M_j [d][d'] (K-major, 128-byte swizzle): Mh, Ml, 2 atoms of 16 KB each
+//   B = S_j [d'][e] (MN-major, one 64-wide group): Sh, Sl, 16 KB each
+constexpr uint32_t kCbMH = 0, kCbML = 32768, kCbSH = 65536, kCbSL = 81920;
+constexpr uint32_t kCbMst = 98304;              // M_{j+1} fp32 [128][128], row-major
+constexpr uint32_t kCbBst = 163840;             // B_j fp32 [128][64], rows of 68 floats
+constexpr uint32_t kCbBld = 68;
+constexpr uint32_t kCbBar = kCbBst + 128 * kCbBld * 4;
+constexpr uint32_t kCbSmem = kCbBar + 64 + 1024;   // + alignment slack
+
+// Eight floats split into bf16 hi / lo halves, one 16-byte chunk each.
+__device__ __forceinline__ void split8_store(const float* x, uint8_t* hi, uint8_t* lo) {
+  float h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    h[i] = __bfloat162float(__float2bfloat16_rn(x[i]));
+    l[i] = x[i] - h[i];
+  }
+  solve64::store8_bf16(hi, h);
+  solve64::store8_bf16(lo, l);
+}
 
 __global__ void __launch_bounds__(128) cp_combine_kernel(const int32_t* __restrict__ seq_seg, int Hv,
                                                          const float* __restrict__ h0, const float* __restrict__ Bst,
                                                          const float* __restrict__ Mst, float* __restrict__ H0s,
-                                                         float* __restrict__ ht) {
-  __shared__ __align__(16) float S[kD][kCSlice];
-  __shared__ __align__(16) float Mb[2][kD][kMld];
-  const int n = blockIdx.x, h = blockIdx.y, e0 = kCSlice * blockIdx.z;
-  const int tid = threadIdx.x, t = tid >> 2, c0 = 4 * (tid & 3);
+                                                         float* __restrict__ ht, int32_t* status) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kCbBar);
+  volatile uint32_t* flags = reinterpret_cast<volatile uint32_t*>(sm + kCbBar + 8);
+  const float* mst = reinterpret_cast<const float*>(sm + kCbMst);
+  const float* bst = reinterpret_cast<const float*>(sm + kCbBst);
+  const int n = blockIdx.x, h = blockIdx.y, e0 = 64 * blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, d = tid;
   const size_t mat = (size_t)kD * kD;
-  const float* h0p = h0 ? h0 + ((size_t)n * Hv + h) * mat : nullptr;
-  for (int i = tid; i < kD * kCSlice; i += 128) {
-    const int r = i / kCSlice, c = i % kCSlice;
-    S[r][c] = h0p ? h0p[(size_t)r * kD + e0 + c] : 0.f;
-  }
   const int j0 = seq_seg[n], j1 = seq_seg[n + 1];
-  const int nb = (j1 - j0) * (kD / kKb);   // k-blocks of all the segments, in order
-  auto stage = [&](int blk) {
-    const float* src = Mst + ((size_t)(j0 + blk / (kD / kKb)) * Hv + h) * mat + (blk % (kD / kKb)) * kKb;
-    float* dst = &Mb[blk & 1][0][0];
-    for (int i = tid; i < kD * (kKb / 4); i += 128) {
-      const int d = i / (kKb / 4), q = i % (kKb / 4);
-      cp_async16(dst + d * kMld + 4 * q, src + (size_t)d * kD + 4 * q);
-    }
-    cp_async_commit();
-  };
-  if (nb > 0) stage(0);
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    mbar_fence_init();
+    flags[1] = 0;
+  }
+  if (warp == 0) tmem_alloc(const_cast<uint32_t*>(flags), 64);
+  tc_fence_before();
   __syncthreads();
-  float acc[4][4];
-  for (int blk = 0; blk < nb; ++blk) {
-    const int j = j0 + blk / (kD / kKb), kbi = blk % (kD / kKb), kb = kbi * kKb;
-    const size_t base = ((size_t)j * Hv + h) * mat;
-    if (kbi == 0) {
-      // segment start: record S_j, start from B_j
+  tc_fence_after();
+  const uint32_t tmem = flags[0];
+  const uint32_t lane_off = static_cast<uint32_t>(32 * warp) << 16;
+  const uint32_t s4 = (smem_u32(sm) & 0x3FFFFu) >> 4;
+  auto mat_of = [&](const float* base, int j) { return base + ((size_t)j * Hv + h) * mat; };
+  // cp.async of M_j (all of it) and of B_j's column slice
+  auto stage_m = [&](int j) {
+    const float* src = mat_of(Mst, j);
+    for (int i = tid; i < kD * kD / 4; i += 128) cp_async16(sm + kCbMst + 16 * i, src + 4 * i);
+  };
+  auto stage_b = [&](int j) {
+    const float* src = mat_of(Bst, j) + e0;
+    for (int i = tid; i < kD * 16; i += 128) {
+      const int r = i >> 4, q = i & 15;
+      cp_async16(sm + kCbBst + (r * kCbBld + 4 * q) * 4, src + (size_t)r * kD + 4 * q);
+    }
+  };
+  // M (staged) -> Mh, Ml: warp w splits rows 32w..32w+31, lane l columns 4l..4l+3
+  auto split_m = [&]() {
+    for (int i = 0; i < 32; ++i) {
+      const int r = 32 * warp + i;
+      const float4 v = *reinterpret_cast<const float4*>(mst + r * kD + 4 * lane);
+      const float x[4] = {v.x, v.y, v.z, v.w};
+      uint32_t hw[2], lw[2];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int d = t + 32 * r;
-        const float4 sv = *reinterpret_cast<const float4*>(&S[d][c0]);
-        *reinterpret_cast<float4*>(H0s + base + (size_t)d * kD + e0 + c0) = sv;
-        const float4 bv = *reinterpret_cast<const float4*>(Bst + base + (size_t)d * kD + e0 + c0);
-        acc[r][0] = bv.x, acc[r][1] = bv.y, acc[r][2] = bv.z, acc[r][3] = bv.w;
+      for (int u = 0; u < 2; ++u) {
+        const float h0f = __bfloat162float(__float2bfloat16_rn(x[2 * u]));
+        const float h1f = __bfloat162float(__float2bfloat16_rn(x[2 * u + 1]));
+        hw[u] = pack_bf16(h0f, h1f);
+        lw[u] = pack_bf16(x[2 * u] - h0f, x[2 * u + 1] - h1f);
       }
+      const int c = 4 * lane;
+      const uint32_t off = (c >> 6) * 16384u + sw128_chunk(r, (c & 63) >> 3) + (c & 7) * 2;
+      *reinterpret_cast<uint2*>(sm + kCbMH + off) = make_uint2(hw[0], hw[1]);
+      *reinterpret_cast<uint2*>(sm + kCbML + off) = make_uint2(lw[0], lw[1]);
     }
-    if (blk + 1 < nb) {
-      stage(blk + 1);
-      cp_async_wait_prev();
-    } else {
-      cp_async_wait_all();
+  };
+  // row d of a state slice -> its record (H0s or ht) and, when another step
+  // follows, Sh / Sl
+  auto emit_row = [&](const float (&x)[64], float* dst, bool split) {
+    if (dst) {
+#pragma unroll
+      for (int i = 0; i < 64; i += 4) *reinterpret_cast<float4*>(dst + i) = make_float4(x[i], x[i + 1], x[i + 2], x[i + 3]);
     }
-    __syncthreads();   // block blk is in shared memory
-    const float* Mk = &Mb[blk & 1][0][0];
-#pragma unroll 2
-    for (int g = 0; g < kKb / 4; ++g) {
-      float m[4][4], x[4][4];
+    if (split) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float4 v = *reinterpret_cast<const float4*>(Mk + (t + 32 * r) * kMld + 4 * g);
-        m[r][0] = v.x, m[r][1] = v.y, m[r][2] = v.z, m[r][3] = v.w;
-      }
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float4 v = *reinterpret_cast<const float4*>(&S[kb + 4 * g + u][c0]);
-        x[u][0] = v.x, x[u][1] = v.y, x[u][2] = v.z, x[u][3] = v.w;
-      }
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int c = 0; c < 4; ++c) acc[r][c] = fmaf(m[r][u], x[u][c], acc[r][c]);
+      for (int cc = 0; cc < 8; ++cc) split8_store(x + 8 * cc, sm + kCbSH + sw128_chunk(d, cc), sm + kCbSL + sw128_chunk(d, cc));
     }
-    __syncthreads();   // this buffer and S read: the next stage and S's update may go ahead
-    if (kbi == kD / kKb - 1) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-        *reinterpret_cast<float4*>(&S[t + 32 * r][c0]) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      __syncthreads();
-    }
+  };
+  auto rec = [&](int j) -> float* {   // where S_j's row d is recorded
+    if (j < j1) return H0s + ((size_t)j * Hv + h) * mat + (size_t)d * kD + e0;
+    return ht ? ht + ((size_t)n * Hv + h) * mat + (size_t)d * kD + e0 : nullptr;
+  };
+
+  if (j1 > j0) {
+    stage_m(j0);
+    cp_async_commit();
   }
-  if (ht) {
-    float* htp = ht + ((size_t)n * Hv + h) * mat;
-    for (int i = tid; i < kD * kCSlice; i += 128) {
-      const int r = i / kCSlice, c = i % kCSlice;
-      htp[(size_t)r * kD + e0 + c] = S[r][c];
+  {
+    const float* h0p = h0 ? h0 + ((size_t)n * Hv + h) * mat + (size_t)d * kD + e0 : nullptr;
+    float x[64];
+#pragma unroll
+    for (int i = 0; i < 64; i += 4) {
+      const float4 v = h0p ? *reinterpret_cast<const float4*>(h0p + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x[i] = v.x, x[i + 1] = v.y, x[i + 2] = v.z, x[i + 3] = v.w;
     }
+    emit_row(x, rec(j0), j1 > j0);
   }
+  if (j1 > j0) {
+    cp_async_wait_all();
+    __syncthreads();
+    split_m();
+  }
+  uint32_t ph = 0;
+#pragma unroll 1
+  for (int j = j0; j < j1; ++j) {
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();   // Mh, Ml, Sh, Sl complete; the staging buffers read
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 64, 0, 1, 0);
+      const uint32_t a_off[3] = {kCbMH, kCbMH, kCbML}, b_off[3] = {kCbSH, kCbSL, kCbSH};
+#pragma unroll
+      for (int t = 0; t < 3; ++t)
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_bf16(tmem, solve64::dsw(s4, a_off[t] + (s >> 2) * 16384 + (s & 3) * 32, 16),
+                   solve64::dsw(s4, b_off[t] + s * 2048, 16384), id, (t | s) ? 1u : 0u);
+      mma_commit(bar);
+    }
+    stage_b(j);
+    if (j + 1 < j1) stage_m(j + 1);
+    cp_async_commit();
+    if (!mbar_wait(bar, ph, status)) flags[1] = 1;
+    ph ^= 1;
+    cp_async_wait_all();
+    __syncwarp();
+    tc_fence_after();
+    __syncthreads();   // the staged B_j and M_{j+1} are visible to every thread
+    if (flags[1]) break;
+    // S_{j+1} row d = D row d + B_j row d
+    {
+      float x[64], y[32];
+      tmem_ld32(tmem + lane_off, y);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[i] = y[i];
+      tmem_ld32(tmem + lane_off + 32, y);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) x[32 + i] = y[i];
+#pragma unroll
+      for (int i = 0; i < 64; i += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(bst + d * kCbBld + i);
+        x[i] += v.x, x[i + 1] += v.y, x[i + 2] += v.z, x[i + 3] += v.w;
+      }
+      emit_row(x, rec(j + 1), j + 1 < j1);
+    }
+    if (j + 1 < j1) split_m();
+    tc_fence_before();
+  }
+  if (tid == 0 && flags[1]) mbar_wait(bar, ph, status, 100000000ull);
+  cp_async_wait_all();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
 }
 
 }  // namespace
@@ -282,7 +363,10 @@ gdn_status run_cp(const gdn_problem& p, const void* q, const void* k, const void
   ps.varlen = 1;
   gdn_status st = run_fused_states(ps, k, v, g, beta, seg_cu, Bst, Mst, status, s);
   if (st != GDN_OK) return st;
-  cp_combine_kernel<<<dim3(p.N, p.Hv, kD / kCSlice), 128, 0, s>>>(seq_seg, p.Hv, h0, Bst, Mst, H0s, ht);
+  if (cudaFuncSetAttribute(cp_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCbSmem) !=
+      cudaSuccess)
+    return GDN_ERR_CUDA;
+  cp_combine_kernel<<<dim3(p.N, p.Hv, 2), 128, kCbSmem, s>>>(seq_seg, p.Hv, h0, Bst, Mst, H0s, ht, status);
   if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   return launch_fused(ps, 0, q, k, v, g, beta, scale, H0s, seg_cu, o, nullptr, nullptr, status, s);
 }
