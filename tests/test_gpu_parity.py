@@ -196,7 +196,11 @@ FUSED_CASES = {
     "d256_V128_h0": (I.WORKLOADS[4].with_(B=2, T=150, Hqk=2, Hv=4, V=128, h0=True), None),
     # 320 (chain, slice) units of 3 chunks over 152 SMs: windows of 7 chunks
     "d256_windows_cut_units": (I.WORKLOADS[4].with_(B=20, T=190, Hqk=2, Hv=8, h0=True), None),
+    # K = 128 with V = 256: two value slices per chain on the one-CTA kernel only
+    "k128_v256_gqa2": (I.WORKLOADS[2].with_(B=2, T=200, Hqk=1, Hv=2, V=256), None),
 }
+# cases that only the one-CTA kernel runs (GDN_PATH_FUSED does not take K = 128 with V = 256)
+FUSED1_ONLY = {"k128_v256_gqa2"}
 
 
 @pytest.mark.parametrize("name", sorted(FUSED_CASES))
@@ -209,6 +213,9 @@ def test_fused_parity(gdn, oracle_mod, name, path):
     d = {k_: (v_.cuda() if isinstance(v_, torch.Tensor) else v_) for k_, v_ in x.items()}
     p = gdn.problem_of(d["q"], d["v"], w.C, d["cu_seqlens"])
     assert gdn.gdn_resolve_path(p) in ("fused", "fused1")
+    if path == "fused" and name in FUSED1_ONLY:
+        assert gdn.gdn_chunk_fwd_workspace_size(p, "fused") == 0   # rejected up front
+        return
     ws = torch.empty(gdn.gdn_chunk_fwd_workspace_size(p, path), dtype=torch.uint8, device="cuda")
     o, ht = gdn.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["scale"], h0=d["h0"],
                               cu_seqlens=d["cu_seqlens"], C=w.C, path=path, workspace=ws)
