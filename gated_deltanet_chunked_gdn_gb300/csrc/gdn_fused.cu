@@ -82,6 +82,9 @@ struct FusedParams {
   int32_t* status;
   int N, Tseq, Ttot, Hqk, Hv, varlen;
   float scale;
+  // packed batches, full pass: block b runs head b % Hv of sequence
+  // order[b / Hv] (longest first); null: sequence b / Hv
+  const int32_t* order;
   // kStates launches only: blocks [0, split) are the chains of a problem started
   // from a zero state (final state -> ht); blocks [split, 2 split) the same
   // chains started from the identity with v = 0 (final state = the chain's
@@ -155,7 +158,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_fused_kernel(const __grid_con
   // one chain per CTA: sequence bounds (validated: a malformed cu_seqlens
   // touches no memory)
   if (!windowed) {
-    const int chain = trans ? (int)blockIdx.x - prm.split : (int)blockIdx.x;
+    int chain = trans ? (int)blockIdx.x - prm.split : (int)blockIdx.x;
+    if (prm.order && !trans) chain = prm.order[chain / prm.Hv] * prm.Hv + chain % prm.Hv;
     n = chain / prm.Hv;
     h = chain % prm.Hv;
     hq = h / (prm.Hv / prm.Hqk);
@@ -715,6 +719,46 @@ bool fused_supported(const gdn_problem& p) { return fused128_supported(p) || (fu
 
 namespace {
 
+constexpr int kOrderThreads = 256;
+
+// Rank of each sequence by chunk count (descending, then by index), one thread
+// per sequence against every sequence's count, tile by tile through shared
+// memory.  The ranks are a permutation of 0..N-1 whatever cu holds.
+__global__ void __launch_bounds__(kOrderThreads) varlen_order_kernel(const int32_t* __restrict__ cu, int N,
+                                                                     int32_t* __restrict__ order) {
+  __shared__ int tile[kOrderThreads];
+  auto chunks = [&](int m) -> int {
+    const int64_t len = (int64_t)cu[m + 1] - cu[m];
+    return len > 0 ? (int)((len + kChunk - 1) / kChunk) : 0;
+  };
+  const int n = blockIdx.x * kOrderThreads + threadIdx.x;
+  const int mine = n < N ? chunks(n) : 0;
+  int rank = 0;
+  for (int base = 0; base < N; base += kOrderThreads) {
+    __syncthreads();
+    const int m = base + threadIdx.x;
+    tile[threadIdx.x] = m < N ? chunks(m) : -1;
+    __syncthreads();
+    const int cnt = N - base < kOrderThreads ? N - base : kOrderThreads;
+    for (int j = 0; j < cnt; ++j) rank += tile[j] > mine || (tile[j] == mine && base + j < n);
+  }
+  if (n < N) order[rank] = n;
+}
+
+}  // namespace
+
+size_t varlen_order_bytes(const gdn_problem& p) {
+  if (!p.varlen || p.N <= 1 || p.N > kOrderMaxN) return 0;
+  return ((sizeof(int32_t) * (size_t)p.N + kAlign - 1) / kAlign) * kAlign;
+}
+
+gdn_status launch_varlen_order(const int32_t* cu, int N, int32_t* order, cudaStream_t s) {
+  varlen_order_kernel<<<(N + kOrderThreads - 1) / kOrderThreads, kOrderThreads, 0, s>>>(cu, N, order);
+  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+namespace {
+
 constexpr int kCtasPerSm = 2;   // resident fused CTAs per SM (shared memory and TMEM halves)
 
 // Window schedule of the full pass over equal-length sequences: W chunks per
@@ -767,7 +811,7 @@ bool fused1_preferred(const gdn_problem& p) {
 size_t fused_workspace_bytes(const gdn_problem& p) {
   if (!fused128_supported(p)) return fused1_workspace_bytes(p);
   const Windows w = fused_windows(p);
-  if (!w.handover()) return kAlign;   // the status word
+  if (!w.handover()) return kAlign + varlen_order_bytes(p);   // the status word (and the order table)
   return sched_bytes(w) + (cuts_chains(p, w) ? (size_t)w.nwin * kD * kD * sizeof(float) : 0);
 }
 size_t fused_status_offset(const gdn_problem&) { return 0; }
@@ -777,7 +821,7 @@ size_t fused_status_offset(const gdn_problem&) { return 0; }
 gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const void* k, const void* v, const float* g,
                         const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
                         float* ht2, int32_t* status, cudaStream_t s, int* sched, float* hand, int64_t nwin,
-                        int64_t W, int drop_flag, unsigned long long wait_ns) {
+                        int64_t W, int drop_flag, unsigned long long wait_ns, const int32_t* order) {
   const int64_t Ttot = (int64_t)p.B * p.T;
   CUtensorMap tq, tk, tv, to;
   memset(&to, 0, sizeof(to));
@@ -819,6 +863,7 @@ gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const voi
   prm.W = (int)W;
   prm.wait_ns = wait_ns;
   prm.drop_flag = drop_flag;
+  prm.order = mode == kFull && p.varlen ? order : nullptr;
   const unsigned chains = (unsigned)((int64_t)p.N * p.Hv);
   auto kernel = mode == kStates ? gdn_fused_kernel<kStates, false>
                : (prm.sched ? gdn_fused_kernel<kFull, true> : gdn_fused_kernel<kFull, false>);
@@ -850,7 +895,16 @@ gdn_status run_fused(const gdn_problem& p, const void* q, const void* k, const v
     }
     return GDN_OK;
   }
-  if (!w.handover()) return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s);
+  if (!w.handover()) {
+    int32_t* order = nullptr;
+    if (varlen_order_bytes(p) > 0) {
+      order = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kAlign);
+      const gdn_status st = launch_varlen_order(cu, p.N, order, s);
+      if (st != GDN_OK) return st;
+    }
+    return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s, nullptr, nullptr, 0, 0,
+                        -1, kWaitLimitNs, order);
+  }
   float* hand = cuts_chains(p, w) ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sched_bytes(w)) : nullptr;
   return launch_fused(p, kFull, q, k, v, g, beta, scale, h0, cu, o, ht, nullptr, status, s, status + 1, hand, w.nwin,
                       w.W, drop_flag, wait_ns);

@@ -104,6 +104,9 @@ struct Params {
   int32_t* status;
   int N, Tseq, Ttot, Hqk, Hv, V, NS, varlen;   // NS = V / kVS slices per chain
   float scale;
+  // packed batches: block b runs unit b % (Hv NS) of sequence order[b / (Hv NS)]
+  // (longest first); null: of sequence b / (Hv NS)
+  const int32_t* order;
   // group-aligned window schedule (null sched: one unit per CTA): nwin = UG x
   // window groups; group m covers positions [m W, (m + 1) W) of the qk heads'
   // chunks laid end to end (each head's in reverse), window w = UG m + k runs
@@ -155,7 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fused1_kernel(const __grid_co
 
   if (!WIN) {
     const int unit = (int)blockIdx.x;
-    const int chain = unit / prm.NS;
+    int chain = unit / prm.NS;
+    if (prm.order) chain = prm.order[unit / (prm.Hv * prm.NS)] * prm.Hv + chain % prm.Hv;
     e0 = (unit % prm.NS) * kVS;
     n = chain / prm.Hv;
     h = chain % prm.Hv;
@@ -713,7 +717,7 @@ bool fused1_supported(const gdn_problem& p) {
 
 size_t fused1_workspace_bytes(const gdn_problem& p) {
   const Windows w = windows_of(p);
-  if (w.nwin == 0) return kAlign;
+  if (w.nwin == 0) return kAlign + varlen_order_bytes(p);   // the status word (and the order table)
   return sched_bytes(w) + (cuts_units(p, w) ? (size_t)w.nwin * p.K * kVS * sizeof(float) : 0);
 }
 
@@ -798,6 +802,13 @@ gdn_status run_fused1(const gdn_problem& p, const void* q, const void* k, const 
   prm.UG = (int)w.UG;
   prm.wait_ns = wait_ns;
   prm.drop_flag = drop_flag;
+  prm.order = nullptr;
+  if (w.nwin == 0 && varlen_order_bytes(p) > 0) {
+    int32_t* order = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + kAlign);
+    const gdn_status st = launch_varlen_order(cu, p.N, order, s);
+    if (st != GDN_OK) return st;
+    prm.order = order;
+  }
   const unsigned grid = prm.sched ? (unsigned)w.nwin : (unsigned)((int64_t)p.N * p.Hv * prm.NS);
   return p.K == 256 ? launch_fused1<256>(prm, grid, tq, tk, tv, to, s) : launch_fused1<128>(prm, grid, tq, tk, tv, to, s);
 }

@@ -79,6 +79,17 @@ gdn_status run_recurrent(const gdn_problem& p, const void* q, const void* k, con
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // default limit of the hand-over wait
 
+// Longest-first order of a packed batch (gdn_fused.cu): order[r] is the
+// sequence of rank r by chunk count, descending, equal counts by index, so
+// that a launch of one chain per CTA starts its longest chains first (the
+// hardware hands out CTAs in index order).  Computed on the device from
+// cu_seqlens (any int32 values: lengths below one token count as empty).
+// varlen_order_bytes: the workspace the table takes (0 when p is not packed or
+// has more than kOrderMaxN sequences: those keep the index order).
+constexpr int kOrderMaxN = 16384;
+size_t varlen_order_bytes(const gdn_problem& p);
+gdn_status launch_varlen_order(const int32_t* cu, int N, int32_t* order, cudaStream_t s);
+
 // Fused paths.  gdn_fused.cu: the two-CTA-per-SM kernel, K = V = 128
 // (GDN_PATH_FUSED).  gdn_fused1.cu: the one-CTA-per-SM kernel, K = 128 or 256,
 // V = 128 or 256 in value slices of 128 columns (GDN_PATH_FUSED1; also what
@@ -141,12 +152,13 @@ int cp_segment_length(const gdn_problem& p);
 bool cp_preferred(const gdn_problem& p);
 // One fused-kernel launch (mode 0: the full pass; 1: final states only).
 // sched / hand / nwin / W: the window schedule of an equal-length full pass
-// (sched null: one chain per CTA).
+// (sched null: one chain per CTA).  order: the longest-first table of a
+// packed full pass (null: index order).
 gdn_status launch_fused(const gdn_problem& p, int mode, const void* q, const void* k, const void* v, const float* g,
                         const float* beta, float scale, const float* h0, const int32_t* cu, void* o, float* ht,
                         float* ht2, int32_t* status, cudaStream_t s, int* sched = nullptr, float* hand = nullptr,
                         int64_t nwin = 0, int64_t W = 0, int drop_flag = -1,
-                        unsigned long long wait_ns = kWaitLimitNs);
+                        unsigned long long wait_ns = kWaitLimitNs, const int32_t* order = nullptr);
 // Streaming multiprocessors of the current device (148 when none can be queried).
 int sm_count();
 // Byte offset of the device status word inside a forward workspace for `path`
