@@ -617,7 +617,7 @@ def main():
     # the fused and chunk-parallel kernels run 64-token chunks whatever C the
     # call asks for (the result does not depend on C): their FLOPs are counted
     # at the chunk length they execute
-    C_exec = 64 if path in ("fused", "cp") else w.C
+    C_exec = 64 if path in ("fused", "fused1", "cp") else w.C
     nbytes, flops = algorithmic(Bx, Tx, w.Hqk, w.Hv, w.K, w.V, C_exec, 2, h0=x["h0"] is not None, N=x["N"])
     _, flops_req = algorithmic(Bx, Tx, w.Hqk, w.Hv, w.K, w.V, w.C, 2, h0=x["h0"] is not None, N=x["N"])
     state_bytes = x["N"] * w.Hv * w.K * w.V * 4 * (2 if x["h0"] is not None else 1)
@@ -632,7 +632,9 @@ def main():
         # a tensor-bound step is one long launch: the sustained bf16 figure
         achieved, peak, unit = flops / sec / 1e12, pk["bf16_tflops_sustained"], "TFLOP/s"
         peak_kind = "bf16 sustained"
-    launches = {"staged": 7, "fused": 1, "fused1": 1, "cp": 4}[path]
+    # a packed batch adds the longest-first ranking launch before a fused pass
+    ranked = path in ("fused", "fused1") and x["cu_seqlens"] is not None and 1 < x["N"] <= 16384
+    launches = {"staged": 7, "fused": 1, "fused1": 1, "cp": 4}[path] + (1 if ranked else 0)
     line = {
         "metric": METRIC if args.workload == "batched_16x8192" else f"GDN chunk-fwd tokens/s ({wname}, bf16); % roofline",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -651,7 +653,8 @@ def main():
                                  if path in ("fused", "fused1") and args.workload == "long_d256" else None),
                      "peak_source": f"{pk['source']} ({peak_kind})",
                      "kernel": (("gdn_fused1_kernel" if (w.K == 256 or path == "fused1") else "gdn_fused_kernel") +
-                                " (the step's only launch)") if path in ("fused", "fused1")
+                                (" (after the ranking launch of the packed batch)" if ranked
+                                 else " (the step's only launch)")) if path in ("fused", "fused1")
                      else "gdn_chunk_fwd call (all launches of one step)",
                      "alg_bytes": nbytes, "alg_flops": flops, "alg_flops_at_requested_C": flops_req,
                      "t_hbm_ms": 1e3 * t_hbm, "t_tensor_ms": 1e3 * t_tc},
