@@ -92,7 +92,10 @@ typedef struct {
  * chains' chunks evenly over the CTAs the current device holds at once (two
  * per SM), cutting a chain in two where a share ends; its workspace then holds
  * one K x V fp32 hand-over state per CTA (about 20 MB on 152 SMs), so query
- * the size with the device that will run the call current.
+ * the size with the device that will run the call current.  On packed
+ * sequences (2 to 16384 of them) the fused paths also keep a table of N int32
+ * there: a launch before the pass ranks the sequences by length so that the
+ * longest chains start first.
  */
 size_t gdn_chunk_fwd_workspace_size(const gdn_problem* p, gdn_path path);
 
