@@ -365,3 +365,36 @@ def test_packed_batch_longest_first_order(gdn, oracle_mod, path):
         if o_ref.size:
             assert rel_fro(o[:, sl, h:h + 1].float().cpu().numpy(), o_ref) <= TOL["bf16"], (n, h)
         assert rel_fro(ht[n:n + 1, h:h + 1].cpu().numpy(), ht_ref) <= TOL["bf16"], (n, h)
+
+
+@pytest.mark.parametrize("N", [16384, 16385])
+@pytest.mark.parametrize("path", ["fused", "fused1"])
+def test_packed_batch_order_at_its_size_limit(gdn, oracle_mod, N, path):
+    """The longest-first ranking covers up to 16384 sequences (64 ranking
+    blocks); one more keeps the index order.  Both sides of the limit: the
+    reversed packing gives the same outputs bit for bit, and sampled chains
+    match the oracle."""
+    gen = np.random.default_rng(N)
+    lens = [int(x) for x in gen.integers(0, 9, size=N)]
+    lens[N // 3] = 200   # one sequence of several chunks
+    w = I.WORKLOADS[3].with_(Hqk=1, Hv=2)
+    x = I.make_inputs(w, "cuda", lengths=lens)
+    cu = x["cu_seqlens"].cpu().tolist()
+    o, ht = gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                              cu_seqlens=x["cu_seqlens"], C=w.C, path=path)
+    idx = torch.cat([torch.arange(cu[n], cu[n + 1]) for n in reversed(range(N))]).to("cuda")
+    cu_r = torch.zeros(N + 1, dtype=torch.int32)
+    cu_r[1:] = torch.cumsum(torch.tensor(lens[::-1], dtype=torch.int64), 0).to(torch.int32)
+    tok = lambda t: t[:, idx].contiguous()
+    o_r, ht_r = gdn.gdn_chunk_fwd(tok(x["q"]), tok(x["k"]), tok(x["v"]), tok(x["g"]), tok(x["beta"]), x["scale"],
+                                  h0=x["h0"].flip(0).contiguous(), cu_seqlens=cu_r.to("cuda"), C=w.C, path=path)
+    torch.cuda.synchronize()
+    assert torch.equal(o_r, tok(o)) and torch.equal(ht_r, ht.flip(0))
+    for n, h in [(N // 3, 0), (N // 3, 1), (0, 1), (N - 1, 0), (N // 2, 1)]:
+        sl = slice(cu[n], cu[n + 1])
+        sub = lambda t, hh: t[:, sl, hh:hh + 1].contiguous().cpu()
+        o_ref, ht_ref = oracle_mod.recurrent(sub(x["q"], 0), sub(x["k"], 0), sub(x["v"], h), sub(x["g"], h),
+                                             sub(x["beta"], h), x["scale"], h0=x["h0"][n:n + 1, h:h + 1].cpu())
+        if o_ref.size:
+            assert rel_fro(o[:, sl, h:h + 1].float().cpu().numpy(), o_ref) <= TOL["bf16"], (n, h)
+        assert rel_fro(ht[n:n + 1, h:h + 1].cpu().numpy(), ht_ref) <= TOL["bf16"], (n, h)
