@@ -64,7 +64,7 @@ def test_conv1d_fixed_batch(gdn, oracle_mod, dtype, W, activation):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_conv1d_varlen_slots(gdn, oracle_mod, dtype):
-    """Packed sequences (empty, shorter than the window, straddling 64-token
+    """Packed sequences (empty, shorter than the window, straddling thread
     runs), a permuted slot map with one sequence without a slot, and one
     sequence that starts from zeros but still writes its slot."""
     lens = [5, 1, 0, 130, 2, 64, 65, 3]
@@ -73,6 +73,16 @@ def test_conv1d_varlen_slots(gdn, oracle_mod, dtype):
     init = torch.tensor([1, 1, 1, 1, 0, 1, 1, 0], dtype=torch.int32)
     y, st, y_ref, s_ref = run_both(gdn, oracle_mod, d, "silu", cache_indices=idx, has_initial_state=init)
     assert_close(y, y_ref, dtype)
+    assert torch.equal(st.cpu(), torch.from_numpy(s_ref).to(st.dtype))
+
+
+def test_conv1d_runs_across_sequences(gdn, oracle_mod):
+    """Packed sequences longer and shorter than a thread's 256-token run, so
+    that runs start inside sequences and hold several whole ones."""
+    lens = [300, 255, 257, 1, 0, 600, 10, 256, 40]
+    d = I.make_conv_inputs(1, 0, 96, 4, "bf16", seed=12, lengths=lens)
+    y, st, y_ref, s_ref = run_both(gdn, oracle_mod, d, "silu")
+    assert_close(y, y_ref, "bf16")
     assert torch.equal(st.cpu(), torch.from_numpy(s_ref).to(st.dtype))
 
 
