@@ -73,3 +73,37 @@ def test_random_draw_against_oracle(gdn, oracle_mod, i):
     if o_ref.size:
         assert rel_fro(o_got, o_ref) <= tol, (w, lens, path, rel_fro(o_got, o_ref))
     assert rel_fro(ht_got, ht_ref) <= tol, (w, lens, path, rel_fro(ht_got, ht_ref))
+
+
+def draw_cp(i):
+    """Draw i of the chunk-parallel sweep: sequences long enough to be cut
+    into several segments, packed or of equal length."""
+    r = np.random.default_rng(9100 + i)
+    Hqk = int(r.choice([1, 2]))
+    Hv = Hqk * int(r.choice([1, 2, 4]))
+    h0 = bool(r.random() < 0.6)
+    C = int(r.choice([64, 128]))
+    if r.random() < 0.5:
+        n = int(r.integers(1, 5))
+        lens = [int(x) for x in r.integers(0, 5000, size=n)]
+        w = I.Workload("random_cp", 1, 0, Hqk, Hv, 128, 128, C, "bf16", "softplus_exp", h0, 300 + i, varlen_n=n)
+        return w, lens
+    w = I.Workload("random_cp", int(r.integers(1, 3)), int(r.integers(500, 5000)), Hqk, Hv, 128, 128, C, "bf16",
+                   "softplus_exp", h0, 300 + i)
+    return w, None
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_chunk_parallel_against_oracle(gdn, oracle_mod, i):
+    w, lens = draw_cp(i)
+    x = I.make_inputs(w, "cuda", lengths=lens)
+    o, ht = gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
+                              cu_seqlens=x["cu_seqlens"], C=w.C, path="cp")
+    torch.cuda.synchronize()
+    cpu = lambda t: None if t is None else t.cpu()
+    o_ref, ht_ref = oracle_mod.recurrent(cpu(x["q"]), cpu(x["k"]), cpu(x["v"]), cpu(x["g"]), cpu(x["beta"]),
+                                         x["scale"], h0=cpu(x["h0"]), cu_seqlens=cpu(x["cu_seqlens"]))
+    o_got, ht_got = o.float().cpu().numpy(), ht.cpu().numpy()
+    if o_ref.size:
+        assert rel_fro(o_got, o_ref) <= TOL["bf16"], (w, lens, rel_fro(o_got, o_ref))
+    assert rel_fro(ht_got, ht_ref) <= TOL["bf16"], (w, lens, rel_fro(ht_got, ht_ref))
