@@ -175,3 +175,31 @@ def test_bwd_fullsize_packed_sampled(gdn, oracle_mod):
                "dh0": r["dh0"][n:n + 1, hv].cpu()}
         for key, val in got.items():
             assert rel_fro(val.numpy(), ref[key]) <= TOL, (n, lens[n], key, rel_fro(val.numpy(), ref[key]))
+
+
+def draw_bwd(i):
+    """Draw i of the randomised backward sweep: shape, GQA ratio, dtype, head
+    dims (K = V = 128 takes the chunked backward, K = 64 the token recurrence),
+    packed lengths, h0 and dht."""
+    r = np.random.default_rng(5200 + i)
+    dtype = "bf16" if r.random() < 0.6 else "f32"
+    K = int(r.choice([64, 128]))
+    V = 128 if K == 128 else int(r.choice([64, 128]))
+    Hqk = int(r.choice([1, 2]))
+    Hv = Hqk * int(r.choice([1, 2]))
+    gate = "softplus_exp" if r.random() < 0.7 else "logsigmoid4"
+    lens = None
+    if r.random() < 0.5:
+        n = int(r.integers(1, 6))
+        lens = [int(x) for x in r.integers(0, 260, size=n)]
+        w = I.Workload("random_bwd", 1, 0, Hqk, Hv, K, V, 64, dtype, gate, True, 500 + i, varlen_n=n)
+    else:
+        w = I.Workload("random_bwd", int(r.integers(1, 3)), int(r.integers(1, 260)), Hqk, Hv, K, V, 64, dtype, gate,
+                       True, 500 + i)
+    return w, lens, bool(r.random() < 0.7), bool(r.random() < 0.7)
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_bwd_random_draw(gdn, oracle_mod, i):
+    w, lens, with_h0, with_dht = draw_bwd(i)
+    check(gdn, oracle_mod, w, lens=lens, with_h0=with_h0, with_dht=with_dht, seed=40 + i)
