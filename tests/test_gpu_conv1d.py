@@ -151,3 +151,30 @@ def test_conv1d_full_size_sampled(gdn, oracle_mod):
                                                 "silu", conv_state=d["conv_state"][:, :, sl].cpu())
         assert_close(y[:, :, sl], y_ref, "bf16")
         assert torch.equal(st[:, :, sl].cpu(), torch.from_numpy(s_ref).to(st.dtype))
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_conv1d_random_draw(gdn, oracle_mod, i):
+    """Seeded draws of dtype, window, channel count, activation, packed or
+    equal lengths (across thread runs), slot map and initial-state flags."""
+    r = np.random.default_rng(6600 + i)
+    dtype = "bf16" if r.random() < 0.6 else "f32"
+    W = int(r.integers(1, 5))
+    D = 8 * int(r.integers(1, 40))
+    act = "silu" if r.random() < 0.7 else "none"
+    kw = {}
+    if r.random() < 0.5:
+        n = int(r.integers(1, 8))
+        lens = [int(x) for x in r.integers(0, 600, size=n)]
+        slots = n + int(r.integers(0, 3))
+        d = I.make_conv_inputs(1, 0, D, W, dtype, seed=40 + i, lengths=lens, slots=slots)
+        perm = r.permutation(slots)[:n].astype(np.int32)
+        perm[r.random(n) < 0.2] = -1
+        kw["cache_indices"] = torch.from_numpy(perm)
+        kw["has_initial_state"] = torch.from_numpy((r.random(n) < 0.7).astype(np.int32))
+    else:
+        d = I.make_conv_inputs(int(r.integers(1, 4)), int(r.integers(1, 700)), D, W, dtype, seed=40 + i)
+    y, st, y_ref, s_ref = run_both(gdn, oracle_mod, d, act, **kw)
+    assert_close(y, y_ref, dtype)
+    if W > 1:
+        assert torch.equal(st.cpu(), torch.from_numpy(s_ref).to(st.dtype))

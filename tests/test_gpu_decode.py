@@ -95,3 +95,38 @@ def test_prefill_then_decode_matches_recurrence(gdn, oracle_mod):
     o = torch.cat(outs, dim=1).float().cpu().numpy()
     assert rel_fro(o, o_ref) <= TOL["bf16"]
     assert rel_fro(ht.cpu().numpy(), ht_ref) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_decode_random_draw(gdn, oracle_mod, i):
+    """Seeded draws of dtype, head dims, GQA ratio, pool size, slot map (with
+    sequences that have no slot), tokens per sequence and dt_bias."""
+    r = np.random.default_rng(6100 + i)
+    dtype = "bf16" if r.random() < 0.6 else "f32"
+    K = int(r.choice([64, 128, 256]))
+    V = int(r.choice([64, 128])) if K != 256 else int(r.choice([128, 256]))
+    Hqk = int(r.choice([1, 2]))
+    Hv = Hqk * int(r.choice([1, 2, 4]))
+    n = int(r.integers(1, 7))
+    lens = [int(x) for x in r.integers(0, 6, size=n)]
+    w = I.WORKLOADS[3].with_(Hqk=Hqk, Hv=Hv, K=K, V=V, dtype=dtype, seed=700 + i)
+    x = I.make_inputs(w, "cpu", lengths=lens)
+    T = sum(lens)
+    a, b, A_log, dt_bias = gating_inputs(1, T, Hv, 800 + i)
+    if r.random() < 0.4:
+        dt_bias = None
+    slots_n = n + int(r.integers(0, 4))
+    perm = r.permutation(slots_n)[:n].astype(np.int32)
+    perm[r.random(n) < 0.2] = -1
+    slots = torch.from_numpy(perm)
+    pool = torch.randn(slots_n, Hv, K, V, generator=torch.Generator().manual_seed(900 + i)) * 0.1
+    o_ref, pool_ref = oracle_mod.gated_recurrent(x["q"], x["k"], x["v"], a, b, A_log, dt_bias, x["scale"], pool,
+                                                 state_indices=slots, cu_seqlens=x["cu_seqlens"])
+    state = pool.cuda()
+    o = gdn.gdn_recurrent_fwd(x["q"].cuda(), x["k"].cuda(), x["v"].cuda(), a.cuda(), b.cuda(), A_log.cuda(), state,
+                              dt_bias=dt_bias.cuda() if dt_bias is not None else None, scale=x["scale"],
+                              state_indices=slots.cuda(), cu_seqlens=x["cu_seqlens"].cuda())
+    torch.cuda.synchronize()
+    if o_ref.size:
+        assert rel_fro(o.float().cpu().numpy(), o_ref) <= TOL[dtype]
+    assert rel_fro(state.cpu().numpy(), pool_ref) <= 1e-5
