@@ -1,7 +1,7 @@
 """GPU parity: the CUDA library against the fp64 oracle on the same seeded
 inputs, through the C ABI (the Python binding only marshals arguments).
 
-Bar (spec tolerances): relative Frobenius error on both o and ht of at
+Bar (the operator's accuracy targets): relative Frobenius error on both o and ht of at
 most 1e-4 for fp32 inputs and 5e-3 for bf16 inputs (fp32 state); chunk
 tables bit-exact.
 """
