@@ -303,11 +303,14 @@ const char* gdn_version(void) { return "gdn 0.1 sm_103a"; }
 // in a host framework that owns every device buffer and hands the op only its
 // inputs and outputs (no workspace), or a caller that cannot afford the
 // implicit device-wide synchronisation of cudaMalloc/cudaFree between its
-// launches.  For them the staged forward pass runs with its intermediates in
-// one file-scope device array, kStaticScratchBytes (32 MiB) per GPU, which
-// every GPU that loads this library holds until the process exits.  The first
-// kAlign bytes of the array hold the status word of the last call (copied
-// there from the staged workspace, which starts right after it), so that
+// launches.  For them the forward pass runs with its workspace in one
+// file-scope device array, kStaticScratchBytes (32 MiB) per GPU, which every
+// GPU that loads this library holds until the process exits: the fused
+// kernels whenever their workspace fits (a status word, the order table of a
+// packed batch, or the window schedule's hand-over states: about 20 MB on 152
+// SMs), else the staged path when its intermediates fit.  The first kAlign
+// bytes of the array hold the status word of the last call (copied there from
+// the workspace, which starts right after it), so that
 // gdn_chunk_fwd_noalloc_get_device_status can read it without the problem.
 #include <cudaTypedefs.h>
 #include <mutex>
@@ -370,6 +373,18 @@ gdn_status static_scratch(void** out) {
   return GDN_OK;
 }
 
+// The path of a gdn_chunk_fwd_noalloc call: AUTO's choice, with the fused
+// kernel in place of the chunk-parallel path (whose per-segment states do
+// not fit the array), when its workspace fits; else the staged path when its
+// intermediates fit; GDN_PATH_AUTO when neither does.
+gdn_path noalloc_path(const gdn_problem& p) {
+  gdn_path path = resolve(p, GDN_PATH_AUTO);
+  if (path == GDN_PATH_CP) path = GDN_PATH_FUSED;
+  if (path != GDN_PATH_STAGED && workspace_for(p, path) <= kStaticStagedBytes) return path;
+  if (workspace_for(p, GDN_PATH_STAGED) <= kStaticStagedBytes) return GDN_PATH_STAGED;
+  return GDN_PATH_AUTO;
+}
+
 }  // namespace
 
 extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* pp, const void* q, const void* k, const void* v,
@@ -377,23 +392,26 @@ extern "C" gdn_status gdn_chunk_fwd_noalloc(const gdn_problem* pp, const void* q
                                             const int32_t* cu_seqlens, void* o, float* ht, void* stream) {
   gdn_problem p;
   if (!problem_ok(pp, &p)) return GDN_ERR_INVALID_ARG;
-  const size_t need = workspace_for(p, GDN_PATH_STAGED);
-  if (need > kStaticStagedBytes) return GDN_ERR_SCRATCH_LIMIT;
+  const gdn_path path = noalloc_path(p);
+  if (path == GDN_PATH_AUTO) return GDN_ERR_SCRATCH_LIMIT;
+  const size_t need = workspace_for(p, path);
   void* scratch = nullptr;
   gdn_status st = static_scratch(&scratch);
   if (st != GDN_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(scratch) + kAlign;
   st = check_call(p, q, k, v, g, beta, h0, cu_seqlens, o, ht, ws, kStaticStagedBytes, need);
   if (st != GDN_OK) return st;
-  // run_staged clears the status word it uses; every other intermediate is
-  // rewritten before it is read, so stale contents of earlier calls are harmless.
+  // each path clears the status word (and the window flags) it uses; every
+  // other intermediate is rewritten before it is read, so stale contents of
+  // earlier calls are harmless.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = run_staged(p, 6, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, ws, s);
+  if (path == GDN_PATH_FUSED) st = run_fused(p, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, ws, s);
+  else if (path == GDN_PATH_FUSED1) st = run_fused1(p, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, ws, s);
+  else st = run_staged(p, 6, q, k, v, g, beta, scale, h0, cu_seqlens, o, ht, ws, s);
   if (st != GDN_OK) return st;
   // the call's status word goes to the fixed slot at the array's start
-  gdn_staged_layout_t L;
-  staged_layout(p, &L);
-  if (cudaMemcpyAsync(scratch, ws + L.status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+  if (cudaMemcpyAsync(scratch, ws + status_offset(p, path), sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
+      cudaSuccess)
     return GDN_ERR_CUDA;
   return GDN_OK;
 }

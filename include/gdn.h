@@ -250,14 +250,16 @@ gdn_status gdn_selftest_handover_timeout(const gdn_problem* p, gdn_path path,
  * op inside a host framework that owns every device buffer and passes the op
  * only its inputs and outputs, or a caller that cannot accept the implicit
  * device-wide synchronisation of cudaMalloc/cudaFree.  This entry point
- * allocates nothing and takes no workspace: it runs the staged path with its
- * intermediates in a file-scope device array of 32 MiB that every GPU which
- * loads libgdn.so holds until the process exits.
+ * allocates nothing and takes no workspace: it runs the forward pass with its
+ * workspace in a file-scope device array of 32 MiB that every GPU which
+ * loads libgdn.so holds until the process exits.  Path: AUTO's choice, with
+ * GDN_PATH_FUSED in place of GDN_PATH_CP, when that path's workspace
+ * (gdn_chunk_fwd_workspace_size) fits 32 MiB - 256 bytes (the array's first
+ * 256 bytes hold the status word) -- the fused kernels need at most about 20
+ * MB -- else GDN_PATH_STAGED when its workspace fits.
  *   Arguments as gdn_chunk_fwd (the caller still passes inputs and outputs).
- *   Returns GDN_ERR_SCRATCH_LIMIT, launching nothing, when the problem's
- *   staged workspace (gdn_chunk_fwd_workspace_size with GDN_PATH_STAGED)
- *   exceeds 32 MiB - 256 bytes (the array's first 256 bytes hold the status
- *   word).
+ *   Returns GDN_ERR_SCRATCH_LIMIT, launching nothing, when neither fits (the
+ *   staged path for problems no fused kernel takes, such as fp32 inputs).
  *   The first call on a device (and the first after a device reset replaced
  *   its context) looks up the array's device address with
  *   cudaGetSymbolAddress, with that device current; make that first call

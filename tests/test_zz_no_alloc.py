@@ -2,16 +2,19 @@
 device memory (a framework that owns every device buffer and hands the op
 only its inputs and outputs, or a caller that cannot accept the implicit
 device-wide synchronisation of cudaMalloc).  It runs with a built-in 32 MiB
-static device scratch instead of a workspace.
+static device scratch instead of a workspace: the fused kernels when their
+workspace fits (AUTO's choice, the two-CTA kernel in place of the
+chunk-parallel path), else the staged path.
 
-Checked through the C ABI against the existing entry point (gdn_chunk_fwd,
-staged path: the same kernels, so the results must be equal bit for bit) on
-calls in a row with different problems -- the larger, differently laid-out
-one first, and the first one again at the end -- so that data left in the
-shared scratch by one call cannot leak into the next; once against the fp64
-oracle; and with malformed cu_seqlens, whose device status the caller reads
-with gdn_chunk_fwd_noalloc_get_device_status.  This file is named to be
-collected last.
+Checked through the C ABI against the existing entry point (gdn_chunk_fwd on
+the same path: the same kernels, so the results must be equal bit for bit) on
+calls in a row with different problems and paths -- the window schedule with
+its hand-over states, a packed batch, an fp32 problem on the staged path, and
+the packed batch again -- so that data left in the shared scratch by one call
+cannot leak into the next; once against the fp64 oracle; and with malformed
+cu_seqlens, whose device status the caller reads with
+gdn_chunk_fwd_noalloc_get_device_status.  This file is named to be collected
+last.
 """
 import ctypes
 
@@ -64,23 +67,42 @@ def noalloc_status(gdn):
     return out.value
 
 
-# the larger, packed case first, then a smaller fp32 one, then the first again
+SCRATCH = (32 << 20) - 256   # the array less its status slot
+
+
+def expected_path(gdn, p):
+    """The path a gdn_chunk_fwd_noalloc call takes (None: it is refused)."""
+    path = gdn.gdn_resolve_path(p)
+    if path == "cp":
+        path = "fused"
+    if path != "staged" and gdn.gdn_chunk_fwd_workspace_size(p, path) <= SCRATCH:
+        return path
+    return "staged" if gdn.gdn_chunk_fwd_workspace_size(p, "staged") <= SCRATCH else None
+
+
+# the window schedule (hand-over states in the scratch), a packed batch, an
+# fp32 problem on the staged path, and the packed batch again
+WINDOWS = (I.WORKLOADS[2].with_(B=16, T=2048), None)                        # bf16, H = 32, windows cut chains
 VARLEN = (I.WORKLOADS[3].with_(Hqk=2, Hv=4, C=128), [70, 0, 5, 130, 300])   # bf16, GQA, varlen, C = 128
 FP32 = (I.WORKLOADS[0], None)                                              # fp32, h0, C = 64
-CASES = [VARLEN, FP32, VARLEN]
+CASES = [WINDOWS, VARLEN, FP32, VARLEN]
 
 
 def test_noalloc_matches_existing_entry_point_bit_for_bit(gdn):
+    paths = []
     for w, lens in CASES:
         x = I.make_inputs(w, "cuda", lengths=lens)
+        path = expected_path(gdn, gdn.problem_of(x["q"], x["v"], w.C, x["cu_seqlens"]))
+        paths.append(path)
         st, o, ht = noalloc_call(gdn, x, w.C)
         assert st == gdn.GDN_OK, gdn.status_string(st)
         assert noalloc_status(gdn) == gdn.DEV_OK
         o_ref, ht_ref = gdn.gdn_chunk_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], x["scale"], h0=x["h0"],
-                                          cu_seqlens=x["cu_seqlens"], C=w.C, path="staged")
+                                          cu_seqlens=x["cu_seqlens"], C=w.C, path=path)
         torch.cuda.synchronize()
         assert torch.equal(o, o_ref)
         assert torch.equal(ht, ht_ref)
+    assert paths == ["fused", "fused1", "staged", "fused1"]
 
 
 def test_noalloc_against_the_oracle(gdn, oracle_mod):
@@ -112,8 +134,10 @@ def test_noalloc_reports_malformed_cu_seqlens(gdn):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(gdn):
-    x = I.make_inputs(I.WORKLOADS[1].with_(T=2048), "cuda")   # staged workspace far above 32 MiB
+    # fp32 inputs: no fused kernel, and a staged workspace above 32 MiB
+    x = I.make_inputs(I.WORKLOADS[0].with_(B=2, T=4096, Hqk=4, Hv=4), "cuda")
     p = gdn.problem_of(x["q"], x["v"], 64)
+    assert expected_path(gdn, p) is None
     assert gdn.gdn_chunk_fwd_workspace_size(p, "staged") > (32 << 20)
     st, _, _ = noalloc_call(gdn, x, 64)
     assert st == 5   # GDN_ERR_SCRATCH_LIMIT
