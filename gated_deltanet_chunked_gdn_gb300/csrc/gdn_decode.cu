@@ -15,7 +15,10 @@
 // One CTA per (sequence, value head, 64-column slice of V); the slice S[K][64]
 // lives in registers (256 threads: 16 float4 column groups x 16 row groups)
 // for all of the sequence's tokens and is read and written once.  The step is
-// bound by HBM traffic on the state (2 * K * V * 4 bytes per head).
+// bound by HBM traffic on the state (2 * K * V * 4 bytes per head): the state
+// goes through L2 with the evict-first (streaming) hint, since a pool larger
+// than L2 is touched once a step, and K <= 128 runs four CTAs an SM (64
+// registers) so that more state loads are in flight.
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -25,7 +28,7 @@ constexpr int kDecThreads = 256;
 constexpr int kCols = 64;   // V slice per CTA
 
 template <typename Tin, int K>
-__global__ void __launch_bounds__(kDecThreads) gdn_recurrent_kernel(
+__global__ void __launch_bounds__(kDecThreads, K <= 128 ? 4 : 2) gdn_recurrent_kernel(
     const Tin* __restrict__ q, const Tin* __restrict__ k, const Tin* __restrict__ v, const float* __restrict__ a,
     const float* __restrict__ b, const float* __restrict__ A_log, const float* __restrict__ dt_bias, float scale,
     float* __restrict__ state, const int32_t* __restrict__ state_indices, int state_slots,
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(kDecThreads) gdn_recurrent_kernel(
   float s[RPG][4];
 #pragma unroll
   for (int r = 0; r < RPG; ++r) {
-    const float4 x = *reinterpret_cast<const float4*>(S + (int64_t)(rg * RPG + r) * V + col);
+    const float4 x = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rg * RPG + r) * V + col));
     s[r][0] = x.x, s[r][1] = x.y, s[r][2] = x.z, s[r][3] = x.w;
   }
   const float decay_rate = expf(A_log[h]);
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kDecThreads) gdn_recurrent_kernel(
   }
 #pragma unroll
   for (int r = 0; r < RPG; ++r)
-    *reinterpret_cast<float4*>(S + (int64_t)(rg * RPG + r) * V + col) = make_float4(s[r][0], s[r][1], s[r][2], s[r][3]);
+    __stcs(reinterpret_cast<float4*>(S + (int64_t)(rg * RPG + r) * V + col), make_float4(s[r][0], s[r][1], s[r][2], s[r][3]));
 }
 
 template <typename Tin>
