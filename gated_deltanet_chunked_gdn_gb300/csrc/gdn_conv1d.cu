@@ -118,10 +118,12 @@ __device__ __forceinline__ float rcp_approx(float y) {
   return r;
 }
 
-// SiLU u sigmoid(u) = u / (1 + e^{-u}) with two MUFU operations (ex2 and rcp)
-// instead of an IEEE division; for very negative u, e^{-u} overflows to +inf
-// and the result is -0.
-__device__ __forceinline__ float silu(float u) { return u * rcp_approx(1.f + sm100::exp_fast(-u)); }
+// SiLU u sigmoid(u) = u / (1 + e^{-u}) is evaluated in emit below with two
+// MUFU operations per value (ex2 of -u log2 e, then rcp) instead of an IEEE
+// division; for very negative u, e^{-u} overflows to +inf and the result is
+// -0.  The multiplies, adds and the convolution's FMAs run on pairs of
+// channels (the packed fp32 instructions of sm_100+, the same IEEE rounding
+// per value as the scalar ones).
 
 template <typename T, int W, bool SILU>
 __global__ void __launch_bounds__(kConvThreads, sizeof(T) == 2 ? 4 : 2) conv1d_kernel(const ConvArgs a) {
@@ -180,20 +182,28 @@ __global__ void __launch_bounds__(kConvThreads, sizeof(T) == 2 ? 4 : 2) conv1d_k
     }
     auto emit = [&](const Vec8<T>& xin, int64_t tt) {
       float acc[8], f[8];
+      float2 a2[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[j] = bs[j];
+      for (int j = 0; j < 4; ++j) a2[j] = make_float2(bs[2 * j], bs[2 * j + 1]);
 #pragma unroll
-      for (int w = 0; w < W - 1; ++w) {
-        win[w].to_float(f);
+      for (int w = 0; w < W; ++w) {
+        if (w < W - 1) win[w].to_float(f);
+        else xin.to_float(f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[j] = fmaf(wt[w][j], f[j], acc[j]);
+        for (int j = 0; j < 4; ++j)
+          a2[j] = __ffma2_rn(make_float2(wt[w][2 * j], wt[w][2 * j + 1]), make_float2(f[2 * j], f[2 * j + 1]), a2[j]);
       }
-      xin.to_float(f);
+      if (SILU) {
+        const float2 nl = make_float2(-sm100::kLog2e, -sm100::kLog2e), one = make_float2(1.f, 1.f);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        acc[j] = fmaf(wt[W - 1][j], f[j], acc[j]);
-        if (SILU) acc[j] = silu(acc[j]);
+        for (int j = 0; j < 4; ++j) {
+          const float2 t = __fmul2_rn(a2[j], nl);
+          const float2 d = __fadd2_rn(make_float2(sm100::ex2_fast(t.x), sm100::ex2_fast(t.y)), one);
+          a2[j] = __fmul2_rn(a2[j], make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+        }
       }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[2 * j] = a2[j].x, acc[2 * j + 1] = a2[j].y;
 #pragma unroll
       for (int w = 0; w + 1 < W - 1; ++w) win[w] = win[w + 1];
       if (W > 1) win[W > 1 ? W - 2 : 0] = xin;
