@@ -650,7 +650,9 @@ def main():
                      "traffic": (measured_traffic("fused", w.B * w.T / 8192 * w.Hv / 32, state_bytes)
                                  if path == "fused" and args.workload == "batched_16x8192" else
                                  measured_traffic("fused1_d256", w.B * w.T / 32768, state_bytes)
-                                 if path in ("fused", "fused1") and args.workload == "long_d256" else None),
+                                 if path in ("fused", "fused1") and args.workload == "long_d256" else
+                                 measured_traffic("fused1_varlen64", 1, state_bytes)
+                                 if path == "fused1" and args.workload == "varlen_64" else None),
                      "peak_source": f"{pk['source']} ({peak_kind})",
                      "kernel": (("gdn_fused1_kernel" if (w.K == 256 or path == "fused1") else "gdn_fused_kernel") +
                                 (" (after the ranking launch of the packed batch)" if ranked
