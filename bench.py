@@ -174,6 +174,8 @@ def cpu_oracle_sample(x: dict, w, nthreads: int, budget_s: float, n_chains: int 
     oracle.build()
     H = w.Hv
     Bx = x["q"].shape[0]
+    if x.get("cu_seqlens") is not None:
+        return cpu_oracle_sample_packed(oracle, x, w, nthreads, budget_s)
     if n_chains is None:
         s0 = {k: x[k][0:1].cpu() for k in ("q", "k", "v", "g", "beta")}
         h0 = x["h0"][0:1].cpu() if x["h0"] is not None else None
@@ -197,6 +199,40 @@ def cpu_oracle_sample(x: dict, w, nthreads: int, budget_s: float, n_chains: int 
             "sample": f"{n} (sequence, head) chains of {w.T} tokens of the {w.B}x{w.T} H={H} workload, "
                       f"fp64 recurrence, {nthreads} threads, {wall:.2f} s wall",
             "wall_s": wall, "chains": n}
+
+
+def cpu_oracle_sample_packed(oracle, x: dict, w, nthreads: int, budget_s: float) -> dict:
+    """The oracle on whole (sequence, head) chains of a packed batch, taken in
+    (sequence, head) order until about ``budget_s`` CPU-seconds of work, sized
+    from one chain of the longest sequence timed on one thread; tokens are
+    counted as in the metric (token positions of all Hv heads)."""
+    H = w.Hv
+    cu = x["cu_seqlens"].cpu().tolist()
+    lens = [cu[i + 1] - cu[i] for i in range(len(cu) - 1)]
+    host = {k: x[k].cpu() for k in ("q", "k", "v", "g", "beta")}
+    h0 = x["h0"].cpu() if x["h0"] is not None else None
+    cuc = x["cu_seqlens"].cpu()
+    nmax = max(range(len(lens)), key=lambda i: lens[i])
+    t = time.perf_counter()
+    oracle.recurrent(host["q"], host["k"], host["v"], host["g"], host["beta"], x["scale"], h0=h0, cu_seqlens=cuc,
+                     chains=[nmax * H], nthreads=1)
+    per_tok = (time.perf_counter() - t) / max(lens[nmax], 1)
+    want = budget_s / max(per_tok, 1e-9)       # chain-tokens the budget buys
+    chains, ctoks = [], 0
+    for c in range(len(lens) * H):
+        if ctoks >= want:
+            break
+        chains.append(c)
+        ctoks += lens[c // H]
+    t = time.perf_counter()
+    oracle.recurrent(host["q"], host["k"], host["v"], host["g"], host["beta"], x["scale"], h0=h0, cu_seqlens=cuc,
+                     chains=chains, nthreads=nthreads)
+    wall = time.perf_counter() - t
+    tokens = ctoks / H
+    return {"value": tokens / wall, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{len(chains)} (sequence, head) chains ({ctoks} chain-tokens) of the packed "
+                      f"{len(lens)}-sequence workload, fp64 recurrence, {nthreads} threads, {wall:.2f} s wall",
+            "wall_s": wall, "chains": len(chains)}
 
 
 def run_reference(args, rank: int, world: int) -> None:
