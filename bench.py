@@ -688,7 +688,10 @@ def main():
                                  measured_traffic("fused1_d256", w.B * w.T / 32768, state_bytes)
                                  if path in ("fused", "fused1") and args.workload == "long_d256" else
                                  measured_traffic("fused1_varlen64", 1, state_bytes)
-                                 if path == "fused1" and args.workload == "varlen_64" else None),
+                                 if path == "fused1" and args.workload == "varlen_64" else
+                                 measured_traffic({"gqa_prefill_1x4096": "cp_1x4096",
+                                                   "long_1x32768": "cp_1x32768"}.get(args.workload, ""), 1)
+                                 if path == "cp" else None),
                      "peak_source": f"{pk['source']} ({peak_kind})",
                      "kernel": (("gdn_fused1_kernel" if (w.K == 256 or path == "fused1") else "gdn_fused_kernel") +
                                 (" (after the ranking launch of the packed batch)" if ranked
